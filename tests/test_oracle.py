@@ -1,0 +1,220 @@
+"""Pins for the fp64 oracle, each against something other than the oracle itself.
+
+CPU only. The pins: a hand-derived worked example (tests/golden), closed forms
+(Q = 0, dominant key, N = 1, causal row 0, V = 1), invariants (gradient sums,
+key shift, logit-scale trade, key permutation), agreement of the three
+independent forward formulations (full matrix, page-1 query chunks, page-2
+online softmax over key blocks), the sampled-row / sampled-column modes, and
+central finite differences of the backward.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _ev(expr):
+    return float(eval(expr, {"ln3": math.log(3), "ln4": math.log(4), "ln2": math.log(2)}))
+
+
+# ---------------------------------------------------------------- golden
+@pytest.mark.parametrize("causal", [False, True])
+def test_golden_two_key_example(causal):
+    g = json.load(open(os.path.join(HERE, "golden", "two_key_example.json")))
+    inp = {k: np.array([_ev(x) for x in v]).reshape(1, 1, 2, 1) for k, v in g["inputs"].items() if k != "scale"}
+    scale = _ev(g["inputs"]["scale"])
+    exp = g["expected"]["causal" if causal else "noncausal"]
+    o, lse = oracle.attention_fwd(inp["q"], inp["k"], inp["v"], scale, causal)
+    dq, dk, dv = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["do"], scale, causal)
+    for name, got in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        want = np.array([_ev(x) for x in exp[name]])
+        np.testing.assert_allclose(got.reshape(-1), want, rtol=0, atol=1e-14, err_msg=name)
+
+
+# ---------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("causal", [False, True])
+def test_q_zero_is_uniform_attention(causal):
+    B, H, N, d = 1, 2, 37, 8
+    q = np.zeros((B, H, N, d))
+    k, v = _rand((B, H, N, d), 1), _rand((B, H, N, d), 2)
+    o, lse = oracle.attention_fwd(q, k, v, 0.3, causal)
+    if causal:
+        want = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+        want_lse = np.log(np.arange(1, N + 1))[None, None, :].repeat(H, 1)
+    else:
+        want = np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape)
+        want_lse = np.full((B, H, N), math.log(N))
+    np.testing.assert_allclose(o, want, atol=1e-13)
+    np.testing.assert_allclose(lse, want_lse, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dominant_key_is_one_hot(causal):
+    B, H, N, d = 1, 1, 50, 4
+    jstar = 17
+    a, b, scale = 8.0, 10.0, 0.5  # scale*a*b = 40
+    q = np.zeros((B, H, N, d)); q[..., 0] = a
+    k = np.zeros((B, H, N, d)); k[0, 0, jstar, 0] = b
+    v = _rand((B, H, N, d), 3)
+    o, _ = oracle.attention_fwd(q, k, v, scale, causal)
+    for i in range(N):
+        if causal and i < jstar:
+            want = v[0, 0, : i + 1].mean(axis=0)  # all visible logits are 0
+            np.testing.assert_allclose(o[0, 0, i], want, atol=1e-13)
+        else:
+            np.testing.assert_allclose(o[0, 0, i], v[0, 0, jstar], atol=N * math.exp(-40) * 10)
+
+
+def test_single_key():
+    q, k, v, do = (_rand((2, 3, 1, 5), s) for s in range(4))
+    scale = 0.7
+    o, lse = oracle.attention_fwd(q, k, v, scale, False)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, scale, False)
+    np.testing.assert_allclose(o, v, atol=1e-15)
+    np.testing.assert_allclose(lse, scale * np.sum(q * k, axis=-1), atol=1e-14)
+    np.testing.assert_allclose(dv, do, atol=1e-15)
+    np.testing.assert_allclose(dq, 0, atol=1e-15)
+    np.testing.assert_allclose(dk, 0, atol=1e-15)
+
+
+def test_causal_row_zero_sees_key_zero():
+    q, k, v = (_rand((1, 2, 33, 8), s) for s in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, 0.35, True)
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], atol=1e-15)
+    np.testing.assert_allclose(lse[:, :, 0], 0.35 * np.sum(q[:, :, 0] * k[:, :, 0], -1), atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_values_give_constant_output(causal):
+    q, k = _rand((1, 2, 40, 8), 5) * 3, _rand((1, 2, 40, 8), 6) * 3
+    o, _ = oracle.attention_fwd(q, k, np.ones_like(q), 0.35, causal)
+    np.testing.assert_allclose(o, 1.0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradient_sums(causal):
+    q, k, v, do = (_rand((2, 2, 45, 8), s) for s in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.4, causal)
+    # softmax is invariant to a shift of all logits of a row -> sum_j dS_ij = 0
+    np.testing.assert_allclose(dk.sum(axis=2), 0, atol=1e-12)
+    # every row of P sums to 1 -> sum_j dV_j = sum_i dO_i
+    np.testing.assert_allclose(dv.sum(axis=2), do.sum(axis=2), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance(causal):
+    q, k, v = (_rand((1, 2, 30, 8), s) for s in range(3))
+    c = _rand((8,), 9)
+    o1, lse1 = oracle.attention_fwd(q, k, v, 0.4, causal)
+    o2, lse2 = oracle.attention_fwd(q, k + c, v, 0.4, causal)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(lse2 - lse1, 0.4 * (q @ c), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_scale_trade(causal):
+    q, k, v = (_rand((1, 2, 30, 8), s) for s in range(3))
+    o1, lse1 = oracle.attention_fwd(q, k, v, 0.4, causal)
+    o2, lse2 = oracle.attention_fwd(2.5 * q, k, v, 0.4 / 2.5, causal)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(lse1, lse2, atol=1e-12)
+
+
+def test_key_permutation_invariance():
+    q, k, v = (_rand((1, 2, 30, 8), s) for s in range(3))
+    perm = np.random.default_rng(4).permutation(30)
+    o1, _ = oracle.attention_fwd(q, k, v, 0.4, False)
+    o2, _ = oracle.attention_fwd(q, k[:, :, perm], v[:, :, perm], 0.4, False)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+
+
+def test_causal_prefix_independence():
+    """Causal row i must not depend on keys/values after i."""
+    q, k, v = (_rand((1, 1, 30, 8), s) for s in range(3))
+    o1, lse1 = oracle.attention_fwd(q, k, v, 0.4, True)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, 20:] = 100.0
+    v2[:, :, 20:] = -7.0
+    o2, lse2 = oracle.attention_fwd(q, k2, v2, 0.4, True)
+    np.testing.assert_allclose(o1[:, :, :20], o2[:, :, :20], atol=1e-14)
+    np.testing.assert_allclose(lse1[:, :, :20], lse2[:, :, :20], atol=1e-14)
+    assert np.abs(o1[:, :, 25] - o2[:, :, 25]).max() > 1e-3
+
+
+# ---------------------------------------------------------------- formulations
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [64, 200, 257])
+def test_chunked_and_online_match_direct(causal, N):
+    q, k, v = (_rand((2, 2, N, 16), s) * 2 for s in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, 0.25, causal)
+    oc, lsec = oracle.chunked_attention_fwd(q, k, v, 0.25, causal, chunk_size=64)
+    oo, lseo = oracle.online_attention_fwd(q, k, v, 0.25, causal, block=48)
+    np.testing.assert_allclose(oc, o, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lsec, lse, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(oo, o, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lseo, lse, rtol=1e-12, atol=1e-12)
+
+
+def test_online_softmax_large_logits():
+    """Logits of several hundred: the running-max rescale must not overflow."""
+    q, k, v = (_rand((1, 1, 300, 8), s) for s in range(3))
+    q *= 40.0
+    o, lse = oracle.attention_fwd(q, k, v, 0.5, True)
+    oo, lseo = oracle.online_attention_fwd(q, k, v, 0.5, True, block=64)
+    assert np.isfinite(o).all() and np.abs(lse).max() > 100
+    np.testing.assert_allclose(oo, o, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(lseo, lse, rtol=1e-12, atol=1e-10)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_modes_match_full(causal):
+    B, H, N, d = 1, 2, 300, 16
+    q, k, v, do = (_rand((B, H, N, d), s) for s in range(4))
+    o, lse = oracle.attention_fwd(q, k, v, 0.25, causal)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.25, causal)
+    rows = [0, 1, 127, 128, 150, 299]
+    ro, rl, rdq = oracle.attention_rows(q, k, v, do, 0.25, causal, rows)
+    np.testing.assert_allclose(ro, o[:, :, rows], atol=1e-13)
+    np.testing.assert_allclose(rl, lse[:, :, rows], atol=1e-13)
+    np.testing.assert_allclose(rdq, dq[:, :, rows], atol=1e-13)
+    cols = [0, 5, 128, 299]
+    ck, cv = oracle.attention_cols(q, k, v, do, 0.25, causal, cols, heads=[(0, 1)], row_block=64)
+    np.testing.assert_allclose(ck[0], dk[0, 1, cols], atol=1e-13)
+    np.testing.assert_allclose(cv[0], dv[0, 1, cols], atol=1e-13)
+
+
+# ---------------------------------------------------------------- finite differences
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(16, 4), (9, 8)])
+def test_backward_matches_central_differences(causal, N, d):
+    B, H = 1, 2
+    q, k, v, do = (_rand((B, H, N, d), 10 + s) for s in range(4))
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, scale, causal)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_fwd(qq, kk, vv, scale, causal)
+        return float(np.sum(do * o))
+
+    h = 1e-6
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        fd = np.zeros_like(grad)
+        args = [q, k, v]
+        for idx in np.ndindex(grad.shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fd[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        assert np.abs(fd - grad).max() <= 1e-6 * np.abs(grad).max(), which

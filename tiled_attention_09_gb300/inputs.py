@@ -1,0 +1,120 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests, the bench and the oracle's tests.
+
+This module holds no attention arithmetic. It draws Q, K, V and dO the same way
+for every consumer, so that the GPU path and the fp64 oracle always see
+bit-identical inputs:
+
+* a CPU ``torch.Generator`` seeded with ``seed``;
+* ``torch.randn`` in float32, drawn in the order Q, K, V, dO, each shaped
+  ``[B, H, N, d]`` (the layout of the pages' own examples: the query-chunked JAX
+  example on page 1 and the XLA example on page 2 both use
+  ``(batch, heads, seq, head_dim)``);
+* a cast to fp16 or bf16 (round to nearest even);
+* for the stress variant, the cast Q and K are multiplied by 8, which is exact
+  in both formats and pushes the scaled logits to a few hundred.
+
+It also holds the sampled-row and sampled-column recipes used where the full
+fp64 oracle is too slow (sequence length above 2048).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes, dtype, mask and input recipe."""
+
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str = "bf16"
+    causal: bool = False
+    stress: float = 1.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    def fwd_flops(self) -> float:
+        """4*B*H*N^2*d, halved when causal (the metric's own count)."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        return 2.5 * self.fwd_flops()
+
+    def name(self) -> str:
+        s = f"B{self.B}_H{self.H}_N{self.N}_d{self.d}_{self.dtype}_{'causal' if self.causal else 'full'}"
+        if self.stress != 1.0:
+            s += f"_x{self.stress:g}"
+        return s
+
+
+# The five workloads the build is measured and checked on.
+SMALL = Workload(1, 2, 256, 64, "fp16", False)
+PAGES_SHAPE = Workload(2, 12, 1024, 64, "fp16", False)
+CAUSAL_4K = Workload(2, 12, 4096, 128, "bf16", True)
+CAUSAL_4K_STRESS = Workload(2, 12, 4096, 128, "bf16", True, stress=8.0)
+LONG_32K = Workload(1, 8, 32768, 128, "bf16", True)
+
+
+def sweep_workloads():
+    out = []
+    for d in (64, 128, 256):
+        for N in (512, 1024, 2048, 4096, 8192, 16384):
+            for dt in ("bf16", "fp16"):
+                for causal in (True, False):
+                    out.append(Workload(2, 12, N, d, dt, causal))
+    return out
+
+
+def make_inputs(w: Workload):
+    """Return q, k, v, do as CPU tensors of ``w.torch_dtype``, shape [B,H,N,d]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    out = []
+    for _ in range(4):  # Q, K, V, dO in this order
+        out.append(torch.randn(shape, generator=g, dtype=torch.float32).to(w.torch_dtype))
+    q, k, v, do = out
+    if w.stress != 1.0:
+        q = q * w.stress
+        k = k * w.stress
+    return q, k, v, do
+
+
+def sample_rows(N: int, n_random: int = 57, seed: int = 1):
+    """Query rows checked when the full oracle is too slow.
+
+    {0, 1, 127, 128, 129, N/2, N-1} plus ``n_random`` distinct random rows drawn
+    with a CPU generator seeded by ``seed``. Sorted, unique, all < N.
+    """
+    fixed = {0, 1, 127, 128, 129, N // 2, N - 1}
+    fixed = {r for r in fixed if 0 <= r < N}
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    perm = torch.randperm(N, generator=g).tolist()
+    extra = [r for r in perm if r not in fixed][:n_random]
+    return sorted(fixed | set(extra))
+
+
+def sample_cols(N: int, n: int = 64, seed: int = 1):
+    """Key columns checked for dK and dV when the full oracle is too slow."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 1000)
+    fixed = {0, N - 1, N // 2}
+    perm = torch.randperm(N, generator=g).tolist()
+    extra = [c for c in perm if c not in fixed][: max(0, n - len(fixed))]
+    return sorted(fixed | set(extra))
