@@ -1,0 +1,140 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) fused attention library (libfa.so).
+ *
+ * Exact scaled-dot-product attention
+ *     O = softmax(scale * Q K^T [+ causal mask]) V
+ * computed as one fused, tiled forward kernel with an online softmax that
+ * saves the per-row log-sum-exp, and a recompute-based backward that rebuilds
+ * P from Q, K and that log-sum-exp. No N x N matrix is ever written to memory.
+ *
+ * Sources (web pages, cited by title and section):
+ *  - "transformer模型详解（十）：FlashAttention优化技术" (Transformer explained,
+ *    part 10: FlashAttention), sections "Kernel Fusion：消灭中间落盘" (one kernel,
+ *    only the final output written), "Tiling 分块策略：匹配硬件极限" (B_q x B_k
+ *    tiles in on-chip memory; online softmax: per-tile max and exp-sum, update
+ *    of the global max with rescaling, one final normalisation),
+ *    "Re-computation 而非缓存" (backward: outer loop over K/V column blocks,
+ *    inner loop over Q row blocks, scores and probabilities recomputed) and
+ *    "硬件依赖不可忽视" (sequence length a multiple of 16, head dimension
+ *    preferably 64/128/256). Its AMP example calls flash_attn_func(q, k, v).
+ *  - "在TPU上移植Flash Attention的工程实践与挑战", Example 2 (chunked attention):
+ *    tensors laid out (batch, heads, seq, head_dim).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors q, k, v, o, dO, dq, dk, dv: dense, contiguous [B, H, N, d] in the
+ *    element type given by `dtype` (fp16 or bf16), row pitch d elements.
+ *    lse: fp32 [B, H, N], natural-log log-sum-exp of the scaled logits.
+ *  - All data pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing on these paths. Every pointer must be 16-byte aligned
+ *    (a TMA requirement), else FA_ERR_ALIGNMENT.
+ *  - Supported shapes: d in {64, 128, 256}; N >= 128 and N % 128 == 0;
+ *    B, H >= 1; B*H*N < 2^31. Anything else: FA_ERR_UNSUPPORTED, no launch.
+ *  - scale: finite and >= 0 (0 gives uniform attention), else
+ *    FA_ERR_INVALID_ARG. The pages use scale = d^-1/2.
+ *  - causal != 0: query i attends to keys j <= i.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Work is enqueued asynchronously; argument errors are returned
+ *    synchronously with nothing enqueued; a failed launch returns FA_ERR_CUDA.
+ *  - Device-side problems (a bounded wait that timed out, a failed index
+ *    check) do not trap: they are recorded in a device status word that
+ *    fa_device_status() reads and clears.
+ *  - The current CUDA device must be a compute capability 10.3 GPU (sm_103a
+ *    code only), else FA_ERR_UNSUPPORTED.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, bad scale, bad enum value */
+  FA_ERR_UNSUPPORTED = 2,  /* shape/dtype/device outside the supported set */
+  FA_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than fa_bwd_workspace_size() */
+  FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 6,      /* a device-side bounded wait expired (from fa_device_status) */
+  FA_ERR_DEVICE_FAULT = 7  /* a device-side check failed (from fa_device_status) */
+} fa_status;
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/*
+ * Forward pass (page 2, "Kernel Fusion" + "Tiling" + online softmax).
+ *   in : q, k, v  [B,H,N,d] dtype
+ *   out: o        [B,H,N,d] dtype  = softmax(scale*q k^T [causal]) v, rounded to dtype
+ *        lse      [B,H,N]   fp32   = ln(sum_j exp(scale * q_i . k_j)) over visible j
+ * One kernel launch. o and lse are written in full.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: fp32 D [B,H,N], fp32 LSE*log2(e)
+ * [B,H,N] and the fp32 dQ accumulator [B,H,N,d], each 256-byte aligned.
+ * Returns 0 for unsupported shapes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass (page 2, "Re-computation"): from the forward's o and lse and
+ * the upstream gradient dO, computes
+ *   D  = rowsum(dO * o)                      (fp32, workspace)
+ *   P  = exp(scale * q k^T - lse)            (recomputed per tile, never stored)
+ *   dV = P^T dO;  dP = dO v^T;  dS = P * (dP - D)
+ *   dQ = scale * dS k;  dK = scale * dS^T q
+ * Writes dq, dk, dv [B,H,N,d] dtype in full (no accumulate-into). Three
+ * launches on `stream`: preprocess (D, LSE*log2e, zero dQ accumulator), the
+ * main kernel (one CTA per 128-key tile, dQ partial tiles added into the fp32
+ * accumulator with bulk reductions), and the dQ conversion. Summation order of
+ * dQ depends on scheduling, so dq is not bitwise reproducible; dk, dv are.
+ * workspace: device memory of at least fa_bwd_workspace_size(B,H,N,d) bytes,
+ * caller-owned, 256-byte aligned; its contents on entry do not matter.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * The three phases of fa_bwd as separate calls (same arguments and rules);
+ * fa_bwd is exactly these three in order. Exposed so each kernel can be timed
+ * on its own.
+ */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
+                            size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream);
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                      void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                      fa_dtype dtype, void* stream);
+fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                            float scale, fa_dtype dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status words of all
+ * kernels. FA_OK if no kernel reported anything; FA_ERR_TIMEOUT if a bounded
+ * wait expired; FA_ERR_DEVICE_FAULT for a failed device-side check;
+ * FA_ERR_CUDA if the synchronisation itself failed.
+ * If `info` is non-NULL it receives {code, where, block, count} of the first report.
+ */
+fa_status fa_device_status(void* stream, unsigned int info[4]);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Upper bound, in nanoseconds, of every device-side wait (default 4e9).
+ * Takes effect for launches after the call; 0 restores the default.
+ */
+void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/* ABI version (major*100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

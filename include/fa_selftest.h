@@ -1,0 +1,38 @@
+/*
+ * fa_selftest.h — tensor-core building-block self-test exported by libfa.so.
+ *
+ * Not part of the attention method: the pages have no counterpart. It checks,
+ * in isolation, the operand forms the attention kernels feed to tcgen05.mma,
+ * so that a descriptor or layout mistake shows up as a wrong matrix product
+ * rather than as a wrong attention result.
+ *
+ * Computes, with one CTA on the current device,
+ *     d[i][j] = sum_t A[i][t] * B[j][t]      (i < 128, j < n, t < k), fp32
+ * from 16-bit inputs of type `dtype`. Storage of the operands in DEVICE memory:
+ *   a_mode 0: a = A stored [128][k] (row-major, k contiguous) -> smem, K-major
+ *   a_mode 1: a = A stored [k][128] (A transposed)            -> smem, MN-major
+ *   a_mode 2: a = A stored [128][k]                           -> tensor memory
+ *   b_mode 0: b = B stored [n][k]                             -> smem, K-major
+ *   b_mode 1: b = B stored [k][n] (B transposed)              -> smem, MN-major
+ *   d: fp32 [128][n] row-major, written in full.
+ * n in {64, 128, 256}, k in {64, 128}; pointers 16-byte aligned.
+ * Returns FA_OK after enqueuing on `stream` (a cudaStream_t as void*), or an
+ * argument / device error from fa.h without launching.
+ */
+#ifndef FA_SELFTEST_H_
+#define FA_SELFTEST_H_
+
+#include "fa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+fa_status fa_selftest_gemm(const void* a, const void* b, float* d, int n, int k, int a_mode, int b_mode,
+                           fa_dtype dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_SELFTEST_H_ */

@@ -1,0 +1,64 @@
+"""Tolerances and comparison helpers shared by the GPU parity tests.
+
+Tolerance reading (fixed before any kernel ran; derivation in the design notes):
+
+* O, elementwise:  |O_gpu - O_orc| <= 2e-3 + half_ulp_dtype(O_orc) + u_dtype * (P|V|)_i
+  where 2e-3 is the stated bound, half_ulp is the unavoidable rounding of the
+  output to fp16/bf16, and u_dtype * (P|V|)_i bounds the error of rounding the
+  probabilities P to the input dtype before the P.V tensor-core product
+  (u_bf16 = 2^-8, u_fp16 = 2^-11; (P|V|)_i is the oracle's attention output
+  with |V| in place of V). The literal max-abs error and the share of elements
+  inside 2e-3 + half_ulp are reported alongside.
+* LSE: |LSE_gpu - LSE_orc| <= 2e-3 (fp32 output).
+* dQ, dK, dV: max|g_gpu - g_orc| <= 1e-2 * max|g_orc|, per tensor.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+UNIT_ROUNDOFF = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}
+MANT_BITS = {"bf16": 7, "fp16": 10}
+
+
+def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1e-30)))
+    if dtype == "fp16":
+        e = np.maximum(e, -14)  # subnormal spacing
+    return np.where(ax > 0, 2.0 ** (e - MANT_BITS[dtype] - 1), 0.0)
+
+
+def o_tolerance(o_ref: np.ndarray, pv_abs: np.ndarray, dtype: str) -> np.ndarray:
+    return 2e-3 + half_ulp(o_ref, dtype) + UNIT_ROUNDOFF[dtype] * pv_abs
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_o(o_gpu: np.ndarray, o_ref: np.ndarray, pv_abs: np.ndarray, dtype: str, what: str = "O"):
+    err = np.abs(o_gpu - o_ref)
+    tol = o_tolerance(o_ref, pv_abs, dtype)
+    bad = err > tol
+    literal = float(np.mean(err <= 2e-3 + half_ulp(o_ref, dtype)))
+    assert np.isfinite(o_gpu).all(), f"{what}: non-finite values"
+    assert not bad.any(), (
+        f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; max err {err.max():.3e}; "
+        f"worst excess {(err - tol).max():.3e}")
+    return {"max_abs": float(err.max()), "within_2e-3+half_ulp": literal}
+
+
+def check_lse(lse_gpu: np.ndarray, lse_ref: np.ndarray, what: str = "LSE"):
+    err = np.abs(lse_gpu - lse_ref)
+    assert np.isfinite(lse_gpu).all(), f"{what}: non-finite values"
+    assert err.max() <= 2e-3, f"{what}: max err {err.max():.3e}"
+    return float(err.max())
+
+
+def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, what: str):
+    scale = np.abs(g_ref).max()
+    err = np.abs(g_gpu - g_ref).max()
+    assert np.isfinite(g_gpu).all(), f"{what}: non-finite values"
+    assert err <= 1e-2 * scale, f"{what}: max err {err:.3e} vs 1e-2 * max|g| = {1e-2 * scale:.3e}"
+    return float(err / scale)

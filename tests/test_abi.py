@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (CPU only: no call here reaches a CUDA API).
+
+The library must load without a GPU, export every function the headers in
+include/ declare, and reject bad arguments synchronously: every case below
+returns before the library touches the device, so fake pointer values are
+never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_attention_09_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from tiled_attention_09_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(?:fa_status|size_t|const char\s*\*|void|int)\s+(fa_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported_and_bound(L):
+    names = _declared_functions()
+    assert "fa_fwd" in names and "fa_bwd" in names and len(names) >= 10
+    bound = {n for n, _, _ in _lib.SIGNATURES}
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in bound, f"{n} has no ctypes signature"
+
+
+def test_status_strings_and_version(L):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert L.fa_status_string(code).decode() == name
+    assert L.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+    assert L.fa_version() == 100
+
+
+def test_workspace_size(L):
+    B, H, N, d = 2, 3, 256, 128
+    rows = B * H * N
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert L.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4) * 2 + r256(rows * d * 4)
+    assert L.fa_bwd_workspace_size(1, 1, 100, 64) == 0
+    assert L.fa_bwd_workspace_size(1, 1, 256, 96) == 0
+
+
+P = 1 << 20  # a 16-byte aligned fake address; never dereferenced (calls fail before any device work)
+V = ctypes.c_void_p
+
+
+def fwd(L, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=256, d=64, scale=0.125, causal=0, dtype=0):
+    return L.fa_fwd(V(q), V(k), V(v), V(o), V(lse), B, H, N, d, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(lse=0), 1),
+    (dict(N=100), 2), (dict(N=0), 2), (dict(N=64), 2), (dict(d=96), 2), (dict(d=32), 2), (dict(B=0), 2),
+    (dict(H=-1), 2), (dict(B=1 << 16, H=1 << 8, N=1 << 8), 2),
+    (dict(dtype=7), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-1.0), 1),
+    (dict(q=P + 8), 3), (dict(o=P + 2), 3), (dict(lse=P + 4), 3),
+])
+def test_fwd_rejects_bad_arguments(L, kw, code):
+    assert fwd(L, **kw) == code
+
+
+def bwd(L, ws=P, ws_bytes=1 << 40, N=256, d=64, scale=0.125, dq=P, **kw):
+    return L.fa_bwd(V(P), V(P), V(P), V(P), V(P), V(P), V(dq), V(P), V(P), V(ws), ws_bytes, 1, 1, N, d, scale, 0, 0,
+                    None)
+
+
+def test_bwd_rejects_bad_arguments(L):
+    assert bwd(L, ws=0) == 4
+    assert bwd(L, ws_bytes=10) == 4
+    assert bwd(L, ws=P + 16) == 3   # workspace must be 256-byte aligned
+    assert bwd(L, N=200) == 2
+    assert bwd(L, scale=float("nan")) == 1
+    assert bwd(L, dq=0) == 1
+    assert bwd(L, dq=P + 4) == 3
+
+
+def test_selftest_rejects_bad_arguments(L):
+    f = L.fa_selftest_gemm
+    assert f(V(0), V(P), V(P), 128, 64, 0, 0, 0, None) == 1
+    assert f(V(P), V(P), V(P), 96, 64, 0, 0, 0, None) == 2
+    assert f(V(P), V(P), V(P), 128, 64, 3, 0, 0, None) == 1
+    assert f(V(P + 2), V(P), V(P), 128, 64, 0, 0, 0, None) == 3
+
+
+def test_python_layer_requires_cuda_tensors():
+    import torch
+    import tiled_attention_09_gb300 as fa
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd(q, q, q)

@@ -1,0 +1,103 @@
+"""Backward parity of the CUDA path (fa_bwd through the C ABI) against the fp64 oracle (GPU).
+
+Full oracle comparison at sizes the oracle finishes in seconds; at the full
+benchmark sizes, dQ on sampled query rows and dK/dV on sampled key columns
+(the oracle recomputes each one from the definition), plus the gradient-sum
+invariants over every head.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_attention_09_gb300 as fa
+from tiled_attention_09_gb300.inputs import (CAUSAL_4K, CAUSAL_4K_STRESS, LONG_32K, PAGES_SHAPE, SMALL, Workload,
+                                             make_inputs, sample_cols, sample_rows)
+from helpers import check_grad, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd_bwd(w):
+    q, k, v, do = make_inputs(w)
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qc, kc, vc, causal=w.causal)
+    dq, dk, dv = fa.bwd(qc, kc, vc, o, lse, doc, causal=w.causal)
+    torch.cuda.synchronize()
+    code, info = fa.device_status()
+    assert code == "FA_OK", info
+    return (q, k, v, do), (o, lse), (dq, dk, dv)
+
+
+FULL_CASES = [
+    SMALL,
+    Workload(1, 2, 256, 64, "fp16", True),
+    Workload(1, 2, 384, 64, "bf16", True),
+    Workload(1, 3, 384, 128, "bf16", False),
+    Workload(1, 3, 384, 128, "bf16", True),
+    Workload(2, 2, 640, 128, "fp16", True),
+    Workload(1, 2, 512, 64, "bf16", True, stress=8.0),
+    Workload(1, 2, 512, 128, "bf16", True, stress=8.0),
+    PAGES_SHAPE,
+    Workload(2, 12, 1024, 128, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("w", FULL_CASES, ids=lambda w: w.name())
+def test_bwd_full_oracle(w):
+    (q, k, v, do), _, (dq, dk, dv) = run_fwd_bwd(w)
+    ref = oracle.attention_bwd(to64(q), to64(k), to64(v), to64(do), w.scale, w.causal)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        check_grad(to64(g), r, name)
+
+
+@pytest.mark.parametrize("w,heads", [
+    (CAUSAL_4K, [(0, 0), (1, 11)]),
+    (CAUSAL_4K_STRESS, [(0, 3)]),
+    (LONG_32K, [(0, 0), (0, 7)]),
+], ids=lambda x: x.name() if isinstance(x, Workload) else "")
+def test_bwd_sampled(w, heads):
+    (q, k, v, do), (o, lse), (dq, dk, dv) = run_fwd_bwd(w)
+    q64, k64, v64, do64 = to64(q), to64(k), to64(v), to64(do)
+    rows = sample_rows(w.N)
+    _, _, dq_ref = oracle.attention_rows(q64, k64, v64, do64, w.scale, w.causal, rows)
+    check_grad(to64(dq[:, :, rows]), dq_ref, "dQ rows")
+    cols = sample_cols(w.N)
+    dk_ref, dv_ref = oracle.attention_cols(q64, k64, v64, do64, w.scale, w.causal, cols, heads, row_block=2048)
+    dk_g = np.stack([to64(dk[b, h, cols]) for b, h in heads])
+    dv_g = np.stack([to64(dv[b, h, cols]) for b, h in heads])
+    check_grad(dk_g, dk_ref, "dK cols")
+    check_grad(dv_g, dv_ref, "dV cols")
+    # invariants over every head: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i
+    dk_sum = dk.double().sum(dim=2).cpu().numpy()
+    dv_sum = dv.double().sum(dim=2).cpu().numpy()
+    do_sum = do.double().sum(dim=2).numpy()
+    dk_scale = dk.double().abs().amax().item()
+    assert np.abs(dk_sum).max() <= 1e-2 * dk_scale * np.sqrt(w.N), np.abs(dk_sum).max()
+    assert np.abs(dv_sum - do_sum).max() <= 1e-2 * np.abs(do_sum).max() + 1e-2 * np.sqrt(w.N)
+
+
+def test_bwd_repeatable_and_autograd():
+    w = Workload(2, 2, 640, 128, "bf16", True)
+    q, k, v, do = make_inputs(w)
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qc, kc, vc, causal=True)
+    g1 = fa.bwd(qc, kc, vc, o, lse, doc, causal=True)
+    g2 = fa.bwd(qc, kc, vc, o, lse, doc, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])  # dK, dV: fixed summation order
+    assert (g1[0].float() - g2[0].float()).abs().max().item() <= 1e-2 * g1[0].float().abs().max().item()
+    qa, ka, va = (t.clone().requires_grad_(True) for t in (qc, kc, vc))
+    out = fa.attention(qa, ka, va, causal=True)
+    out.backward(doc)
+    assert torch.equal(out, o)
+    assert torch.equal(ka.grad, g1[1]) and torch.equal(va.grad, g1[2])
+
+
+def test_bwd_head_dim_256_is_reported_unsupported():
+    w = Workload(1, 1, 256, 256, "bf16", False)
+    q, k, v, do = (t.cuda() for t in make_inputs(w))
+    o, lse = fa.fwd(q, k, v)
+    with pytest.raises(fa.FAError) as e:
+        fa.bwd(q, k, v, o, lse, do)
+    assert e.value.code == 2

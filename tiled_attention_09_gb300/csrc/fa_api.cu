@@ -1,0 +1,254 @@
+// C ABI of libfa.so: argument checks, TMA tensor maps, dispatch, status words.
+// Declarations and the contract of every entry point are in include/fa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "launch.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+unsigned long long g_timeout_ns = 4000000000ull;
+
+// 2-D map over a [rows, d] row-major 16-bit tensor; box = {64 elements, box_rows}; 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, long long rows, int d, bool bf16, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype) {
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 128 || (N % 128) != 0) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * N >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status check_scale(float scale) {
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t off_D, off_lse2, off_dq, total;
+};
+WsLayout ws_layout(int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  WsLayout w;
+  w.off_D = 0;
+  w.off_lse2 = align256(rows * 4);
+  w.off_dq = w.off_lse2 + align256(rows * 4);
+  w.total = w.off_dq + align256(rows * static_cast<size_t>(d) * 4);
+  return w;
+}
+
+fa_status bwd_common(fa::BwdArgs* a, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                     float scale, int causal, fa_dtype dtype, void* stream) {
+  fa_status s = check_shape(B, H, N, d, dtype);
+  if (s != FA_OK) return s;
+  if ((s = check_scale(scale)) != FA_OK) return s;
+  if (!workspace) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
+  WsLayout w = ws_layout(B, H, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  a->ws_D = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_D);
+  a->ws_lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse2);
+  a->ws_dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_dq);
+  a->B = B;
+  a->H = H;
+  a->N = N;
+  a->d = d;
+  a->scale = scale;
+  a->causal = causal != 0;
+  a->bf16 = dtype == FA_BF16;
+  a->timeout_ns = g_timeout_ns;
+  a->stream = static_cast<cudaStream_t>(stream);
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+void fa_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns ? ns : 4000000000ull; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_DEVICE_FAULT: return "FA_ERR_DEVICE_FAULT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status s = check_shape(B, H, N, d, dtype);
+  if (s != FA_OK) return s;
+  if ((s = check_scale(scale)) != FA_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  fa::FwdArgs a;
+  const long long rows = static_cast<long long>(B) * H * N;
+  const bool bf16 = dtype == FA_BF16;
+  if (!make_map(&a.tm_q, q, rows, d, bf16, 128) || !make_map(&a.tm_k, k, rows, d, bf16, 128) ||
+      !make_map(&a.tm_v, v, rows, d, bf16, 128) || !make_map(&a.tm_o, o, rows, d, bf16, 128))
+    return FA_ERR_CUDA;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal != 0;
+  a.bf16 = bf16;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return fa::launch_fwd(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
+  return ws_layout(B, H, N, d).total;
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
+                            size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream) {
+  if (!o || !dO || !lse) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{};
+  fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, 1.0f, 0, dtype, stream);
+  if (s != FA_OK) return s;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  return fa::launch_bwd_preprocess(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                      void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                      fa_dtype dtype, void* stream) {
+  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{};
+  fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
+  if (s != FA_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  const int bq = fa::bwd_query_tile(d);
+  if (bq == 0) return FA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (!make_map(&a.tm_q, q, rows, d, a.bf16, bq) || !make_map(&a.tm_do, dO, rows, d, a.bf16, bq) ||
+      !make_map(&a.tm_k, k, rows, d, a.bf16, 128) || !make_map(&a.tm_v, v, rows, d, a.bf16, 128) ||
+      !make_map(&a.tm_dk, dk, rows, d, a.bf16, 128) || !make_map(&a.tm_dv, dv, rows, d, a.bf16, 128))
+    return FA_ERR_CUDA;
+  a.dO = dO;
+  a.dk = dk;
+  a.dv = dv;
+  return fa::launch_bwd_main(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                            float scale, fa_dtype dtype, void* stream) {
+  if (!dq) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{};
+  fa_status s = bwd_common(&a, const_cast<void*>(workspace), workspace_bytes, B, H, N, d, scale, 0, dtype, stream);
+  if (s != FA_OK) return s;
+  if (!aligned16(dq)) return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  a.dq = dq;
+  return fa::launch_bwd_dq_convert(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  // Validate everything before enqueuing anything.
+  fa::BwdArgs probe{};
+  fa_status s = bwd_common(&probe, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
+  if (s != FA_OK) return s;
+  if (fa::bwd_query_tile(d) == 0) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  if ((s = fa_bwd_preprocess(o, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK) return s;
+  if ((s = fa_bwd_main(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream)) !=
+      FA_OK)
+    return s;
+  return fa_bwd_dq_convert(dq, workspace, workspace_bytes, B, H, N, d, scale, dtype, stream);
+}
+
+fa_status fa_device_status(void* stream, unsigned int info[4]) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  fa::DevStatusHost a{}, b{};
+  if (fa::read_clear_status_fwd(&a, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::read_clear_status_bwd(&b, st) != cudaSuccess) return FA_ERR_CUDA;
+  const fa::DevStatusHost& first = a.code ? a : b;
+  if (info) {
+    info[0] = first.code;
+    info[1] = first.where;
+    info[2] = first.block;
+    info[3] = a.count + b.count;
+  }
+  if (first.code == 1u) return FA_ERR_TIMEOUT;
+  if (first.code != 0u) return FA_ERR_DEVICE_FAULT;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Attention backward for sm_103a: preprocess (K2), main kernel (K3), dQ convert (K4).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "fa_bwd_aux.cuh"
+#include "fa_bwd_main.cuh"
+#include "launch.h"
+
+namespace fa {
+namespace {
+
+int grid_for(size_t n_vec) {
+  size_t blocks = (n_vec + 255) / 256;
+  const size_t cap = 152 * 16;
+  return static_cast<int>(blocks < cap ? blocks : cap);
+}
+
+template <int VPR>
+cudaError_t launch_pre_t(const BwdArgs& a, size_t n_vec) {
+  if (a.bf16)
+    fa_bwd_preprocess_kernel<VPR, true><<<grid_for(n_vec), 256, 0, a.stream>>>(
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
+        reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
+  else
+    fa_bwd_preprocess_kernel<VPR, false><<<grid_for(n_vec), 256, 0, a.stream>>>(
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
+        reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const BwdArgs& a) {
+  const size_t n_vec = static_cast<size_t>(a.B) * a.H * a.N * (a.d / 8);
+  switch (a.d) {
+    case 64: return launch_pre_t<8>(a, n_vec);
+    case 128: return launch_pre_t<16>(a, n_vec);
+    case 256: return launch_pre_t<32>(a, n_vec);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dq_convert(const BwdArgs& a) {
+  const size_t n_vec = static_cast<size_t>(a.B) * a.H * a.N * (a.d / 8);
+  if (a.bf16)
+    fa_bwd_dq_convert_kernel<true><<<grid_for(n_vec), 256, 0, a.stream>>>(
+        reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, n_vec);
+  else
+    fa_bwd_dq_convert_kernel<false><<<grid_for(n_vec), 256, 0, a.stream>>>(
+        reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, n_vec);
+  return cudaGetLastError();
+}
+
+namespace {
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_main_t(const BwdArgs& a) {
+  using C = BwdCfg<D>;
+  auto kern = fa_bwd_main_kernel<D, BF16, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  BwdParams p;
+  p.tm_q = a.tm_q;
+  p.tm_k = a.tm_k;
+  p.tm_v = a.tm_v;
+  p.tm_do = a.tm_do;
+  p.tm_dk = a.tm_dk;
+  p.tm_dv = a.tm_dv;
+  p.lse2 = a.ws_lse2;
+  p.Dvec = a.ws_D;
+  p.dqacc = a.ws_dqacc;
+  p.N = a.N;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.timeout_ns = a.timeout_ns;
+  dim3 grid(a.B * a.H, a.N / 128, 1);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(p);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_bwd_main(const BwdArgs& a) {
+#define FA_BWD_CASE(D_)                                                                                   \
+  if (a.d == D_) {                                                                                        \
+    if (a.bf16) return a.causal ? launch_main_t<D_, true, true>(a) : launch_main_t<D_, true, false>(a);   \
+    return a.causal ? launch_main_t<D_, false, true>(a) : launch_main_t<D_, false, false>(a);             \
+  }
+  FA_BWD_CASE(64)
+  FA_BWD_CASE(128)
+#undef FA_BWD_CASE
+  return cudaErrorNotSupported;
+}
+
+cudaError_t read_clear_status_bwd(DevStatusHost* out, cudaStream_t s) {
+  DevStatus zero{0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(DevStatus), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (out->code != 0 || out->count != 0)
+    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(DevStatus), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
+}  // namespace fa

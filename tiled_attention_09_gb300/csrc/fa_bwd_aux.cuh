@@ -1,0 +1,88 @@
+// Bandwidth-bound helper kernels of the backward pass (no tensor cores):
+//   K2 preprocess: D_i = sum_k dO_ik * O_ik (fp32), LSE_i * log2(e), dQ accumulator := 0
+//   K4 dQ convert: dQ = dtype(scale * dQacc)
+// Each thread owns one 16-byte vector (8 elements) of a row; the d/8 threads of
+// a row sit in one warp and reduce with shuffles. Grid-stride loops keep the
+// grid at a few waves of the 152 SMs.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+namespace fa {
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF16) {
+      __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+      float2 t = __bfloat1622float2(h);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    } else {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 t = __half22float2(h);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2f(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// VPR = vectors (of 8 elements) per row = d / 8, a power of two <= 32.
+template <int VPR, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __restrict__ o,
+                                                                 const uint4* __restrict__ dO,
+                                                                 const float* __restrict__ lse, float* __restrict__ D,
+                                                                 float* __restrict__ lse2, float4* __restrict__ dqacc,
+                                                                 size_t n_vec) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
+    float a[8], b[8];
+    unpack8<BF16>(__ldg(&o[i]), a);
+    unpack8<BF16>(__ldg(&dO[i]), b);
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc = fmaf(a[k], b[k], acc);
+#pragma unroll
+    for (int off = VPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, VPR);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    dqacc[2 * i] = z;
+    dqacc[2 * i + 1] = z;
+    if ((i % VPR) == 0) {
+      const size_t row = i / VPR;
+      D[row] = acc;
+      lse2[row] = lse[row] * 1.4426950408889634f;
+    }
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __restrict__ dqacc,
+                                                                uint4* __restrict__ dq, float scale, size_t n_vec) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
+    const float4 x = dqacc[2 * i], y = dqacc[2 * i + 1];
+    uint4 v;
+    v.x = pack2f<BF16>(x.x * scale, x.y * scale);
+    v.y = pack2f<BF16>(x.z * scale, x.w * scale);
+    v.z = pack2f<BF16>(y.x * scale, y.y * scale);
+    v.w = pack2f<BF16>(y.z * scale, y.w * scale);
+    dq[i] = v;
+  }
+}
+
+}  // namespace fa

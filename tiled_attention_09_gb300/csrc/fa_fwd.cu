@@ -1,0 +1,411 @@
+// Fused attention forward for sm_103a (K1).
+//
+// Method (page "transformer模型详解（十）：FlashAttention优化技术"): one kernel keeps
+// every intermediate on chip ("Kernel Fusion"), walks the scores in B_q x B_k
+// tiles ("Tiling 分块策略") and runs the online softmax of that section: per
+// tile the local row max and exponential sum, an update of the running max
+// with a rescale of the running sum and of the output accumulator, and one
+// normalisation at the end. Only O and the per-row log-sum-exp go to HBM.
+//
+// GB300 design. One CTA owns NT query tiles of 128 rows of one (b, h) head
+// (NT = 2 for d <= 128, 1 for d = 256) and streams the head's K/V tiles of 128
+// keys through a ring of shared-memory slots filled by TMA. Roles:
+//   warps 0..4NT-1  softmax: one warpgroup per query tile; thread r owns row r
+//                   of S, P and O in tensor memory (TMEM lane r), so row max
+//                   and row sum need no shuffles.
+//   warp 4NT        producer: TMA loads of Q (once) and K_j, V_j (ring order
+//                   K0 V0 K1 V1 ...).
+//   warp 4NT+1      MMA issuer: tcgen05.mma S_t = Q_t K_j^T (both operands in
+//                   smem) and O_t += P_t V_j (P from TMEM, V from smem), with
+//                   tcgen05.commit arrivals on mbarriers.
+// TMEM columns: S_t at 128t (fp32 128x128; P_t as 16-bit pairs over its first
+// 64 columns), O_t at 256 + d*t (fp32 128 x d).
+// Issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j); the commit
+// that announces S_t(j) also covers PV_t(j-1), so when the softmax sees S_t(j)
+// the accumulator O_t is quiescent and can be rescaled in place.
+// Rescaling is lazy: the running max used for the exponentials only moves when
+// the row max grows by more than 2^8; the final O / l and LSE use that same
+// max, so the result is exact up to rounding.
+// Causal: tiles above the diagonal are never loaded or computed; the
+// diagonal tile masks keys > query inside the softmax.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace fa {
+namespace {
+
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  float* lse;
+  int N;
+  int n_qblk;
+  float scale_log2;
+  float rescale_threshold;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NT = (D <= 128) ? 2 : 1;                   // query tiles per CTA
+  static constexpr int CHUNK = 128 * 128;                         // 128 rows x 64 elems x 2 B
+  static constexpr int NCHUNK = D / 64;
+  static constexpr int TILE = 128 * D * 2;                        // one 128-row tile
+  static constexpr int NS = (D == 64) ? 6 : (D == 128 ? 4 : 2);   // ring slots
+  static constexpr int SMEM_Q = NT * TILE;
+  static constexpr int SMEM_RING = NS * TILE;
+  static constexpr int NBAR = 1 + 2 * NS + 3 * NT + 1;
+  static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NBAR * 8 + 16;
+  static constexpr int THREADS = 128 * NT + 64;
+  static constexpr uint32_t TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + D * t; }
+  static_assert(O_COL(NT - 1) + D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// where-codes for timeouts
+enum : uint32_t { W_Q = 1, W_RING_EMPTY = 2, W_RING_FULL = 3, W_P = 4, W_S = 5, W_O = 6, W_DRAIN = 7 };
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int NT = C::NT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sRing = sQ + C::SMEM_Q;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_Q + C::SMEM_RING);
+  const uint32_t b_q = smem_u32(&bars[0]);
+  auto b_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto b_empty = [&](int s) { return smem_u32(&bars[1 + C::NS + s]); };
+  auto b_s = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + t]); };
+  auto b_p = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + NT + t]); };
+  auto b_o = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + 2 * NT + t]); };
+  const uint32_t b_drain = smem_u32(&bars[1 + 2 * C::NS + 3 * NT]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[C::NBAR]);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int N = p.N;
+  const int bh = blockIdx.x;
+  const int qb = CAUSAL ? (p.n_qblk - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+  const int q_row0 = qb * 128 * NT;  // first query row of this CTA within the head
+  const int row_base = bh * N;       // row of (b, h, 0) in the [B*H*N, d] view
+  int n_valid = (N - q_row0) / 128;
+  if (n_valid > NT) n_valid = NT;
+  int n_t[NT];
+  int nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    n_t[t] = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : (N / 128)) : 0;
+    nmax = n_t[t] > nmax ? n_t[t] : nmax;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(b_full(s), 1);
+      mbar_init(b_empty(s), 1);
+    }
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(b_s(t), 1);
+      mbar_init(b_p(t), 128);
+      mbar_init(b_o(t), 1);
+    }
+    mbar_init(b_drain, 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 4 * NT + 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4 * NT) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(b_q, n_valid * C::TILE);
+      for (int t = 0; t < n_valid; ++t)
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_2d(sQ + t * C::TILE + c * C::CHUNK, &p.tm_q, b_q, c * 64, row_base + q_row0 + t * 128);
+      int issued = 0;
+      for (int s = 0; s < 2 * nmax; ++s) {
+        const int slot = s % C::NS, use = s / C::NS;
+        if (use > 0 && !wait_bar(b_empty(slot), (use - 1) & 1, p.timeout_ns, abort_flag, W_RING_EMPTY)) break;
+        mbar_arrive_expect_tx(b_full(slot), C::TILE);
+        const void* map = (s & 1) ? static_cast<const void*>(&p.tm_v) : static_cast<const void*>(&p.tm_k);
+        const int krow = row_base + (s >> 1) * 128;
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_2d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow);
+        ++issued;
+      }
+      // Drain: every issued load must have landed before the CTA may exit.
+      for (int s = (issued > C::NS ? issued - C::NS : 0); s < issued; ++s)
+        wait_bar(b_full(s % C::NS), (s / C::NS) & 1, p.timeout_ns, abort_flag, W_DRAIN);
+      if (n_valid > 0) wait_bar(b_q, 0, p.timeout_ns, abort_flag, W_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == 4 * NT + 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
+      constexpr uint32_t idesc_pv = make_idesc(128, D, BF16, false, true);
+      bool ok = (n_valid == 0) || wait_bar(b_q, 0, p.timeout_ns, abort_flag, W_Q);
+      for (int j = 0; ok && j <= nmax; ++j) {
+        const int sK = 2 * j, sV = 2 * j - 1;
+        if (j > 0 && !wait_bar(b_full(sV % C::NS), (sV / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL)) break;
+        if (j < nmax && !wait_bar(b_full(sK % C::NS), (sK / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (j >= 1 && j <= n_t[t]) {
+            if (!wait_bar(b_p(t), (j - 1) & 1, p.timeout_ns, abort_flag, W_P)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vaddr = sRing + (sV % C::NS) * C::TILE;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, make_sdesc(vaddr + k * 2048, C::CHUNK, 1024),
+                     idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+            if (j == n_t[t]) mma_commit(b_o(t));
+          }
+          if (j < n_t[t]) {
+            const uint32_t kaddr = sRing + (sK % C::NS) * C::TILE;
+            const uint32_t qaddr = sQ + t * C::TILE;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
+              mma_ss(tmem + C::S_COL(t), make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024),
+                     idesc_s, k > 0 ? 1u : 0u);
+            }
+            mma_commit(b_s(t));
+          }
+        }
+        if (!ok) break;
+        if (j < nmax) mma_commit(b_empty(sK % C::NS));
+        if (j > 0) mma_commit(b_empty(sV % C::NS));
+      }
+      // Drain: all issued MMAs complete before teardown.
+      mma_commit(b_drain);
+      wait_bar(b_drain, 0, p.timeout_ns, abort_flag, W_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int r = threadIdx.x & 127;  // row within the query tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::S_COL(t);
+    const uint32_t tO = tmem + lane_off + C::O_COL(t);
+    const float sl2 = p.scale_log2;
+    const int my_n = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : (N / 128)) : 0;
+    float m_used = 0.f, l = 0.f;
+    bool ok = my_n > 0;
+    for (int j = 0; ok && j < my_n; ++j) {
+      // warp-uniform outcome: tcgen05.ld/st below are warp-collective
+      if (!__all_sync(0xffffffffu, wait_bar(b_s(t), j & 1, p.timeout_ns, abort_flag, W_S))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tS + 32 * c, u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(u[i]);
+      }
+      const bool diag = CAUSAL && (j == my_n - 1);
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, c + 0 > r ? -INFINITY : s[c + 0]);
+          mx1 = fmaxf(mx1, c + 1 > r ? -INFINITY : s[c + 1]);
+          mx2 = fmaxf(mx2, c + 2 > r ? -INFINITY : s[c + 2]);
+          mx3 = fmaxf(mx3, c + 3 > r ? -INFINITY : s[c + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, s[c + 0]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+      }
+      const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {
+        m_used = m_new;
+      } else if (m_new > m_used + p.rescale_threshold) {
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+        l *= alpha;
+        rescale = true;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tO + 32 * c, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(tO + 32 * c, u);
+        }
+      }
+      const float neg_m = -m_used;
+      float ls0 = 0.f, ls1 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
+        float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
+        if (diag) {
+          p0 = (c > r) ? 0.f : p0;
+          p1 = (c + 1 > r) ? 0.f : p1;
+        }
+        ls0 += p0;
+        ls1 += p1;
+        pk[c >> 1] = pack2<BF16>(p0, p1);
+      }
+      l += ls0 + ls1;
+      {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+        tmem_st32(tS, lo);
+        tmem_st32(tS + 32, hi);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(b_p(t));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_o(t), 0, p.timeout_ns, abort_flag, W_O));
+    uint8_t* stage = smem + t * C::TILE;  // Q_t is dead once O_t is final
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tO + 32 * c, u);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int col = 32 * c + 8 * g;  // first of 8 columns = one 16-byte unit
+          uint4 v;
+          v.x = pack2<BF16>(__uint_as_float(u[8 * g + 0]) * inv_l, __uint_as_float(u[8 * g + 1]) * inv_l);
+          v.y = pack2<BF16>(__uint_as_float(u[8 * g + 2]) * inv_l, __uint_as_float(u[8 * g + 3]) * inv_l);
+          v.z = pack2<BF16>(__uint_as_float(u[8 * g + 4]) * inv_l, __uint_as_float(u[8 * g + 5]) * inv_l);
+          v.w = pack2<BF16>(__uint_as_float(u[8 * g + 6]) * inv_l, __uint_as_float(u[8 * g + 7]) * inv_l);
+          const int chunk = col >> 6, unit = (col & 63) >> 3;
+          *reinterpret_cast<uint4*>(stage + chunk * C::CHUNK + r * 128 + ((unit ^ (r & 7)) << 4)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      // LSE in natural log: (m_used + log2 l) * ln 2
+      p.lse[static_cast<size_t>(row_base) + q_row0 + t * 128 + r] = (m_used + log2f(l)) * 0.69314718055994531f;
+    }
+    if (my_n > 0) {
+      // Every warp of the warpgroup reaches this barrier exactly once (all waits are bounded).
+      named_bar_sync(1 + t, 128);
+      if (r == 0 && ok && *abort_flag == 0u) {
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_store_2d(&p.tm_o, smem_u32(stage) + c * C::CHUNK, c * 64, row_base + q_row0 + t * 128);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4 * NT + 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdArgs& a) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+  static bool attr_set = false;  // per instantiation; attribute is per-device but identical everywhere
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  (void)attr_set;
+  FwdParams p;
+  p.tm_q = a.tm_q;
+  p.tm_k = a.tm_k;
+  p.tm_v = a.tm_v;
+  p.tm_o = a.tm_o;
+  p.lse = a.lse;
+  p.N = a.N;
+  p.n_qblk = (a.N + 128 * C::NT - 1) / (128 * C::NT);
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.rescale_threshold = 8.0f;
+  p.timeout_ns = a.timeout_ns;
+  dim3 grid(a.B * a.H, p.n_qblk, 1);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a) {
+#define FA_FWD_CASE(D_)                                                                    \
+  if (a.d == D_) {                                                                         \
+    if (a.bf16) return a.causal ? launch_fwd_t<D_, true, true>(a) : launch_fwd_t<D_, true, false>(a); \
+    return a.causal ? launch_fwd_t<D_, false, true>(a) : launch_fwd_t<D_, false, false>(a);          \
+  }
+  FA_FWD_CASE(64)
+  FA_FWD_CASE(128)
+  FA_FWD_CASE(256)
+#undef FA_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_clear_status_fwd(DevStatusHost* out, cudaStream_t s) {
+  DevStatus zero{0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(DevStatus), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (out->code != 0 || out->count != 0)
+    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(DevStatus), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
+}  // namespace fa

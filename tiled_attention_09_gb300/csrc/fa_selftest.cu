@@ -1,0 +1,192 @@
+// Descriptor self-test: one CTA computes D[128 x n] = A[128 x k] * B[n x k]^T with
+// tcgen05.mma, using exactly the operand forms the attention kernels use
+// (K-major and MN-major operands in 128-byte-swizzled shared memory filled by
+// TMA, and an A operand held in tensor memory). Tests compare it with a CPU
+// matrix product, which checks the hand-encoded shared-memory descriptors, the
+// instruction descriptor, the TMEM data-path layout and the 16-bit packing of
+// TMEM operands independently of any attention arithmetic.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fa.h"
+#include "../../include/fa_selftest.h"
+#include "common.cuh"
+
+namespace fa {
+namespace {
+
+struct STParams {
+  CUtensorMap tm_a, tm_b;
+  const uint32_t* a_glob;  // for a_mode 2: a[128][k] as 16-bit pairs
+  float* d;
+  int n, k, a_mode, b_mode;
+  unsigned long long timeout_ns;
+};
+
+constexpr int ST_SMEM = 1024 + 32768 + 65536 + 64;
+
+template <bool BF16>
+__global__ void __launch_bounds__(128, 1) fa_selftest_kernel(const __grid_constant__ STParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA = smem_u32(smem);
+  const uint32_t sB = sA + 32768;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 32768 + 65536);
+  const uint32_t b_ld = smem_u32(&bars[0]), b_mma = smem_u32(&bars[1]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[2]);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = p.n, k = p.k;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_ld, 1);
+    mbar_init(b_mma, 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+
+  if (threadIdx.x == 0) {
+    uint32_t bytes = static_cast<uint32_t>(n * k * 2);
+    if (p.a_mode < 2) bytes += 128u * k * 2;
+    mbar_arrive_expect_tx(b_ld, bytes);
+    if (p.a_mode == 0)
+      for (int c = 0; c < k / 64; ++c) tma_load_2d(sA + c * 16384, &p.tm_a, b_ld, c * 64, 0);
+    else if (p.a_mode == 1)
+      for (int c = 0; c < 2; ++c) tma_load_2d(sA + c * (k * 128), &p.tm_a, b_ld, c * 64, 0);
+    if (p.b_mode == 0)
+      for (int c = 0; c < k / 64; ++c) tma_load_2d(sB + c * (n * 128), &p.tm_b, b_ld, c * 64, 0);
+    else
+      for (int c = 0; c < n / 64; ++c) tma_load_2d(sB + c * (k * 128), &p.tm_b, b_ld, c * 64, 0);
+  }
+  if (p.a_mode == 2) {
+    // row threadIdx.x of A -> TMEM lane threadIdx.x, columns 256 .. 256 + k/2 (two 16-bit values per column)
+    const uint32_t* row = p.a_glob + static_cast<size_t>(threadIdx.x) * (k / 2);
+    for (int c = 0; c < k / 64; ++c) {
+      uint32_t u[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) u[i] = row[32 * c + i];
+      tmem_st32(tmem + lane_off + 256 + 32 * c, u);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (threadIdx.x == 0) {
+    if (wait_bar(b_ld, 0, p.timeout_ns, abort_flag, 1)) {
+      tc_fence_after();
+      const uint32_t idesc = make_idesc(128, n, BF16, p.a_mode == 1, p.b_mode == 1);
+      for (int kk = 0; kk < k / 16; ++kk) {
+        const uint64_t bdesc = (p.b_mode == 0)
+                                   ? make_sdesc(sB + (kk >> 2) * (n * 128) + (kk & 3) * 32, 16, 1024)
+                                   : make_sdesc(sB + kk * 2048, k * 128, 1024);
+        if (p.a_mode == 2) {
+          mma_ts(tmem, tmem + 256 + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+        } else {
+          const uint64_t adesc = (p.a_mode == 0) ? make_sdesc(sA + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024)
+                                                 : make_sdesc(sA + kk * 2048, k * 128, 1024);
+          mma_ss(tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+        }
+      }
+    }
+    mma_commit(b_mma);
+  }
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, wait_bar(b_mma, 0, p.timeout_ns, abort_flag, 2));
+  if (ok) {
+    tc_fence_after();
+    for (int c = 0; c < n / 32; ++c) {
+      uint32_t u[32];
+      tmem_ld32(tmem + lane_off + 32 * c, u);
+      float* out = p.d + static_cast<size_t>(warp * 32 + lane) * n + 32 * c;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(u[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool st_map(CUtensorMap* m, const void* base, int rows, int cols, bool bf16, int box_rows) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  return reinterpret_cast<EncodeTiledFn>(fn)(
+             m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_selftest_gemm(const void* a, const void* b, float* d, int n, int k, int a_mode, int b_mode,
+                                      fa_dtype dtype, void* stream) {
+  using namespace fa;
+  if (!a || !b || !d) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (!(n == 64 || n == 128 || n == 256) || !(k == 64 || k == 128)) return FA_ERR_UNSUPPORTED;
+  if (a_mode < 0 || a_mode > 2 || b_mode < 0 || b_mode > 1) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(d)) & 15u)
+    return FA_ERR_ALIGNMENT;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  const bool bf16 = dtype == FA_BF16;
+  STParams p{};
+  // A: mode 0 -> [128][k] (box 128 rows); mode 1 -> [k][128] (box k rows); mode 2 -> read by threads
+  if (a_mode == 0 && !st_map(&p.tm_a, a, 128, k, bf16, 128)) return FA_ERR_CUDA;
+  if (a_mode == 1 && !st_map(&p.tm_a, a, k, 128, bf16, k)) return FA_ERR_CUDA;
+  if (a_mode == 2) p.tm_a = CUtensorMap{};
+  if (b_mode == 0 && !st_map(&p.tm_b, b, n, k, bf16, n)) return FA_ERR_CUDA;
+  if (b_mode == 1 && !st_map(&p.tm_b, b, k, n, bf16, k)) return FA_ERR_CUDA;
+  p.a_glob = static_cast<const uint32_t*>(a);
+  p.d = d;
+  p.n = n;
+  p.k = k;
+  p.a_mode = a_mode;
+  p.b_mode = b_mode;
+  p.timeout_ns = 2000000000ull;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (bf16) {
+    if (cudaFuncSetAttribute(fa_selftest_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ST_SMEM) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    fa_selftest_kernel<true><<<1, 128, ST_SMEM, s>>>(p);
+  } else {
+    if (cudaFuncSetAttribute(fa_selftest_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ST_SMEM) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    fa_selftest_kernel<false><<<1, 128, ST_SMEM, s>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

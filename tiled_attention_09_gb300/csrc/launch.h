@@ -1,0 +1,56 @@
+// Host-side interface between the C ABI (fa_api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fa {
+
+struct DevStatusHost {
+  uint32_t code, where, block, count;
+};
+
+// 2-D tensor maps over the [rows, d] view of a [B,H,N,d] tensor (rows = B*H*N),
+// box {64 elements, box_rows rows}, 128-byte swizzle.
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // box rows 128
+  float* lse;
+  int B, H, N, d;
+  float scale;
+  bool causal, bf16;
+  uint64_t timeout_ns;
+  cudaStream_t stream;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // q, dO: box rows = query tile; k, v: box rows 128
+  CUtensorMap tm_dk, tm_dv;             // box rows 128
+  const void* o;
+  const void* dO;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* ws_D;      // [B*H*N]
+  float* ws_lse2;   // [B*H*N]  lse * log2(e)
+  float* ws_dqacc;  // [B*H*N*d]
+  int B, H, N, d;
+  float scale;
+  bool causal, bf16;
+  uint64_t timeout_ns;
+  cudaStream_t stream;
+};
+
+// Query-tile height of the backward main kernel for head dimension d (0 = unsupported).
+inline int bwd_query_tile(int d) { return d == 64 ? 128 : (d == 128 ? 64 : 0); }
+
+cudaError_t launch_fwd(const FwdArgs& a);
+cudaError_t launch_bwd_preprocess(const BwdArgs& a);
+cudaError_t launch_bwd_main(const BwdArgs& a);
+cudaError_t launch_bwd_dq_convert(const BwdArgs& a);
+
+cudaError_t read_clear_status_fwd(DevStatusHost* out, cudaStream_t s);
+cudaError_t read_clear_status_bwd(DevStatusHost* out, cudaStream_t s);
+
+}  // namespace fa
