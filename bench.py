@@ -1,0 +1,419 @@
+"""Benchmark: attention fwd+bwd TFLOP/s (bf16, causal) on GB300 through the libfa.so C ABI.
+
+One step = the whole hot path over one batch of synthetic input: fa_fwd_ex (the
+forward, also writing the rounding residual of O that the backward's D uses),
+then fa_bwd's three phases (preprocess, main, dQ convert), on the workload
+B=2, H=12, N=4096, d=128, bf16, causal (Q, K, V, dO iid N(0,1), seed 0).
+FLOPs follow the metric's own count: forward 4*B*H*N^2*d halved when causal,
+backward 2.5x that; value = 3.5*F_fwd / (t_fwd + t_bwd).
+
+Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
+barrier and torch.cuda.synchronize(); the L2 cache is flushed (a 256 MiB write)
+before each step, outside the CUDA-event-timed interval of that step. The max
+over ranks is reported; under torchrun every rank runs the same workload on its
+own GPU (weak scaling, no data-path collective).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "attention fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense tensor peak"
+KERNEL_SOURCES = ["tiled_attention_09_gb300/csrc/fa_bwd_main.cuh", "tiled_attention_09_gb300/csrc/fa_fwd.cu",
+                  "tiled_attention_09_gb300/csrc/ptx.cuh", "tiled_attention_09_gb300/csrc/common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle's timed sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[5:9]):
+                if flag.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def _visible(w, r0, r1):
+    """Number of (query, key) pairs the metric counts for query rows [r0, r1) of one head."""
+    if w.causal:
+        return (r1 * (r1 + 1) - r0 * (r0 + 1)) // 2
+    return (r1 - r0) * w.N
+
+
+class OracleSampler:
+    """Times the fp64 oracle, as it stands, on row blocks of the workload (fwd + bwd of those rows).
+
+    A row block of one (b, h) head is the definition restricted to query rows
+    [r0, r1): O, LSE and dQ of those rows and their shares of dK and dV. Its
+    useful FLOPs are 3.5 * 4 * d * (visible (query, key) pairs), the metric's
+    own count restricted to the block.
+    """
+
+    def __init__(self, w):
+        from tiled_attention_09_gb300.inputs import make_inputs
+        self.w = w
+        self.q, self.k, self.v, self.do = make_inputs(w)
+        self.cursor = 0  # (head, row) position, walks the workload in order
+
+    def run(self, rows):
+        import oracle
+        w = self.w
+        head, r0 = divmod(self.cursor, w.N)
+        head %= w.B * w.H
+        r1 = min(w.N, r0 + rows)
+        b, h = divmod(head, w.H)
+        sl = lambda t: t[b:b + 1, h:h + 1].double().numpy()
+        q, k, v, do = sl(self.q), sl(self.k), sl(self.v), sl(self.do)
+        t0 = time.perf_counter()
+        oracle.attention_row_block(q, k, v, do, w.scale, w.causal, 0, 0, r0, r1)
+        dt = time.perf_counter() - t0
+        self.cursor = head * w.N + r1 if r1 < w.N else (head + 1) * w.N
+        return 3.5 * 4 * w.d * _visible(w, r0, r1), dt, (b, h, r0, r1)
+
+
+def oracle_baseline(w, budget_s=12.0, block=512):
+    """cpu_baseline: the oracle on consecutive row blocks until about budget_s of CPU work."""
+    smp = OracleSampler(w)
+    smp.run(64)  # page in, start BLAS threads
+    smp.cursor = 0
+    flops = secs = 0.0
+    blocks = []
+    while secs < budget_s:
+        f, dt, where = smp.run(block)
+        flops += f
+        secs += dt
+        blocks.append(where)
+    first, last = blocks[0], blocks[-1]
+    sample = (f"{len(blocks)} row blocks of {block} query rows, (b,h,rows) {first[:2]}:{first[2]} .. "
+              f"{last[:2]}:{last[3]} of {w.name()}, fwd+bwd of those rows, {secs:.1f} s")
+    return flops / secs / 1e12, sample
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle on a bounded sample of the same workload per step."""
+    from tiled_attention_09_gb300.inputs import CAUSAL_4K
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    w = CAUSAL_4K
+    smp = OracleSampler(w)
+    smp.run(64)
+    # size the per-step sample so warm-up + timed steps stay within ~2.5 minutes
+    f, dt, _ = smp.run(256)
+    per_step = min(3.0, 150.0 / (args.steps + args.warmup))
+    rows = int(max(64, min(w.N, 256 * per_step / max(dt, 1e-3))) // 64 * 64)
+    smp.cursor = 0
+    for _ in range(args.warmup):
+        smp.run(rows)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, dt, _ = smp.run(rows)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    cores = cpu_cores()
+    sample = f"{rows} query rows of one (b,h) head of {w.name()} per step (fwd+bwd of those rows), fp64 numpy oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name(), "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True,
+                   "sample": f"{rows} query rows per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    import torch
+    import tiled_attention_09_gb300 as fa
+    from tiled_attention_09_gb300 import _lib
+    from tiled_attention_09_gb300.inputs import CAUSAL_4K, make_inputs
+
+    world, rank, local, dist = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = CAUSAL_4K
+    B, H, N, d = w.B, w.H, w.N, w.d
+    F = w.fwd_flops()
+    step_flops = 3.5 * F
+
+    # CPU baseline first (rank 0, N=1 only), before the GPU work starts
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, sample = oracle_baseline(w, budget_s=args.cpu_seconds)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample}
+
+    L = _lib.load()
+    q, k, v, do = make_inputs(w)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_bytes = int(L.fa_bwd_workspace_size(B, H, N, d))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    scale = w.scale
+    DT = _lib.FA_BF16
+
+    def launch(ptrs, evs=None):
+        qp, kp, vp, op, lp, dop, dqp, dkp, dvp, lop = ptrs
+        if evs:
+            evs[0].record(stream)
+        _lib.check("fa_fwd_ex", L.fa_fwd_ex(qp, kp, vp, op, lp, lop, B, H, N, d, scale, 1, DT, sp))
+        if evs:
+            evs[1].record(stream)
+        _lib.check("pre", L.fa_bwd_preprocess(op, lop, dop, lp, ws.data_ptr(), ws_bytes, B, H, N, d, DT, sp))
+        if evs:
+            evs[2].record(stream)
+        _lib.check("main", L.fa_bwd_main(qp, kp, vp, dop, dkp, dvp, ws.data_ptr(), ws_bytes, B, H, N, d, scale, 1,
+                                         DT, sp))
+        if evs:
+            evs[3].record(stream)
+        _lib.check("conv", L.fa_bwd_dq_convert(dqp, ws.data_ptr(), ws_bytes, B, H, N, d, scale, DT, sp))
+        if evs:
+            evs[4].record(stream)
+
+    o_lo = torch.empty_like(qd)
+    dptrs = [t.data_ptr() for t in (qd, kd, vd, o, lse, dod, dq, dk, dv, o_lo)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch(dptrs)
+    torch.cuda.synchronize()
+    code, info = fa.device_status(stream.cuda_stream)
+    if code != "FA_OK":
+        raise RuntimeError(f"device status after warm-up: {code} {info}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.zero_()
+        launch(dptrs, evs[s])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    code, info = fa.device_status(stream.cuda_stream)
+    if code != "FA_OK":
+        raise RuntimeError(f"device status after timed steps: {code} {info}")
+    t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_pre = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    t_main = sum(e[2].elapsed_time(e[3]) for e in evs) / 1e3
+    t_conv = sum(e[3].elapsed_time(e[4]) for e in evs) / 1e3
+    total = t_fwd + t_pre + t_main + t_conv
+    if dist:
+        tt = torch.tensor([total], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total = tt.item()
+    K = args.steps
+    value = world * step_flops * K / total / 1e12
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv, hlse))
+
+    def e2e_step():
+        for src, dst in ((hq, qd), (hk, kd), (hv, vd), (hdo, dod)):
+            dst.copy_(src, non_blocking=True)
+        o_, lse_, lo_ = fa.fwd(qd, kd, vd, causal=True, out=o, lse=lse, residual=True, o_lo=o_lo)
+        fa.bwd(qd, kd, vd, o_, lse_, dod, causal=True, workspace=ws, dq=dq, dk=dk, dv=dv, o_lo=lo_)
+        for src, dst in ((o, ho), (dq, hdq), (dk, hdk), (dv, hdv), (lse, hlse)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(K, 50))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = ev0.elapsed_time(ev1) / 1e3
+    if dist:
+        tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = tt.item()
+    e2e_value = world * step_flops * e2e_steps / t_e2e / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    main_avg = t_main / K
+    main_flops = 2.5 * F
+    achieved = main_flops / main_avg / 1e12
+    peak = peaks["bf16_tflops"]
+    fwd_avg = t_fwd / K
+    traffic = recorded_traffic("fa_bwd_main_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name(), "B": B, "H": H, "N": N, "d": d, "causal": True, "seed": 0,
+                   "l2": "flushed before every step (256 MiB write, outside the timed interval)",
+                   "parallelism": f"weak: {world} independent replica(s)"},
+        "pct_of_peak": value / (world * peak), "peak_tflops": peak, "peak_source": f"{peak_src} (bf16 burst)",
+        "kernels_ms": {"fa_fwd_kernel": 1e3 * fwd_avg, "fa_bwd_preprocess_kernel": 1e3 * t_pre / K,
+                       "fa_bwd_main_kernel": 1e3 * main_avg, "fa_bwd_dq_convert_kernel": 1e3 * t_conv / K},
+        "fwd_tflops": F / fwd_avg / 1e12,
+        "bwd_tflops": 2.5 * F / ((t_pre + t_main + t_conv) / K) / 1e12,
+        "roofline": {"kernel": "fa_bwd_main_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst"},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * K,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -74,6 +74,18 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
+ * fa_fwd that also writes o_lo [B,H,N,d] dtype = dtype(O_fp32 - float(o)), the
+ * rounding residual of the stored output (same kernel, same o and lse). Passed
+ * to fa_bwd, o + o_lo restores O to fp32 accuracy for D = rowsum(dO * O).
+ * That matters when rows are nearly one-hot: dP - D then cancels, and the
+ * output rounding of o alone would leak into dS (the pages fix no precision for
+ * this step; see the backward's contract). o_lo NULL behaves as fa_fwd.
+ * o_lo must be 16-byte aligned.
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H, int N,
+                    int d, float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 D [B,H,N], fp32 LSE*log2(e)
  * [B,H,N] and the fp32 dQ accumulator [B,H,N,d], each 256-byte aligned.
  * Returns 0 for unsupported shapes.
@@ -83,10 +95,12 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 /*
  * Backward pass (page 2, "Re-computation"): from the forward's o and lse and
  * the upstream gradient dO, computes
- *   D  = rowsum(dO * o)                      (fp32, workspace)
+ *   D  = rowsum(dO * O), O = o + o_lo        (fp32, workspace; O = o if o_lo is NULL)
  *   P  = exp(scale * q k^T - lse)            (recomputed per tile, never stored)
  *   dV = P^T dO;  dP = dO v^T;  dS = P * (dP - D)
  *   dQ = scale * dS k;  dK = scale * dS^T q
+ * d must be 64 or 128 here (d = 256: FA_ERR_UNSUPPORTED, nothing enqueued).
+ * o_lo: NULL, or the residual written by fa_fwd_ex for this o.
  * Writes dq, dk, dv [B,H,N,d] dtype in full (no accumulate-into). Three
  * launches on `stream`: preprocess (D, LSE*log2e, zero dQ accumulator), the
  * main kernel (one CTA per 128-key tile, dQ partial tiles added into the fp32
@@ -96,15 +110,15 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * caller-owned, 256-byte aligned; its contents on entry do not matter.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, void* stream);
+                 void* dq, void* dk, void* dv, const void* o_lo, void* workspace, size_t workspace_bytes, int B, int H,
+                 int N, int d, float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
  * The three phases of fa_bwd as separate calls (same arguments and rules);
  * fa_bwd is exactly these three in order. Exposed so each kernel can be timed
  * on its own.
  */
-fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
+fa_status fa_bwd_preprocess(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
                             size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream);
 fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,

@@ -51,6 +51,7 @@ __all__ = [
     "online_attention_fwd",
     "attention_rows",
     "attention_cols",
+    "attention_row_block",
     "head_scores",
 ]
 
@@ -256,3 +257,24 @@ def attention_cols(q, k, v, do, scale, causal, cols, heads, row_block=1024):
             dv[t] += pc.T @ dob
             dk[t] += scale * (dsc.T @ qb)
     return dk, dv
+
+
+def attention_row_block(q, k, v, do, scale, causal, b, h, row0, row1):
+    """Forward and backward of one (b, h) head restricted to query rows [row0, row1).
+
+    Every quantity is the definition applied to those rows only: S = scale * Q_blk K^T
+    (masked), P = exp(S - LSE), O_blk = P V, D = rowsum(dO_blk * O_blk),
+    dS = P * (dO_blk V^T - D), dQ_blk = scale * dS K, and the block's shares of
+    the key gradients dK_part = scale * dS^T Q_blk, dV_part = P^T dO_blk. Summing
+    the shares over a partition of the rows gives the head's dK and dV.
+    Returns (O_blk, LSE_blk, dQ_blk, dK_part, dV_part).
+    """
+    qb = _as64(q[b, h, row0:row1])
+    kh, vh = _as64(k[b, h]), _as64(v[b, h])
+    dob = _as64(do[b, h, row0:row1])
+    s = head_scores(qb, kh, scale, causal, row0=row0)
+    p, lse = _softmax_rows(s)
+    o = p @ vh
+    D = np.sum(dob * o, axis=-1, keepdims=True)
+    ds = p * (dob @ vh.T - D)
+    return o, lse, scale * (ds @ kh), scale * (ds.T @ qb), p.T @ dob

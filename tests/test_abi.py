@@ -80,9 +80,9 @@ def test_fwd_rejects_bad_arguments(L, kw, code):
     assert fwd(L, **kw) == code
 
 
-def bwd(L, ws=P, ws_bytes=1 << 40, N=256, d=64, scale=0.125, dq=P, **kw):
-    return L.fa_bwd(V(P), V(P), V(P), V(P), V(P), V(P), V(dq), V(P), V(P), V(ws), ws_bytes, 1, 1, N, d, scale, 0, 0,
-                    None)
+def bwd(L, ws=P, ws_bytes=1 << 40, N=256, d=64, scale=0.125, dq=P, o_lo=None, **kw):
+    return L.fa_bwd(V(P), V(P), V(P), V(P), V(P), V(P), V(dq), V(P), V(P), V(o_lo), V(ws), ws_bytes, 1, 1, N, d,
+                    scale, 0, 0, None)
 
 
 def test_bwd_rejects_bad_arguments(L):
@@ -93,6 +93,12 @@ def test_bwd_rejects_bad_arguments(L):
     assert bwd(L, scale=float("nan")) == 1
     assert bwd(L, dq=0) == 1
     assert bwd(L, dq=P + 4) == 3
+    assert bwd(L, o_lo=P + 8) == 3
+
+
+def test_fwd_ex_rejects_misaligned_residual(L):
+    assert L.fa_fwd_ex(V(P), V(P), V(P), V(P), V(P), V(P + 2), 1, 1, 256, 64, 0.125, 0, 0, None) == 3
+    assert L.fa_fwd_ex(V(P), V(P), V(P), V(P), V(0), V(P), 1, 1, 256, 64, 0.125, 0, 0, None) == 1
 
 
 def test_selftest_rejects_bad_arguments(L):

@@ -18,11 +18,14 @@ from helpers import check_grad, to64
 pytestmark = pytest.mark.gpu
 
 
-def run_fwd_bwd(w):
+def run_fwd_bwd(w, residual=True):
     q, k, v, do = make_inputs(w)
     qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
-    o, lse = fa.fwd(qc, kc, vc, causal=w.causal)
-    dq, dk, dv = fa.bwd(qc, kc, vc, o, lse, doc, causal=w.causal)
+    if residual:
+        o, lse, o_lo = fa.fwd(qc, kc, vc, causal=w.causal, residual=True)
+    else:
+        (o, lse), o_lo = fa.fwd(qc, kc, vc, causal=w.causal), None
+    dq, dk, dv = fa.bwd(qc, kc, vc, o, lse, doc, causal=w.causal, o_lo=o_lo)
     torch.cuda.synchronize()
     code, info = fa.device_status()
     assert code == "FA_OK", info
@@ -46,6 +49,15 @@ FULL_CASES = [
 @pytest.mark.parametrize("w", FULL_CASES, ids=lambda w: w.name())
 def test_bwd_full_oracle(w):
     (q, k, v, do), _, (dq, dk, dv) = run_fwd_bwd(w)
+    ref = oracle.attention_bwd(to64(q), to64(k), to64(v), to64(do), w.scale, w.causal)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        check_grad(to64(g), r, name)
+
+
+@pytest.mark.parametrize("w", [SMALL, Workload(1, 3, 384, 128, "bf16", True), PAGES_SHAPE], ids=lambda w: w.name())
+def test_bwd_without_residual(w):
+    """D from the stored (rounded) O alone: still within tolerance on unscaled inputs."""
+    (q, k, v, do), _, (dq, dk, dv) = run_fwd_bwd(w, residual=False)
     ref = oracle.attention_bwd(to64(q), to64(k), to64(v), to64(do), w.scale, w.causal)
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         check_grad(to64(g), r, name)
@@ -81,9 +93,9 @@ def test_bwd_repeatable_and_autograd():
     w = Workload(2, 2, 640, 128, "bf16", True)
     q, k, v, do = make_inputs(w)
     qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
-    o, lse = fa.fwd(qc, kc, vc, causal=True)
-    g1 = fa.bwd(qc, kc, vc, o, lse, doc, causal=True)
-    g2 = fa.bwd(qc, kc, vc, o, lse, doc, causal=True)
+    o, lse, o_lo = fa.fwd(qc, kc, vc, causal=True, residual=True)
+    g1 = fa.bwd(qc, kc, vc, o, lse, doc, causal=True, o_lo=o_lo)
+    g2 = fa.bwd(qc, kc, vc, o, lse, doc, causal=True, o_lo=o_lo)
     torch.cuda.synchronize()
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])  # dK, dV: fixed summation order
     assert (g1[0].float() - g2[0].float()).abs().max().item() <= 1e-2 * g1[0].float().abs().max().item()

@@ -104,6 +104,25 @@ def test_fwd_closed_form_constant_v_and_row0():
     assert (lse[:, :, 0].double().cpu() - want).abs().max().item() < 1e-4
 
 
+@pytest.mark.parametrize("w", [Workload(1, 2, 512, 128, "bf16", True, stress=8.0), PAGES_SHAPE,
+                               Workload(1, 2, 384, 256, "bf16", False)], ids=lambda w: w.name())
+def test_fwd_residual_restores_fp32_output(w):
+    """o + o_lo carries O to fp32 accuracy: only the P-rounding term of the tolerance remains."""
+    q, k, v, _ = make_inputs(w)
+    o, lse, o_lo = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, residual=True)
+    o2, lse2 = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    q64, k64, v64 = to64(q), to64(k), to64(v)
+    o_ref, _ = oracle.attention_fwd(q64, k64, v64, w.scale, w.causal)
+    pv_abs, _ = oracle.attention_fwd(q64, k64, np.abs(v64), w.scale, w.causal)
+    from helpers import UNIT_ROUNDOFF
+    err = np.abs(to64(o) + to64(o_lo) - o_ref)
+    assert (err <= 2e-3 + UNIT_ROUNDOFF[w.dtype] * pv_abs).all(), err.max()
+    # the residual is at most half an ulp of the stored value
+    assert (np.abs(to64(o_lo)) <= np.abs(to64(o)) * 2.0 ** -8 + 1e-30).all()
+
+
 def test_fwd_is_deterministic_and_leaves_guard_bytes():
     w = Workload(1, 2, 384, 128, "bf16", True)
     q, k, v, _ = make_inputs(w)

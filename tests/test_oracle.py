@@ -194,6 +194,25 @@ def test_sampled_modes_match_full(causal):
     np.testing.assert_allclose(cv[0], dv[0, 1, cols], atol=1e-13)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_blocks_partition_the_head(causal):
+    B, H, N, d = 1, 2, 200, 8
+    q, k, v, do = (_rand((B, H, N, d), 20 + s) for s in range(4))
+    o, lse = oracle.attention_fwd(q, k, v, 0.3, causal)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.3, causal)
+    dk_sum, dv_sum = np.zeros((N, d)), np.zeros((N, d))
+    for r0 in range(0, N, 64):
+        r1 = min(N, r0 + 64)
+        ob, lb, dqb, dkp, dvp = oracle.attention_row_block(q, k, v, do, 0.3, causal, 0, 1, r0, r1)
+        np.testing.assert_allclose(ob, o[0, 1, r0:r1], atol=1e-13)
+        np.testing.assert_allclose(lb, lse[0, 1, r0:r1], atol=1e-13)
+        np.testing.assert_allclose(dqb, dq[0, 1, r0:r1], atol=1e-13)
+        dk_sum += dkp
+        dv_sum += dvp
+    np.testing.assert_allclose(dk_sum, dk[0, 1], atol=1e-12)
+    np.testing.assert_allclose(dv_sum, dv[0, 1], atol=1e-12)
+
+
 # ---------------------------------------------------------------- finite differences
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,d", [(16, 4), (9, 8)])

@@ -75,24 +75,33 @@ def workspace_size(B, H, N, d) -> int:
     return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
 
 
-def fwd(q, k, v, causal=False, scale=None, out=None, lse=None):
-    """Forward: returns (o, lse)."""
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, residual=False, o_lo=None):
+    """Forward: returns (o, lse), or (o, lse, o_lo) with residual=True (fa_fwd_ex).
+
+    o_lo is the rounding residual of o (O_fp32 - o in the same dtype); pass it
+    to ``bwd`` so that D = rowsum(dO * O) uses O at fp32 accuracy.
+    """
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    if residual and o_lo is None:
+        o_lo = torch.empty_like(q)
     L = _lib.load()
-    code = L.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
-                    int(bool(causal)), _DT[q.dtype], _stream_ptr(q))
-    _lib.check("fa_fwd", code)
-    _after("fa_fwd", q)
-    return o, lse
+    code = L.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       o_lo.data_ptr() if residual else None, B, H, N, d, scale, int(bool(causal)), _DT[q.dtype],
+                       _stream_ptr(q))
+    _lib.check("fa_fwd_ex", code)
+    _after("fa_fwd_ex", q)
+    return (o, lse, o_lo) if residual else (o, lse)
 
 
-def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None):
-    """Backward: returns (dq, dk, dv)."""
+def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None, o_lo=None):
+    """Backward: returns (dq, dk, dv). o_lo: the residual from ``fwd(..., residual=True)``, or None."""
     _check_qkv(q, k, v, o, do)
+    if o_lo is not None:
+        _check_qkv(q, o_lo)
     B, H, N, d = q.shape
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
     L = _lib.load()
@@ -103,8 +112,9 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     code = L.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, N, d,
-                    scale, int(bool(causal)), _DT[q.dtype], _stream_ptr(q))
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o_lo.data_ptr() if o_lo is not None else None,
+                    workspace.data_ptr(), workspace.numel(), B, H, N, d, scale, int(bool(causal)), _DT[q.dtype],
+                    _stream_ptr(q))
     _lib.check("fa_bwd", code)
     _after("fa_bwd", q)
     return dq, dk, dv
@@ -114,15 +124,15 @@ class _AttentionFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, causal, scale):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        o, lse = fwd(q, k, v, causal, scale)
-        ctx.save_for_backward(q, k, v, o, lse)
+        o, lse, o_lo = fwd(q, k, v, causal, scale, residual=True)
+        ctx.save_for_backward(q, k, v, o, lse, o_lo)
         ctx.causal, ctx.scale = causal, scale
         return o
 
     @staticmethod
     def backward(ctx, do):
-        q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), ctx.causal, ctx.scale)
+        q, k, v, o, lse, o_lo = ctx.saved_tensors
+        dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), ctx.causal, ctx.scale, o_lo=o_lo)
         return dq, dk, dv, None, None
 
 

@@ -135,11 +135,17 @@ const char* fa_status_string(fa_status s) {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, fa_dtype dtype, void* stream) {
+  return fa_fwd_ex(q, k, v, o, lse, nullptr, B, H, N, d, scale, causal, dtype, stream);
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H, int N,
+                    int d, float scale, int causal, fa_dtype dtype, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   fa_status s = check_shape(B, H, N, d, dtype);
   if (s != FA_OK) return s;
   if ((s = check_scale(scale)) != FA_OK) return s;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(o_lo))
+    return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
   fa::FwdArgs a;
   const long long rows = static_cast<long long>(B) * H * N;
@@ -148,6 +154,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
       !make_map(&a.tm_v, v, rows, d, bf16, 128) || !make_map(&a.tm_o, o, rows, d, bf16, 128))
     return FA_ERR_CUDA;
   a.lse = lse;
+  a.o_lo = o_lo;
   a.B = B;
   a.H = H;
   a.N = N;
@@ -165,15 +172,16 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return ws_layout(B, H, N, d).total;
 }
 
-fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
+fa_status fa_bwd_preprocess(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
                             size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream) {
   if (!o || !dO || !lse) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a{};
   fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, 1.0f, 0, dtype, stream);
   if (s != FA_OK) return s;
-  if (!aligned16(o) || !aligned16(dO) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  if (!aligned16(o) || !aligned16(o_lo) || !aligned16(dO) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
   a.o = o;
+  a.o_lo = o_lo;
   a.dO = dO;
   a.lse = lse;
   return fa::launch_bwd_preprocess(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -215,8 +223,8 @@ fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_by
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, void* stream) {
+                 void* dq, void* dk, void* dv, const void* o_lo, void* workspace, size_t workspace_bytes, int B, int H,
+                 int N, int d, float scale, int causal, fa_dtype dtype, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   // Validate everything before enqueuing anything.
   fa::BwdArgs probe{};
@@ -224,9 +232,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (s != FA_OK) return s;
   if (fa::bwd_query_tile(d) == 0) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(o_lo))
     return FA_ERR_ALIGNMENT;
-  if ((s = fa_bwd_preprocess(o, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK) return s;
+  if ((s = check_device()) != FA_OK) return s;
+  if ((s = fa_bwd_preprocess(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK)
+    return s;
   if ((s = fa_bwd_main(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream)) !=
       FA_OK)
     return s;

@@ -19,11 +19,13 @@ template <int VPR>
 cudaError_t launch_pre_t(const BwdArgs& a, size_t n_vec) {
   if (a.bf16)
     fa_bwd_preprocess_kernel<VPR, true><<<grid_for(n_vec), 256, 0, a.stream>>>(
-        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo), static_cast<const uint4*>(a.dO), a.lse,
+        a.ws_D, a.ws_lse2,
         reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
   else
     fa_bwd_preprocess_kernel<VPR, false><<<grid_for(n_vec), 256, 0, a.stream>>>(
-        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo), static_cast<const uint4*>(a.dO), a.lse,
+        a.ws_D, a.ws_lse2,
         reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
   return cudaGetLastError();
 }

@@ -1,5 +1,6 @@
 // Bandwidth-bound helper kernels of the backward pass (no tensor cores):
-//   K2 preprocess: D_i = sum_k dO_ik * O_ik (fp32), LSE_i * log2(e), dQ accumulator := 0
+//   K2 preprocess: D_i = sum_k dO_ik * O_ik (fp32; O = o + o_lo when the forward's rounding
+//                  residual o_lo is given), LSE_i * log2(e), dQ accumulator := 0
 //   K4 dQ convert: dQ = dtype(scale * dQacc)
 // Each thread owns one 16-byte vector (8 elements) of a row; the d/8 threads of
 // a row sit in one warp and reduce with shuffles. Grid-stride loops keep the
@@ -45,6 +46,7 @@ __device__ __forceinline__ uint32_t pack2f(float lo, float hi) {
 // VPR = vectors (of 8 elements) per row = d / 8, a power of two <= 32.
 template <int VPR, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __restrict__ o,
+                                                                 const uint4* __restrict__ o_lo,
                                                                  const uint4* __restrict__ dO,
                                                                  const float* __restrict__ lse, float* __restrict__ D,
                                                                  float* __restrict__ lse2, float4* __restrict__ dqacc,
@@ -54,6 +56,12 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
     float a[8], b[8];
     unpack8<BF16>(__ldg(&o[i]), a);
     unpack8<BF16>(__ldg(&dO[i]), b);
+    if (o_lo) {  // O reconstructed to fp32 accuracy: o + residual
+      float r[8];
+      unpack8<BF16>(__ldg(&o_lo[i]), r);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] += r[k];
+    }
     float acc = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc = fmaf(a[k], b[k], acc);

@@ -41,6 +41,7 @@ namespace {
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   float* lse;
+  uint16_t* o_lo;  // optional [B*H*N, d]: dtype(O_fp32 - float(O)), the rounding residual of O
   int N;
   int n_qblk;
   float scale_log2;
@@ -76,6 +77,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+}
+
+// Rounds (a, b) to a packed dtype pair and returns the packed pair of the rounding residuals.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2_residual(float a, float b, uint32_t& rounded) {
+  rounded = pack2<BF16>(a, b);
+  float ra, rb;
+  if constexpr (BF16) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rounded));
+    ra = f.x;
+    rb = f.y;
+  } else {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&rounded));
+    ra = f.x;
+    rb = f.y;
+  }
+  return pack2<BF16>(a - ra, b - rb);
 }
 
 // where-codes for timeouts
@@ -316,6 +334,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
+      uint4* lo_row = p.o_lo ? reinterpret_cast<uint4*>(p.o_lo + (static_cast<size_t>(row_base) + q_row0 +
+                                                                    t * 128 + r) * D)
+                             : nullptr;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
@@ -323,13 +344,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int col = 32 * c + 8 * g;  // first of 8 columns = one 16-byte unit
-          uint4 v;
-          v.x = pack2<BF16>(__uint_as_float(u[8 * g + 0]) * inv_l, __uint_as_float(u[8 * g + 1]) * inv_l);
-          v.y = pack2<BF16>(__uint_as_float(u[8 * g + 2]) * inv_l, __uint_as_float(u[8 * g + 3]) * inv_l);
-          v.z = pack2<BF16>(__uint_as_float(u[8 * g + 4]) * inv_l, __uint_as_float(u[8 * g + 5]) * inv_l);
-          v.w = pack2<BF16>(__uint_as_float(u[8 * g + 6]) * inv_l, __uint_as_float(u[8 * g + 7]) * inv_l);
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(u[8 * g + e]) * inv_l;
+          uint4 v, lo;
+          lo.x = pack2_residual<BF16>(x[0], x[1], v.x);
+          lo.y = pack2_residual<BF16>(x[2], x[3], v.y);
+          lo.z = pack2_residual<BF16>(x[4], x[5], v.z);
+          lo.w = pack2_residual<BF16>(x[6], x[7], v.w);
           const int chunk = col >> 6, unit = (col & 63) >> 3;
           *reinterpret_cast<uint4*>(stage + chunk * C::CHUNK + r * 128 + ((unit ^ (r & 7)) << 4)) = v;
+          if (lo_row) lo_row[col >> 3] = lo;
         }
       }
       fence_proxy_async_smem();
@@ -371,6 +396,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a) {
   p.tm_v = a.tm_v;
   p.tm_o = a.tm_o;
   p.lse = a.lse;
+  p.o_lo = static_cast<uint16_t*>(a.o_lo);
   p.N = a.N;
   p.n_qblk = (a.N + 128 * C::NT - 1) / (128 * C::NT);
   p.scale_log2 = a.scale * 1.4426950408889634f;

@@ -16,6 +16,7 @@ struct DevStatusHost {
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;  // box rows 128
   float* lse;
+  void* o_lo;  // optional rounding residual of O (nullptr: not written)
   int B, H, N, d;
   float scale;
   bool causal, bf16;
@@ -27,6 +28,7 @@ struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // q, dO: box rows = query tile; k, v: box rows 128
   CUtensorMap tm_dk, tm_dv;             // box rows 128
   const void* o;
+  const void* o_lo;  // optional rounding residual of O (nullptr: D from o alone)
   const void* dO;
   const float* lse;
   void* dq;
