@@ -114,6 +114,31 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int N, int d, float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
+ * fa_bwd for callers that cannot allocate device memory: the workspace is a
+ * fixed array inside this library instead of caller memory. The pages have no
+ * counterpart; this entry point exists only for how the library is called.
+ * It is meant for code that runs where allocating is not allowed or not wise:
+ * an inference runtime's plugin hook or a framework extension point whose
+ * contract forbids allocation while enqueuing work, or a process whose device
+ * memory is owned by another allocator (cudaMalloc may also synchronise).
+ * Same arguments and results as fa_bwd, minus the workspace. Limits and rules:
+ *  - problems whose fa_bwd_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
+ *    (64 MiB; for d = 128 that is B*H*N up to about 129,000 rows) return
+ *    FA_ERR_WORKSPACE with nothing enqueued;
+ *  - every device that calls it keeps its own 64 MiB copy of the array for as
+ *    long as the library stays loaded;
+ *  - the first call on a device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture;
+ *  - all calls share the array: calls whose GPU work can overlap (different
+ *    streams without ordering) race on it and must be serialised by the caller.
+ * Calls no cudaMalloc/cudaFree and no allocating library routine.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, const void* o_lo, int B, int H, int N, int d,
+                         float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
  * The three phases of fa_bwd as separate calls (same arguments and rules);
  * fa_bwd is exactly these three in order. Exposed so each kernel can be timed
  * on its own.
