@@ -15,7 +15,13 @@
 //   * dS^T goes to a double-buffered shared-memory tile (the dQ operand), and
 //     Q, dO, LSE*log2e, D stream through a three-stage TMA ring.
 // TMEM (512 columns): buffer b at 128b holds S^T/P^T (cols 0-63, then dQ^T)
-// and dP^T/dS^T (cols 64-127); dV at 256, dK at 384.
+// and dP^T/dS^T (cols 64-127); dV at 256, dK at 384. Packed 16-bit P^T of
+// queries 32g..32g+31 sits in columns 32g..32g+15 (dS^T likewise from 64).
+// Roles (16 warps, 4 per SM sub-partition): warps 0-7 elementwise, in two
+// groups that each own 32 of the tile's 64 query columns; warps 8-11 dQ
+// read-out and the dK epilogue; warp 12 TMA producer; warp 13 MMA issuer (it
+// builds each shared-memory descriptor once and advances it by constant
+// offsets, so issuing keeps ahead of the tensor core); warps 14-15 idle.
 #pragma once
 #include "fa_bwd_main.cuh"
 
@@ -41,7 +47,7 @@ struct BwdPipeCfg {
   // bars: kv, q_full[3], q_empty[3], sdp_full[2], ds_full[2], dq_full[2], dq_free[2], done, drain
   static constexpr int NBAR = 1 + 2 * NSTAGE + 8 + 2;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 512;
   __host__ __device__ static constexpr uint32_t BUF(int b) { return 128u * b; }
   static constexpr uint32_t DV_COL = 256, DK_COL = 384;
   static_assert(NSTAGE * Q_TILE >= KV_TILE, "epilogue staging reuses the Q and dO stages");
@@ -49,7 +55,7 @@ struct BwdPipeCfg {
 };
 
 template <bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdPipeCfg;
   constexpr int BQ = C::BQ, D = C::D, NS = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(b_sdp(b), 1);
-      mbar_init(b_ds(b), 128);
+      mbar_init(b_ds(b), 256);
       mbar_init(b_dqfull(b), 1);
       mbar_init(b_dqfree(b), 128);
     }
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
     mbar_fence_init();
     fence_proxy_async_smem();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
       tma_prefetch_desc(&p.tm_q);
@@ -136,29 +142,34 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
         wait_bar(b_qfull(it % NS), (it / NS) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t idesc_sdp = make_idesc(128, BQ, BF16, false, false);
       constexpr uint32_t idesc_acc = make_idesc(128, D, BF16, false, true);
       constexpr uint32_t idesc_dq = make_idesc(128, BQ, BF16, true, true);
+      // Descriptors are built once; a K or row step only adds a constant to the 14-bit start-address
+      // field (start >> 4), which never carries out of it (shared memory is below 256 KB).
+      const uint64_t dK_k = make_sdesc(sK, 16, 1024), dV_k = make_sdesc(sV, 16, 1024);  // K-major
+      const uint64_t dK_mn = make_sdesc(sK, C::KV_CHUNK, 1024);                         // MN-major (dQ^T's A)
+      const uint64_t dQ_k = make_sdesc(sQ, 16, 1024), dDO_k = make_sdesc(sDO, 16, 1024);
+      const uint64_t dQ_mn = make_sdesc(sQ, C::Q_CHUNK, 1024), dDO_mn = make_sdesc(sDO, C::Q_CHUNK, 1024);
+      const uint64_t dDS_mn = make_sdesc(sDS, 128 * 128, 1024);
       // S^T(i) = K_j Q_i^T and dP^T(i) = V_j dO_i^T into TMEM buffer i & 1 (M = 128 keys, N = 64, K = d)
       auto issue_sdp = [&](int it) {
-        const int s = it % NS;
-        const uint32_t sQs = sQ + s * C::Q_TILE, sDOs = sDO + s * C::Q_TILE;
+        const uint64_t so = static_cast<uint64_t>((it % NS) * C::Q_TILE) >> 4;
         const uint32_t tb = tmem + C::BUF(it & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          const uint32_t ob = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-          mma_ss(tb, make_sdesc(sK + oa, 16, 1024), make_sdesc(sQs + ob, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+          const uint64_t oa = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
+          const uint64_t ob = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss(tb, dK_k + oa, dQ_k + so + ob, idesc_sdp, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          const uint32_t ob = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-          mma_ss(tb + 64, make_sdesc(sV + oa, 16, 1024), make_sdesc(sDOs + ob, 16, 1024), idesc_sdp,
-                 kk > 0 ? 1u : 0u);
+          const uint64_t oa = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
+          const uint64_t ob = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss(tb + 64, dV_k + oa, dDO_k + so + ob, idesc_sdp, kk > 0 ? 1u : 0u);
         }
         mma_commit(b_sdp(it & 1));
       };
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
         if (it + 1 < n_it) {
           const int nx = it + 1, u1 = nx >> 1;
           if (!wait_bar(b_qfull(nx % NS), (nx / NS) & 1, p.timeout_ns, abort_flag, WB_QF)) break;
-          // buffer nx & 1 still holds dQ^T(it - 1) until warps 4-7 have read it out
+          // buffer nx & 1 still holds dQ^T(it - 1) until warps 8-11 have read it out
           if (u1 >= 1 && !wait_bar(b_dqfree(nx & 1), (u1 - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE)) break;
           tc_fence_after();
           issue_sdp(nx);
@@ -181,24 +192,25 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
         if (!wait_bar(b_ds(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
         tc_fence_after();
         const int s = it % NS;
-        const uint32_t sQs = sQ + s * C::Q_TILE, sDOs = sDO + s * C::Q_TILE;
+        const uint64_t so = static_cast<uint64_t>(s * C::Q_TILE) >> 4;
         const uint32_t tb = tmem + C::BUF(b);
-        // dV += P^T dO_i ; dK += dS^T Q_i   (M = 128 keys, N = d, K = 64; A from TMEM, B MN-major)
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
+        // dV += P^T dO_i ; dK += dS^T Q_i   (M = 128 keys, N = d, K = 64; A from TMEM, B MN-major).
+        // Packed P^T / dS^T of queries 16kk .. 16kk+15 sit at column (kk / 2) * 32 + (kk % 2) * 8.
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::DV_COL, tb + kk * 8, make_sdesc(sDOs + kk * 2048, C::Q_CHUNK, 1024), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DV_COL, tb + (kk >> 1) * 32 + (kk & 1) * 8, dDO_mn + so + ((kk * 2048) >> 4), idesc_acc,
+                 kk > 0 ? 1u : acc0);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::DK_COL, tb + 64 + kk * 8, make_sdesc(sQs + kk * 2048, C::Q_CHUNK, 1024), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DK_COL, tb + 64 + (kk >> 1) * 32 + (kk & 1) * 8, dQ_mn + so + ((kk * 2048) >> 4),
+                 idesc_acc, kk > 0 ? 1u : acc0);
         mma_commit(b_qempty(s));
         // dQ^T(i) = K_j^T dS^T(i) over S^T(i)'s columns (M = d, N = 64 queries, K = 128 keys)
-        const uint32_t sDSb = sDS + b * C::DS_TILE;
+        const uint64_t bo = static_cast<uint64_t>(b * C::DS_TILE) >> 4;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tb, make_sdesc(sK + kk * 2048, C::KV_CHUNK, 1024), make_sdesc(sDSb + kk * 2048, 128 * 128, 1024),
-                 idesc_dq, kk > 0 ? 1u : 0u);
+          mma_ss(tb, dK_mn + ((kk * 2048) >> 4), dDS_mn + bo + ((kk * 2048) >> 4), idesc_dq, kk > 0 ? 1u : 0u);
         mma_commit(b_dqfull(b));
       }
       mma_commit(b_done);
@@ -206,10 +218,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
       wait_bar(b_drain, 0, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ elementwise: P^T, dS^T
-    const int k = threadIdx.x;  // key within the tile == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int g = warp >> 2;        // column group: queries 32g .. 32g+31 of the tile
+    const int k = threadIdx.x & 127;  // key within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
@@ -225,66 +238,62 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
       }
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + C::BUF(b), tDP = tS + 64;
-      const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * BQ * 4);
-      const float* dd_s = reinterpret_cast<const float*>(smem + C::OFF_DD + s * BQ * 4);
-      const int q0 = (it0 + it) * BQ;
+      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE + s * BQ * 4) + 8 * g;
+      const float4* dd4 = reinterpret_cast<const float4*>(smem + C::OFF_DD + s * BQ * 4) + 8 * g;
+      const int q0 = (it0 + it) * BQ + 32 * g;  // first query of this group's columns
       const bool need_mask = CAUSAL && (q0 < key0 + 127);
       const int kq = key0 + k - q0;  // masked where column c < kq (key > query)
-      float pv[64];
-      {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tS, u0);
-        tmem_ld32(tS + 32, u1);
+      uint32_t u[32];
+      tmem_ld32(tS + 32 * g, u);
+      float pv[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pv[c] = ex2_approx(fmaf(__uint_as_float(u0[c]), sl2, -lse_s[c]));
-          pv[32 + c] = ex2_approx(fmaf(__uint_as_float(u1[c]), sl2, -lse_s[32 + c]));
-        }
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l = lse4[c4];
+        pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 0]), sl2, -l.x));
+        pv[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 1]), sl2, -l.y));
+        pv[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 2]), sl2, -l.z));
+        pv[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 3]), sl2, -l.w));
       }
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = (c < kq) ? 0.f : pv[c];
+        for (int c = 0; c < 32; ++c) pv[c] = (c < kq) ? 0.f : pv[c];
       }
-      {
-        uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = bpack2<BF16>(pv[2 * c], pv[2 * c + 1]);
-        tmem_st32(tS, pk);
-      }
-      uint32_t dk32[32];
-      {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tDP, u0);
-        tmem_ld32(tDP + 32, u1);
+      for (int c = 0; c < 16; ++c) pk[c] = bpack2<BF16>(pv[2 * c], pv[2 * c + 1]);
+      // Each group packs into the first half of its own 32 columns, never into columns the other
+      // group may still be reading: queries 32g + 2c, 2c+1 go to column 32g + c.
+      tmem_st16(tS + 32 * g, pk);
+      tmem_ld32(tDP + 32 * g, u);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a0 = pv[2 * c] * (__uint_as_float(u0[2 * c]) - dd_s[2 * c]);
-          const float a1 = pv[2 * c + 1] * (__uint_as_float(u0[2 * c + 1]) - dd_s[2 * c + 1]);
-          dk32[c] = bpack2<BF16>(a0, a1);
-          const float b0 = pv[32 + 2 * c] * (__uint_as_float(u1[2 * c]) - dd_s[32 + 2 * c]);
-          const float b1 = pv[33 + 2 * c] * (__uint_as_float(u1[2 * c + 1]) - dd_s[33 + 2 * c]);
-          dk32[16 + c] = bpack2<BF16>(b0, b1);
-        }
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 dd = dd4[c4];
+        pk[2 * c4] = bpack2<BF16>(pv[4 * c4] * (__uint_as_float(u[4 * c4]) - dd.x),
+                                  pv[4 * c4 + 1] * (__uint_as_float(u[4 * c4 + 1]) - dd.y));
+        pk[2 * c4 + 1] = bpack2<BF16>(pv[4 * c4 + 2] * (__uint_as_float(u[4 * c4 + 2]) - dd.z),
+                                      pv[4 * c4 + 3] * (__uint_as_float(u[4 * c4 + 3]) - dd.w));
       }
-      tmem_st32(tDP, dk32);
-      // dS^T row k (queries 0..63): one 128-byte swizzled row of buffer b
+      tmem_st16(tDP + 32 * g, pk);
+      // dS^T row k, queries 32g .. 32g+31: 16-byte units 4g .. 4g+3 of the 128-byte swizzled row
       uint8_t* row = smem + C::OFF_DS + b * C::DS_TILE + k * 128;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(row + ((u ^ (k & 7)) << 4)) =
-            make_uint4(dk32[4 * u], dk32[4 * u + 1], dk32[4 * u + 2], dk32[4 * u + 3]);
+      for (int u4 = 0; u4 < 4; ++u4)
+        *reinterpret_cast<uint4*>(row + (((4 * g + u4) ^ (k & 7)) << 4)) =
+            make_uint4(pk[4 * u4], pk[4 * u4 + 1], pk[4 * u4 + 2], pk[4 * u4 + 3]);
       fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(b_ds(b));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_done, 0, p.timeout_ns, abort_flag, WB_DONE));
-    if (ok) tc_fence_after();
-    bwd_store_acc<D, BF16>(tmem + lane_off + C::DV_COL, smem + C::OFF_Q, &p.tm_dv, row_base + key0, k, 1.0f, 1, ok,
-                           abort_flag);
-  } else {
+    if (g == 0) {
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_done, 0, p.timeout_ns, abort_flag, WB_DONE));
+      if (ok) tc_fence_after();
+      bwd_store_acc<D, BF16>(tmem + lane_off + C::DV_COL, smem + C::OFF_Q, &p.tm_dv, row_base + key0, k, 1.0f, 1, ok,
+                             abort_flag);
+    }
+  } else if (warp < 12) {
     // ------------------------------------------------------------ dQ read-out, then dK epilogue
-    const int t = threadIdx.x - 128;  // TMEM lane = d index of dQ^T
+    const int t = threadIdx.x - 256;  // TMEM lane = d index of dQ^T
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
     // Every warp runs all n_it steps and both named barriers of each step, even after an
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_pipe_kernel(const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
