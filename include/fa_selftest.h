@@ -31,6 +31,21 @@ extern "C" {
 fa_status fa_selftest_gemm(const void* a, const void* b, float* d, int n, int k, int a_mode, int b_mode,
                            fa_dtype dtype, void* stream);
 
+/*
+ * Tensor-core rate microbenchmark: `blocks` CTAs (one per SM when blocks is
+ * the SM count) each issue reps x 8 back-to-back tcgen05.mma of shape
+ * M = 128, N = n, K = 16 (bf16 -> fp32) from one thread, A from shared memory
+ * (a_tmem = 0) or from tensor memory (a_tmem = 1), B from shared memory,
+ * cycling over n_acc in {1, 2, 4} independent accumulators (n * n_acc <= 512,
+ * <= 480 with a_tmem), and
+ * write the clock64 cycles from first issue to completion to cycles[block]
+ * (DEVICE pointer, `blocks` entries). Cycles / (8 reps) is the sustained cost
+ * of one instruction of that shape; 2*128*n*16 / that is FLOP/clock/SM.
+ * n in {64, 128, 256}; 1 <= reps <= 2^20; 1 <= blocks <= 4096.
+ */
+fa_status fa_selftest_mma_rate(int n, int a_tmem, int n_acc, int reps, int blocks, unsigned long long* cycles,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,3 +31,25 @@ def test_selftest_gemm(dtype, n, k, a_mode, b_mode):
     got = d.double().cpu()
     err = (got - ref).abs().max().item()
     assert err <= 1e-5 * k * ref.abs().max().item() + 1e-4, err
+
+
+@pytest.mark.parametrize("n,a_tmem,n_acc", [(64, 0, 1), (64, 0, 2), (64, 0, 4), (64, 1, 4), (128, 0, 1),
+                                            (128, 0, 2), (128, 0, 4), (128, 1, 2), (256, 0, 1), (256, 1, 1),
+                                            (256, 0, 2)])
+def test_mma_rate_microbenchmark(n, a_tmem, n_acc):
+    """Sustained cycles per tcgen05.mma (M=128, N=n, K=16): never faster than the nominal dense rate."""
+    import ctypes
+    from tiled_attention_09_gb300 import _lib
+    L = _lib.load()
+    blocks = torch.cuda.get_device_properties(0).multi_processor_count
+    reps = 2048
+    cyc = torch.zeros(blocks, dtype=torch.int64, device="cuda")
+    code = L.fa_selftest_mma_rate(n, a_tmem, n_acc, reps, blocks, ctypes.c_void_p(cyc.data_ptr()),
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    torch.cuda.synchronize()
+    assert fa.device_status()[0] == "FA_OK"
+    per_mma = cyc.double().median().item() / (8 * reps)
+    flop_per_clk = 2 * 128 * n * 16 / per_mma
+    print(f"MMA rate n={n} a_tmem={a_tmem} n_acc={n_acc}: {per_mma:.1f} cycles/instr, {flop_per_clk:.0f} FLOP/clk/SM")
+    assert per_mma >= n / 2 * 0.95  # nominal 8192 dense bf16 FLOP/clk/SM

@@ -43,6 +43,7 @@ SIGNATURES = [
     ("fa_status_string", ctypes.c_char_p, [c_int]),
     ("fa_set_wait_timeout_ns", None, [ctypes.c_ulonglong]),
     ("fa_version", c_int, []),
+    ("fa_selftest_mma_rate", c_int, [c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     ("fa_selftest_gemm", c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
 ]
 

@@ -6,12 +6,11 @@
 // the saved LSE). What changes is the schedule, so that the tensor core never
 // waits for the elementwise warps:
 //   * S^T and dP^T of query tile i go to one of two TMEM buffers (i & 1);
-//   * the MMA warp issues S^T(i+1), dP^T(i+1) into the other buffer *before* it
-//     waits for P^T(i), dS^T(i), so the tensor core computes the next scores
-//     while warps 0-3 turn the current ones into P and dS;
+//   * S^T(i+1), dP^T(i+1) are issued into the other buffer *before* the
+//     issuers wait for P^T(i), dS^T(i), so the tensor core computes the next
+//     scores while the elementwise warps turn the current ones into P and dS;
 //   * dQ^T(i) = K^T dS^T(i) is written over S^T(i)'s columns once dV(i) has
-//     read P^T(i) from them (tcgen05.mma from one thread executes in order),
-//     and read out by warps 4-7 before S^T(i+2) reuses the buffer;
+//     read P^T(i) from them, and read out before S^T(i+2) reuses the buffer;
 //   * dS^T goes to a double-buffered shared-memory tile (the dQ operand), and
 //     Q, dO, LSE*log2e, D stream through a three-stage TMA ring.
 // TMEM (512 columns): buffer b at 128b holds S^T/P^T (cols 0-63, then dQ^T)
@@ -19,9 +18,8 @@
 // queries 32g..32g+31 sits in columns 32g..32g+15 (dS^T likewise from 64).
 // Roles (16 warps, 4 per SM sub-partition): warps 0-7 elementwise, in two
 // groups that each own 32 of the tile's 64 query columns; warps 8-11 dQ
-// read-out and the dK epilogue; warp 12 TMA producer; warp 13 MMA issuer (it
-// builds each shared-memory descriptor once and advances it by constant
-// offsets, so issuing keeps ahead of the tensor core); warps 14-15 idle.
+// read-out and the dK epilogue; warp 12 TMA producer; warps 13-15 MMA issuers
+// (S^T + dV, dP^T + dK, dQ^T), since one thread cannot issue fast enough.
 #pragma once
 #include "fa_bwd_main.cuh"
 
@@ -44,8 +42,9 @@ struct BwdPipeCfg {
   static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;         // NSTAGE x BQ floats
   static constexpr int OFF_DD = OFF_LSE + NSTAGE * BQ * 4;  // NSTAGE x BQ floats
   static constexpr int OFF_BAR = OFF_DD + NSTAGE * BQ * 4;
-  // bars: kv, q_full[3], q_empty[3], sdp_full[2], ds_full[2], dq_full[2], dq_free[2], done, drain
-  static constexpr int NBAR = 1 + 2 * NSTAGE + 8 + 2;
+  // bars: kv, q_full[3], q_empty[3], sdp_full[2], ds_full[2], dq_full[2], dq_free[2], dv_done[2], done,
+  // drain[3]
+  static constexpr int NBAR = 1 + 2 * NSTAGE + 10 + 1 + 3;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr int THREADS = 512;
   __host__ __device__ static constexpr uint32_t BUF(int b) { return 128u * b; }
@@ -71,8 +70,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   auto b_ds = [&](int b) { return smem_u32(&bars[3 + 2 * NS + b]); };
   auto b_dqfull = [&](int b) { return smem_u32(&bars[5 + 2 * NS + b]); };
   auto b_dqfree = [&](int b) { return smem_u32(&bars[7 + 2 * NS + b]); };
-  const uint32_t b_done = smem_u32(&bars[9 + 2 * NS]);
-  const uint32_t b_drain = smem_u32(&bars[10 + 2 * NS]);
+  auto b_dvdone = [&](int b) { return smem_u32(&bars[9 + 2 * NS + b]); };
+  const uint32_t b_done = smem_u32(&bars[11 + 2 * NS]);
+  auto b_drain = [&](int i) { return smem_u32(&bars[12 + 2 * NS + i]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[C::NBAR]);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -88,16 +88,17 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     mbar_init(b_kv, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(b_qfull(s), 1);
-      mbar_init(b_qempty(s), 1);
+      mbar_init(b_qempty(s), 2);  // released by issuers A (after dV) and B (after dK)
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(b_sdp(b), 1);
+      mbar_init(b_sdp(b), 2);  // S^T from issuer A, dP^T from issuer B
       mbar_init(b_ds(b), 256);
       mbar_init(b_dqfull(b), 1);
       mbar_init(b_dqfree(b), 128);
+      mbar_init(b_dvdone(b), 1);
     }
-    mbar_init(b_done, 1);
-    mbar_init(b_drain, 1);
+    mbar_init(b_done, 3);
+    for (int i = 0; i < 3; ++i) mbar_init(b_drain(i), 1);
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -142,80 +143,92 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         wait_bar(b_qfull(it % NS), (it / NS) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 13) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread issues a tcgen05.mma only every ~100+ cycles, so the step's 32 MMAs are spread
+    // over three warps: A = S^T and dV, B = dP^T and dK, C = dQ^T. A's and B's accumulators are
+    // disjoint; C writes dQ^T over the S^T/P^T columns of the step, so it first waits for dV
+    // (issuer A) to have read P^T there (dv_done). A only re-fills a buffer after warps 8-11 have
+    // read the dQ^T that C left in it (dq_free).
+    const int role = warp - 13;
     if (elect_one()) {
       constexpr uint32_t idesc_sdp = make_idesc(128, BQ, BF16, false, false);
       constexpr uint32_t idesc_acc = make_idesc(128, D, BF16, false, true);
       constexpr uint32_t idesc_dq = make_idesc(128, BQ, BF16, true, true);
       // Descriptors are built once; a K or row step only adds a constant to the 14-bit start-address
       // field (start >> 4), which never carries out of it (shared memory is below 256 KB).
-      const uint64_t dK_k = make_sdesc(sK, 16, 1024), dV_k = make_sdesc(sV, 16, 1024);  // K-major
-      const uint64_t dK_mn = make_sdesc(sK, C::KV_CHUNK, 1024);                         // MN-major (dQ^T's A)
-      const uint64_t dQ_k = make_sdesc(sQ, 16, 1024), dDO_k = make_sdesc(sDO, 16, 1024);
-      const uint64_t dQ_mn = make_sdesc(sQ, C::Q_CHUNK, 1024), dDO_mn = make_sdesc(sDO, C::Q_CHUNK, 1024);
-      const uint64_t dDS_mn = make_sdesc(sDS, 128 * 128, 1024);
-      // S^T(i) = K_j Q_i^T and dP^T(i) = V_j dO_i^T into TMEM buffer i & 1 (M = 128 keys, N = 64, K = d)
-      auto issue_sdp = [&](int it) {
+      const uint64_t dKV_k = make_sdesc(role == 0 ? sK : sV, 16, 1024);            // A: K, B: V (K-major)
+      const uint64_t dQO_k = make_sdesc(role == 0 ? sQ : sDO, 16, 1024);           // A: Q, B: dO (K-major)
+      const uint64_t dOQ_mn = make_sdesc(role == 0 ? sDO : sQ, C::Q_CHUNK, 1024);  // A: dO, B: Q (MN-major)
+      const uint64_t dK_mn = make_sdesc(sK, C::KV_CHUNK, 1024);                    // C: K^T (MN-major)
+      const uint64_t dDS_mn = make_sdesc(sDS, 128 * 128, 1024);                    // C: dS^T (MN-major)
+      const uint32_t col = role == 0 ? 0u : 64u;  // A: S^T / P^T half of a buffer, B: dP^T / dS^T half
+      const uint32_t acc_col = role == 0 ? C::DV_COL : C::DK_COL;
+      // A: S^T(i) = K_j Q_i^T ; B: dP^T(i) = V_j dO_i^T  (M = 128 keys, N = 64, K = d) into buffer i & 1
+      auto issue_score = [&](int it) {
         const uint64_t so = static_cast<uint64_t>((it % NS) * C::Q_TILE) >> 4;
-        const uint32_t tb = tmem + C::BUF(it & 1);
+        const uint32_t tb = tmem + C::BUF(it & 1) + col;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t oa = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
           const uint64_t ob = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tb, dK_k + oa, dQ_k + so + ob, idesc_sdp, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
-          const uint64_t ob = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tb + 64, dV_k + oa, dDO_k + so + ob, idesc_sdp, kk > 0 ? 1u : 0u);
+          mma_ss(tb, dKV_k + oa, dQO_k + so + ob, idesc_sdp, kk > 0 ? 1u : 0u);
         }
         mma_commit(b_sdp(it & 1));
       };
-      bool ok = wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_KV) &&
-                wait_bar(b_qfull(0), 0, p.timeout_ns, abort_flag, WB_QF);
-      if (ok) {
-        tc_fence_after();
-        issue_sdp(0);
-      }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int b = it & 1;
-        if (it + 1 < n_it) {
-          const int nx = it + 1, u1 = nx >> 1;
-          if (!wait_bar(b_qfull(nx % NS), (nx / NS) & 1, p.timeout_ns, abort_flag, WB_QF)) break;
-          // buffer nx & 1 still holds dQ^T(it - 1) until warps 8-11 have read it out
-          if (u1 >= 1 && !wait_bar(b_dqfree(nx & 1), (u1 - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE)) break;
+      bool ok = true;
+      if (role < 2) {
+        ok = wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_KV) &&
+             wait_bar(b_qfull(0), 0, p.timeout_ns, abort_flag, WB_QF);
+        if (ok) {
           tc_fence_after();
-          issue_sdp(nx);
+          issue_score(0);
         }
-        if (!wait_bar(b_ds(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
-        tc_fence_after();
-        const int s = it % NS;
-        const uint64_t so = static_cast<uint64_t>(s * C::Q_TILE) >> 4;
-        const uint32_t tb = tmem + C::BUF(b);
-        const uint32_t acc0 = it > 0 ? 1u : 0u;
-        // dV += P^T dO_i ; dK += dS^T Q_i   (M = 128 keys, N = d, K = 64; A from TMEM, B MN-major).
-        // Packed P^T / dS^T of queries 16kk .. 16kk+15 sit at column (kk / 2) * 32 + (kk % 2) * 8.
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int b = it & 1;
+          if (it + 1 < n_it) {
+            const int nx = it + 1, u1 = nx >> 1;
+            if (!wait_bar(b_qfull(nx % NS), (nx / NS) & 1, p.timeout_ns, abort_flag, WB_QF)) break;
+            // A: buffer nx & 1 still holds dQ^T(it - 1) until warps 8-11 have read it out
+            if (role == 0 && u1 >= 1 &&
+                !wait_bar(b_dqfree(nx & 1), (u1 - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE))
+              break;
+            tc_fence_after();
+            issue_score(nx);
+          }
+          if (!wait_bar(b_ds(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
+          tc_fence_after();
+          const int s = it % NS;
+          const uint64_t so = static_cast<uint64_t>(s * C::Q_TILE) >> 4;
+          const uint32_t tb = tmem + C::BUF(b) + col;
+          const uint32_t acc0 = it > 0 ? 1u : 0u;
+          // A: dV += P^T dO_i ; B: dK += dS^T Q_i  (M = 128 keys, N = d, K = 64; A from TMEM, B MN-major).
+          // Packed P^T / dS^T of queries 16kk .. 16kk+15 sit at column (kk / 2) * 32 + (kk % 2) * 8.
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::DV_COL, tb + (kk >> 1) * 32 + (kk & 1) * 8, dDO_mn + so + ((kk * 2048) >> 4), idesc_acc,
-                 kk > 0 ? 1u : acc0);
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ts(tmem + acc_col, tb + (kk >> 1) * 32 + (kk & 1) * 8, dOQ_mn + so + ((kk * 2048) >> 4), idesc_acc,
+                   kk > 0 ? 1u : acc0);
+          mma_commit(b_qempty(s));
+          if (role == 0) mma_commit(b_dvdone(b));
+        }
+      } else {
+        // C: dQ^T(i) = K_j^T dS^T(i) over S^T(i)'s columns (M = d, N = 64 queries, K = 128 keys)
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int b = it & 1;
+          if (!wait_bar(b_ds(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
+          if (!wait_bar(b_dvdone(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + C::BUF(b);
+          const uint64_t bo = static_cast<uint64_t>(b * C::DS_TILE) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::DK_COL, tb + 64 + (kk >> 1) * 32 + (kk & 1) * 8, dQ_mn + so + ((kk * 2048) >> 4),
-                 idesc_acc, kk > 0 ? 1u : acc0);
-        mma_commit(b_qempty(s));
-        // dQ^T(i) = K_j^T dS^T(i) over S^T(i)'s columns (M = d, N = 64 queries, K = 128 keys)
-        const uint64_t bo = static_cast<uint64_t>(b * C::DS_TILE) >> 4;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tb, dK_mn + ((kk * 2048) >> 4), dDS_mn + bo + ((kk * 2048) >> 4), idesc_dq, kk > 0 ? 1u : 0u);
-        mma_commit(b_dqfull(b));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tb, dK_mn + ((kk * 2048) >> 4), dDS_mn + bo + ((kk * 2048) >> 4), idesc_dq, kk > 0 ? 1u : 0u);
+          mma_commit(b_dqfull(b));
+        }
       }
       mma_commit(b_done);
-      mma_commit(b_drain);
-      wait_bar(b_drain, 0, p.timeout_ns, abort_flag, WB_DRAIN);
+      mma_commit(b_drain(role));
+      wait_bar(b_drain(role), 0, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -243,8 +256,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       const int q0 = (it0 + it) * BQ + 32 * g;  // first query of this group's columns
       const bool need_mask = CAUSAL && (q0 < key0 + 127);
       const int kq = key0 + k - q0;  // masked where column c < kq (key > query)
-      uint32_t u[32];
-      tmem_ld32(tS + 32 * g, u);
+      uint32_t u[32], w[32];
+      tmem_ld32_pair(tS + 32 * g, tDP + 32 * g, u, w);  // S^T and dP^T columns in one round trip
       float pv[32];
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
@@ -264,14 +277,13 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       // Each group packs into the first half of its own 32 columns, never into columns the other
       // group may still be reading: queries 32g + 2c, 2c+1 go to column 32g + c.
       tmem_st16(tS + 32 * g, pk);
-      tmem_ld32(tDP + 32 * g, u);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 dd = dd4[c4];
-        pk[2 * c4] = bpack2<BF16>(pv[4 * c4] * (__uint_as_float(u[4 * c4]) - dd.x),
-                                  pv[4 * c4 + 1] * (__uint_as_float(u[4 * c4 + 1]) - dd.y));
-        pk[2 * c4 + 1] = bpack2<BF16>(pv[4 * c4 + 2] * (__uint_as_float(u[4 * c4 + 2]) - dd.z),
-                                      pv[4 * c4 + 3] * (__uint_as_float(u[4 * c4 + 3]) - dd.w));
+        pk[2 * c4] = bpack2<BF16>(pv[4 * c4] * (__uint_as_float(w[4 * c4]) - dd.x),
+                                  pv[4 * c4 + 1] * (__uint_as_float(w[4 * c4 + 1]) - dd.y));
+        pk[2 * c4 + 1] = bpack2<BF16>(pv[4 * c4 + 2] * (__uint_as_float(w[4 * c4 + 2]) - dd.z),
+                                      pv[4 * c4 + 3] * (__uint_as_float(w[4 * c4 + 3]) - dd.w));
       }
       tmem_st16(tDP + 32 * g, pk);
       // dS^T row k, queries 32g .. 32g+31: 16-byte units 4g .. 4g+3 of the 128-byte swizzled row
@@ -304,8 +316,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       uint32_t u0[32], u1[32];
       if (ok) {
         tc_fence_after();
-        tmem_ld32(tmem + lane_off + C::BUF(b), u0);
-        tmem_ld32(tmem + lane_off + C::BUF(b) + 32, u1);
+        tmem_ld32_pair(tmem + lane_off + C::BUF(b), tmem + lane_off + C::BUF(b) + 32, u0, u1);
         tc_fence_before();
         mbar_arrive(b_dqfree(b));
       } else {

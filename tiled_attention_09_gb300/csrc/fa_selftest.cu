@@ -190,3 +190,105 @@ extern "C" fa_status fa_selftest_gemm(const void* a, const void* b, float* d, in
   }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------- MMA issue-rate microbenchmark
+// One CTA per SM issues `reps` x 8 back-to-back tcgen05.mma (M = 128, K = 16, bf16 -> fp32) of one
+// shape from a single thread, rotating over n_acc independent accumulators (consecutive
+// instructions then do not depend on each other when n_acc > 1), and records the clock64 cycles
+// from the first issue to the completion of the last (tcgen05.commit + mbarrier). Operands are zeroed shared memory (K-major, 128-byte
+// swizzle) or zeroed TMEM columns; only the timing is of interest.
+namespace fa {
+namespace {
+constexpr int MR_SMEM = 1024 + 16384 + 32768 + 128;
+
+__global__ void __launch_bounds__(128, 1) fa_mma_rate_kernel(int n, int a_tmem, int n_acc, int tmem_mode, int reps,
+                                                            unsigned long long* out, unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA = smem_u32(smem), sB = sA + 16384;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 16384 + 32768);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < (16384 + 32768) / 16; i += 128) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(bar), 1);
+    mbar_init(smem_u32(bar + 2), 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_ld_base = *tmem_slot;
+  const uint32_t tmem = tmem_ld_base;
+  if (tmem_mode == 2 && tmem != 0u) report_status(FA_DEV_BAD_INDEX, 99);
+  {
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+    tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 480, z);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // tmem_mode 3: threads 0 and 32 both issue, each into its own accumulator columns.
+  if (threadIdx.x == 0 || (tmem_mode == 3 && threadIdx.x == 32)) {
+    // tmem_mode 0: base address as loaded from shared memory; 1: broadcast with a shuffle;
+    // 2: the constant 0 (a CTA that owns all 512 columns always gets column 0, lane 0).
+    const uint32_t tmem = tmem_mode == 2 ? 0u : (tmem_mode == 1 ? __shfl_sync(1u, tmem_ld_base, 0) : tmem_ld_base);
+    const uint32_t idesc = make_idesc(128, n, true, false, false);
+    const uint64_t da = make_sdesc(sA, 16, 1024), db = make_sdesc(sB, 16, 1024);
+    const long long t0 = clock64();
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t off = static_cast<uint64_t>((kk & 3) * 32) >> 4;
+        const uint32_t d = tmem + static_cast<uint32_t>((kk % n_acc) * n) + (threadIdx.x == 32 ? 256u : 0u);
+        if (a_tmem)
+          mma_ts(d, tmem + 480 + (kk & 3) * 8, db + off, idesc, 1u);
+        else
+          mma_ss(d, da + off, db + off, idesc, 1u);
+      }
+    }
+    const uint32_t mybar = smem_u32(threadIdx.x == 32 ? bar + 2 : bar);
+    mma_commit(mybar);
+    wait_bar(mybar, 0, timeout_ns, abort_flag, 1);
+    if (threadIdx.x == 0) out[blockIdx.x] = static_cast<unsigned long long>(clock64() - t0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_selftest_mma_rate(int n, int a_tmem, int n_acc, int reps, int blocks,
+                                          unsigned long long* cycles, void* stream) {
+  const int tmem_mode = (n_acc >> 4) & 3;  // test-only: bits 4-5 select how the TMEM base is obtained
+  n_acc &= 15;
+  using namespace fa;
+  if (!cycles) return FA_ERR_INVALID_ARG;
+  if (!(n == 64 || n == 128 || n == 256) || reps < 1 || reps > (1 << 20) || blocks < 1 || blocks > 4096)
+    return FA_ERR_UNSUPPORTED;
+  if (!(n_acc == 1 || n_acc == 2 || n_acc == 4) || n * n_acc > (a_tmem ? 480 : 512)) return FA_ERR_UNSUPPORTED;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(fa_mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MR_SMEM) != cudaSuccess)
+    return FA_ERR_CUDA;
+  fa_mma_rate_kernel<<<blocks, 128, MR_SMEM, static_cast<cudaStream_t>(stream)>>>(n, a_tmem ? 1 : 0, n_acc, tmem_mode, reps, cycles,
+                                                                                 2000000000ull);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
