@@ -15,13 +15,12 @@
 //                   and row sum need no shuffles.
 //   warp 4NT        producer: TMA loads of Q (once) and K_j, V_j (ring order
 //                   K0 V0 K1 V1 ...).
-//   warps 4NT+1 ..  MMA issuers, one per query tile: tcgen05.mma S_t = Q_t K_j^T
-//                   (both operands in smem) and O_t += P_t V_j (P from TMEM, V
-//                   from smem), with tcgen05.commit arrivals on mbarriers. A
-//                   ring slot is free once every tile's issuer has released it.
+//   warp 4NT+1      MMA issuer: tcgen05.mma S_t = Q_t K_j^T (both operands in
+//                   smem) and O_t += P_t V_j (P from TMEM, V from smem), with
+//                   tcgen05.commit arrivals on mbarriers.
 // TMEM columns: S_t at 128t (fp32 128x128; P_t as 16-bit pairs over its first
 // 64 columns), O_t at 256 + d*t (fp32 128 x d).
-// Issue order of tile t's warp per key tile j: PV_t(j-1), S_t(j); the commit
+// Issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j); the commit
 // that announces S_t(j) also covers PV_t(j-1), so when the softmax sees S_t(j)
 // the accumulator O_t is quiescent and can be rescaled in place.
 // Rescaling is lazy: the running max used for the exponentials only moves when
@@ -59,9 +58,9 @@ struct FwdCfg {
   static constexpr int NS = (D == 64) ? 6 : (D == 128 ? 4 : 2);   // ring slots
   static constexpr int SMEM_Q = NT * TILE;
   static constexpr int SMEM_RING = NS * TILE;
-  static constexpr int NBAR = 1 + 2 * NS + 4 * NT;  // q, ring full/empty, per tile: s, p, o, drain
+  static constexpr int NBAR = 1 + 2 * NS + 3 * NT + 1;
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NBAR * 8 + 16;
-  static constexpr int THREADS = 128 * NT + 32 + 32 * NT;  // softmax groups, producer, one MMA warp per tile
+  static constexpr int THREADS = 128 * NT + 64;
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + D * t; }
@@ -115,7 +114,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
   auto b_s = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + t]); };
   auto b_p = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + NT + t]); };
   auto b_o = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + 2 * NT + t]); };
-  auto b_drain = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + 3 * NT + t]); };
+  const uint32_t b_drain = smem_u32(&bars[1 + 2 * C::NS + 3 * NT]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[C::NBAR]);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -139,14 +138,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     mbar_init(b_q, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(b_full(s), 1);
-      mbar_init(b_empty(s), n_valid > 0 ? n_valid : 1);  // released by every tile's MMA warp
+      mbar_init(b_empty(s), 1);
     }
     for (int t = 0; t < NT; ++t) {
       mbar_init(b_s(t), 1);
       mbar_init(b_p(t), 128);
       mbar_init(b_o(t), 1);
     }
-    for (int t = 0; t < NT; ++t) mbar_init(b_drain(t), 1);
+    mbar_init(b_drain, 1);
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -189,49 +188,52 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       if (n_valid > 0) wait_bar(b_q, 0, p.timeout_ns, abort_flag, W_DRAIN);
     }
     __syncwarp();
-  } else if (warp > 4 * NT) {
-    // ------------------------------------------------------------ MMA issuers, one warp per query tile
-    // One thread issues a tcgen05.mma only every ~100+ cycles, so each query tile gets its own
-    // issuing warp; the two streams touch disjoint TMEM (S_t, O_t) and both release a ring slot.
-    const int t = warp - 4 * NT - 1;
+  } else if (warp == 4 * NT + 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
       constexpr uint32_t idesc_pv = make_idesc(128, D, BF16, false, true);
-      const int nt = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : (N / 128)) : 0;
-      // descriptors built once; steps add constants to the 14-bit start-address field
-      const uint64_t dQt = make_sdesc(sQ + t * C::TILE, 16, 1024);
-      const uint64_t dRk = make_sdesc(sRing, 16, 1024), dRv = make_sdesc(sRing, C::CHUNK, 1024);
-      const uint32_t tS = tmem + C::S_COL(t), tO = tmem + C::O_COL(t);
-      bool ok = (nt == 0) || wait_bar(b_q, 0, p.timeout_ns, abort_flag, W_Q);
-      for (int j = 0; ok && j <= nt; ++j) {
+      bool ok = (n_valid == 0) || wait_bar(b_q, 0, p.timeout_ns, abort_flag, W_Q);
+      for (int j = 0; ok && j <= nmax; ++j) {
         const int sK = 2 * j, sV = 2 * j - 1;
-        if (j >= 1) {
-          if (!wait_bar(b_full(sV % C::NS), (sV / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL)) break;
-          if (!wait_bar(b_p(t), (j - 1) & 1, p.timeout_ns, abort_flag, W_P)) break;
-          tc_fence_after();
-          const uint64_t vo = static_cast<uint64_t>((sV % C::NS) * C::TILE) >> 4;
+        if (j > 0 && !wait_bar(b_full(sV % C::NS), (sV / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL)) break;
+        if (j < nmax && !wait_bar(b_full(sK % C::NS), (sK / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL))
+          break;
+        tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tO, tS + k * 8, dRv + vo + ((k * 2048) >> 4), idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
-          if (j == nt) mma_commit(b_o(t));
-          mma_commit(b_empty(sV % C::NS));
-        }
-        if (j < nt) {
-          if (!wait_bar(b_full(sK % C::NS), (sK / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL)) break;
-          tc_fence_after();
-          const uint64_t ko = static_cast<uint64_t>((sK % C::NS) * C::TILE) >> 4;
+        for (int t = 0; t < NT; ++t) {
+          if (j >= 1 && j <= n_t[t]) {
+            if (!wait_bar(b_p(t), (j - 1) & 1, p.timeout_ns, abort_flag, W_P)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vaddr = sRing + (sV % C::NS) * C::TILE;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint64_t off = static_cast<uint64_t>((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4;
-            mma_ss(tS, dQt + off, dRk + ko + off, idesc_s, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, make_sdesc(vaddr + k * 2048, C::CHUNK, 1024),
+                     idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+            if (j == n_t[t]) mma_commit(b_o(t));
           }
-          mma_commit(b_s(t));
-          mma_commit(b_empty(sK % C::NS));
+          if (j < n_t[t]) {
+            const uint32_t kaddr = sRing + (sK % C::NS) * C::TILE;
+            const uint32_t qaddr = sQ + t * C::TILE;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
+              mma_ss(tmem + C::S_COL(t), make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024),
+                     idesc_s, k > 0 ? 1u : 0u);
+            }
+            mma_commit(b_s(t));
+          }
         }
+        if (!ok) break;
+        if (j < nmax) mma_commit(b_empty(sK % C::NS));
+        if (j > 0) mma_commit(b_empty(sV % C::NS));
       }
-      // Drain: all MMAs this warp issued complete before teardown.
-      mma_commit(b_drain(t));
-      wait_bar(b_drain(t), 0, p.timeout_ns, abort_flag, W_DRAIN);
+      // Drain: all issued MMAs complete before teardown.
+      mma_commit(b_drain);
+      wait_bar(b_drain, 0, p.timeout_ns, abort_flag, W_DRAIN);
     }
     __syncwarp();
   } else {
@@ -260,22 +262,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
       }
       const bool diag = CAUSAL && (j == my_n - 1);
+      // row max: two new values per three-input max, four independent chains
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
       if (diag) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, c + 0 > r ? -INFINITY : s[c + 0]);
-          mx1 = fmaxf(mx1, c + 1 > r ? -INFINITY : s[c + 1]);
-          mx2 = fmaxf(mx2, c + 2 > r ? -INFINITY : s[c + 2]);
-          mx3 = fmaxf(mx3, c + 3 > r ? -INFINITY : s[c + 3]);
+        for (int c = 0; c < 128; c += 8) {
+          mx0 = max3f(mx0, c + 0 > r ? -INFINITY : s[c + 0], c + 1 > r ? -INFINITY : s[c + 1]);
+          mx1 = max3f(mx1, c + 2 > r ? -INFINITY : s[c + 2], c + 3 > r ? -INFINITY : s[c + 3]);
+          mx2 = max3f(mx2, c + 4 > r ? -INFINITY : s[c + 4], c + 5 > r ? -INFINITY : s[c + 5]);
+          mx3 = max3f(mx3, c + 6 > r ? -INFINITY : s[c + 6], c + 7 > r ? -INFINITY : s[c + 7]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, s[c + 0]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 0; c < 128; c += 8) {
+          mx0 = max3f(mx0, s[c + 0], s[c + 1]);
+          mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+          mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+          mx3 = max3f(mx3, s[c + 6], s[c + 7]);
         }
       }
       const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;

@@ -256,6 +256,12 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool bf16, bool 
 }
 
 // ------------------------------------------------------------------ math
+// Three-input max (one instruction for two new values of a running max).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
