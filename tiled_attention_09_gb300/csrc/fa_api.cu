@@ -151,8 +151,9 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
   const long long rows = static_cast<long long>(B) * H * N;
   const bool bf16 = dtype == FA_BF16;
   if (!make_map(&a.tm_q, q, rows, d, bf16, 128) || !make_map(&a.tm_k, k, rows, d, bf16, 128) ||
-      !make_map(&a.tm_v, v, rows, d, bf16, 128) || !make_map(&a.tm_o, o, rows, d, bf16, 128))
+      !make_map(&a.tm_v, v, rows, d, bf16, 128))
     return FA_ERR_CUDA;
+  a.o = o;
   a.lse = lse;
   a.o_lo = o_lo;
   a.B = B;

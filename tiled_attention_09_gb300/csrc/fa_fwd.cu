@@ -39,8 +39,9 @@ namespace fa {
 namespace {
 
 struct FwdParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;
-  float* lse;
+  CUtensorMap tm_q, tm_k, tm_v;
+  uint16_t* o;     // [B*H*N, d] in the input dtype
+  float* lse;      // [B*H*N]
   uint16_t* o_lo;  // optional [B*H*N, d]: dtype(O_fp32 - float(O)), the rounding residual of O
   int N;
   int n_qblk;
@@ -51,21 +52,59 @@ struct FwdParams {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NT = (D <= 128) ? 2 : 1;                   // query tiles per CTA
+  static constexpr int NT = (D <= 128) ? 2 : 1;                   // query tiles per work item
   static constexpr int CHUNK = 128 * 128;                         // 128 rows x 64 elems x 2 B
   static constexpr int NCHUNK = D / 64;
   static constexpr int TILE = 128 * D * 2;                        // one 128-row tile
   static constexpr int NS = (D == 64) ? 6 : (D == 128 ? 4 : 2);   // ring slots
   static constexpr int SMEM_Q = NT * TILE;
   static constexpr int SMEM_RING = NS * TILE;
-  static constexpr int NBAR = 1 + 2 * NS + 3 * NT + 1;
-  static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NBAR * 8 + 16;
-  static constexpr int THREADS = 128 * NT + 64;
+  // q, qfree, full[NS], empty[NS], s[NT], p[NT], o[NT], ofree[NT], clc, item_full[2], item_empty[2], drain
+  static constexpr int NBAR = 2 + 2 * NS + 4 * NT + 1 + 4 + 1;
+  static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
+  // after the barriers: the 16-byte launch-control answer, the item queue (2 x {x, y}), TMEM slot + abort flag
+  static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + BAR_BYTES + 16 + 16 + 16;
+  // NT softmax warpgroups + one warpgroup with the producer, the MMA issuer and two idle warps
+  static constexpr int THREADS = 128 * NT + 128;
+  // Register split (NT = 2): launched with LAUNCH_REGS per thread (three warps per SM
+  // sub-partition), the softmax warpgroups then take SOFTMAX_REGS and the other
+  // warpgroup keeps OTHER_REGS. The host refuses to launch unless the compiled
+  // count equals LAUNCH_REGS, so the increase always finds its registers.
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int SOFTMAX_REGS = 224;
+  static constexpr int OTHER_REGS = 56;
+  static_assert(NT == 1 || 128 * NT * SOFTMAX_REGS + 128 * OTHER_REGS <= THREADS * LAUNCH_REGS, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + D * t; }
   static_assert(O_COL(NT - 1) + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
+};
+
+// One work item: NT consecutive query tiles of one (b, h) head, named by the
+// blockIdx of the CTA that was launched for it (x = head, y = launch rank; under
+// causal masking rank 0 is the last and heaviest query block, so the hardware's
+// launch order is longest-first).
+template <int NT, bool CAUSAL>
+struct FwdItem {
+  int q_row0;    // first query row of the item within the head
+  int row_base;  // row of (b, h, 0) in the [B*H*N, d] view
+  int n_valid;   // query tiles that exist (the last block can hold one tile fewer)
+  int nmax;      // key tiles streamed for the item
+  int n_t[NT];   // key tiles that tile t needs
+  __device__ __forceinline__ FwdItem(int x, int y, int N, int n_qblk) {
+    const int qb = CAUSAL ? (n_qblk - 1 - y) : y;
+    q_row0 = qb * 128 * NT;
+    row_base = x * N;
+    n_valid = (N - q_row0) / 128;
+    if (n_valid > NT) n_valid = NT;
+    nmax = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      n_t[t] = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : (N / 128)) : 0;
+      nmax = n_t[t] > nmax ? n_t[t] : nmax;
+    }
+  }
 };
 
 template <bool BF16>
@@ -97,45 +136,45 @@ __device__ __forceinline__ uint32_t pack2_residual(float a, float b, uint32_t& r
 }
 
 // where-codes for timeouts
-enum : uint32_t { W_Q = 1, W_RING_EMPTY = 2, W_RING_FULL = 3, W_P = 4, W_S = 5, W_O = 6, W_DRAIN = 7 };
+enum : uint32_t {
+  W_Q = 1, W_RING_EMPTY = 2, W_RING_FULL = 3, W_P = 4, W_S = 5, W_O = 6, W_DRAIN = 7,
+  W_QFREE = 8, W_CLC = 9, W_ITEM = 10, W_OFREE = 11
+};
 
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
+  using Item = FwdItem<C::NT, CAUSAL>;
   constexpr int NT = C::NT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sRing = sQ + C::SMEM_Q;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_Q + C::SMEM_RING);
+  uint8_t* aux = smem + C::SMEM_Q + C::SMEM_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(aux);
   const uint32_t b_q = smem_u32(&bars[0]);
-  auto b_full = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto b_empty = [&](int s) { return smem_u32(&bars[1 + C::NS + s]); };
-  auto b_s = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + t]); };
-  auto b_p = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + NT + t]); };
-  auto b_o = [&](int t) { return smem_u32(&bars[1 + 2 * C::NS + 2 * NT + t]); };
-  const uint32_t b_drain = smem_u32(&bars[1 + 2 * C::NS + 3 * NT]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[C::NBAR]);
+  const uint32_t b_qfree = smem_u32(&bars[1]);
+  auto b_full = [&](int s) { return smem_u32(&bars[2 + s]); };
+  auto b_empty = [&](int s) { return smem_u32(&bars[2 + C::NS + s]); };
+  auto b_s = [&](int t) { return smem_u32(&bars[2 + 2 * C::NS + t]); };
+  auto b_p = [&](int t) { return smem_u32(&bars[2 + 2 * C::NS + NT + t]); };
+  auto b_o = [&](int t) { return smem_u32(&bars[2 + 2 * C::NS + 2 * NT + t]); };
+  auto b_ofree = [&](int t) { return smem_u32(&bars[2 + 2 * C::NS + 3 * NT + t]); };
+  const uint32_t b_clc = smem_u32(&bars[2 + 2 * C::NS + 4 * NT]);
+  auto b_item_full = [&](int i) { return smem_u32(&bars[3 + 2 * C::NS + 4 * NT + i]); };
+  auto b_item_empty = [&](int i) { return smem_u32(&bars[5 + 2 * C::NS + 4 * NT + i]); };
+  const uint32_t b_drain = smem_u32(&bars[7 + 2 * C::NS + 4 * NT]);
+  const uint32_t clc_resp = smem_u32(aux + C::BAR_BYTES);
+  volatile int* items = reinterpret_cast<volatile int*>(aux + C::BAR_BYTES + 16);  // [2][2]: x, y (x < 0: none)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + C::BAR_BYTES + 32);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
   const int N = p.N;
-  const int bh = blockIdx.x;
-  const int qb = CAUSAL ? (p.n_qblk - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
-  const int q_row0 = qb * 128 * NT;  // first query row of this CTA within the head
-  const int row_base = bh * N;       // row of (b, h, 0) in the [B*H*N, d] view
-  int n_valid = (N - q_row0) / 128;
-  if (n_valid > NT) n_valid = NT;
-  int n_t[NT];
-  int nmax = 0;
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    n_t[t] = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : (N / 128)) : 0;
-    nmax = n_t[t] > nmax ? n_t[t] : nmax;
-  }
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
+    mbar_init(b_qfree, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(b_full(s), 1);
       mbar_init(b_empty(s), 1);
@@ -144,6 +183,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       mbar_init(b_s(t), 1);
       mbar_init(b_p(t), 128);
       mbar_init(b_o(t), 1);
+      mbar_init(b_ofree(t), 128);
+    }
+    mbar_init(b_clc, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_item_full(i), 1);
+      mbar_init(b_item_empty(i), 1 + 4 * NT);  // the MMA thread and one lane per softmax warp
     }
     mbar_init(b_drain, 1);
     *abort_flag = 0u;
@@ -159,221 +204,323 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Work loop shared by all roles. The CTA starts with the item it was launched
+  // for; the producer then takes over not-yet-launched CTAs one at a time
+  // (cluster launch control, asked while the current item's last K/V tiles are
+  // loaded) and passes their ids to the other roles through a two-entry queue in
+  // shared memory. An id x < 0 ends the loop. Barrier phases run on per-role
+  // counters across items, so nothing is re-initialised between items.
+  // Each role changes its register budget (NT = 2) and ends with its own copy of
+  // the teardown barrier, so no code is shared between the two budgets.
   if (warp == 4 * NT) {
     // ------------------------------------------------------------ producer
+    if constexpr (NT == 2) setmaxnreg_dec<C::OTHER_REGS>();
     if (elect_one()) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(b_q, n_valid * C::TILE);
-      for (int t = 0; t < n_valid; ++t)
+      int ix = blockIdx.x, iy = blockIdx.y;
+      uint32_t seq = 0;      // K/V loads issued (ring position)
+      int n_items = 0;       // items whose loads were issued
+      bool clc_live = true;  // no "nothing left" answer yet
+      bool clc_pending = false;
+      uint32_t clc_phase = 0;
+      bool ok = true;
+      while (ok) {
+        const Item w(ix, iy, N, p.n_qblk);
+        // Q_t of the previous item is dead once its last S MMA has completed
+        if (n_items > 0 && !wait_bar(b_qfree, (n_items - 1) & 1, p.timeout_ns, abort_flag, W_QFREE)) break;
+        mbar_arrive_expect_tx(b_q, w.n_valid * C::TILE);
+        for (int t = 0; t < w.n_valid; ++t)
 #pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_2d(sQ + t * C::TILE + c * C::CHUNK, &p.tm_q, b_q, c * 64, row_base + q_row0 + t * 128);
-      int issued = 0;
-      for (int s = 0; s < 2 * nmax; ++s) {
-        const int slot = s % C::NS, use = s / C::NS;
-        if (use > 0 && !wait_bar(b_empty(slot), (use - 1) & 1, p.timeout_ns, abort_flag, W_RING_EMPTY)) break;
-        mbar_arrive_expect_tx(b_full(slot), C::TILE);
-        const void* map = (s & 1) ? static_cast<const void*>(&p.tm_v) : static_cast<const void*>(&p.tm_k);
-        const int krow = row_base + (s >> 1) * 128;
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_2d(sQ + t * C::TILE + c * C::CHUNK, &p.tm_q, b_q, c * 64, w.row_base + w.q_row0 + t * 128);
+        ++n_items;
+        const int nload = 2 * w.nmax;
+        const int ask_at = nload - 2;  // with the item's last K/V pair
+        for (int s = 0; s < nload; ++s) {
+          if (s == ask_at && clc_live) {
+            fence_proxy_async_smem();  // earlier generic reads of the answer slot come first
+            mbar_arrive_expect_tx(b_clc, 16);
+            clc_try_cancel(clc_resp, b_clc);
+            clc_pending = true;
+          }
+          const uint32_t slot = seq % C::NS, use = seq / C::NS;
+          if (use > 0 && !wait_bar(b_empty(slot), (use - 1) & 1, p.timeout_ns, abort_flag, W_RING_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(b_full(slot), C::TILE);
+          const void* map = (s & 1) ? static_cast<const void*>(&p.tm_v) : static_cast<const void*>(&p.tm_k);
+          const int krow = w.row_base + (s >> 1) * 128;
 #pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_2d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow);
-        ++issued;
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_2d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow);
+          ++seq;
+        }
+        if (!ok) break;
+        int nx = -1, ny = 0;
+        if (clc_live) {
+          if (!wait_bar(b_clc, clc_phase, p.timeout_ns, abort_flag, W_CLC)) break;
+          clc_pending = false;
+          clc_phase ^= 1u;
+          if (!clc_query(clc_resp, nx, ny)) {
+            clc_live = false;
+            nx = -1;
+          }
+        }
+        const int qi = n_items - 1;  // queue entry qi names the item after item qi
+        if (qi >= 2 && !wait_bar(b_item_empty(qi & 1), ((qi >> 1) - 1) & 1, p.timeout_ns, abort_flag, W_ITEM)) break;
+        items[2 * (qi & 1)] = nx;
+        items[2 * (qi & 1) + 1] = ny;
+        mbar_arrive(b_item_full(qi & 1));  // release: readers acquire through their wait
+        if (nx < 0) break;
+        ix = nx;
+        iy = ny;
       }
-      // Drain: every issued load must have landed before the CTA may exit.
-      for (int s = (issued > C::NS ? issued - C::NS : 0); s < issued; ++s)
+      // Drain: every issued copy must have landed before the CTA may exit.
+      if (clc_pending) wait_bar(b_clc, clc_phase, p.timeout_ns, abort_flag, W_DRAIN);
+      for (uint32_t s = (seq > C::NS ? seq - C::NS : 0u); s < seq; ++s)
         wait_bar(b_full(s % C::NS), (s / C::NS) & 1, p.timeout_ns, abort_flag, W_DRAIN);
-      if (n_valid > 0) wait_bar(b_q, 0, p.timeout_ns, abort_flag, W_DRAIN);
+      if (n_items > 0) wait_bar(b_q, (n_items - 1) & 1, p.timeout_ns, abort_flag, W_DRAIN);
     }
     __syncwarp();
+    __syncthreads();
   } else if (warp == 4 * NT + 1) {
     // ------------------------------------------------------------ MMA issuer
+    if constexpr (NT == 2) setmaxnreg_dec<C::OTHER_REGS>();
     if (elect_one()) {
       constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
       constexpr uint32_t idesc_pv = make_idesc(128, D, BF16, false, true);
-      bool ok = (n_valid == 0) || wait_bar(b_q, 0, p.timeout_ns, abort_flag, W_Q);
-      for (int j = 0; ok && j <= nmax; ++j) {
-        const int sK = 2 * j, sV = 2 * j - 1;
-        if (j > 0 && !wait_bar(b_full(sV % C::NS), (sV / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL)) break;
-        if (j < nmax && !wait_bar(b_full(sK % C::NS), (sK / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL))
-          break;
-        tc_fence_after();
+      int ix = blockIdx.x, iy = blockIdx.y;
+      uint32_t seq = 0;        // ring position of the item's K_0
+      uint32_t n_p[NT] = {};   // P_t tiles consumed
+      uint32_t n_o[NT] = {};   // items in which tile t produced an output
+      int n_items = 0;
+      bool ok = true;
+      while (ok) {
+        const Item w(ix, iy, N, p.n_qblk);
+        if (!wait_bar(b_q, n_items & 1, p.timeout_ns, abort_flag, W_Q)) break;
+        for (int j = 0; ok && j <= w.nmax; ++j) {
+          const uint32_t sK = seq + 2 * j, sV = seq + 2 * j - 1;
+          if (j > 0 && !wait_bar(b_full(sV % C::NS), (sV / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL)) break;
+          if (j < w.nmax && !wait_bar(b_full(sK % C::NS), (sK / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL))
+            break;
+          tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (j >= 1 && j <= n_t[t]) {
-            if (!wait_bar(b_p(t), (j - 1) & 1, p.timeout_ns, abort_flag, W_P)) {
-              ok = false;
-              break;
+          for (int t = 0; t < NT; ++t) {
+            if (j >= 1 && j <= w.n_t[t]) {
+              if (!wait_bar(b_p(t), n_p[t] & 1, p.timeout_ns, abort_flag, W_P)) {
+                ok = false;
+                break;
+              }
+              ++n_p[t];
+              // the first P V of an item overwrites O_t: the previous item's epilogue must have read it
+              if (j == 1 && n_o[t] > 0 && !wait_bar(b_ofree(t), (n_o[t] - 1) & 1, p.timeout_ns, abort_flag, W_OFREE)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t vaddr = sRing + (sV % C::NS) * C::TILE;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, make_sdesc(vaddr + k * 2048, C::CHUNK, 1024),
+                       idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+              if (j == w.n_t[t]) {
+                mma_commit(b_o(t));
+                ++n_o[t];
+              }
             }
-            tc_fence_after();
-            const uint32_t vaddr = sRing + (sV % C::NS) * C::TILE;
+            if (j < w.n_t[t]) {
+              const uint32_t kaddr = sRing + (sK % C::NS) * C::TILE;
+              const uint32_t qaddr = sQ + t * C::TILE;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, make_sdesc(vaddr + k * 2048, C::CHUNK, 1024),
-                     idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
-            if (j == n_t[t]) mma_commit(b_o(t));
-          }
-          if (j < n_t[t]) {
-            const uint32_t kaddr = sRing + (sK % C::NS) * C::TILE;
-            const uint32_t qaddr = sQ + t * C::TILE;
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
-              mma_ss(tmem + C::S_COL(t), make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024),
-                     idesc_s, k > 0 ? 1u : 0u);
+              for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
+                mma_ss(tmem + C::S_COL(t), make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024),
+                       idesc_s, k > 0 ? 1u : 0u);
+              }
+              mma_commit(b_s(t));
             }
-            mma_commit(b_s(t));
           }
+          if (!ok) break;
+          if (j == w.nmax - 1) mma_commit(b_qfree);  // every S MMA of the item has been issued
+          if (j < w.nmax) mma_commit(b_empty(sK % C::NS));
+          if (j > 0) mma_commit(b_empty(sV % C::NS));
         }
         if (!ok) break;
-        if (j < nmax) mma_commit(b_empty(sK % C::NS));
-        if (j > 0) mma_commit(b_empty(sV % C::NS));
+        seq += 2 * w.nmax;
+        const int qi = n_items++;
+        if (!wait_bar(b_item_full(qi & 1), (qi >> 1) & 1, p.timeout_ns, abort_flag, W_ITEM)) break;
+        const int nx = items[2 * (qi & 1)], ny = items[2 * (qi & 1) + 1];
+        mbar_arrive(b_item_empty(qi & 1));
+        if (nx < 0) break;
+        ix = nx;
+        iy = ny;
       }
       // Drain: all issued MMAs complete before teardown.
       mma_commit(b_drain);
       wait_bar(b_drain, 0, p.timeout_ns, abort_flag, W_DRAIN);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax
+    tc_fence_before();
+    __syncthreads();  // every role is done with TMEM
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  } else if (warp < 4 * NT) {
+    // ------------------------------------------------------------ softmax + epilogue
+    if constexpr (NT == 2) setmaxnreg_inc<C::SOFTMAX_REGS>();
     const int t = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the query tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::S_COL(t);
     const uint32_t tO = tmem + lane_off + C::O_COL(t);
     const float sl2 = p.scale_log2;
-    const int my_n = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : (N / 128)) : 0;
-    float m_used = 0.f, l = 0.f;
-    bool ok = my_n > 0;
-    for (int j = 0; ok && j < my_n; ++j) {
-      // warp-uniform outcome: tcgen05.ld/st below are warp-collective
-      if (!__all_sync(0xffffffffu, wait_bar(b_s(t), j & 1, p.timeout_ns, abort_flag, W_S))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[128];
-      {
-        uint32_t u[128];
-        tmem_ld128(tS, u);  // the whole row in one TMEM round trip
-#pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
-      }
-      const bool diag = CAUSAL && (j == my_n - 1);
-      // row max: two new values per three-input max, four independent chains
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-      if (diag) {
-#pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          mx0 = max3f(mx0, c + 0 > r ? -INFINITY : s[c + 0], c + 1 > r ? -INFINITY : s[c + 1]);
-          mx1 = max3f(mx1, c + 2 > r ? -INFINITY : s[c + 2], c + 3 > r ? -INFINITY : s[c + 3]);
-          mx2 = max3f(mx2, c + 4 > r ? -INFINITY : s[c + 4], c + 5 > r ? -INFINITY : s[c + 5]);
-          mx3 = max3f(mx3, c + 6 > r ? -INFINITY : s[c + 6], c + 7 > r ? -INFINITY : s[c + 7]);
+    int ix = blockIdx.x, iy = blockIdx.y;
+    uint32_t n_s = 0;  // S_t tiles consumed
+    uint32_t n_o = 0;  // outputs written
+    int n_items = 0;
+    bool ok = true;
+    while (ok) {
+      const Item w(ix, iy, N, p.n_qblk);
+      const int my_n = (t < w.n_valid) ? (CAUSAL ? (w.q_row0 / 128 + t + 1) : (N / 128)) : 0;  // t is not a constant here
+      float m_used = 0.f, l = 0.f;
+      for (int j = 0; ok && j < my_n; ++j) {
+        // warp-uniform outcome: tcgen05.ld/st below are warp-collective
+        if (!__all_sync(0xffffffffu, wait_bar(b_s(t), n_s & 1, p.timeout_ns, abort_flag, W_S))) {
+          ok = false;
+          break;
         }
-      } else {
+        ++n_s;
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t u[128];
+          tmem_ld128(tS, u);  // the whole row in one TMEM round trip
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          mx0 = max3f(mx0, s[c + 0], s[c + 1]);
-          mx1 = max3f(mx1, s[c + 2], s[c + 3]);
-          mx2 = max3f(mx2, s[c + 4], s[c + 5]);
-          mx3 = max3f(mx3, s[c + 6], s[c + 7]);
+          for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
         }
-      }
-      const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (j == 0) {
-        m_used = m_new;
-      } else if (m_new > m_used + p.rescale_threshold) {
-        alpha = ex2_approx(m_used - m_new);
-        m_used = m_new;
-        l *= alpha;
-        rescale = true;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tO + 32 * c, u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(tO + 32 * c, u);
-        }
-      }
-      const float neg_m = -m_used;
-      float ls0 = 0.f, ls1 = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
-        float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
+        const bool diag = CAUSAL && (j == my_n - 1);
+        // row max: two new values per three-input max, four independent chains
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
         if (diag) {
-          p0 = (c > r) ? 0.f : p0;
-          p1 = (c + 1 > r) ? 0.f : p1;
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            mx0 = max3f(mx0, c + 0 > r ? -INFINITY : s[c + 0], c + 1 > r ? -INFINITY : s[c + 1]);
+            mx1 = max3f(mx1, c + 2 > r ? -INFINITY : s[c + 2], c + 3 > r ? -INFINITY : s[c + 3]);
+            mx2 = max3f(mx2, c + 4 > r ? -INFINITY : s[c + 4], c + 5 > r ? -INFINITY : s[c + 5]);
+            mx3 = max3f(mx3, c + 6 > r ? -INFINITY : s[c + 6], c + 7 > r ? -INFINITY : s[c + 7]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            mx0 = max3f(mx0, s[c + 0], s[c + 1]);
+            mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+            mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+            mx3 = max3f(mx3, s[c + 6], s[c + 7]);
+          }
         }
-        ls0 += p0;
-        ls1 += p1;
-        pk[c >> 1] = pack2<BF16>(p0, p1);
-      }
-      l += ls0 + ls1;
-      tmem_st64(tS, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(b_p(t));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_o(t), 0, p.timeout_ns, abort_flag, W_O));
-    uint8_t* stage = smem + t * C::TILE;  // Q_t is dead once O_t is final
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      uint4* lo_row = p.o_lo ? reinterpret_cast<uint4*>(p.o_lo + (static_cast<size_t>(row_base) + q_row0 +
-                                                                    t * 128 + r) * D)
-                             : nullptr;
+        const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_used = m_new;
+        } else if (m_new > m_used + p.rescale_threshold) {
+          alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+          l *= alpha;
+          rescale = true;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // the commit that announced S_t(j) also covers P_t(j-1) V: O_t is quiescent
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tO + 32 * c, u);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tO + 32 * c, u);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int col = 32 * c + 8 * g;  // first of 8 columns = one 16-byte unit
-          float x[8];
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(tO + 32 * c, u);
+          }
+        }
+        const float neg_m = -m_used;
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t pk[64];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(u[8 * g + e]) * inv_l;
-          uint4 v, lo;
-          lo.x = pack2_residual<BF16>(x[0], x[1], v.x);
-          lo.y = pack2_residual<BF16>(x[2], x[3], v.y);
-          lo.z = pack2_residual<BF16>(x[4], x[5], v.z);
-          lo.w = pack2_residual<BF16>(x[6], x[7], v.w);
-          const int chunk = col >> 6, unit = (col & 63) >> 3;
-          *reinterpret_cast<uint4*>(stage + chunk * C::CHUNK + r * 128 + ((unit ^ (r & 7)) << 4)) = v;
-          if (lo_row) lo_row[col >> 3] = lo;
+        for (int c = 0; c < 128; c += 2) {
+          float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
+          float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
+          if (diag) {
+            p0 = (c > r) ? 0.f : p0;
+            p1 = (c + 1 > r) ? 0.f : p1;
+          }
+          ls0 += p0;
+          ls1 += p1;
+          pk[c >> 1] = pack2<BF16>(p0, p1);
+        }
+        l += ls0 + ls1;
+        tmem_st64(tS, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_p(t));
+      }
+      if (ok && my_n > 0) {
+        // ---------------------------------------------------------- epilogue of tile t
+        ok = __all_sync(0xffffffffu, wait_bar(b_o(t), n_o & 1, p.timeout_ns, abort_flag, W_O));
+        ++n_o;
+        if (ok) {
+          tc_fence_after();
+          const float inv_l = 1.f / l;
+          const size_t grow = static_cast<size_t>(w.row_base) + w.q_row0 + t * 128 + r;
+          uint4* o_row = reinterpret_cast<uint4*>(p.o + grow * D);
+          uint4* lo_row = p.o_lo ? reinterpret_cast<uint4*>(p.o_lo + grow * D) : nullptr;
+          constexpr int EC = D < 128 ? D : 128;  // columns per TMEM round trip
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += EC) {
+            uint32_t u[EC];
+            if constexpr (EC == 128)
+              tmem_ld128(tO + c0, u);
+            else
+              tmem_ld64(tO + c0, u);
+            if (c0 + EC == D) {
+              // O_t is in registers: the next item's first P V may overwrite it
+              tc_fence_before();
+              mbar_arrive(b_ofree(t));
+            }
+#pragma unroll
+            for (int g = 0; g < EC / 8; ++g) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(u[8 * g + e]) * inv_l;
+              uint4 v, lo;
+              lo.x = pack2_residual<BF16>(x[0], x[1], v.x);
+              lo.y = pack2_residual<BF16>(x[2], x[3], v.y);
+              lo.z = pack2_residual<BF16>(x[4], x[5], v.z);
+              lo.w = pack2_residual<BF16>(x[6], x[7], v.w);
+              o_row[(c0 >> 3) + g] = v;
+              if (lo_row) lo_row[(c0 >> 3) + g] = lo;
+            }
+          }
+          // LSE in natural log: (m_used + log2 l) * ln 2
+          p.lse[grow] = (m_used + log2f(l)) * 0.69314718055994531f;
         }
       }
-      fence_proxy_async_smem();
-      // LSE in natural log: (m_used + log2 l) * ln 2
-      p.lse[static_cast<size_t>(row_base) + q_row0 + t * 128 + r] = (m_used + log2f(l)) * 0.69314718055994531f;
+      if (!ok) break;
+      const int qi = n_items++;
+      if (!__all_sync(0xffffffffu, wait_bar(b_item_full(qi & 1), (qi >> 1) & 1, p.timeout_ns, abort_flag, W_ITEM)))
+        break;
+      const int nx = items[2 * (qi & 1)], ny = items[2 * (qi & 1) + 1];
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(b_item_empty(qi & 1));
+      if (nx < 0) break;
+      ix = nx;
+      iy = ny;
     }
-    if (my_n > 0) {
-      // Every warp of the warpgroup reaches this barrier exactly once (all waits are bounded).
-      named_bar_sync(1 + t, 128);
-      if (r == 0 && ok && *abort_flag == 0u) {
-#pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_store_2d(&p.tm_o, smem_u32(stage) + c * C::CHUNK, c * 64, row_base + q_row0 + t * 128);
-        bulk_commit();
-        bulk_wait_read0();
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 4 * NT + 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+  } else {
+    // ------------------------------------------------------------ idle warps of the last warpgroup
+    if constexpr (NT == 2) setmaxnreg_dec<C::OTHER_REGS>();
+    __syncthreads();
   }
 }
 
@@ -381,15 +528,22 @@ template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
-  static bool attr_set = false;  // per instantiation; attribute is per-device but identical everywhere
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  (void)attr_set;
+  if constexpr (C::NT == 2) {
+    static int checked = 0;  // 1: the compiled register count matches the split
+    if (!checked) {
+      cudaFuncAttributes fa_attr;
+      if ((e = cudaFuncGetAttributes(&fa_attr, kern)) != cudaSuccess) return e;
+      if (fa_attr.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+      checked = 1;
+    }
+  }
   FwdParams p;
   p.tm_q = a.tm_q;
   p.tm_k = a.tm_k;
   p.tm_v = a.tm_v;
-  p.tm_o = a.tm_o;
+  p.o = static_cast<uint16_t*>(a.o);
   p.lse = a.lse;
   p.o_lo = static_cast<uint16_t*>(a.o_lo);
   p.N = a.N;

@@ -14,7 +14,8 @@ struct DevStatusHost {
 // 2-D tensor maps over the [rows, d] view of a [B,H,N,d] tensor (rows = B*H*N),
 // box {64 elements, box_rows rows}, 128-byte swizzle.
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // box rows 128
+  CUtensorMap tm_q, tm_k, tm_v;  // box rows 128
+  void* o;     // [B*H*N, d] output
   float* lse;
   void* o_lo;  // optional rounding residual of O (nullptr: not written)
   int B, H, N, d;

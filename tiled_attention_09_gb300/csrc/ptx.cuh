@@ -255,6 +255,48 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool bf16, bool 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ------------------------------------------------------------------ register split
+// Moves registers between warpgroups: every thread of a warpgroup executes the
+// same call. An increase waits until other warpgroups' decreases have freed
+// enough of the registers the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------------------------ cluster launch control
+// Asks the hardware to cancel the launch of a CTA (a cluster of one) that has not
+// started yet, so that the calling CTA can do its work instead. The 16-byte answer
+// lands in shared memory at `resp` and completes 16 transaction bytes on `bar`
+// (the caller arms it with mbar_arrive_expect_tx(bar, 16)). After one answer says
+// "nothing cancelled" the CTA must not ask again.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+// Reads an answer: true, with the cancelled CTA's blockIdx.x / .y, if a launch was taken over.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int& x, int& y) {
+  uint32_t ok, cx = 0u, cy = 0u;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%3];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, %2, _, _}, h;\n\t}"
+      : "=r"(ok), "+r"(cx), "+r"(cy)
+      : "r"(resp)
+      : "memory");
+  x = static_cast<int>(cx);
+  y = static_cast<int>(cy);
+  return ok != 0u;
+}
+
 // ------------------------------------------------------------------ math
 // Three-input max (one instruction for two new values of a running max).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
