@@ -71,8 +71,8 @@ struct FwdCfg {
   // warpgroup keeps OTHER_REGS. The host refuses to launch unless the compiled
   // count equals LAUNCH_REGS, so the increase always finds its registers.
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int SOFTMAX_REGS = 224;
-  static constexpr int OTHER_REGS = 56;
+  static constexpr int SOFTMAX_REGS = 216;
+  static constexpr int OTHER_REGS = 72;
   static_assert(NT == 1 || 128 * NT * SOFTMAX_REGS + 128 * OTHER_REGS <= THREADS * LAUNCH_REGS, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
@@ -292,6 +292,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     if (elect_one()) {
       constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
       constexpr uint32_t idesc_pv = make_idesc(128, D, BF16, false, true);
+      // Descriptors are built once; an MMA only adds (byte offset >> 4) to the start-address
+      // field, which cannot carry out of its 14 bits because shared memory ends below 256 KB.
+      const uint64_t dq0 = make_sdesc(sQ, 16, 1024);           // Q_t, K-major
+      const uint64_t dk0 = make_sdesc(sRing, 16, 1024);        // K in a ring slot, K-major
+      const uint64_t dv0 = make_sdesc(sRing, C::CHUNK, 1024);  // V in a ring slot, MN-major
       int ix = blockIdx.x, iy = blockIdx.y;
       uint32_t seq = 0;        // ring position of the item's K_0
       uint32_t n_p[NT] = {};   // P_t tiles consumed
@@ -321,24 +326,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
                 break;
               }
               tc_fence_after();
-              const uint32_t vaddr = sRing + (sV % C::NS) * C::TILE;
+              const uint64_t dv = dv0 + static_cast<uint64_t>(((sV % C::NS) * C::TILE) >> 4);
+              const uint32_t tO = tmem + C::O_COL(t), tP = tmem + C::S_COL(t);
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + k * 8, make_sdesc(vaddr + k * 2048, C::CHUNK, 1024),
-                       idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 16 rows of V = 2048 bytes
+                mma_ts(tO, tP + k * 8, dv + static_cast<uint64_t>(k * (2048 >> 4)), idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
               if (j == w.n_t[t]) {
                 mma_commit(b_o(t));
                 ++n_o[t];
               }
             }
             if (j < w.n_t[t]) {
-              const uint32_t kaddr = sRing + (sK % C::NS) * C::TILE;
-              const uint32_t qaddr = sQ + t * C::TILE;
+              const uint64_t dk = dk0 + static_cast<uint64_t>(((sK % C::NS) * C::TILE) >> 4);
+              const uint64_t dq = dq0 + static_cast<uint64_t>((t * C::TILE) >> 4);
+              const uint32_t tS = tmem + C::S_COL(t);
 #pragma unroll
-              for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
-                mma_ss(tmem + C::S_COL(t), make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024),
-                       idesc_s, k > 0 ? 1u : 0u);
+              for (int k = 0; k < D / 16; ++k) {  // 16 head dims per MMA: 32 bytes inside a 64-wide chunk
+                const uint64_t off = static_cast<uint64_t>(((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4);
+                mma_ss(tS, dq + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
               }
               mma_commit(b_s(t));
             }
