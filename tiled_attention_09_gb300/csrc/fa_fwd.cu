@@ -7,28 +7,43 @@
 // with a rescale of the running sum and of the output accumulator, and one
 // normalisation at the end. Only O and the per-row log-sum-exp go to HBM.
 //
-// GB300 design. One CTA owns NT query tiles of 128 rows of one (b, h) head
-// (NT = 2 for d <= 128, 1 for d = 256) and streams the head's K/V tiles of 128
-// keys through a ring of shared-memory slots filled by TMA. Roles:
-//   warps 0..4NT-1  softmax: one warpgroup per query tile; thread r owns row r
-//                   of S, P and O in tensor memory (TMEM lane r), so row max
-//                   and row sum need no shuffles.
-//   warp 4NT        producer: TMA loads of Q (once) and K_j, V_j (ring order
-//                   K0 V0 K1 V1 ...).
+// GB300 design. A work item is NT query tiles of 128 rows of one (b, h) head
+// (NT = 2 for d <= 128, 1 for d = 256); the item streams the head's K/V tiles
+// of 128 keys through a ring of shared-memory slots filled by TMA. The kernel
+// is persistent in the Blackwell way: the grid has one CTA per item, but a
+// running CTA takes over CTAs that have not been launched yet (cluster launch
+// control) instead of exiting, so Q/K loads, TMEM allocation and the first
+// S = Q K^T of the next item overlap the end of the current one, and the
+// hardware's launch order (heaviest query blocks first under causal masking)
+// is kept. Roles:
+//   warps 0..4NT-1  softmax + epilogue: one warpgroup per query tile; thread r
+//                   owns row r of S, P and O in tensor memory (TMEM lane r), so
+//                   row max and row sum need no shuffles.
+//   warp 4NT        producer: TMA loads of Q_t and K_j, V_j (ring order
+//                   K0 V0 K1 V1 ...); asks for the next item and passes its id
+//                   to the other roles through a two-entry queue.
 //   warp 4NT+1      MMA issuer: tcgen05.mma S_t = Q_t K_j^T (both operands in
 //                   smem) and O_t += P_t V_j (P from TMEM, V from smem), with
 //                   tcgen05.commit arrivals on mbarriers.
+//   warps 4NT+2..   idle (they complete the last warpgroup).
+// With NT = 2 the block is launched with 168 registers a thread (three warps
+// per SM sub-partition) and setmaxnreg moves them to the softmax warpgroups
+// (216) from the producer/MMA warpgroup (72).
 // TMEM columns: S_t at 128t (fp32 128x128; P_t as 16-bit pairs over its first
 // 64 columns), O_t at 256 + d*t (fp32 128 x d).
 // Issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j); the commit
 // that announces S_t(j) also covers PV_t(j-1), so when the softmax sees S_t(j)
 // the accumulator O_t is quiescent and can be rescaled in place.
-// Rescaling is lazy: the running max used for the exponentials only moves when
-// the row max grows by more than 2^8; the final O / l and LSE use that same
-// max, so the result is exact up to rounding.
+// Rescaling is lazy: the running max m used for the exponentials only moves when
+// the row max grows by more than 2^8. From the second key tile on, the softmax
+// exponentiates against the current m and finds the new row max in the same
+// pass; only a row whose max grew past the threshold rescales O and repeats the
+// pass. The final O / l and LSE use the same m, so the result is exact up to
+// rounding.
 // Causal: tiles above the diagonal are never loaded or computed; the
 // diagonal tile masks keys > query inside the softmax.
 #include <cuda.h>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -406,17 +421,45 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
         }
         const bool diag = CAUSAL && (j == my_n - 1);
-        // row max: two new values per three-input max, four independent chains
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
         if (diag) {
+          // keys past the query's own position do not exist for this row
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = c > r ? -INFINITY : s[c];
+        }
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t pk[64];
+        // P = 2^(s * scale * log2 e - m_used), its row sum, and (TRACK) the row max of s on the side
+        auto exp_pass = [&](auto track) -> float {
+          constexpr bool TRACK = decltype(track)::value;
+          const float neg_m = -m_used;
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+          ls0 = 0.f;
+          ls1 = 0.f;
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
-            mx0 = max3f(mx0, c + 0 > r ? -INFINITY : s[c + 0], c + 1 > r ? -INFINITY : s[c + 1]);
-            mx1 = max3f(mx1, c + 2 > r ? -INFINITY : s[c + 2], c + 3 > r ? -INFINITY : s[c + 3]);
-            mx2 = max3f(mx2, c + 4 > r ? -INFINITY : s[c + 4], c + 5 > r ? -INFINITY : s[c + 5]);
-            mx3 = max3f(mx3, c + 6 > r ? -INFINITY : s[c + 6], c + 7 > r ? -INFINITY : s[c + 7]);
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = fmaf(s[c + e], sl2, neg_m);
+            if constexpr (TRACK) {
+              mx0 = max3f(mx0, x[0], x[1]);
+              mx1 = max3f(mx1, x[2], x[3]);
+              mx2 = max3f(mx2, x[4], x[5]);
+              mx3 = max3f(mx3, x[6], x[7]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float p0 = ex2_approx(x[e]);
+              const float p1 = ex2_approx(x[e + 1]);
+              ls0 += p0;
+              ls1 += p1;
+              pk[(c + e) >> 1] = pack2<BF16>(p0, p1);
+            }
           }
-        } else {
+          return fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));  // max of s * sl2 - m_used
+        };
+        if (j == 0) {
+          // first key tile: the row max comes first (two new values per three-input max, four chains)
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
             mx0 = max3f(mx0, s[c + 0], s[c + 1]);
@@ -424,43 +467,30 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
             mx2 = max3f(mx2, s[c + 4], s[c + 5]);
             mx3 = max3f(mx3, s[c + 6], s[c + 7]);
           }
-        }
-        const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (j == 0) {
-          m_used = m_new;
-        } else if (m_new > m_used + p.rescale_threshold) {
-          alpha = ex2_approx(m_used - m_new);
-          m_used = m_new;
-          l *= alpha;
-          rescale = true;
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-          // the commit that announced S_t(j) also covers P_t(j-1) V: O_t is quiescent
+          m_used = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+          exp_pass(std::false_type{});
+        } else {
+          // later tiles: exponentiate against the running max and find the new row max on the way;
+          // only a row whose max grew by more than the threshold redoes the pass
+          const float m_new = exp_pass(std::true_type{}) + m_used;
+          const bool rescale = m_new > m_used + p.rescale_threshold;
+          if (__any_sync(0xffffffffu, rescale)) {
+            const float alpha = rescale ? ex2_approx(m_used - m_new) : 1.f;
+            if (rescale) {
+              m_used = m_new;
+              l *= alpha;
+            }
+            // the commit that announced S_t(j) also covers P_t(j-1) V: O_t is quiescent
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32(tO + 32 * c, u);
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t u[32];
+              tmem_ld32(tO + 32 * c, u);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(tO + 32 * c, u);
+              for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+              tmem_st32(tO + 32 * c, u);
+            }
+            exp_pass(std::false_type{});
           }
-        }
-        const float neg_m = -m_used;
-        float ls0 = 0.f, ls1 = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
-          float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
-          if (diag) {
-            p0 = (c > r) ? 0.f : p0;
-            p1 = (c + 1 > r) ? 0.f : p1;
-          }
-          ls0 += p0;
-          ls1 += p1;
-          pk[c >> 1] = pack2<BF16>(p0, p1);
         }
         l += ls0 + ls1;
         tmem_st64(tS, pk);
