@@ -102,10 +102,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * d must be 64 or 128 here (d = 256: FA_ERR_UNSUPPORTED, nothing enqueued).
  * o_lo: NULL, or the residual written by fa_fwd_ex for this o.
  * Writes dq, dk, dv [B,H,N,d] dtype in full (no accumulate-into). Three
- * launches on `stream`: preprocess (D, LSE*log2e, zero dQ accumulator), the
- * main kernel (one CTA per 128-key tile, dQ partial tiles added into the fp32
- * accumulator with bulk reductions), and the dQ conversion. Summation order of
- * dQ depends on scheduling, so dq is not bitwise reproducible; dk, dv are.
+ * launches on `stream`: preprocess (D, LSE*log2e, zero the fp32 dQ
+ * accumulator), the main kernel (one CTA per 128-key tile, dQ partial tiles
+ * added into the accumulator with bulk reductions), and the dQ conversion.
+ * Summation order of dQ depends on scheduling, so dq is not bitwise
+ * reproducible; dk, dv are.
  * workspace: device memory of at least fa_bwd_workspace_size(B,H,N,d) bytes,
  * caller-owned, 256-byte aligned; its contents on entry do not matter.
  */
@@ -139,13 +140,16 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
- * The three phases of fa_bwd as separate calls (same arguments and rules);
- * fa_bwd is exactly these three in order. Exposed so each kernel can be timed
- * on its own.
+ * The phases of fa_bwd as separate calls (same arguments and rules), exposed
+ * so each kernel can be timed on its own. fa_bwd is fa_bwd_preprocess followed
+ * by fa_bwd_main with dq given. fa_bwd_main's dq is optional: given, the dQ
+ * conversion is enqueued right after the main kernel, so dq is complete when
+ * the call's work completes; NULL, dQ is left (unscaled, fp32) in the
+ * workspace and fa_bwd_dq_convert turns it into dq afterwards.
  */
 fa_status fa_bwd_preprocess(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
                             size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream);
-fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, void* dq,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                       fa_dtype dtype, void* stream);
 fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,

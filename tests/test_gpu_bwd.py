@@ -113,3 +113,36 @@ def test_bwd_head_dim_256_is_reported_unsupported():
     with pytest.raises(fa.FAError) as e:
         fa.bwd(q, k, v, o, lse, do)
     assert e.value.code == 2
+
+
+@pytest.mark.parametrize("w", [Workload(1, 3, 384, 128, "bf16", True), Workload(2, 2, 640, 128, "fp16", False),
+                               Workload(1, 2, 384, 64, "bf16", True), Workload(1, 2, 256, 64, "fp16", False)],
+                         ids=lambda w: w.name())
+def test_bwd_staged_phases_match_fa_bwd(w):
+    """fa_bwd_preprocess + fa_bwd_main(dq = NULL) + fa_bwd_dq_convert against fa_bwd, whose main phase
+    finishes dQ itself (per-tile arrival counters) for d = 128: dK, dV identical; dQ within the
+    gradient tolerance (its summation order depends on scheduling)."""
+    import ctypes
+    from tiled_attention_09_gb300 import _lib
+    L = _lib.load()
+    q, k, v, do = (t.cuda() for t in make_inputs(w))
+    o, lse, o_lo = fa.fwd(q, k, v, causal=w.causal, residual=True)
+    ref = fa.bwd(q, k, v, o, lse, do, causal=w.causal, o_lo=o_lo)
+    B, H, N, d = q.shape
+    ws_bytes = L.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.full((ws_bytes,), 0x7f, dtype=torch.uint8, device="cuda")  # contents on entry do not matter
+    dq, dk, dv = torch.full_like(q, 7.0), torch.empty_like(k), torch.empty_like(v)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    dt = _lib.FA_BF16 if w.dtype == "bf16" else _lib.FA_F16
+    P = lambda t: t.data_ptr()
+    assert L.fa_bwd_preprocess(P(o), P(o_lo), P(do), P(lse), P(ws), ws_bytes, B, H, N, d, dt, st) == 0
+    assert L.fa_bwd_main(P(q), P(k), P(v), P(do), P(dk), P(dv), None, P(ws), ws_bytes, B, H, N, d, w.scale,
+                         int(w.causal), dt, st) == 0
+    torch.cuda.synchronize()
+    assert torch.all(dq == 7.0), "dq must not be touched when fa_bwd_main gets no dq"
+    assert L.fa_bwd_dq_convert(P(dq), P(ws), ws_bytes, B, H, N, d, w.scale, dt, st) == 0
+    torch.cuda.synchronize()
+    code, info = fa.device_status()
+    assert code == "FA_OK", info
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    check_grad(to64(dq), to64(ref[0]), "dQ")

@@ -35,7 +35,7 @@ SIGNATURES = [
                                          c_void_p]),
     ("fa_bwd_noalloc", c_int, [c_void_p] * 10 + [c_int, c_int, c_int, c_int, c_float, c_int, c_int, c_void_p]),
     ("fa_bwd_preprocess", c_int, [c_void_p] * 5 + [c_size_t, c_int, c_int, c_int, c_int, c_int, c_void_p]),
-    ("fa_bwd_main", c_int, [c_void_p] * 6 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+    ("fa_bwd_main", c_int, [c_void_p] * 7 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
                                              c_void_p]),
     ("fa_bwd_dq_convert", c_int, [c_void_p, c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int,
                                   c_void_p]),

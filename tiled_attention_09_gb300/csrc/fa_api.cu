@@ -188,14 +188,15 @@ fa_status fa_bwd_preprocess(const void* o, const void* o_lo, const void* dO, con
   return fa::launch_bwd_preprocess(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, void* dq,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                       fa_dtype dtype, void* stream) {
   if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a{};
   fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
   if (s != FA_OK) return s;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) || !aligned16(dv))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(dq))
     return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
   const int bq = fa::bwd_query_tile(d);
@@ -208,6 +209,7 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* d
   a.dO = dO;
   a.dk = dk;
   a.dv = dv;
+  a.dq = dq;  // optional: when given, the dQ conversion is enqueued right after the main kernel
   return fa::launch_bwd_main(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -238,10 +240,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if ((s = check_device()) != FA_OK) return s;
   if ((s = fa_bwd_preprocess(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK)
     return s;
-  if ((s = fa_bwd_main(q, k, v, dO, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream)) !=
-      FA_OK)
-    return s;
-  return fa_bwd_dq_convert(dq, workspace, workspace_bytes, B, H, N, d, scale, dtype, stream);
+  // given dq, fa_bwd_main enqueues the dQ conversion right after the main kernel
+  return fa_bwd_main(q, k, v, dO, dk, dv, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
 }
 
 fa_status fa_device_status(void* stream, unsigned int info[4]) {

@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
 
   const int warp = threadIdx.x >> 5;
   const int N = p.N;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // shared memory and TMEM are set up; global memory only from here on
 
   // Work loop shared by all roles. The CTA starts with the item it was launched
   // for; the producer then takes over not-yet-launched CTAs one at a time
@@ -587,8 +589,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a) {
   p.rescale_threshold = 8.0f;
   p.timeout_ns = a.timeout_ns;
   dim3 grid(a.B * a.H, p.n_qblk, 1);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
 }
 
 }  // namespace
