@@ -9,9 +9,13 @@ backward 2.5x that; value = 3.5*F_fwd / (t_fwd + t_bwd).
 
 Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
 barrier and torch.cuda.synchronize(); the L2 cache is flushed (a 256 MiB write)
-before each step, outside the CUDA-event-timed interval of that step. The max
-over ranks is reported; under torchrun every rank runs the same workload on its
-own GPU (weak scaling, no data-path collective).
+before each step, outside the CUDA-event-timed interval of that step. A step is
+timed between two events (fa_fwd_ex, fa_bwd through the C ABI), so the kernels
+keep their programmatic dependent launch; per-kernel times (kernels_ms and the
+roofline's launch duration) come from a second pass of min(K, 50) steps with an
+event between every two kernels. The max over ranks is reported; under torchrun
+every rank runs the same workload on its own GPU (weak scaling, no data-path
+collective).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -283,23 +287,30 @@ def run_native(args):
     DT = _lib.FA_BF16
 
     def launch(ptrs, evs=None):
+        """One step through the public entry points (fa_fwd_ex, fa_bwd); evs: [start, end] events or None."""
         qp, kp, vp, op, lp, dop, dqp, dkp, dvp, lop = ptrs
         if evs:
             evs[0].record(stream)
         _lib.check("fa_fwd_ex", L.fa_fwd_ex(qp, kp, vp, op, lp, lop, B, H, N, d, scale, 1, DT, sp))
+        _lib.check("fa_bwd", L.fa_bwd(qp, kp, vp, op, dop, lp, dqp, dkp, dvp, lop, ws.data_ptr(), ws_bytes, B, H, N, d,
+                                      scale, 1, DT, sp))
         if evs:
             evs[1].record(stream)
+
+    def launch_phases(ptrs, evs):
+        """The same step as its four kernels with an event between each (per-kernel times; an event between
+        two kernels can keep the second from starting early, so this pass is not the step time)."""
+        qp, kp, vp, op, lp, dop, dqp, dkp, dvp, lop = ptrs
+        evs[0].record(stream)
+        _lib.check("fa_fwd_ex", L.fa_fwd_ex(qp, kp, vp, op, lp, lop, B, H, N, d, scale, 1, DT, sp))
+        evs[1].record(stream)
         _lib.check("pre", L.fa_bwd_preprocess(op, lop, dop, lp, ws.data_ptr(), ws_bytes, B, H, N, d, DT, sp))
-        if evs:
-            evs[2].record(stream)
-        # dq = NULL: the conversion is launched on its own below, so each kernel is timed separately
+        evs[2].record(stream)
         _lib.check("main", L.fa_bwd_main(qp, kp, vp, dop, dkp, dvp, None, ws.data_ptr(), ws_bytes, B, H, N, d, scale,
                                          1, DT, sp))
-        if evs:
-            evs[3].record(stream)
+        evs[3].record(stream)
         _lib.check("conv", L.fa_bwd_dq_convert(dqp, ws.data_ptr(), ws_bytes, B, H, N, d, scale, DT, sp))
-        if evs:
-            evs[4].record(stream)
+        evs[4].record(stream)
 
     o_lo = torch.empty_like(qd)
     dptrs = [t.data_ptr() for t in (qd, kd, vd, o, lse, dod, dq, dk, dv, o_lo)]
@@ -311,7 +322,9 @@ def run_native(args):
     if code != "FA_OK":
         raise RuntimeError(f"device status after warm-up: {code} {info}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    K2 = max(3, min(args.steps, 50))
+    pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K2)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.25)
@@ -322,17 +335,22 @@ def run_native(args):
         flush.zero_()
         launch(dptrs, evs[s])
     torch.cuda.synchronize()
+    for s in range(K2):
+        flush.zero_()
+        launch_phases(dptrs, pevs[s])
+    torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clk = clocks.stop()
     code, info = fa.device_status(stream.cuda_stream)
     if code != "FA_OK":
         raise RuntimeError(f"device status after timed steps: {code} {info}")
-    t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
-    t_pre = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
-    t_main = sum(e[2].elapsed_time(e[3]) for e in evs) / 1e3
-    t_conv = sum(e[3].elapsed_time(e[4]) for e in evs) / 1e3
-    total = t_fwd + t_pre + t_main + t_conv
+    total = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    # per-kernel averages from the phase pass
+    t_fwd = sum(e[0].elapsed_time(e[1]) for e in pevs) / 1e3 / K2
+    t_pre = sum(e[1].elapsed_time(e[2]) for e in pevs) / 1e3 / K2
+    t_main = sum(e[2].elapsed_time(e[3]) for e in pevs) / 1e3 / K2
+    t_conv = sum(e[3].elapsed_time(e[4]) for e in pevs) / 1e3 / K2
     if dist:
         tt = torch.tensor([total], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -380,11 +398,11 @@ def run_native(args):
             dist.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
-    main_avg = t_main / K
+    main_avg = t_main
     main_flops = 2.5 * F
     achieved = main_flops / main_avg / 1e12
     peak = peaks["bf16_tflops"]
-    fwd_avg = t_fwd / K
+    fwd_avg = t_fwd
     traffic = recorded_traffic(ROOFLINE_KERNEL)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -392,12 +410,14 @@ def run_native(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name(), "B": B, "H": H, "N": N, "d": d, "causal": True, "seed": 0,
                    "l2": "flushed before every step (256 MiB write, outside the timed interval)",
+                   "timing": "value: whole step between two events; kernels_ms/roofline: a second pass of "
+                             f"{K2} steps with events between kernels",
                    "parallelism": f"weak: {world} independent replica(s)"},
         "pct_of_peak": value / (world * peak), "peak_tflops": peak, "peak_source": f"{peak_src} (bf16 burst)",
-        "kernels_ms": {"fa_fwd_kernel": 1e3 * fwd_avg, "fa_bwd_preprocess_kernel": 1e3 * t_pre / K,
-                       ROOFLINE_KERNEL: 1e3 * main_avg, "fa_bwd_dq_convert_kernel": 1e3 * t_conv / K},
+        "kernels_ms": {"fa_fwd_kernel": 1e3 * fwd_avg, "fa_bwd_preprocess_kernel": 1e3 * t_pre,
+                       ROOFLINE_KERNEL: 1e3 * main_avg, "fa_bwd_dq_convert_kernel": 1e3 * t_conv},
         "fwd_tflops": F / fwd_avg / 1e12,
-        "bwd_tflops": 2.5 * F / ((t_pre + t_main + t_conv) / K) / 1e12,
+        "bwd_tflops": 2.5 * F / (t_pre + t_main + t_conv) / 1e12,
         "roofline": {"kernel": ROOFLINE_KERNEL, "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 burst"},
