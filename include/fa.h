@@ -99,7 +99,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   P  = exp(scale * q k^T - lse)            (recomputed per tile, never stored)
  *   dV = P^T dO;  dP = dO v^T;  dS = P * (dP - D)
  *   dQ = scale * dS k;  dK = scale * dS^T q
- * d must be 64 or 128 here (d = 256: FA_ERR_UNSUPPORTED, nothing enqueued).
+ * d is 64, 128 or 256 (for d = 256 each 128-key block makes two passes, one
+ * per half of the head dimension, recomputing S and dP in each).
  * o_lo: NULL, or the residual written by fa_fwd_ex for this o.
  * Writes dq, dk, dv [B,H,N,d] dtype in full (no accumulate-into). Three
  * launches on `stream`: preprocess (D, LSE*log2e, zero the fp32 dQ

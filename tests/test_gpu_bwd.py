@@ -106,17 +106,21 @@ def test_bwd_repeatable_and_autograd():
     assert torch.equal(ka.grad, g1[1]) and torch.equal(va.grad, g1[2])
 
 
-def test_bwd_head_dim_256_is_reported_unsupported():
-    w = Workload(1, 1, 256, 256, "bf16", False)
-    q, k, v, do = (t.cuda() for t in make_inputs(w))
-    o, lse = fa.fwd(q, k, v)
-    with pytest.raises(fa.FAError) as e:
-        fa.bwd(q, k, v, o, lse, do)
-    assert e.value.code == 2
+@pytest.mark.parametrize("w", [Workload(1, 2, 256, 256, "bf16", False), Workload(1, 2, 384, 256, "bf16", True),
+                               Workload(2, 1, 640, 256, "fp16", True), Workload(1, 2, 512, 256, "bf16", True, stress=8.0)],
+                         ids=lambda w: w.name())
+def test_bwd_head_dim_256(w):
+    """d = 256: two passes per key block (one per half of the head dimension), both halves of dQ, dK, dV
+    against the oracle; the ragged causal tail (N % 256 == 128) and a stressed input included."""
+    (q, k, v, do), _, (dq, dk, dv) = run_fwd_bwd(w)
+    ref = oracle.attention_bwd(to64(q), to64(k), to64(v), to64(do), w.scale, w.causal)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        check_grad(to64(g), r, name)
 
 
 @pytest.mark.parametrize("w", [Workload(1, 3, 384, 128, "bf16", True), Workload(2, 2, 640, 128, "fp16", False),
-                               Workload(1, 2, 384, 64, "bf16", True), Workload(1, 2, 256, 64, "fp16", False)],
+                               Workload(1, 2, 384, 64, "bf16", True), Workload(1, 2, 256, 64, "fp16", False),
+                               Workload(1, 2, 384, 256, "bf16", True)],
                          ids=lambda w: w.name())
 def test_bwd_staged_phases_match_fa_bwd(w):
     """fa_bwd_preprocess + fa_bwd_main(dq = NULL) + fa_bwd_dq_convert against fa_bwd, whose main phase

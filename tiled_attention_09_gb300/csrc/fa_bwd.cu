@@ -4,6 +4,7 @@
 #include "common.cuh"
 #include "fa_bwd_aux.cuh"
 #include "fa_bwd_main.cuh"
+#include "fa_bwd_d256.cuh"
 #include "fa_bwd_pipe.cuh"
 #include "launch.h"
 
@@ -100,9 +101,38 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
 }
+template <bool BF16, bool CAUSAL>
+cudaError_t launch_d256_t(const BwdArgs& a) {
+  using C = BwdD256Cfg;
+  auto kern = fa_bwd_d256_kernel<BF16, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  BwdParams p;
+  p.tm_q = a.tm_q;
+  p.tm_k = a.tm_k;
+  p.tm_v = a.tm_v;
+  p.tm_do = a.tm_do;
+  p.tm_dk = a.tm_dk;
+  p.tm_dv = a.tm_dv;
+  p.lse2 = a.ws_lse2;
+  p.Dvec = a.ws_D;
+  p.dqacc = a.ws_dqacc;
+  p.N = a.N;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.timeout_ns = a.timeout_ns;
+  dim3 grid(a.B * a.H, a.N / 128, 1);
+  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  if (e != cudaSuccess || a.dq == nullptr) return e;
+  return launch_bwd_dq_convert(a);
+}
 }  // namespace
 
 cudaError_t launch_bwd_main(const BwdArgs& a) {
+  if (a.d == 256) {  // head-dimension split: two passes per key block
+    if (a.bf16) return a.causal ? launch_d256_t<true, true>(a) : launch_d256_t<true, false>(a);
+    return a.causal ? launch_d256_t<false, true>(a) : launch_d256_t<false, false>(a);
+  }
   if (a.d == 128) {  // software-pipelined kernel
     if (a.bf16) return a.causal ? launch_pipe_t<true, true>(a) : launch_pipe_t<true, false>(a);
     return a.causal ? launch_pipe_t<false, true>(a) : launch_pipe_t<false, false>(a);

@@ -1,0 +1,337 @@
+// Attention backward main kernel for d = 256 (K3, head-dimension split).
+//
+// Method and per-step arithmetic as fa_bwd_main_kernel (page
+// "transformer模型详解（十）：FlashAttention优化技术", section "Re-computation 而非缓存":
+// outer loop over K/V column blocks, inner loop over Q row blocks, P rebuilt from
+// the saved LSE). What d = 256 changes is the memory plan: the fp32 accumulators
+// dV and dK of a 128-key block are 256 tensor-memory columns each, all of TMEM.
+// So a CTA makes two passes over its query tiles, one per half h of the head
+// dimension. Each pass recomputes
+//   S^T = K Q^T and dP^T = V dO^T          (contracted over the full d = 256),
+//   P = exp2(S^T * scale * log2 e - LSE * log2 e),  dS = P (dP - D),
+// and accumulates only that pass's half of the outputs:
+//   dV[:, h] += P^T dO[:, h],  dK[:, h] += dS^T Q[:, h],  dQ[:, h] += dS K[:, h].
+// S^T and dP^T are computed twice, so the kernel does 1.4x the useful FLOPs.
+// Shared memory: K and V of the block stay resident (128 KB); Q and dO of one
+// 64-query step (64 KB) and dS^T (16 KB) complete it, with no room for a second
+// stage, so the producer loads step i + 1 once step i's MMAs have read step i.
+// dQ^T of a step goes from TMEM straight to the fp32 accumulator with coalesced
+// global reductions (a warp covers 128 contiguous bytes per query), and the
+// dV/dK epilogue of a pass is staged in the Q and dO tiles.
+// TMEM: S^T (P^T packed over it) at 0, dP^T (dS^T packed over it) at 64,
+// dQ^T at 128, dV half at 256, dK half at 384.
+// Roles (320 threads): warps 0-3 elementwise and the dV epilogue, warps 4-7 dQ
+// read-out and the dK epilogue, warp 8 TMA producer, warp 9 MMA issuer.
+#pragma once
+#include "fa_bwd_main.cuh"
+
+namespace fa {
+
+struct BwdD256Cfg {
+  static constexpr int D = 256, DH = 128, BK = 128, BQ = 64, NCH = D / 64;
+  static constexpr int KV_CHUNK = BK * 128;    // 16 KB: 128 rows x 64 elements
+  static constexpr int KV_TILE = BK * D * 2;   // 64 KB
+  static constexpr int Q_CHUNK = BQ * 128;     // 8 KB: 64 rows x 64 elements
+  static constexpr int Q_TILE = BQ * D * 2;    // 32 KB
+  static constexpr int DS_TILE = BK * BQ * 2;  // 16 KB: dS^T [128 keys][64 queries]
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_TILE;
+  static constexpr int OFF_Q = OFF_V + KV_TILE;
+  static constexpr int OFF_DO = OFF_Q + Q_TILE;
+  static constexpr int OFF_DS = OFF_DO + Q_TILE;
+  static constexpr int OFF_LSE = OFF_DS + DS_TILE;
+  static constexpr int OFF_DD = OFF_LSE + BQ * 4;
+  static constexpr int OFF_BAR = OFF_DD + BQ * 4;
+  // bars: kv, q_full, q_empty, sdp, ds, dq_full, dq_free, done, epi, drain
+  static constexpr int NBAR = 10;
+  static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t S_COL = 0, DP_COL = 64, DQ_COL = 128, DV_COL = 256, DK_COL = 384;
+  static_assert(SMEM_BYTES <= 232448, "smem budget");
+  static_assert(Q_TILE >= BK * DH * 2, "a pass's dV or dK half (bf16) is staged in the Q or dO tile");
+};
+
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdD256Cfg;
+  constexpr int BQ = C::BQ, D = C::D, DH = C::DH;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q, sDO = s0 + C::OFF_DO;
+  const uint32_t sDS = s0 + C::OFF_DS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t b_kv = smem_u32(&bars[0]);
+  const uint32_t b_qfull = smem_u32(&bars[1]);
+  const uint32_t b_qempty = smem_u32(&bars[2]);
+  const uint32_t b_sdp = smem_u32(&bars[3]);
+  const uint32_t b_ds = smem_u32(&bars[4]);
+  const uint32_t b_dqfull = smem_u32(&bars[5]);
+  const uint32_t b_dqfree = smem_u32(&bars[6]);
+  const uint32_t b_done = smem_u32(&bars[7]);
+  const uint32_t b_epi = smem_u32(&bars[8]);
+  const uint32_t b_drain = smem_u32(&bars[9]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[C::NBAR]);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int N = p.N;
+  const int bh = blockIdx.x;
+  const int key0 = blockIdx.y * 128;
+  const int row_base = bh * N;
+  const int it0 = CAUSAL ? (key0 / BQ) : 0;
+  const int n_it = N / BQ - it0;  // query steps per pass
+  const int n_g = 2 * n_it;        // steps of both passes: g = h * n_it + it
+
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    mbar_init(b_kv, 1);
+    mbar_init(b_qfull, 1);
+    mbar_init(b_qempty, 1);
+    mbar_init(b_sdp, 1);
+    mbar_init(b_ds, 128);
+    mbar_init(b_dqfull, 1);
+    mbar_init(b_dqfree, 128);
+    mbar_init(b_done, 1);
+    mbar_init(b_epi, 2);  // one thread of each epilogue group, once per pass
+    mbar_init(b_drain, 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // shared memory and TMEM are set up; global memory only from here on
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      mbar_arrive_expect_tx(b_kv, 2 * C::KV_TILE);
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c) {
+        tma_load_2d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, row_base + key0);
+        tma_load_2d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, row_base + key0);
+      }
+      int issued = 0;
+      for (int g = 0; g < n_g; ++g) {
+        const int it = g % n_it;
+        // the single stage is free once step g - 1's MMAs have read it; the first step of the
+        // second pass also waits for the first pass's epilogue, which staged dV / dK there
+        if (g > 0 && !wait_bar(b_qempty, (g - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) break;
+        if (g == n_it && !wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_QE)) break;
+        const int qrow = row_base + (it0 + it) * BQ;
+        mbar_arrive_expect_tx(b_qfull, 2 * C::Q_TILE + 2 * BQ * 4);
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_2d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfull, c * 64, qrow);
+          tma_load_2d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfull, c * 64, qrow);
+        }
+        bulk_load(s0 + C::OFF_LSE, p.lse2 + qrow, BQ * 4, b_qfull);
+        bulk_load(s0 + C::OFF_DD, p.Dvec + qrow, BQ * 4, b_qfull);
+        ++issued;
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_DRAIN);
+      if (issued > 0) wait_bar(b_qfull, (issued - 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc_sdp = make_idesc(128, BQ, BF16, false, false);
+      constexpr uint32_t idesc_acc = make_idesc(128, DH, BF16, false, true);
+      constexpr uint32_t idesc_dq = make_idesc(128, BQ, BF16, true, true);
+      // Descriptors are built once; steps add (byte offset >> 4) to the 14-bit start-address
+      // field, which cannot carry out of it (shared memory ends below 256 KB).
+      const uint64_t dK_k = make_sdesc(sK, 16, 1024), dV_k = make_sdesc(sV, 16, 1024);  // K-major
+      const uint64_t dQ_k = make_sdesc(sQ, 16, 1024), dO_k = make_sdesc(sDO, 16, 1024);  // K-major
+      const uint64_t dQ_mn = make_sdesc(sQ, C::Q_CHUNK, 1024), dO_mn = make_sdesc(sDO, C::Q_CHUNK, 1024);
+      const uint64_t dKT_mn = make_sdesc(sK, C::KV_CHUNK, 1024);  // K^T as the A operand of dQ^T
+      const uint64_t dDS_mn = make_sdesc(sDS, 128 * 128, 1024);   // dS^T as the B operand of dQ^T
+      bool ok = wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_KV);
+      for (int g = 0; ok && g < n_g; ++g) {
+        const int h = g / n_it, it = g % n_it;
+        if (!wait_bar(b_qfull, g & 1, p.timeout_ns, abort_flag, WB_QF)) break;
+        // a new pass overwrites the dV / dK halves: the previous pass's epilogue must have read them
+        if (g == n_it && !wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_DONE)) break;
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T  (M = 128 keys, N = 64 queries, K = d = 256)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
+          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + C::S_COL, dK_k + oa, dQ_k + ob, idesc_sdp, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
+          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + C::DP_COL, dV_k + oa, dO_k + ob, idesc_sdp, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(b_sdp);
+        if (!wait_bar(b_ds, g & 1, p.timeout_ns, abort_flag, WB_DS)) break;
+        tc_fence_after();
+        // dV[:, h] += P^T dO[:, h] ; dK[:, h] += dS^T Q[:, h]
+        //   (M = 128 keys, N = 128 = half of d, K = 64 queries; A from TMEM, B MN-major from chunks 2h, 2h+1)
+        const uint64_t half_q = static_cast<uint64_t>((2 * h * C::Q_CHUNK) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, dO_mn + half_q + ((kk * 2048) >> 4), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, dQ_mn + half_q + ((kk * 2048) >> 4), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        // dQ^T[h-half][q] = sum_k K[k][h-half] dS^T[k][q]  (M = 128 = half of d, N = 64, K = 128 keys)
+        if (g > 0 && !wait_bar(b_dqfree, (g - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE)) break;
+        tc_fence_after();
+        const uint64_t half_k = static_cast<uint64_t>((2 * h * C::KV_CHUNK) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::DQ_COL, dKT_mn + half_k + ((kk * 2048) >> 4), dDS_mn + ((kk * 2048) >> 4), idesc_dq,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(b_dqfull);
+        mma_commit(b_qempty);
+        if (it == n_it - 1) mma_commit(b_done);  // this pass's dV / dK halves are final
+      }
+      mma_commit(b_drain);
+      wait_bar(b_drain, 0, p.timeout_ns, abort_flag, WB_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ elementwise: P^T, dS^T; dV epilogue
+    const int k = threadIdx.x;  // key within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::S_COL, tDP = tmem + lane_off + C::DP_COL;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int g = 0; g < n_g; ++g) {
+      const int h = g / n_it, it = g % n_it;
+      if (ok && !__all_sync(0xffffffffu, wait_bar(b_sdp, g & 1, p.timeout_ns, abort_flag, WB_SDP))) ok = false;
+      // LSE / D of the step were landed by the producer on q_full; acquire them here too.
+      if (ok && !__all_sync(0xffffffffu, wait_bar(b_qfull, g & 1, p.timeout_ns, abort_flag, WB_QF))) ok = false;
+      if (ok) {
+        tc_fence_after();
+        const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
+        const float* dd_s = reinterpret_cast<const float*>(smem + C::OFF_DD);
+        const int q0 = (it0 + it) * BQ;  // first query of the tile
+        const bool need_mask = CAUSAL && (q0 < key0 + 127);
+        const int kq = key0 + k - q0;  // masked where column c < kq (key > query)
+        float pv[64];
+        {
+          uint32_t u0[32], u1[32];
+          tmem_ld32(tS, u0);
+          tmem_ld32(tS + 32, u1);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            pv[c] = ex2_approx(fmaf(__uint_as_float(u0[c]), sl2, -lse_s[c]));
+            pv[32 + c] = ex2_approx(fmaf(__uint_as_float(u1[c]), sl2, -lse_s[32 + c]));
+          }
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) pv[c] = (c < kq) ? 0.f : pv[c];
+        }
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = bpack2<BF16>(pv[2 * c], pv[2 * c + 1]);
+          tmem_st32(tS, pk);
+        }
+        uint32_t ds32[32];
+        {
+          uint32_t u0[32], u1[32];
+          tmem_ld32(tDP, u0);
+          tmem_ld32(tDP + 32, u1);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float a0 = pv[2 * c] * (__uint_as_float(u0[2 * c]) - dd_s[2 * c]);
+            const float a1 = pv[2 * c + 1] * (__uint_as_float(u0[2 * c + 1]) - dd_s[2 * c + 1]);
+            ds32[c] = bpack2<BF16>(a0, a1);
+            const float b0 = pv[32 + 2 * c] * (__uint_as_float(u1[2 * c]) - dd_s[32 + 2 * c]);
+            const float b1 = pv[33 + 2 * c] * (__uint_as_float(u1[2 * c + 1]) - dd_s[33 + 2 * c]);
+            ds32[16 + c] = bpack2<BF16>(b0, b1);
+          }
+        }
+        tmem_st32(tDP, ds32);
+        // dS^T row k (64 queries): one 128-byte swizzled row
+        uint8_t* row = smem + C::OFF_DS + k * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(row + ((u ^ (k & 7)) << 4)) =
+              make_uint4(ds32[4 * u], ds32[4 * u + 1], ds32[4 * u + 2], ds32[4 * u + 3]);
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_ds);
+      }
+      if (it == n_it - 1) {
+        // end of pass h: dV[:, h] (128 keys x 128) staged in the Q tile, stored with TMA
+        bool ok_e = ok && __all_sync(0xffffffffu, wait_bar(b_done, h & 1, p.timeout_ns, abort_flag, WB_DONE));
+        if (ok_e) tc_fence_after();
+        bwd_store_acc<DH, BF16>(tmem + lane_off + C::DV_COL, smem + C::OFF_Q, &p.tm_dv, row_base + key0, k, 1.0f, 1,
+                                ok_e, abort_flag, h * DH);
+        if (k == 0) {
+          tc_fence_before();
+          mbar_arrive(b_epi);
+        }
+        ok = ok_e;
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ read-out; dK epilogue
+    const int t = threadIdx.x - 128;  // TMEM lane = index within the head-dimension half
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int g = 0; g < n_g; ++g) {
+      const int h = g / n_it, it = g % n_it;
+      if (ok && !__all_sync(0xffffffffu, wait_bar(b_dqfull, g & 1, p.timeout_ns, abort_flag, WB_DQF))) ok = false;
+      if (ok) {
+        uint32_t u0[32], u1[32];
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + C::DQ_COL, u0);
+        tmem_ld32(tmem + lane_off + C::DQ_COL + 32, u1);
+        tc_fence_before();
+        mbar_arrive(b_dqfree);
+        if (*abort_flag == 0u) {
+          // dQ[q][h*128 + t] += dQ^T[t][q]: a warp covers 128 contiguous bytes per query
+          float* dst = p.dqacc + static_cast<size_t>(row_base + (it0 + it) * BQ) * D + h * DH + t;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            atomicAdd(dst + c * D, __uint_as_float(u0[c]));
+            atomicAdd(dst + (32 + c) * D, __uint_as_float(u1[c]));
+          }
+        }
+      }
+      if (it == n_it - 1) {
+        // end of pass h: dK[:, h] = scale * accumulator, staged in the dO tile
+        bool ok_e = ok && __all_sync(0xffffffffu, wait_bar(b_done, h & 1, p.timeout_ns, abort_flag, WB_DONE));
+        if (ok_e) tc_fence_after();
+        bwd_store_acc<DH, BF16>(tmem + lane_off + C::DK_COL, smem + C::OFF_DO, &p.tm_dk, row_base + key0, t, p.scale,
+                                2, ok_e, abort_flag, h * DH);
+        if (t == 0) {
+          tc_fence_before();
+          mbar_arrive(b_epi);
+        }
+        ok = ok_e;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fa

@@ -89,10 +89,11 @@ enum : uint32_t {
 };
 
 // Write one 128 x d accumulator (thread = row, TMEM lane) as dtype into a 128-byte-swizzled
-// staging tile and store it with TMA at rows [row0, row0 + 128).
+// staging tile and store it with TMA at rows [row0, row0 + 128), columns [x0, x0 + d).
 template <int D, bool BF16>
 __device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, const void* map, int row0, int r,
-                                              float mul, uint32_t bar_id, bool ok, volatile uint32_t* abort_flag) {
+                                              float mul, uint32_t bar_id, bool ok, volatile uint32_t* abort_flag,
+                                              int x0 = 0) {
   if (ok) {
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
@@ -115,7 +116,7 @@ __device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, con
   named_bar_sync(bar_id, 128);
   if (r == 0 && ok && *abort_flag == 0u) {
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) tma_store_2d(map, smem_u32(stage) + c * (128 * 128), c * 64, row0);
+    for (int c = 0; c < D / 64; ++c) tma_store_2d(map, smem_u32(stage) + c * (128 * 128), x0 + c * 64, row0);
     bulk_commit();
     bulk_wait_read0();
   }
