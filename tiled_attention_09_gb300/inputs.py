@@ -83,19 +83,25 @@ def sweep_workloads():
     return out
 
 
-def make_inputs(w: Workload):
-    """Return q, k, v, do as CPU tensors of ``w.torch_dtype``, shape [B,H,N,d]."""
+def make_inputs_fp32(w: Workload):
+    """The fp32 draws behind ``make_inputs`` (before the cast and the stress factor)."""
     rng = np.random.Generator(np.random.PCG64(w.seed))
     shape = (w.B, w.H, w.N, w.d)
-    out = []
-    for _ in range(4):  # Q, K, V, dO in this order
-        x = rng.standard_normal(shape, dtype=np.float32)
-        out.append(torch.from_numpy(x).to(w.torch_dtype))
-    q, k, v, do = out
+    return tuple(torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)) for _ in range(4))  # Q, K, V, dO
+
+
+def cast_inputs(w: Workload, fp32):
+    """``make_inputs`` from already drawn fp32 values: cast to ``w.torch_dtype`` (RNE), then stress Q and K."""
+    q, k, v, do = (x.to(w.torch_dtype) for x in fp32)
     if w.stress != 1.0:
         q = q * w.stress
         k = k * w.stress
     return q, k, v, do
+
+
+def make_inputs(w: Workload):
+    """Return q, k, v, do as CPU tensors of ``w.torch_dtype``, shape [B,H,N,d]."""
+    return cast_inputs(w, make_inputs_fp32(w))
 
 
 def sample_rows(N: int, n_random: int = 57, seed: int = 1):
