@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle's timed sample")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
+                         "instead of the headline step; one JSON line per point")
     return ap.parse_args()
 
 
@@ -431,11 +434,78 @@ def run_native(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """One JSON line per sweep point: forward and forward+backward, each timed between two events on the
+    launching stream (L2 flushed before every step), TFLOP/s, % of the measured bf16 peak, and % of the
+    attainable min(peak, HBM bandwidth x algorithmic intensity) with the algorithmic bytes per head
+    8Nd + 4N (forward) and 16Nd + 8N more (backward), at 2 bytes per element and 4 per LSE / D value."""
+    import torch
+    import tiled_attention_09_gb300 as fa
+    from tiled_attention_09_gb300.inputs import Workload, cast_inputs, make_inputs_fp32
+    peaks, peak_src = load_peaks()
+    peak, bw = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    steps, warmup = max(3, min(args.steps, 20)), max(3, args.warmup)
+    for d in (64, 128, 256):
+        for N in (512, 1024, 2048, 4096, 8192, 16384):
+            fp32 = make_inputs_fp32(Workload(2, 12, N, d, "bf16", True))
+            for dtype in ("bf16", "fp16"):
+                for causal in (True, False):
+                    w = Workload(2, 12, N, d, dtype, causal)
+                    q, k, v, do = (t.to(dev) for t in cast_inputs(w, fp32))
+                    o, lse, o_lo = fa.fwd(q, k, v, causal=causal, residual=True)
+                    ws = torch.empty(fa.workspace_size(w.B, w.H, N, d), dtype=torch.uint8, device=dev)
+                    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+                    def fwd():
+                        fa.fwd(q, k, v, causal=causal, out=o, lse=lse, residual=True, o_lo=o_lo)
+
+                    def step():
+                        fwd()
+                        fa.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws, dq=dq, dk=dk, dv=dv, o_lo=o_lo)
+
+                    times = {}
+                    for name, fn in (("fwd", fwd), ("fwd_bwd", step)):
+                        for _ in range(warmup):
+                            flush.zero_()
+                            fn()
+                        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                               for _ in range(steps)]
+                        for e0, e1 in evs:
+                            flush.zero_()
+                            e0.record()
+                            fn()
+                            e1.record()
+                        torch.cuda.synchronize()
+                        times[name] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+                    code, info = fa.device_status()
+                    if code != "FA_OK":
+                        raise RuntimeError(f"{w.name()}: {code} {info}")
+                    F = w.fwd_flops()
+                    heads = w.B * w.H
+                    bytes_fwd = heads * (4 * N * d * 2 + 4 * N)  # Q, K, V in, O out; LSE
+                    bytes_bwd = heads * (8 * N * d * 2 + 8 * N)  # Q, K, V, dO in; dQ, dK, dV out (+ O); LSE, D
+                    line = {"point": w.name(), "N": N, "d": d, "dtype": dtype, "causal": causal}
+                    for name, flops, nbytes in (("fwd", F, bytes_fwd), ("fwd_bwd", 3.5 * F, bytes_fwd + bytes_bwd)):
+                        tf = flops / times[name] / 1e12
+                        attainable = min(peak, bw * 1e9 * flops / nbytes / 1e12)
+                        line[name] = {"ms": 1e3 * times[name], "tflops": tf, "pct_of_peak": tf / peak,
+                                      "pct_of_attainable": tf / attainable}
+                    line["peak_tflops"] = peak
+                    line["peak_source"] = peak_src
+                    print(json.dumps(line), flush=True)
+                    del q, k, v, do, o, lse, o_lo, ws, dq, dk, dv
+            torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

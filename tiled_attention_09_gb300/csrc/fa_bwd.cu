@@ -20,11 +20,11 @@ int grid_for(size_t n_vec) {
 template <int VPR>
 cudaError_t launch_pre_t(const BwdArgs& a, size_t n_vec) {
   if (a.bf16)
-    return launch_pdl(fa_bwd_preprocess_kernel<VPR, true>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
+    return launch_kernel(fa_bwd_preprocess_kernel<VPR, true>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
                       static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
                       static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
                       reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
-  return launch_pdl(fa_bwd_preprocess_kernel<VPR, false>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
+  return launch_kernel(fa_bwd_preprocess_kernel<VPR, false>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
                     static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo), static_cast<const uint4*>(a.dO),
                     a.lse, a.ws_D, a.ws_lse2, reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
 }
@@ -44,9 +44,9 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a) {
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a) {
   const size_t n_vec = static_cast<size_t>(a.B) * a.H * a.N * (a.d / 8);
   if (a.bf16)
-    return launch_pdl(fa_bwd_dq_convert_kernel<true>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
+    return launch_kernel(fa_bwd_dq_convert_kernel<true>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
                       reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, n_vec);
-  return launch_pdl(fa_bwd_dq_convert_kernel<false>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
+  return launch_kernel(fa_bwd_dq_convert_kernel<false>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
                     reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, n_vec);
 }
 
@@ -72,7 +72,7 @@ cudaError_t launch_main_t(const BwdArgs& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
   dim3 grid(a.B * a.H, a.N / 128, 1);
-  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
 }
@@ -97,7 +97,7 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
   dim3 grid(a.B * a.H, a.N / 128, 1);
-  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
 }
@@ -122,7 +122,7 @@ cudaError_t launch_d256_t(const BwdArgs& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
   dim3 grid(a.B * a.H, a.N / 128, 1);
-  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
 }

@@ -53,8 +53,6 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
                                                                  const float* __restrict__ lse, float* __restrict__ D,
                                                                  float* __restrict__ lse2, float4* __restrict__ dqacc,
                                                                  size_t n_vec) {
-  pdl_trigger();
-  pdl_wait();
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
     float a[8], b[8];
@@ -85,8 +83,6 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
 template <bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __restrict__ dqacc,
                                                                 uint4* __restrict__ dq, float scale, size_t n_vec) {
-  pdl_trigger();
-  pdl_wait();
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
     const float4 x = dqacc[2 * i], y = dqacc[2 * i + 1];

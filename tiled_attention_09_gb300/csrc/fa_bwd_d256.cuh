@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
   const int n_it = N / BQ - it0;  // query steps per pass
   const int n_g = 2 * n_it;        // steps of both passes: g = h * n_it + it
 
-  pdl_trigger();
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
     mbar_init(b_qfull, 1);
@@ -107,7 +106,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // shared memory and TMEM are set up; global memory only from here on
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer

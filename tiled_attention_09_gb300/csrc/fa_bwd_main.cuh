@@ -152,7 +152,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_main_kernel(const __grid_consta
   const int it0 = CAUSAL ? (key0 / BQ) : 0;
   const int n_it = N / BQ - it0;
 
-  pdl_trigger();
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
     for (int s = 0; s < 2; ++s) {
@@ -177,7 +176,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_main_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // shared memory and TMEM are set up; global memory only from here on
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer

@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   const int row_base = bh * N;
   const int it0 = CAUSAL ? (key0 / BQ) : 0;
   const int n_it = N / BQ - it0;
-  pdl_trigger();
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
@@ -112,7 +111,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // shared memory and TMEM are set up; global memory only from here on
 
   if (warp == 12) {
     // ------------------------------------------------------------ producer

@@ -153,7 +153,8 @@ __device__ __forceinline__ uint32_t pack2_residual(float a, float b, uint32_t& r
 // where-codes for timeouts
 enum : uint32_t {
   W_Q = 1, W_RING_EMPTY = 2, W_RING_FULL = 3, W_P = 4, W_S = 5, W_O = 6, W_DRAIN = 7,
-  W_QFREE = 8, W_CLC = 9, W_ITEM = 10, W_OFREE = 11
+  W_QFREE = 8, W_CLC = 9, W_ITEM = 10, W_OFREE = 11,
+  B_CLC_ID = 20, B_OUT_ROW = 21  // where-codes for FA_DEV_BAD_INDEX
 };
 
 template <int D, bool BF16, bool CAUSAL>
@@ -186,7 +187,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
 
   const int warp = threadIdx.x >> 5;
   const int N = p.N;
-  pdl_trigger();
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -219,7 +219,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // shared memory and TMEM are set up; global memory only from here on
 
   // Work loop shared by all roles. The CTA starts with the item it was launched
   // for; the producer then takes over not-yet-launched CTAs one at a time
@@ -282,6 +281,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           clc_pending = false;
           clc_phase ^= 1u;
           if (!clc_query(clc_resp, nx, ny)) {
+            clc_live = false;
+            nx = -1;
+          } else if (nx < 0 || ny < 0 || nx >= static_cast<int>(gridDim.x) || ny >= static_cast<int>(gridDim.y)) {
+            // a taken-over CTA must be one of this grid's: anything else ends the CTA's work
+            report_status(FA_DEV_BAD_INDEX, B_CLC_ID);
             clc_live = false;
             nx = -1;
           }
@@ -504,10 +508,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         // ---------------------------------------------------------- epilogue of tile t
         ok = __all_sync(0xffffffffu, wait_bar(b_o(t), n_o & 1, p.timeout_ns, abort_flag, W_O));
         ++n_o;
+        const size_t grow = static_cast<size_t>(w.row_base) + w.q_row0 + t * 128 + r;
+        // rows exist only below B*H*N (warp-uniform: the bound is a multiple of 128 rows)
+        if (ok && !__all_sync(0xffffffffu, grow < static_cast<size_t>(gridDim.x) * N)) {
+          if ((threadIdx.x & 31) == 0) report_status(FA_DEV_BAD_INDEX, B_OUT_ROW);
+          ok = false;
+        }
         if (ok) {
           tc_fence_after();
           const float inv_l = 1.f / l;
-          const size_t grow = static_cast<size_t>(w.row_base) + w.q_row0 + t * 128 + r;
           uint4* o_row = reinterpret_cast<uint4*>(p.o + grow * D);
           uint4* lo_row = p.o_lo ? reinterpret_cast<uint4*>(p.o_lo + grow * D) : nullptr;
           constexpr int EC = D < 128 ? D : 128;  // columns per TMEM round trip
@@ -589,7 +598,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a) {
   p.rescale_threshold = 8.0f;
   p.timeout_ns = a.timeout_ns;
   dim3 grid(a.B * a.H, p.n_qblk, 1);
-  return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  return launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
 }
 
 }  // namespace

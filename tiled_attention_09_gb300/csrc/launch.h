@@ -7,23 +7,12 @@
 
 namespace fa {
 
-// Launch with programmatic stream serialization: the kernel may be scheduled
-// while the previous kernel of the stream still runs; it must execute pdl_wait
-// (griddepcontrol.wait) before touching global memory.
+// Plain stream-ordered launch, returning the launch error.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  kern<<<grid, block, smem, stream>>>(static_cast<Args&&>(args)...);
+  return cudaGetLastError();
 }
 
 struct DevStatusHost {

@@ -255,15 +255,6 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool bf16, bool 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// ------------------------------------------------------------------ programmatic dependent launch
-// The kernels of one stream form a chain: each lets the next one be scheduled
-// early (pdl_trigger at its start) and waits for the previous one to complete,
-// with its memory visible (pdl_wait), before its first global-memory access.
-// Because every kernel waits before it completes, completion is transitive
-// along the chain. Both are no-ops for a kernel launched without the attribute.
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // ------------------------------------------------------------------ register split
 // Moves registers between warpgroups: every thread of a warpgroup executes the
 // same call. An increase waits until other warpgroups' decreases have freed
