@@ -53,5 +53,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t
   }
 }
 
+
 // Host-side reader for this translation unit's status word (defined per TU).
 }  // namespace fa

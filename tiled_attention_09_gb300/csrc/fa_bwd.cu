@@ -67,6 +67,8 @@ cudaError_t launch_main_t(const BwdArgs& a) {
   p.lse2 = a.ws_lse2;
   p.Dvec = a.ws_D;
   p.dqacc = a.ws_dqacc;
+  p.dk = a.dk;
+  p.dv = a.dv;
   p.N = a.N;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -82,6 +84,13 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
   auto kern = fa_bwd_pipe_kernel<BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  static int checked = 0;  // 1: the compiled register count matches the kernel's register split
+  if (!checked) {
+    cudaFuncAttributes fa_attr;
+    if ((e = cudaFuncGetAttributes(&fa_attr, kern)) != cudaSuccess) return e;
+    if (fa_attr.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    checked = 1;
+  }
   BwdParams p;
   p.tm_q = a.tm_q;
   p.tm_k = a.tm_k;
@@ -92,6 +101,8 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
   p.lse2 = a.ws_lse2;
   p.Dvec = a.ws_D;
   p.dqacc = a.ws_dqacc;
+  p.dk = a.dk;
+  p.dv = a.dv;
   p.N = a.N;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -117,6 +128,8 @@ cudaError_t launch_d256_t(const BwdArgs& a) {
   p.lse2 = a.ws_lse2;
   p.Dvec = a.ws_D;
   p.dqacc = a.ws_dqacc;
+  p.dk = a.dk;
+  p.dv = a.dv;
   p.N = a.N;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;

@@ -37,6 +37,8 @@ struct BwdParams {
   const float* lse2;  // [B*H*N] LSE * log2(e)
   const float* Dvec;  // [B*H*N] rowsum(dO * O)
   float* dqacc;       // [B*H*N, d] fp32
+  void* dk;           // [B*H*N, d] dtype outputs, written directly by kernels that store from registers
+  void* dv;
   int N;
   float scale;
   float scale_log2;
@@ -85,7 +87,8 @@ __device__ __forceinline__ uint32_t bpack2(float lo, float hi) {
 }
 
 enum : uint32_t {
-  WB_KV = 11, WB_QE = 12, WB_QF = 13, WB_SDP = 14, WB_DS = 15, WB_DQF = 16, WB_DQFREE = 17, WB_DONE = 18, WB_DRAIN = 19
+  WB_KV = 11, WB_QE = 12, WB_QF = 13, WB_SDP = 14, WB_DS = 15, WB_DQF = 16, WB_DQFREE = 17, WB_DONE = 18, WB_DRAIN = 19,
+  WB_ITEM = 20, WB_CLC = 21
 };
 
 // Write one 128 x d accumulator (thread = row, TMEM lane) as dtype into a 128-byte-swizzled

@@ -42,27 +42,53 @@ struct BwdPipeCfg {
   static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;         // NSTAGE x BQ floats
   static constexpr int OFF_DD = OFF_LSE + NSTAGE * BQ * 4;  // NSTAGE x BQ floats
   static constexpr int OFF_BAR = OFF_DD + NSTAGE * BQ * 4;
-  // bars: kv, q_full[3], q_empty[3], sdp_full[2], ds_full[2], dq_full[2], dq_free[2], dv_done[2], done,
-  // drain[3]
-  static constexpr int NBAR = 1 + 2 * NSTAGE + 10 + 1 + 3;
-  static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
+  // bars: kv, q_full[3], q_empty[3], sdp[2], ds[2], dq_full[2], dq_free[2], dv_done[2], done, drain[3],
+  // v_free, k_free, clc, item_full[2], item_empty[2]
+  static constexpr int NBAR = 1 + 2 * NSTAGE + 10 + 1 + 3 + 2 + 1 + 4;
+  static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
+  // after the barriers: the 16-byte launch-control answer, the item queue (2 x {x, y}), TMEM slot + abort flag
+  static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES + 16 + 16 + 16;
   static constexpr int THREADS = 512;
+  // Register split: launched at LAUNCH_REGS a thread (four warps per SM sub-partition); the
+  // elementwise warpgroups then take EW_REGS from the producer / MMA warpgroup (OTHER_REGS); the
+  // read-out warpgroup keeps the launch count. The host refuses to launch unless the compiled count
+  // equals LAUNCH_REGS, so the increase always finds its registers.
+  static constexpr int LAUNCH_REGS = 128, EW_REGS = 136, OTHER_REGS = 112;
+  static_assert(128 * (2 * EW_REGS + LAUNCH_REGS + OTHER_REGS) <= THREADS * LAUNCH_REGS, "register split");
+  static constexpr int ITEM_READERS = 3 + 8 + 1;  // the MMA threads, one lane per elementwise warp, read-out thread 0
   __host__ __device__ static constexpr uint32_t BUF(int b) { return 128u * b; }
   static constexpr uint32_t DV_COL = 256, DK_COL = 384;
-  static_assert(NSTAGE * Q_TILE >= KV_TILE, "epilogue staging reuses the Q and dO stages");
   static_assert(SMEM_BYTES <= 232448, "smem budget");
+};
+
+// One work item: the 128-key block y of head x (blockIdx of the CTA launched for it; under
+// causal masking block 0 has the most query steps, so the launch order is longest-first).
+template <bool CAUSAL>
+struct BwdItem {
+  int row_base;  // row of (b, h, 0) in the [B*H*N, d] view
+  int key0;      // first key of the block
+  int it0;       // first 64-query step (causal: the block's diagonal)
+  int n_it;      // query steps
+  __device__ __forceinline__ BwdItem(int x, int y, int N) {
+    row_base = x * N;
+    key0 = y * 128;
+    it0 = CAUSAL ? (key0 / BwdPipeCfg::BQ) : 0;
+    n_it = N / BwdPipeCfg::BQ - it0;
+  }
 };
 
 template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdPipeCfg;
+  using Item = BwdItem<CAUSAL>;
   constexpr int BQ = C::BQ, D = C::D, NS = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q, sDO = s0 + C::OFF_DO;
   const uint32_t sDS = s0 + C::OFF_DS, sDQ = s0 + C::OFF_DQ;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint8_t* aux = smem + C::OFF_BAR;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(aux);
   const uint32_t b_kv = smem_u32(&bars[0]);
   auto b_qfull = [&](int s) { return smem_u32(&bars[1 + s]); };
   auto b_qempty = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
@@ -73,16 +99,19 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   auto b_dvdone = [&](int b) { return smem_u32(&bars[9 + 2 * NS + b]); };
   const uint32_t b_done = smem_u32(&bars[11 + 2 * NS]);
   auto b_drain = [&](int i) { return smem_u32(&bars[12 + 2 * NS + i]); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[C::NBAR]);
+  const uint32_t b_vfree = smem_u32(&bars[15 + 2 * NS]);
+  const uint32_t b_kfree = smem_u32(&bars[16 + 2 * NS]);
+  const uint32_t b_clc = smem_u32(&bars[17 + 2 * NS]);
+  auto b_item_full = [&](int i) { return smem_u32(&bars[18 + 2 * NS + i]); };
+  auto b_item_empty = [&](int i) { return smem_u32(&bars[20 + 2 * NS + i]); };
+  const uint32_t clc_resp = smem_u32(aux + C::BAR_BYTES);
+  volatile int* items = reinterpret_cast<volatile int*>(aux + C::BAR_BYTES + 16);  // [2][2]: x, y (x < 0: none)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + C::BAR_BYTES + 32);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile int* dq_next = reinterpret_cast<volatile int*>(tmem_slot + 2);  // read-out group's copy of {x, y}
 
   const int warp = threadIdx.x >> 5;
   const int N = p.N;
-  const int bh = blockIdx.x;
-  const int key0 = blockIdx.y * 128;
-  const int row_base = bh * N;
-  const int it0 = CAUSAL ? (key0 / BQ) : 0;
-  const int n_it = N / BQ - it0;
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
@@ -99,6 +128,13 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     }
     mbar_init(b_done, 3);
     for (int i = 0; i < 3; ++i) mbar_init(b_drain(i), 1);
+    mbar_init(b_vfree, 256);
+    mbar_init(b_kfree, 128);
+    mbar_init(b_clc, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_item_full(i), 1);
+      mbar_init(b_item_empty(i), C::ITEM_READERS);
+    }
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -112,22 +148,43 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Work loop shared by all roles (as in the forward): the CTA starts with the key block it was
+  // launched for; the producer takes over not-yet-launched CTAs (cluster launch control, asked
+  // two query steps before the end of the current block) and passes their ids through a
+  // two-entry queue; an id x < 0 ends the loop. Barrier phases run on per-role step and block
+  // counters, so nothing is re-initialised between blocks. The next block's K and V overwrite
+  // the current ones once every MMA of the current block has completed (done); its first query
+  // stages are loaded before that. dV and dK are read out of TMEM at the end of a block
+  // (v_free, k_free release the accumulators to the next block) and stored from registers.
+  // Reads the queue entry that names the block after block index `n` (the MMA threads and one
+  // lane of each elementwise / read-out warp read it; the caller has already synchronised its warp).
+  auto next_item = [&](int n, bool arrive, int& x, int& y) -> bool {
+    if (!wait_bar(b_item_full(n & 1), (n >> 1) & 1, p.timeout_ns, abort_flag, WB_ITEM)) return false;
+    x = items[2 * (n & 1)];
+    y = items[2 * (n & 1) + 1];
+    if (arrive) mbar_arrive(b_item_empty(n & 1));
+    return x >= 0;
+  };
+
+  // Each role changes its register budget (the read-out warpgroup keeps it) and ends with its own
+  // copy of the teardown barrier, so no code is shared between two budgets.
   if (warp == 12) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<C::OTHER_REGS>();
     if (elect_one()) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_do);
-      mbar_arrive_expect_tx(b_kv, 2 * C::KV_TILE);
-#pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        tma_load_2d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, row_base + key0);
-        tma_load_2d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, row_base + key0);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % NS, use = it / NS;
-        if (use > 0 && !wait_bar(b_qempty(s), (use - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) break;
-        const int qrow = row_base + (it0 + it) * BQ;
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      int ix = blockIdx.x, iy = blockIdx.y;
+      uint32_t gs = 0;  // query stages issued (all blocks)
+      int nb = 0;       // blocks whose K/V were issued
+      bool clc_live = true, clc_pending = false, ok = true;
+      uint32_t clc_phase = 0;
+      auto load_stage = [&](const Item& w, int it) -> bool {
+        const uint32_t s = gs % NS, use = gs / NS;
+        if (use > 0 && !wait_bar(b_qempty(s), (use - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) return false;
+        const int qrow = w.row_base + (w.it0 + it) * BQ;
         mbar_arrive_expect_tx(b_qfull(s), 2 * C::Q_TILE + 2 * BQ * 4);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
@@ -136,20 +193,80 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         }
         bulk_load(s0 + C::OFF_LSE + s * BQ * 4, p.lse2 + qrow, BQ * 4, b_qfull(s));
         bulk_load(s0 + C::OFF_DD + s * BQ * 4, p.Dvec + qrow, BQ * 4, b_qfull(s));
-        ++issued;
+        ++gs;
+        return true;
+      };
+      auto ask = [&]() {
+        if (!clc_live) return;
+        fence_proxy_async_smem();  // earlier generic reads of the answer slot come first
+        mbar_arrive_expect_tx(b_clc, 16);
+        clc_try_cancel(clc_resp, b_clc);
+        clc_pending = true;
+      };
+      while (ok) {
+        const Item w(ix, iy, N);
+        const int pre = w.n_it < 2 ? w.n_it : 2;  // stages issued before the block's K/V can be
+        const int ask_at = w.n_it - 2 > 0 ? w.n_it - 2 : 0;
+        int it = 0;
+        for (; ok && it < pre; ++it) ok = load_stage(w, it);
+        if (!ok) break;
+        // K and V of the previous block are dead once all of its MMAs have completed
+        if (nb > 0 && !wait_bar(b_done, (nb - 1) & 1, p.timeout_ns, abort_flag, WB_DONE)) break;
+        mbar_arrive_expect_tx(b_kv, 2 * C::KV_TILE);
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_2d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, w.row_base + w.key0);
+          tma_load_2d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, w.row_base + w.key0);
+        }
+        ++nb;
+        if (ask_at < pre) ask();
+        for (; ok && it < w.n_it; ++it) {
+          if (it == ask_at) ask();
+          ok = load_stage(w, it);
+        }
+        if (!ok) break;
+        int nx = -1, ny = 0;
+        if (clc_live) {
+          if (!wait_bar(b_clc, clc_phase, p.timeout_ns, abort_flag, WB_CLC)) break;
+          clc_pending = false;
+          clc_phase ^= 1u;
+          if (!clc_query(clc_resp, nx, ny)) {
+            clc_live = false;
+            nx = -1;
+          } else if (nx < 0 || ny < 0 || nx >= static_cast<int>(gridDim.x) || ny >= static_cast<int>(gridDim.y)) {
+            report_status(FA_DEV_BAD_INDEX, WB_CLC);  // a taken-over CTA must be one of this grid's
+            clc_live = false;
+            nx = -1;
+          }
+        }
+        const int qi = nb - 1;  // queue entry qi names the block after block qi
+        if (qi >= 2 && !wait_bar(b_item_empty(qi & 1), ((qi >> 1) - 1) & 1, p.timeout_ns, abort_flag, WB_ITEM))
+          break;
+        items[2 * (qi & 1)] = nx;
+        items[2 * (qi & 1) + 1] = ny;
+        mbar_arrive(b_item_full(qi & 1));  // release: readers acquire through their wait
+        if (nx < 0) break;
+        ix = nx;
+        iy = ny;
       }
-      wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_DRAIN);
-      for (int it = (issued > NS ? issued - NS : 0); it < issued; ++it)
-        wait_bar(b_qfull(it % NS), (it / NS) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
+      // Drain: every issued copy has landed before the CTA may exit.
+      if (clc_pending) wait_bar(b_clc, clc_phase, p.timeout_ns, abort_flag, WB_DRAIN);
+      if (nb > 0) wait_bar(b_kv, (nb - 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
+      for (uint32_t g = (gs > NS ? gs - NS : 0u); g < gs; ++g)
+        wait_bar(b_qfull(g % NS), (g / NS) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
+    tc_fence_before();
+    __syncthreads();
   } else if (warp >= 13) {
     // ------------------------------------------------------------ MMA issuers
     // One thread issues a tcgen05.mma only every ~100+ cycles, so the step's 32 MMAs are spread
     // over three warps: A = S^T and dV, B = dP^T and dK, C = dQ^T. A's and B's accumulators are
     // disjoint; C writes dQ^T over the S^T/P^T columns of the step, so it first waits for dV
     // (issuer A) to have read P^T there (dv_done). A only re-fills a buffer after warps 8-11 have
-    // read the dQ^T that C left in it (dq_free).
+    // read the dQ^T that C left in it (dq_free). The first dV / dK MMA of a block overwrites the
+    // accumulator, so it waits until the previous block's epilogue has read it (v_free / k_free).
+    setmaxnreg_dec<C::OTHER_REGS>();
     const int role = warp - 13;
     if (elect_one()) {
       constexpr uint32_t idesc_sdp = make_idesc(128, BQ, BF16, false, false);
@@ -164,193 +281,295 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       const uint64_t dDS_mn = make_sdesc(sDS, 128 * 128, 1024);                    // C: dS^T (MN-major)
       const uint32_t col = role == 0 ? 0u : 64u;  // A: S^T / P^T half of a buffer, B: dP^T / dS^T half
       const uint32_t acc_col = role == 0 ? C::DV_COL : C::DK_COL;
-      // A: S^T(i) = K_j Q_i^T ; B: dP^T(i) = V_j dO_i^T  (M = 128 keys, N = 64, K = d) into buffer i & 1
-      auto issue_score = [&](int it) {
-        const uint64_t so = static_cast<uint64_t>((it % NS) * C::Q_TILE) >> 4;
-        const uint32_t tb = tmem + C::BUF(it & 1) + col;
+      // A: S^T(g) = K Q_g^T ; B: dP^T(g) = V dO_g^T  (M = 128 keys, N = 64, K = d) into buffer g & 1,
+      // g counting query steps over all blocks
+      auto issue_score = [&](uint32_t g) {
+        const uint64_t so = static_cast<uint64_t>((g % NS) * C::Q_TILE) >> 4;
+        const uint32_t tb = tmem + C::BUF(g & 1) + col;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t oa = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
           const uint64_t ob = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
           mma_ss(tb, dKV_k + oa, dQO_k + so + ob, idesc_sdp, kk > 0 ? 1u : 0u);
         }
-        mma_commit(b_sdp(it & 1));
+        mma_commit(b_sdp(g & 1));
       };
+      // A: the buffer of step g still holds dQ^T(g - 2) until warps 8-11 have read it out
+      auto score_ready = [&](uint32_t g) -> bool {
+        if (!wait_bar(b_qfull(g % NS), (g / NS) & 1, p.timeout_ns, abort_flag, WB_QF)) return false;
+        if (role == 0 && g >= 2 &&
+            !wait_bar(b_dqfree(g & 1), ((g >> 1) - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE))
+          return false;
+        return true;
+      };
+      int ix = blockIdx.x, iy = blockIdx.y;
+      uint32_t gs = 0;  // query steps of the finished blocks
+      int nb = 0;       // finished blocks
       bool ok = true;
-      if (role < 2) {
-        ok = wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_KV) &&
-             wait_bar(b_qfull(0), 0, p.timeout_ns, abort_flag, WB_QF);
-        if (ok) {
+      while (ok) {
+        const Item w(ix, iy, N);
+        if (!wait_bar(b_kv, nb & 1, p.timeout_ns, abort_flag, WB_KV)) break;
+        if (role < 2) {
+          if (!score_ready(gs)) break;
           tc_fence_after();
-          issue_score(0);
-        }
-        for (int it = 0; ok && it < n_it; ++it) {
-          const int b = it & 1;
-          if (it + 1 < n_it) {
-            const int nx = it + 1, u1 = nx >> 1;
-            if (!wait_bar(b_qfull(nx % NS), (nx / NS) & 1, p.timeout_ns, abort_flag, WB_QF)) break;
-            // A: buffer nx & 1 still holds dQ^T(it - 1) until warps 8-11 have read it out
-            if (role == 0 && u1 >= 1 &&
-                !wait_bar(b_dqfree(nx & 1), (u1 - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE))
+          issue_score(gs);
+          for (int it = 0; ok && it < w.n_it; ++it) {
+            const uint32_t g = gs + it, b = g & 1;
+            if (it + 1 < w.n_it) {  // the next step's scores go to the other buffer first
+              if (!score_ready(g + 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_score(g + 1);
+            }
+            if (!wait_bar(b_ds(b), (g >> 1) & 1, p.timeout_ns, abort_flag, WB_DS) ||
+                (it == 0 && nb > 0 &&
+                 !wait_bar(role == 0 ? b_vfree : b_kfree, (nb - 1) & 1, p.timeout_ns, abort_flag, WB_DONE))) {
+              ok = false;
               break;
+            }
             tc_fence_after();
-            issue_score(nx);
+            const int s = g % NS;
+            const uint64_t so = static_cast<uint64_t>(s * C::Q_TILE) >> 4;
+            const uint32_t tb = tmem + C::BUF(b) + col;
+            const uint32_t acc0 = it > 0 ? 1u : 0u;
+            // A: dV += P^T dO_g ; B: dK += dS^T Q_g  (M = 128 keys, N = d, K = 64; A from TMEM, B MN-major).
+            // Packed P^T / dS^T of queries 16kk .. 16kk+15 sit at column (kk / 2) * 32 + (kk % 2) * 8.
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)
+              mma_ts(tmem + acc_col, tb + (kk >> 1) * 32 + (kk & 1) * 8, dOQ_mn + so + ((kk * 2048) >> 4),
+                     idesc_acc, kk > 0 ? 1u : acc0);
+            mma_commit(b_qempty(s));
+            if (role == 0) mma_commit(b_dvdone(b));
           }
-          if (!wait_bar(b_ds(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
-          tc_fence_after();
-          const int s = it % NS;
-          const uint64_t so = static_cast<uint64_t>(s * C::Q_TILE) >> 4;
-          const uint32_t tb = tmem + C::BUF(b) + col;
-          const uint32_t acc0 = it > 0 ? 1u : 0u;
-          // A: dV += P^T dO_i ; B: dK += dS^T Q_i  (M = 128 keys, N = d, K = 64; A from TMEM, B MN-major).
-          // Packed P^T / dS^T of queries 16kk .. 16kk+15 sit at column (kk / 2) * 32 + (kk % 2) * 8.
+        } else {
+          // C: dQ^T(g) = K^T dS^T(g) over S^T(g)'s columns (M = d, N = 64 queries, K = 128 keys)
+          for (int it = 0; ok && it < w.n_it; ++it) {
+            const uint32_t g = gs + it, b = g & 1;
+            if (!wait_bar(b_ds(b), (g >> 1) & 1, p.timeout_ns, abort_flag, WB_DS) ||
+                !wait_bar(b_dvdone(b), (g >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t tb = tmem + C::BUF(b);
+            const uint64_t bo = static_cast<uint64_t>(b * C::DS_TILE) >> 4;
 #pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tmem + acc_col, tb + (kk >> 1) * 32 + (kk & 1) * 8, dOQ_mn + so + ((kk * 2048) >> 4), idesc_acc,
-                   kk > 0 ? 1u : acc0);
-          mma_commit(b_qempty(s));
-          if (role == 0) mma_commit(b_dvdone(b));
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tb, dK_mn + ((kk * 2048) >> 4), dDS_mn + bo + ((kk * 2048) >> 4), idesc_dq, kk > 0 ? 1u : 0u);
+            mma_commit(b_dqfull(b));
+          }
         }
-      } else {
-        // C: dQ^T(i) = K_j^T dS^T(i) over S^T(i)'s columns (M = d, N = 64 queries, K = 128 keys)
-        for (int it = 0; ok && it < n_it; ++it) {
-          const int b = it & 1;
-          if (!wait_bar(b_ds(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
-          if (!wait_bar(b_dvdone(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) break;
-          tc_fence_after();
-          const uint32_t tb = tmem + C::BUF(b);
-          const uint64_t bo = static_cast<uint64_t>(b * C::DS_TILE) >> 4;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tb, dK_mn + ((kk * 2048) >> 4), dDS_mn + bo + ((kk * 2048) >> 4), idesc_dq, kk > 0 ? 1u : 0u);
-          mma_commit(b_dqfull(b));
-        }
+        if (!ok) break;
+        mma_commit(b_done);  // once these MMAs complete, dV / dK are final and K / V may be replaced
+        gs += w.n_it;
+        ok = next_item(nb++, true, ix, iy);
       }
-      mma_commit(b_done);
       mma_commit(b_drain(role));
       wait_bar(b_drain(role), 0, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
+    tc_fence_before();
+    __syncthreads();  // every role is done with TMEM
+    if (warp == 13) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
   } else if (warp < 8) {
-    // ------------------------------------------------------------ elementwise: P^T, dS^T
-    const int g = warp >> 2;        // column group: queries 32g .. 32g+31 of the tile
+    // ------------------------------------------------------------ elementwise: P^T, dS^T; dV epilogue
+    setmaxnreg_inc<C::EW_REGS>();
+    const int g = warp >> 2;          // column group: queries 32g .. 32g+31 of the tile
     const int k = threadIdx.x & 127;  // key within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
+    int ix = blockIdx.x, iy = blockIdx.y;
+    uint32_t gs = 0;
+    int nb = 0;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int b = it & 1, s = it % NS;
-      if (!__all_sync(0xffffffffu, wait_bar(b_sdp(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_SDP))) {
-        ok = false;
-        break;
-      }
-      // LSE/D of this stage were landed by the producer on q_full[s]; acquire them here too.
-      if (!__all_sync(0xffffffffu, wait_bar(b_qfull(s), (it / NS) & 1, p.timeout_ns, abort_flag, WB_QF))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tS = tmem + lane_off + C::BUF(b), tDP = tS + 64;
-      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE + s * BQ * 4) + 8 * g;
-      const float4* dd4 = reinterpret_cast<const float4*>(smem + C::OFF_DD + s * BQ * 4) + 8 * g;
-      const int q0 = (it0 + it) * BQ + 32 * g;  // first query of this group's columns
-      const bool need_mask = CAUSAL && (q0 < key0 + 127);
-      const int kq = key0 + k - q0;  // masked where column c < kq (key > query)
-      uint32_t u[32], w[32];
-      tmem_ld32_pair(tS + 32 * g, tDP + 32 * g, u, w);  // S^T and dP^T columns in one round trip
-      float pv[32];
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l = lse4[c4];
-        pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 0]), sl2, -l.x));
-        pv[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 1]), sl2, -l.y));
-        pv[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 2]), sl2, -l.z));
-        pv[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 3]), sl2, -l.w));
-      }
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c] = (c < kq) ? 0.f : pv[c];
-      }
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = bpack2<BF16>(pv[2 * c], pv[2 * c + 1]);
-      // Each group packs into the first half of its own 32 columns, never into columns the other
-      // group may still be reading: queries 32g + 2c, 2c+1 go to column 32g + c.
-      tmem_st16(tS + 32 * g, pk);
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 dd = dd4[c4];
-        pk[2 * c4] = bpack2<BF16>(pv[4 * c4] * (__uint_as_float(w[4 * c4]) - dd.x),
-                                  pv[4 * c4 + 1] * (__uint_as_float(w[4 * c4 + 1]) - dd.y));
-        pk[2 * c4 + 1] = bpack2<BF16>(pv[4 * c4 + 2] * (__uint_as_float(w[4 * c4 + 2]) - dd.z),
-                                      pv[4 * c4 + 3] * (__uint_as_float(w[4 * c4 + 3]) - dd.w));
-      }
-      tmem_st16(tDP + 32 * g, pk);
-      // dS^T row k, queries 32g .. 32g+31: 16-byte units 4g .. 4g+3 of the 128-byte swizzled row
-      uint8_t* row = smem + C::OFF_DS + b * C::DS_TILE + k * 128;
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4)
-        *reinterpret_cast<uint4*>(row + (((4 * g + u4) ^ (k & 7)) << 4)) =
-            make_uint4(pk[4 * u4], pk[4 * u4 + 1], pk[4 * u4 + 2], pk[4 * u4 + 3]);
-      fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(b_ds(b));
-    }
-    if (g == 0) {
-      if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_done, 0, p.timeout_ns, abort_flag, WB_DONE));
-      if (ok) tc_fence_after();
-      bwd_store_acc<D, BF16>(tmem + lane_off + C::DV_COL, smem + C::OFF_Q, &p.tm_dv, row_base + key0, k, 1.0f, 1, ok,
-                             abort_flag);
-    }
-  } else if (warp < 12) {
-    // ------------------------------------------------------------ dQ read-out, then dK epilogue
-    const int t = threadIdx.x - 256;  // TMEM lane = d index of dQ^T
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    bool ok = true;
-    // Every warp runs all n_it steps and both named barriers of each step, even after an
-    // abort (waits then return at once), so no warp of this group can be left at a barrier.
-    for (int it = 0; it < n_it; ++it) {
-      const int b = it & 1;
-      ok = ok && __all_sync(0xffffffffu, wait_bar(b_dqfull(b), (it >> 1) & 1, p.timeout_ns, abort_flag, WB_DQF));
-      uint32_t u0[32], u1[32];
-      if (ok) {
+    while (ok) {
+      const Item w(ix, iy, N);
+      for (int it = 0; it < w.n_it; ++it) {
+        const uint32_t gq = gs + it, b = gq & 1, s = gq % NS;
+        if (!__all_sync(0xffffffffu, wait_bar(b_sdp(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_SDP))) {
+          ok = false;
+          break;
+        }
+        // LSE/D of this stage were landed by the producer on q_full[s]; acquire them here too.
+        if (!__all_sync(0xffffffffu, wait_bar(b_qfull(s), (gq / NS) & 1, p.timeout_ns, abort_flag, WB_QF))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        tmem_ld32_pair(tmem + lane_off + C::BUF(b), tmem + lane_off + C::BUF(b) + 32, u0, u1);
+        const uint32_t tS = tmem + lane_off + C::BUF(b), tDP = tS + 64;
+        const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE + s * BQ * 4) + 8 * g;
+        const float4* dd4 = reinterpret_cast<const float4*>(smem + C::OFF_DD + s * BQ * 4) + 8 * g;
+        const int q0 = (w.it0 + it) * BQ + 32 * g;  // first query of this group's columns
+        const bool need_mask = CAUSAL && (q0 < w.key0 + 127);
+        const int kq = w.key0 + k - q0;  // masked where column c < kq (key > query)
+        uint32_t u[32], v[32];
+        tmem_ld32_pair(tS + 32 * g, tDP + 32 * g, u, v);  // S^T and dP^T columns in one round trip
+        float pv[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l = lse4[c4];
+          pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 0]), sl2, -l.x));
+          pv[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 1]), sl2, -l.y));
+          pv[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 2]), sl2, -l.z));
+          pv[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 3]), sl2, -l.w));
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pv[c] = (c < kq) ? 0.f : pv[c];
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = bpack2<BF16>(pv[2 * c], pv[2 * c + 1]);
+        // Each group packs into the first half of its own 32 columns, never into columns the other
+        // group may still be reading: queries 32g + 2c, 2c+1 go to column 32g + c.
+        tmem_st16(tS + 32 * g, pk);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dd = dd4[c4];
+          pk[2 * c4] = bpack2<BF16>(pv[4 * c4] * (__uint_as_float(v[4 * c4]) - dd.x),
+                                    pv[4 * c4 + 1] * (__uint_as_float(v[4 * c4 + 1]) - dd.y));
+          pk[2 * c4 + 1] = bpack2<BF16>(pv[4 * c4 + 2] * (__uint_as_float(v[4 * c4 + 2]) - dd.z),
+                                        pv[4 * c4 + 3] * (__uint_as_float(v[4 * c4 + 3]) - dd.w));
+        }
+        tmem_st16(tDP + 32 * g, pk);
+        // dS^T row k, queries 32g .. 32g+31: 16-byte units 4g .. 4g+3 of the 128-byte swizzled row
+        uint8_t* row = smem + C::OFF_DS + b * C::DS_TILE + k * 128;
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4)
+          *reinterpret_cast<uint4*>(row + (((4 * g + u4) ^ (k & 7)) << 4)) =
+              make_uint4(pk[4 * u4], pk[4 * u4 + 1], pk[4 * u4 + 2], pk[4 * u4 + 3]);
+        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b_dqfree(b));
-      } else {
+        mbar_arrive(b_ds(b));
+      }
+      if (!ok) break;
+      gs += w.n_it;
+      // ---------------------------------------------------------- dV epilogue: group g, columns 64g ..
+      if (!__all_sync(0xffffffffu, wait_bar(b_done, nb & 1, p.timeout_ns, abort_flag, WB_DONE))) break;
+      tc_fence_after();
+      {
+        uint32_t a[64];
+        tmem_ld64(tmem + lane_off + C::DV_COL + 64 * g, a);
+        tc_fence_before();
+        mbar_arrive(b_vfree);  // the next block's first dV MMA may overwrite the accumulator
+        uint4* dst = reinterpret_cast<uint4*>(
+            reinterpret_cast<uint16_t*>(p.dv) + (static_cast<size_t>(w.row_base) + w.key0 + k) * D + 64 * g);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) u0[c] = u1[c] = 0u;
+        for (int u8 = 0; u8 < 8; ++u8)
+          dst[u8] = make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]), __uint_as_float(a[8 * u8 + 1])),
+                               bpack2<BF16>(__uint_as_float(a[8 * u8 + 2]), __uint_as_float(a[8 * u8 + 3])),
+                               bpack2<BF16>(__uint_as_float(a[8 * u8 + 4]), __uint_as_float(a[8 * u8 + 5])),
+                               bpack2<BF16>(__uint_as_float(a[8 * u8 + 6]), __uint_as_float(a[8 * u8 + 7])));
       }
-      // the single staging buffer is free once the previous reduce has read it
-      if (t == 0) bulk_wait_read0();
-      named_bar_sync(2, 128);
-      float* st = reinterpret_cast<float*>(smem + C::OFF_DQ);
+      int nx = -1, ny = 0;
+      bool more = false;
+      if ((threadIdx.x & 31) == 0) more = next_item(nb, true, nx, ny);
+      more = __shfl_sync(0xffffffffu, more, 0);
+      nx = __shfl_sync(0xffffffffu, nx, 0);
+      ny = __shfl_sync(0xffffffffu, ny, 0);
+      ++nb;
+      if (!more) break;
+      ix = nx;
+      iy = ny;
+    }
+    tc_fence_before();
+    __syncthreads();
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ dQ read-out; dK epilogue
+    // The four warps of this group share the staging buffer through named barrier 2, so their
+    // control flow stays uniform: each of the group's barriers also ANDs every thread's "no
+    // timeout" flag (bar.red.and), and thread 0 reads the item queue for the whole group.
+    const int t = threadIdx.x - 256;  // TMEM lane = d index of dQ^T, key of dK
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int ix = blockIdx.x, iy = blockIdx.y;
+    uint32_t gs = 0;
+    int nb = 0;
+    bool ok = true;
+    while (ok) {
+      const Item w(ix, iy, N);
+      for (int it = 0; it < w.n_it; ++it) {
+        const uint32_t gq = gs + it, b = gq & 1;
+        const bool full =
+            __all_sync(0xffffffffu, wait_bar(b_dqfull(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_DQF));
+        uint32_t u0[32], u1[32];
+        if (full) {
+          tc_fence_after();
+          tmem_ld32_pair(tmem + lane_off + C::BUF(b), tmem + lane_off + C::BUF(b) + 32, u0, u1);
+          tc_fence_before();
+          mbar_arrive(b_dqfree(b));
+        } else {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {  // lane t = d index; column c = query
-        st[c * D + t] = __uint_as_float(u0[c]);
-        st[(32 + c) * D + t] = __uint_as_float(u1[c]);
+          for (int c = 0; c < 32; ++c) u0[c] = u1[c] = 0u;
+        }
+        // the single staging buffer is free once the previous reduction has read it
+        if (t == 0) bulk_wait_read0();
+        if (!named_bar_and(2, 128, full && *abort_flag == 0u)) {
+          ok = false;
+          break;
+        }
+        float* st = reinterpret_cast<float*>(smem + C::OFF_DQ);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {  // lane t = d index; column c = query
+          st[c * D + t] = __uint_as_float(u0[c]);
+          st[(32 + c) * D + t] = __uint_as_float(u1[c]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (t == 0) {
+          bulk_reduce_add_f32(p.dqacc + static_cast<size_t>(w.row_base + (w.it0 + it) * BQ) * D, sDQ,
+                              C::DQ_STAGE);
+          bulk_commit();
+        }
       }
-      fence_proxy_async_smem();
+      if (!ok) break;
+      gs += w.n_it;
+      // ---------------------------------------------------------- dK epilogue: dK = scale * accumulator
+      const bool done = __all_sync(0xffffffffu, wait_bar(b_done, nb & 1, p.timeout_ns, abort_flag, WB_DONE));
+      if (!named_bar_and(2, 128, done)) break;
+      tc_fence_after();
+      {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dk) +
+                                              (static_cast<size_t>(w.row_base) + w.key0 + t) * D);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[64];
+          tmem_ld64(tmem + lane_off + C::DK_COL + 64 * h, a);
+          if (h == 1) {
+            tc_fence_before();
+            mbar_arrive(b_kfree);  // the next block's first dK MMA may overwrite the accumulator
+          }
+          const float sc = p.scale;
+#pragma unroll
+          for (int u8 = 0; u8 < 8; ++u8)
+            dst[8 * h + u8] =
+                make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]) * sc, __uint_as_float(a[8 * u8 + 1]) * sc),
+                           bpack2<BF16>(__uint_as_float(a[8 * u8 + 2]) * sc, __uint_as_float(a[8 * u8 + 3]) * sc),
+                           bpack2<BF16>(__uint_as_float(a[8 * u8 + 4]) * sc, __uint_as_float(a[8 * u8 + 5]) * sc),
+                           bpack2<BF16>(__uint_as_float(a[8 * u8 + 6]) * sc, __uint_as_float(a[8 * u8 + 7]) * sc));
+        }
+      }
+      if (t == 0) {
+        int nx = -1, ny = 0;
+        const bool more = next_item(nb, true, nx, ny);
+        dq_next[0] = more ? nx : -1;
+        dq_next[1] = ny;
+      }
       named_bar_sync(2, 128);
-      if (t == 0 && ok && *abort_flag == 0u) {
-        bulk_reduce_add_f32(p.dqacc + static_cast<size_t>(row_base + (it0 + it) * BQ) * D, sDQ, C::DQ_STAGE);
-        bulk_commit();
-      }
+      ix = dq_next[0];
+      iy = dq_next[1];
+      ++nb;
+      if (ix < 0) break;
+      named_bar_sync(2, 128);  // every thread has read dq_next before thread 0 writes it again
     }
     if (t == 0) bulk_wait0();
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_done, 0, p.timeout_ns, abort_flag, WB_DONE));
-    if (ok) tc_fence_after();
-    bwd_store_acc<D, BF16>(tmem + lane_off + C::DK_COL, smem + C::OFF_DO, &p.tm_dk, row_base + key0, t, p.scale, 3,
-                           ok, abort_flag);
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 13) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tc_fence_before();
+    __syncthreads();
   }
 }
 
