@@ -52,36 +52,9 @@ cudaError_t launch_bwd_dq_convert(const BwdArgs& a) {
 
 namespace {
 template <int D, bool BF16, bool CAUSAL>
-cudaError_t launch_main_t(const BwdArgs& a) {
-  using C = BwdCfg<D>;
-  auto kern = fa_bwd_main_kernel<D, BF16, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  BwdParams p;
-  p.tm_q = a.tm_q;
-  p.tm_k = a.tm_k;
-  p.tm_v = a.tm_v;
-  p.tm_do = a.tm_do;
-  p.tm_dk = a.tm_dk;
-  p.tm_dv = a.tm_dv;
-  p.lse2 = a.ws_lse2;
-  p.Dvec = a.ws_D;
-  p.dqacc = a.ws_dqacc;
-  p.dk = a.dk;
-  p.dv = a.dv;
-  p.N = a.N;
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.timeout_ns = a.timeout_ns;
-  dim3 grid(a.B * a.H, a.N / 128, 1);
-  e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
-  if (e != cudaSuccess || a.dq == nullptr) return e;
-  return launch_bwd_dq_convert(a);
-}
-template <bool BF16, bool CAUSAL>
 cudaError_t launch_pipe_t(const BwdArgs& a) {
-  using C = BwdPipeCfg;
-  auto kern = fa_bwd_pipe_kernel<BF16, CAUSAL>;
+  using C = BwdPipeCfg<D>;
+  auto kern = fa_bwd_pipe_kernel<D, BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   static int checked = 0;  // 1: the compiled register count matches the kernel's register split
@@ -146,17 +119,14 @@ cudaError_t launch_bwd_main(const BwdArgs& a) {
     if (a.bf16) return a.causal ? launch_d256_t<true, true>(a) : launch_d256_t<true, false>(a);
     return a.causal ? launch_d256_t<false, true>(a) : launch_d256_t<false, false>(a);
   }
-  if (a.d == 128) {  // software-pipelined kernel
-    if (a.bf16) return a.causal ? launch_pipe_t<true, true>(a) : launch_pipe_t<true, false>(a);
-    return a.causal ? launch_pipe_t<false, true>(a) : launch_pipe_t<false, false>(a);
+  if (a.d == 128) {  // software-pipelined, persistent kernel
+    if (a.bf16) return a.causal ? launch_pipe_t<128, true, true>(a) : launch_pipe_t<128, true, false>(a);
+    return a.causal ? launch_pipe_t<128, false, true>(a) : launch_pipe_t<128, false, false>(a);
   }
-#define FA_BWD_CASE(D_)                                                                                   \
-  if (a.d == D_) {                                                                                        \
-    if (a.bf16) return a.causal ? launch_main_t<D_, true, true>(a) : launch_main_t<D_, true, false>(a);   \
-    return a.causal ? launch_main_t<D_, false, true>(a) : launch_main_t<D_, false, false>(a);             \
+  if (a.d == 64) {  // the same kernel, K^T zero-padded to 128 rows for dQ^T
+    if (a.bf16) return a.causal ? launch_pipe_t<64, true, true>(a) : launch_pipe_t<64, true, false>(a);
+    return a.causal ? launch_pipe_t<64, false, true>(a) : launch_pipe_t<64, false, false>(a);
   }
-  FA_BWD_CASE(64)
-#undef FA_BWD_CASE
   return cudaErrorNotSupported;
 }
 

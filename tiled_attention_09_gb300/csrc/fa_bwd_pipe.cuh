@@ -1,10 +1,13 @@
-// Attention backward main kernel, software-pipelined variant for d = 128 (K3).
+// Attention backward main kernel for d = 64 and 128 (K3), software-pipelined.
 //
-// Same method and per-step arithmetic as fa_bwd_main_kernel (page
-// "transformer模型详解（十）：FlashAttention优化技术", section "Re-computation 而非缓存":
-// outer loop over K/V column blocks, inner loop over Q row blocks, P rebuilt from
-// the saved LSE). What changes is the schedule, so that the tensor core never
-// waits for the elementwise warps:
+// Method (page "transformer模型详解（十）：FlashAttention优化技术", section
+// "Re-computation 而非缓存"): outer loop over K/V column blocks, inner loop over Q
+// row blocks, P rebuilt from the saved LSE: P = exp(scale * S - LSE),
+// dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P * (dP - D_i), dK_j += scale * dS^T Q_i,
+// dQ_i += scale * dS K_j. Keys are the MMA's M dimension, so S and dP are
+// produced transposed with one key per TMEM lane, and P^T / dS^T feed dV and dK
+// straight from TMEM. The schedule keeps the tensor core from waiting for the
+// elementwise warps:
 //   * S^T and dP^T of query tile i go to one of two TMEM buffers (i & 1);
 //   * S^T(i+1), dP^T(i+1) are issued into the other buffer *before* the
 //     issuers wait for P^T(i), dS^T(i), so the tensor core computes the next
@@ -12,10 +15,13 @@
 //   * dQ^T(i) = K^T dS^T(i) is written over S^T(i)'s columns once dV(i) has
 //     read P^T(i) from them, and read out before S^T(i+2) reuses the buffer;
 //   * dS^T goes to a double-buffered shared-memory tile (the dQ operand), and
-//     Q, dO, LSE*log2e, D stream through a three-stage TMA ring.
+//     Q, dO, LSE*log2e, D stream through a three-stage TMA ring;
+//   * for d = 64, dQ^T = K^T dS^T still has M = 128: a zeroed chunk after K
+//     pads K^T with 64 zero rows, whose dQ^T lanes are never read.
 // TMEM (512 columns): buffer b at 128b holds S^T/P^T (cols 0-63, then dQ^T)
-// and dP^T/dS^T (cols 64-127); dV at 256, dK at 384. Packed 16-bit P^T of
-// queries 32g..32g+31 sits in columns 32g..32g+15 (dS^T likewise from 64).
+// and dP^T/dS^T (cols 64-127); dV at 256, dK at 384 (d columns each). Packed
+// 16-bit P^T of queries 32g..32g+31 sits in columns 32g..32g+15 (dS^T likewise
+// from 64).
 // Roles (16 warps, 4 per SM sub-partition): warps 0-7 elementwise, in two
 // groups that each own 32 of the tile's 64 query columns; warps 8-11 dQ
 // read-out and the dK epilogue; warp 12 TMA producer; warps 13-15 MMA issuers
@@ -25,16 +31,20 @@
 
 namespace fa {
 
+template <int D_>
 struct BwdPipeCfg {
-  static constexpr int D = 128, BK = 128, BQ = 64, NCH = 2, NSTAGE = 3;
-  static constexpr int KV_CHUNK = BK * 128;  // 16 KB: 128 rows x 128 bytes
-  static constexpr int KV_TILE = BK * D * 2;  // 32 KB
+  static constexpr int D = D_, BK = 128, BQ = 64, NCH = D / 64, NSTAGE = 3;
+  static constexpr int KV_CHUNK = BK * 128;   // 16 KB: 128 rows x 128 bytes (64 elements)
+  static constexpr int KV_TILE = BK * D * 2;  // 32 KB (d = 128), 16 KB (d = 64)
+  // dQ^T = K^T dS^T needs M = 128 rows of K^T: for d = 64 a zeroed chunk follows K, so the MMA
+  // sees K^T padded with 64 zero rows (those dQ^T lanes are never read)
+  static constexpr int K_REGION = (D < 128 ? 2 : NCH) * KV_CHUNK;
   static constexpr int Q_CHUNK = BQ * 128;    // 8 KB
-  static constexpr int Q_TILE = BQ * D * 2;   // 16 KB
+  static constexpr int Q_TILE = BQ * D * 2;   // 16 KB (d = 128), 8 KB (d = 64)
   static constexpr int DS_TILE = BK * BQ * 2;  // 16 KB: dS^T [128 keys][64 queries]
-  static constexpr int DQ_STAGE = BQ * D * 4;  // 32 KB fp32 [64 queries][128]
+  static constexpr int DQ_STAGE = BQ * D * 4;  // fp32 [64 queries][d]
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + KV_TILE;
+  static constexpr int OFF_V = OFF_K + K_REGION;
   static constexpr int OFF_Q = OFF_V + KV_TILE;             // NSTAGE stages
   static constexpr int OFF_DO = OFF_Q + NSTAGE * Q_TILE;    // NSTAGE stages
   static constexpr int OFF_DS = OFF_DO + NSTAGE * Q_TILE;   // 2 buffers
@@ -57,7 +67,8 @@ struct BwdPipeCfg {
   static_assert(128 * (2 * EW_REGS + LAUNCH_REGS + OTHER_REGS) <= THREADS * LAUNCH_REGS, "register split");
   static constexpr int ITEM_READERS = 3 + 8 + 1;  // the MMA threads, one lane per elementwise warp, read-out thread 0
   __host__ __device__ static constexpr uint32_t BUF(int b) { return 128u * b; }
-  static constexpr uint32_t DV_COL = 256, DK_COL = 384;
+  static constexpr uint32_t DV_COL = 256, DK_COL = 256 + (D < 128 ? 128 : D);
+  static_assert(D == 64 || D == 128, "d = 64 or 128");
   static_assert(SMEM_BYTES <= 232448, "smem budget");
 };
 
@@ -72,14 +83,14 @@ struct BwdItem {
   __device__ __forceinline__ BwdItem(int x, int y, int N) {
     row_base = x * N;
     key0 = y * 128;
-    it0 = CAUSAL ? (key0 / BwdPipeCfg::BQ) : 0;
-    n_it = N / BwdPipeCfg::BQ - it0;
+    it0 = CAUSAL ? (key0 / 64) : 0;  // 64-query steps
+    n_it = N / 64 - it0;
   }
 };
 
-template <bool BF16, bool CAUSAL>
+template <int D_, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_constant__ BwdParams p) {
-  using C = BwdPipeCfg;
+  using C = BwdPipeCfg<D_>;
   using Item = BwdItem<CAUSAL>;
   constexpr int BQ = C::BQ, D = C::D, NS = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
@@ -142,6 +153,12 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
+  }
+  if constexpr (D < 128) {
+    // the zero rows that pad K^T to M = 128 for dQ^T; never overwritten
+    uint4* z = reinterpret_cast<uint4*>(smem + C::OFF_K + C::KV_CHUNK);
+    for (int i = threadIdx.x; i < C::KV_CHUNK / 16; i += C::THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // visible to the tensor core (async proxy)
   }
   tc_fence_before();
   __syncthreads();
@@ -450,18 +467,22 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       }
       if (!ok) break;
       gs += w.n_it;
-      // ---------------------------------------------------------- dV epilogue: group g, columns 64g ..
+      // ---------------------------------------------------------- dV epilogue: group g, columns g*D/2 ..
       if (!__all_sync(0xffffffffu, wait_bar(b_done, nb & 1, p.timeout_ns, abort_flag, WB_DONE))) break;
       tc_fence_after();
       {
-        uint32_t a[64];
-        tmem_ld64(tmem + lane_off + C::DV_COL + 64 * g, a);
+        constexpr int HC = D / 2;  // columns per group
+        uint32_t a[HC];
+        if constexpr (HC == 64)
+          tmem_ld64(tmem + lane_off + C::DV_COL + HC * g, a);
+        else
+          tmem_ld32(tmem + lane_off + C::DV_COL + HC * g, a);
         tc_fence_before();
         mbar_arrive(b_vfree);  // the next block's first dV MMA may overwrite the accumulator
         uint4* dst = reinterpret_cast<uint4*>(
-            reinterpret_cast<uint16_t*>(p.dv) + (static_cast<size_t>(w.row_base) + w.key0 + k) * D + 64 * g);
+            reinterpret_cast<uint16_t*>(p.dv) + (static_cast<size_t>(w.row_base) + w.key0 + k) * D + HC * g);
 #pragma unroll
-        for (int u8 = 0; u8 < 8; ++u8)
+        for (int u8 = 0; u8 < HC / 8; ++u8)
           dst[u8] = make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]), __uint_as_float(a[8 * u8 + 1])),
                                bpack2<BF16>(__uint_as_float(a[8 * u8 + 2]), __uint_as_float(a[8 * u8 + 3])),
                                bpack2<BF16>(__uint_as_float(a[8 * u8 + 4]), __uint_as_float(a[8 * u8 + 5])),
@@ -514,10 +535,12 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
           break;
         }
         float* st = reinterpret_cast<float*>(smem + C::OFF_DQ);
+        if (t < D) {  // lanes >= d hold the zero-padded rows of dQ^T (d = 64)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {  // lane t = d index; column c = query
-          st[c * D + t] = __uint_as_float(u0[c]);
-          st[(32 + c) * D + t] = __uint_as_float(u1[c]);
+          for (int c = 0; c < 32; ++c) {  // lane t = d index; column c = query
+            st[c * D + t] = __uint_as_float(u0[c]);
+            st[(32 + c) * D + t] = __uint_as_float(u1[c]);
+          }
         }
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
@@ -537,10 +560,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dk) +
                                               (static_cast<size_t>(w.row_base) + w.key0 + t) * D);
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < D / 64; ++h) {
           uint32_t a[64];
           tmem_ld64(tmem + lane_off + C::DK_COL + 64 * h, a);
-          if (h == 1) {
+          if (h == D / 64 - 1) {
             tc_fence_before();
             mbar_arrive(b_kfree);  // the next block's first dK MMA may overwrite the accumulator
           }

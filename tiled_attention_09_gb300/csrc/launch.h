@@ -54,7 +54,7 @@ struct BwdArgs {
 };
 
 // Query-tile height of the backward main kernel for head dimension d (0 = unsupported).
-inline int bwd_query_tile(int d) { return d == 64 ? 128 : ((d == 128 || d == 256) ? 64 : 0); }
+inline int bwd_query_tile(int d) { return (d == 64 || d == 128 || d == 256) ? 64 : 0; }
 
 cudaError_t launch_fwd(const FwdArgs& a);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a);
