@@ -27,8 +27,10 @@
  *  - All data pointers are DEVICE pointers owned by the caller; the library
  *    allocates nothing on these paths. Every pointer must be 16-byte aligned
  *    (a TMA requirement), else FA_ERR_ALIGNMENT.
- *  - Supported shapes: d in {64, 128, 256}; N >= 128 and N % 128 == 0;
- *    B, H >= 1; B*H*N < 2^31. Anything else: FA_ERR_UNSUPPORTED, no launch.
+ *  - Supported shapes: d in {64, 128, 256}; any N >= 1 (a last tile that
+ *    runs past N is zero-filled on load, masked, and not stored); B, H >= 1;
+ *    B*H*N' < 2^31 with N' = N rounded up to 128. Anything else:
+ *    FA_ERR_UNSUPPORTED, no launch.
  *  - scale: finite and >= 0 (0 gives uniform attention), else
  *    FA_ERR_INVALID_ARG. The pages use scale = d^-1/2.
  *  - causal != 0: query i attends to keys j <= i.
@@ -86,8 +88,10 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
                     int d, float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: fp32 D [B,H,N], fp32 LSE*log2(e)
- * [B,H,N] and the fp32 dQ accumulator [B,H,N,d], each 256-byte aligned.
+ * Bytes of device workspace fa_bwd needs: fp32 D [B,H,Np], fp32 LSE*log2(e)
+ * [B,H,Np] and the fp32 dQ accumulator [B,H,Np,d], each 256-byte aligned,
+ * with Np = N rounded up to 64 (each head's rows padded so that every
+ * 64-query step of the main kernel starts aligned and stays in its head).
  * Returns 0 for unsupported shapes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);

@@ -10,7 +10,10 @@ Tolerance reading (fixed before any kernel ran; derivation in the design notes):
   with |V| in place of V). The literal max-abs error and the share of elements
   inside 2e-3 + half_ulp are reported alongside.
 * LSE: |LSE_gpu - LSE_orc| <= 2e-3 (fp32 output).
-* dQ, dK, dV: max|g_gpu - g_orc| <= 1e-2 * max|g_orc|, per tensor.
+* dQ, dK, dV: max|g_gpu - g_orc| <= 1e-2 * max|g_orc|, per tensor. Where the exact
+  gradient is zero (a single key: the softmax is the constant 1, so dQ = dK = 0
+  and dS = P (dP - D) is pure cancellation), that relative rule has no scale;
+  there the bound is fp32 rounding of the cancelling terms (cancel_tol).
 """
 from __future__ import annotations
 
@@ -56,9 +59,25 @@ def check_lse(lse_gpu: np.ndarray, lse_ref: np.ndarray, what: str = "LSE"):
     return float(err.max())
 
 
-def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, what: str):
+def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, what: str, abs_tol: float = 0.0):
     scale = np.abs(g_ref).max()
     err = np.abs(g_gpu - g_ref).max()
+    tol = max(1e-2 * scale, abs_tol)
     assert np.isfinite(g_gpu).all(), f"{what}: non-finite values"
-    assert err <= 1e-2 * scale, f"{what}: max err {err:.3e} vs 1e-2 * max|g| = {1e-2 * scale:.3e}"
-    return float(err / scale)
+    assert err <= tol, f"{what}: max err {err:.3e} vs tolerance {tol:.3e} (1e-2 * max|g| = {1e-2 * scale:.3e})"
+    return float(err / scale) if scale > 0 else 0.0
+
+
+def cancel_tol(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, scale: float) -> dict:
+    """Absolute error bound for dQ and dK from fp32 cancellation in dS = P (dP - D).
+
+    dP_ij = dO_i . V_j and D_i = dO_i . O_i are d-term fp32 dot products, each within
+    d * 2^-24 * sum_k |dO_ik V_jk| of its exact value; their difference is that large even when
+    the exact gradient is 0. Doubled for the two products, doubled again for P's rounding, then
+    carried through dQ = scale * dS K (dK = scale * dS^T Q) for one key (or query): the bound
+    matters only where the exact gradient vanishes.
+    """
+    d = q.shape[-1]
+    absdot = np.einsum("bhik,bhjk->bhij", np.abs(do), np.abs(v)).max()
+    base = 4 * d * 2.0 ** -24 * scale * absdot
+    return {"dQ": base * np.abs(k).max(), "dK": base * np.abs(q).max(), "dV": 0.0}

@@ -54,10 +54,12 @@ def test_status_strings_and_version(L):
 
 def test_workspace_size(L):
     B, H, N, d = 2, 3, 256, 128
-    rows = B * H * N
+    rows = B * H * ((N + 63) // 64 * 64)  # each head's rows padded to a multiple of 64
     r256 = lambda x: (x + 255) // 256 * 256
     assert L.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4) * 2 + r256(rows * d * 4)
-    assert L.fa_bwd_workspace_size(1, 1, 100, 64) == 0
+    assert L.fa_bwd_workspace_size(1, 1, 100, 64) == r256(128 * 4) * 2 + r256(128 * 64 * 4)  # any N >= 1
+    assert L.fa_bwd_workspace_size(2, 3, 65, 128) == r256(768 * 4) * 2 + r256(768 * 128 * 4)
+    assert L.fa_bwd_workspace_size(1, 1, 0, 64) == 0
     assert L.fa_bwd_workspace_size(1, 1, 256, 96) == 0
 
 
@@ -71,7 +73,7 @@ def fwd(L, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=256, d=64, scale=0.125, causal
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=0), 1), (dict(lse=0), 1),
-    (dict(N=100), 2), (dict(N=0), 2), (dict(N=64), 2), (dict(d=96), 2), (dict(d=32), 2), (dict(B=0), 2),
+    (dict(N=0), 2), (dict(N=-5), 2), (dict(d=96), 2), (dict(d=32), 2), (dict(B=0), 2),
     (dict(H=-1), 2), (dict(B=1 << 16, H=1 << 8, N=1 << 8), 2),
     (dict(dtype=7), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-1.0), 1),
     (dict(q=P + 8), 3), (dict(o=P + 2), 3), (dict(lse=P + 4), 3),
@@ -89,7 +91,7 @@ def test_bwd_rejects_bad_arguments(L):
     assert bwd(L, ws=0) == 4
     assert bwd(L, ws_bytes=10) == 4
     assert bwd(L, ws=P + 16) == 3   # workspace must be 256-byte aligned
-    assert bwd(L, N=200) == 2
+    assert bwd(L, N=0) == 2
     assert bwd(L, scale=float("nan")) == 1
     assert bwd(L, dq=0) == 1
     assert bwd(L, dq=P + 4) == 3

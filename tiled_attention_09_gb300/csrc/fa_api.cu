@@ -33,15 +33,17 @@ EncodeTiledFn get_encode_fn() {
 
 unsigned long long g_timeout_ns = 4000000000ull;
 
-// 2-D map over a [rows, d] row-major 16-bit tensor; box = {64 elements, box_rows}; 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, long long rows, int d, bool bf16, int box_rows) {
+// 3-D map over a [heads][N][d] row-major 16-bit tensor (heads = B*H); box = {64 elements, box_rows, 1};
+// 128-byte swizzle. Rows past N are outside a head, so a tile that runs past the end of a sequence
+// is zero-filled by the hardware instead of reading the next head's rows.
+bool make_map(CUtensorMap* m, const void* base, long long heads, int N, int d, bool bf16, int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -61,9 +63,10 @@ fa_status check_device() {
 
 fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype) {
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 128 || (N % 128) != 0) return FA_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * H * N >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  // row indices (including the backward workspace's per-head padding) stay in 32-bit ints
+  if (static_cast<long long>(B) * H * ((N + 127) / 128 * 128) >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -77,8 +80,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t off_D, off_lse2, off_dq, total;
 };
+// Each head's rows are padded to Npad = N rounded up to 64: every 64-query step of the backward
+// then starts 256-byte aligned (bulk copies need 16) and the last, partial step of a sequence
+// reads LSE*log2e and D of its own (zeroed, masked) padding rows and adds zero dQ partials there.
+int pad_rows(int N) { return (N + 63) / 64 * 64; }
 WsLayout ws_layout(int B, int H, int N, int d) {
-  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t rows = static_cast<size_t>(B) * H * pad_rows(N);
   WsLayout w;
   w.off_D = 0;
   w.off_lse2 = align256(rows * 4);
@@ -102,6 +109,7 @@ fa_status bwd_common(fa::BwdArgs* a, void* workspace, size_t workspace_bytes, in
   a->B = B;
   a->H = H;
   a->N = N;
+  a->Npad = pad_rows(N);
   a->d = d;
   a->scale = scale;
   a->causal = causal != 0;
@@ -148,10 +156,10 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
     return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
   fa::FwdArgs a;
-  const long long rows = static_cast<long long>(B) * H * N;
   const bool bf16 = dtype == FA_BF16;
-  if (!make_map(&a.tm_q, q, rows, d, bf16, 128) || !make_map(&a.tm_k, k, rows, d, bf16, 128) ||
-      !make_map(&a.tm_v, v, rows, d, bf16, 128))
+  const long long heads = static_cast<long long>(B) * H;
+  if (!make_map(&a.tm_q, q, heads, N, d, bf16, 128) || !make_map(&a.tm_k, k, heads, N, d, bf16, 128) ||
+      !make_map(&a.tm_v, v, heads, N, d, bf16, 128))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;
@@ -201,10 +209,10 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* d
   if ((s = check_device()) != FA_OK) return s;
   const int bq = fa::bwd_query_tile(d);
   if (bq == 0) return FA_ERR_UNSUPPORTED;
-  const long long rows = static_cast<long long>(B) * H * N;
-  if (!make_map(&a.tm_q, q, rows, d, a.bf16, bq) || !make_map(&a.tm_do, dO, rows, d, a.bf16, bq) ||
-      !make_map(&a.tm_k, k, rows, d, a.bf16, 128) || !make_map(&a.tm_v, v, rows, d, a.bf16, 128) ||
-      !make_map(&a.tm_dk, dk, rows, d, a.bf16, 128) || !make_map(&a.tm_dv, dv, rows, d, a.bf16, 128))
+  const long long heads = static_cast<long long>(B) * H;
+  if (!make_map(&a.tm_q, q, heads, N, d, a.bf16, bq) || !make_map(&a.tm_do, dO, heads, N, d, a.bf16, bq) ||
+      !make_map(&a.tm_k, k, heads, N, d, a.bf16, 128) || !make_map(&a.tm_v, v, heads, N, d, a.bf16, 128) ||
+      !make_map(&a.tm_dk, dk, heads, N, d, a.bf16, 128) || !make_map(&a.tm_dv, dv, heads, N, d, a.bf16, 128))
     return FA_ERR_CUDA;
   a.dO = dO;
   a.dk = dk;

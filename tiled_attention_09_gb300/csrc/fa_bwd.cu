@@ -18,36 +18,48 @@ int grid_for(size_t n_vec) {
 }
 
 template <int VPR>
-cudaError_t launch_pre_t(const BwdArgs& a, size_t n_vec) {
+cudaError_t launch_pre_t(const BwdArgs& a) {
+  const size_t n_vec_pad = static_cast<size_t>(a.B) * a.H * a.Npad * VPR;
   if (a.bf16)
-    return launch_kernel(fa_bwd_preprocess_kernel<VPR, true>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
-                      static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
-                      static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
-                      reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
-  return launch_kernel(fa_bwd_preprocess_kernel<VPR, false>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
-                    static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo), static_cast<const uint4*>(a.dO),
-                    a.lse, a.ws_D, a.ws_lse2, reinterpret_cast<float4*>(a.ws_dqacc), n_vec);
+    return launch_kernel(fa_bwd_preprocess_kernel<VPR, true>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
+                         static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
+                         static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
+                         reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
+  return launch_kernel(fa_bwd_preprocess_kernel<VPR, false>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
+                       static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
+                       static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
+                       reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
+}
+template <int VPR>
+cudaError_t launch_convert_t(const BwdArgs& a) {
+  const size_t n_vec = static_cast<size_t>(a.B) * a.H * a.N * VPR;
+  if (a.bf16)
+    return launch_kernel(fa_bwd_dq_convert_kernel<VPR, true>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
+                         reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, a.N,
+                         a.Npad, n_vec);
+  return launch_kernel(fa_bwd_dq_convert_kernel<VPR, false>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
+                       reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, a.N, a.Npad,
+                       n_vec);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a) {
-  const size_t n_vec = static_cast<size_t>(a.B) * a.H * a.N * (a.d / 8);
   switch (a.d) {
-    case 64: return launch_pre_t<8>(a, n_vec);
-    case 128: return launch_pre_t<16>(a, n_vec);
-    case 256: return launch_pre_t<32>(a, n_vec);
+    case 64: return launch_pre_t<8>(a);
+    case 128: return launch_pre_t<16>(a);
+    case 256: return launch_pre_t<32>(a);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a) {
-  const size_t n_vec = static_cast<size_t>(a.B) * a.H * a.N * (a.d / 8);
-  if (a.bf16)
-    return launch_kernel(fa_bwd_dq_convert_kernel<true>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
-                      reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, n_vec);
-  return launch_kernel(fa_bwd_dq_convert_kernel<false>, dim3(grid_for(n_vec)), dim3(256), 0, a.stream,
-                    reinterpret_cast<const float4*>(a.ws_dqacc), static_cast<uint4*>(a.dq), a.scale, n_vec);
+  switch (a.d) {
+    case 64: return launch_convert_t<8>(a);
+    case 128: return launch_convert_t<16>(a);
+    case 256: return launch_convert_t<32>(a);
+  }
+  return cudaErrorInvalidValue;
 }
 
 namespace {
@@ -77,10 +89,11 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.N = a.N;
+  p.Npad = a.Npad;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
-  dim3 grid(a.B * a.H, a.N / 128, 1);
+  dim3 grid(a.B * a.H, (a.N + 127) / 128, 1);  // key blocks; the last may run past N
   e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
@@ -104,10 +117,11 @@ cudaError_t launch_d256_t(const BwdArgs& a) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.N = a.N;
+  p.Npad = a.Npad;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
-  dim3 grid(a.B * a.H, a.N / 128, 1);
+  dim3 grid(a.B * a.H, (a.N + 127) / 128, 1);  // key blocks; the last may run past N
   e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);

@@ -1,6 +1,6 @@
 // Bandwidth-bound helper kernels of the backward pass (no tensor cores):
 //   K2 preprocess: D_i = sum_k dO_ik * O_ik (fp32; O = o + o_lo when the forward's rounding
-//                  residual o_lo is given), LSE_i * log2(e), dQ accumulator := 0
+//                  residual o_lo is given), LSE_i * log2(e), dQ accumulator := 0 (padded rows)
 //   K4 dQ convert: dQ = dtype(scale * dQacc)
 // Each thread owns one 16-byte vector (8 elements) of a row; the d/8 threads of
 // a row sit in one warp and reduce with shuffles. Grid-stride loops keep the
@@ -45,6 +45,10 @@ __device__ __forceinline__ uint32_t pack2f(float lo, float hi) {
   }
 }
 
+// Workspace rows are padded per head: row (bh, r) of D, LSE*log2e and the dQ accumulator sits at
+// bh * Npad + r with Npad = N rounded up to 64, so every 64-query step of the backward starts
+// 256-byte aligned (a bulk copy needs 16) and stays inside its own head. Padding rows hold D = 0 and
+// LSE*log2e = 0 (finite: a masked query still multiplies them by zero).
 // VPR = vectors (of 8 elements) per row = d / 8, a power of two <= 32.
 template <int VPR, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __restrict__ o,
@@ -52,40 +56,52 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
                                                                  const uint4* __restrict__ dO,
                                                                  const float* __restrict__ lse, float* __restrict__ D,
                                                                  float* __restrict__ lse2, float4* __restrict__ dqacc,
-                                                                 size_t n_vec) {
+                                                                 int N, int Npad, size_t n_vec_pad) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
-    float a[8], b[8];
-    unpack8<BF16>(__ldg(&o[i]), a);
-    unpack8<BF16>(__ldg(&dO[i]), b);
-    if (o_lo) {  // O reconstructed to fp32 accuracy: o + residual
-      float r[8];
-      unpack8<BF16>(__ldg(&o_lo[i]), r);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) a[k] += r[k];
-    }
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec_pad; i += stride) {
+    const uint32_t row_pad = static_cast<uint32_t>(i / VPR);
+    const uint32_t bh = row_pad / static_cast<uint32_t>(Npad), r = row_pad - bh * static_cast<uint32_t>(Npad);
+    const bool real = r < static_cast<uint32_t>(N);
+    const size_t row = static_cast<size_t>(bh) * N + r;  // the row in the caller's [B*H*N] layout
     float acc = 0.f;
+    if (real) {
+      const size_t src = row * VPR + (i % VPR);
+      float a[8], b[8];
+      unpack8<BF16>(__ldg(&o[src]), a);
+      unpack8<BF16>(__ldg(&dO[src]), b);
+      if (o_lo) {  // O reconstructed to fp32 accuracy: o + residual
+        float rr[8];
+        unpack8<BF16>(__ldg(&o_lo[src]), rr);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc = fmaf(a[k], b[k], acc);
+        for (int k = 0; k < 8; ++k) a[k] += rr[k];
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc = fmaf(a[k], b[k], acc);
+    }
+    // every lane of a row's VPR-lane group takes the same branch (rows never straddle a group)
 #pragma unroll
     for (int off = VPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, VPR);
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     dqacc[2 * i] = z;
     dqacc[2 * i + 1] = z;
     if ((i % VPR) == 0) {
-      const size_t row = i / VPR;
-      D[row] = acc;
-      lse2[row] = lse[row] * 1.4426950408889634f;
+      D[row_pad] = acc;
+      lse2[row_pad] = real ? lse[row] * 1.4426950408889634f : 0.f;
     }
   }
 }
 
-template <bool BF16>
+// dQ = dtype(scale * accumulator), from the padded accumulator rows to the caller's rows.
+template <int VPR, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __restrict__ dqacc,
-                                                                uint4* __restrict__ dq, float scale, size_t n_vec) {
+                                                                uint4* __restrict__ dq, float scale, int N, int Npad,
+                                                                size_t n_vec) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
-    const float4 x = dqacc[2 * i], y = dqacc[2 * i + 1];
+    const uint32_t row = static_cast<uint32_t>(i / VPR);
+    const uint32_t bh = row / static_cast<uint32_t>(N), r = row - bh * static_cast<uint32_t>(N);
+    const size_t src = (static_cast<size_t>(bh) * Npad + r) * VPR + (i % VPR);
+    const float4 x = dqacc[2 * src], y = dqacc[2 * src + 1];
     uint4 v;
     v.x = pack2f<BF16>(x.x * scale, x.y * scale);
     v.y = pack2f<BF16>(x.z * scale, x.w * scale);

@@ -78,9 +78,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
   const int N = p.N;
   const int bh = blockIdx.x;
   const int key0 = blockIdx.y * 128;
-  const int row_base = bh * N;
+  const int ws_base = bh * p.Npad;  // row of (b, h, 0) in the workspace's padded rows
   const int it0 = CAUSAL ? (key0 / BQ) : 0;
-  const int n_it = N / BQ - it0;  // query steps per pass
+  const int n_it = (N + BQ - 1) / BQ - it0;  // query steps per pass (the last may run past N: masked)
   const int n_g = 2 * n_it;        // steps of both passes: g = h * n_it + it
 
   if (threadIdx.x == 0) {
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
       mbar_arrive_expect_tx(b_kv, 2 * C::KV_TILE);
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_2d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, row_base + key0);
-        tma_load_2d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, row_base + key0);
+        tma_load_3d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, key0, bh);
+        tma_load_3d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, key0, bh);
       }
       int issued = 0;
       for (int g = 0; g < n_g; ++g) {
@@ -125,12 +125,13 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         // second pass also waits for the first pass's epilogue, which staged dV / dK there
         if (g > 0 && !wait_bar(b_qempty, (g - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) break;
         if (g == n_it && !wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_QE)) break;
-        const int qrow = row_base + (it0 + it) * BQ;
+        const int q_in = (it0 + it) * BQ;  // within the head; rows past N arrive as zeros
+        const int qrow = ws_base + q_in;    // LSE*log2e / D past N: the head's zero padding, masked
         mbar_arrive_expect_tx(b_qfull, 2 * C::Q_TILE + 2 * BQ * 4);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_2d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfull, c * 64, qrow);
-          tma_load_2d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfull, c * 64, qrow);
+          tma_load_3d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfull, c * 64, q_in, bh);
+          tma_load_3d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfull, c * 64, q_in, bh);
         }
         bulk_load(s0 + C::OFF_LSE, p.lse2 + qrow, BQ * 4, b_qfull);
         bulk_load(s0 + C::OFF_DD, p.Dvec + qrow, BQ * 4, b_qfull);
@@ -221,8 +222,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
         const float* dd_s = reinterpret_cast<const float*>(smem + C::OFF_DD);
         const int q0 = (it0 + it) * BQ;  // first query of the tile
-        const bool need_mask = CAUSAL && (q0 < key0 + 127);
-        const int kq = key0 + k - q0;  // masked where column c < kq (key > query)
+        // masked: column c < kq (key > query, causal), q0 + c >= N (query past the sequence) or the
+        // whole row when the key is past the sequence (zero K row: S = 0, exp(-LSE) need not be finite)
+        const bool need_mask = (CAUSAL && (q0 < key0 + 127)) || (q0 + BQ > N) || (key0 + 128 > N);
+        const int kq = CAUSAL ? (key0 + k - q0) : 0;
+        const int qn = key0 + k < N ? N - q0 : 0;
         float pv[64];
         {
           uint32_t u0[32], u1[32];
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         }
         if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pv[c] = (c < kq) ? 0.f : pv[c];
+          for (int c = 0; c < 64; ++c) pv[c] = (c < kq || c >= qn) ? 0.f : pv[c];
         }
         {
           uint32_t pk[32];
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         // end of pass h: dV[:, h] (128 keys x 128) staged in the Q tile, stored with TMA
         bool ok_e = ok && __all_sync(0xffffffffu, wait_bar(b_done, h & 1, p.timeout_ns, abort_flag, WB_DONE));
         if (ok_e) tc_fence_after();
-        bwd_store_acc<DH, BF16>(tmem + lane_off + C::DV_COL, smem + C::OFF_Q, &p.tm_dv, row_base + key0, k, 1.0f, 1,
+        bwd_store_acc<DH, BF16>(tmem + lane_off + C::DV_COL, smem + C::OFF_Q, &p.tm_dv, key0, bh, k, 1.0f, 1,
                                 ok_e, abort_flag, h * DH);
         if (k == 0) {
           tc_fence_before();
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         mbar_arrive(b_dqfree);
         if (*abort_flag == 0u) {
           // dQ[q][h*128 + t] += dQ^T[t][q]: a warp covers 128 contiguous bytes per query
-          float* dst = p.dqacc + static_cast<size_t>(row_base + (it0 + it) * BQ) * D + h * DH + t;
+          float* dst = p.dqacc + static_cast<size_t>(ws_base + (it0 + it) * BQ) * D + h * DH + t;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             atomicAdd(dst + c * D, __uint_as_float(u0[c]));
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         // end of pass h: dK[:, h] = scale * accumulator, staged in the dO tile
         bool ok_e = ok && __all_sync(0xffffffffu, wait_bar(b_done, h & 1, p.timeout_ns, abort_flag, WB_DONE));
         if (ok_e) tc_fence_after();
-        bwd_store_acc<DH, BF16>(tmem + lane_off + C::DK_COL, smem + C::OFF_DO, &p.tm_dk, row_base + key0, t, p.scale,
+        bwd_store_acc<DH, BF16>(tmem + lane_off + C::DK_COL, smem + C::OFF_DO, &p.tm_dk, key0, bh, t, p.scale,
                                 2, ok_e, abort_flag, h * DH);
         if (t == 0) {
           tc_fence_before();

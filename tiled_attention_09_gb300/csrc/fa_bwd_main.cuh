@@ -24,12 +24,13 @@ namespace fa {
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;
-  const float* lse2;  // [B*H*N] LSE * log2(e)
-  const float* Dvec;  // [B*H*N] rowsum(dO * O)
-  float* dqacc;       // [B*H*N, d] fp32
+  const float* lse2;  // [B*H*Npad] LSE * log2(e); row (bh, r) at bh * Npad + r
+  const float* Dvec;  // [B*H*Npad] rowsum(dO * O), same rows
+  float* dqacc;       // [B*H*Npad, d] fp32, same rows
   void* dk;           // [B*H*N, d] dtype outputs, written directly by kernels that store from registers
   void* dv;
   int N;
+  int Npad;           // N rounded up to 64: the per-head row stride of lse2, Dvec and dqacc
   float scale;
   float scale_log2;
   unsigned long long timeout_ns;
@@ -53,9 +54,10 @@ enum : uint32_t {
 };
 
 // Write one 128 x d accumulator (thread = row, TMEM lane) as dtype into a 128-byte-swizzled
-// staging tile and store it with TMA at rows [row0, row0 + 128), columns [x0, x0 + d).
+// staging tile and store it with TMA at rows [row0, row0 + 128) of head `head`, columns
+// [x0, x0 + d); rows past the sequence's end are dropped by the tensor map.
 template <int D, bool BF16>
-__device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, const void* map, int row0, int r,
+__device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, const void* map, int row0, int head, int r,
                                               float mul, uint32_t bar_id, bool ok, volatile uint32_t* abort_flag,
                                               int x0 = 0) {
   if (ok) {
@@ -80,7 +82,7 @@ __device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, con
   named_bar_sync(bar_id, 128);
   if (r == 0 && ok && *abort_flag == 0u) {
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) tma_store_2d(map, smem_u32(stage) + c * (128 * 128), x0 + c * 64, row0);
+    for (int c = 0; c < D / 64; ++c) tma_store_3d(map, smem_u32(stage) + c * (128 * 128), x0 + c * 64, row0, head);
     bulk_commit();
     bulk_wait_read0();
   }

@@ -76,15 +76,19 @@ struct BwdPipeCfg {
 // causal masking block 0 has the most query steps, so the launch order is longest-first).
 template <bool CAUSAL>
 struct BwdItem {
-  int row_base;  // row of (b, h, 0) in the [B*H*N, d] view
+  int bh;        // head (b, h): the z coordinate of the tensor maps
+  int row_base;  // row of (b, h, 0) in the [B*H*N, d] view of the inputs and outputs
+  int ws_base;   // row of (b, h, 0) in the workspace's padded [B*H*Npad] rows
   int key0;      // first key of the block
   int it0;       // first 64-query step (causal: the block's diagonal)
-  int n_it;      // query steps
-  __device__ __forceinline__ BwdItem(int x, int y, int N) {
+  int n_it;      // query steps (the last may run past N: its extra queries are masked)
+  __device__ __forceinline__ BwdItem(int x, int y, int N, int Npad) {
+    bh = x;
     row_base = x * N;
+    ws_base = x * Npad;
     key0 = y * 128;
     it0 = CAUSAL ? (key0 / 64) : 0;  // 64-query steps
-    n_it = N / 64 - it0;
+    n_it = (N + 63) / 64 - it0;
   }
 };
 
@@ -201,13 +205,16 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       auto load_stage = [&](const Item& w, int it) -> bool {
         const uint32_t s = gs % NS, use = gs / NS;
         if (use > 0 && !wait_bar(b_qempty(s), (use - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) return false;
-        const int qrow = w.row_base + (w.it0 + it) * BQ;
+        const int q_in = (w.it0 + it) * BQ;  // first query of the step within the head
+        const int qrow = w.ws_base + q_in;
         mbar_arrive_expect_tx(b_qfull(s), 2 * C::Q_TILE + 2 * BQ * 4);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_2d(sQ + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_q, b_qfull(s), c * 64, qrow);
-          tma_load_2d(sDO + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_do, b_qfull(s), c * 64, qrow);
+          tma_load_3d(sQ + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_q, b_qfull(s), c * 64, q_in, w.bh);
+          tma_load_3d(sDO + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_do, b_qfull(s), c * 64, q_in, w.bh);
         }
+        // LSE*log2e and D rows past N (a step that runs past the sequence) are the head's padding
+        // rows (zeros), and the queries they belong to are masked
         bulk_load(s0 + C::OFF_LSE + s * BQ * 4, p.lse2 + qrow, BQ * 4, b_qfull(s));
         bulk_load(s0 + C::OFF_DD + s * BQ * 4, p.Dvec + qrow, BQ * 4, b_qfull(s));
         ++gs;
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         clc_pending = true;
       };
       while (ok) {
-        const Item w(ix, iy, N);
+        const Item w(ix, iy, N, p.Npad);
         const int pre = w.n_it < 2 ? w.n_it : 2;  // stages issued before the block's K/V can be
         const int ask_at = w.n_it - 2 > 0 ? w.n_it - 2 : 0;
         int it = 0;
@@ -232,8 +239,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         mbar_arrive_expect_tx(b_kv, 2 * C::KV_TILE);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_2d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, w.row_base + w.key0);
-          tma_load_2d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, w.row_base + w.key0);
+          tma_load_3d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, w.key0, w.bh);
+          tma_load_3d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, w.key0, w.bh);
         }
         ++nb;
         if (ask_at < pre) ask();
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       int nb = 0;       // finished blocks
       bool ok = true;
       while (ok) {
-        const Item w(ix, iy, N);
+        const Item w(ix, iy, N, p.Npad);
         if (!wait_bar(b_kv, nb & 1, p.timeout_ns, abort_flag, WB_KV)) break;
         if (role < 2) {
           if (!score_ready(gs)) break;
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     int nb = 0;
     bool ok = true;
     while (ok) {
-      const Item w(ix, iy, N);
+      const Item w(ix, iy, N, p.Npad);
       for (int it = 0; it < w.n_it; ++it) {
         const uint32_t gq = gs + it, b = gq & 1, s = gq % NS;
         if (!__all_sync(0xffffffffu, wait_bar(b_sdp(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_SDP))) {
@@ -422,8 +429,12 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE + s * BQ * 4) + 8 * g;
         const float4* dd4 = reinterpret_cast<const float4*>(smem + C::OFF_DD + s * BQ * 4) + 8 * g;
         const int q0 = (w.it0 + it) * BQ + 32 * g;  // first query of this group's columns
-        const bool need_mask = CAUSAL && (q0 < w.key0 + 127);
-        const int kq = w.key0 + k - q0;  // masked where column c < kq (key > query)
+        // masked: column c < kq (key > query, causal), q0 + c >= N (query past the sequence) or the
+        // whole row when the key is past the sequence (its zero-filled K row gives S = 0, and
+        // exp(-LSE) need not be finite)
+        const bool need_mask = (CAUSAL && (q0 < w.key0 + 127)) || (q0 + 32 > N) || (w.key0 + 128 > N);
+        const int kq = CAUSAL ? (w.key0 + k - q0) : 0;
+        const int qn = w.key0 + k < N ? N - q0 : 0;
         uint32_t u[32], v[32];
         tmem_ld32_pair(tS + 32 * g, tDP + 32 * g, u, v);  // S^T and dP^T columns in one round trip
         float pv[32];
@@ -437,7 +448,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         }
         if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pv[c] = (c < kq) ? 0.f : pv[c];
+          for (int c = 0; c < 32; ++c) pv[c] = (c < kq || c >= qn) ? 0.f : pv[c];
         }
         uint32_t pk[16];
 #pragma unroll
@@ -481,9 +492,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         mbar_arrive(b_vfree);  // the next block's first dV MMA may overwrite the accumulator
         uint4* dst = reinterpret_cast<uint4*>(
             reinterpret_cast<uint16_t*>(p.dv) + (static_cast<size_t>(w.row_base) + w.key0 + k) * D + HC * g);
+        const bool key_ok = w.key0 + k < N;  // keys past N exist only as zero rows of the block
 #pragma unroll
         for (int u8 = 0; u8 < HC / 8; ++u8)
-          dst[u8] = make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]), __uint_as_float(a[8 * u8 + 1])),
+          if (key_ok) dst[u8] = make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]), __uint_as_float(a[8 * u8 + 1])),
                                bpack2<BF16>(__uint_as_float(a[8 * u8 + 2]), __uint_as_float(a[8 * u8 + 3])),
                                bpack2<BF16>(__uint_as_float(a[8 * u8 + 4]), __uint_as_float(a[8 * u8 + 5])),
                                bpack2<BF16>(__uint_as_float(a[8 * u8 + 6]), __uint_as_float(a[8 * u8 + 7])));
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     int nb = 0;
     bool ok = true;
     while (ok) {
-      const Item w(ix, iy, N);
+      const Item w(ix, iy, N, p.Npad);
       for (int it = 0; it < w.n_it; ++it) {
         const uint32_t gq = gs + it, b = gq & 1;
         const bool full =
@@ -545,7 +557,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
         if (t == 0) {
-          bulk_reduce_add_f32(p.dqacc + static_cast<size_t>(w.row_base + (w.it0 + it) * BQ) * D, sDQ,
+          bulk_reduce_add_f32(p.dqacc + static_cast<size_t>(w.ws_base + (w.it0 + it) * BQ) * D, sDQ,
                               C::DQ_STAGE);
           bulk_commit();
         }
@@ -568,9 +580,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
             mbar_arrive(b_kfree);  // the next block's first dK MMA may overwrite the accumulator
           }
           const float sc = p.scale;
+          const bool key_ok = w.key0 + t < N;
 #pragma unroll
           for (int u8 = 0; u8 < 8; ++u8)
-            dst[8 * h + u8] =
+            if (key_ok) dst[8 * h + u8] =
                 make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]) * sc, __uint_as_float(a[8 * u8 + 1]) * sc),
                            bpack2<BF16>(__uint_as_float(a[8 * u8 + 2]) * sc, __uint_as_float(a[8 * u8 + 3]) * sc),
                            bpack2<BF16>(__uint_as_float(a[8 * u8 + 4]) * sc, __uint_as_float(a[8 * u8 + 5]) * sc),

@@ -102,6 +102,7 @@ struct FwdCfg {
 // launch order is longest-first).
 template <int NT, bool CAUSAL>
 struct FwdItem {
+  int bh;        // head (b, h): the z coordinate of the tensor maps
   int q_row0;    // first query row of the item within the head
   int row_base;  // row of (b, h, 0) in the [B*H*N, d] view
   int n_valid;   // query tiles that exist (the last block can hold one tile fewer)
@@ -109,14 +110,15 @@ struct FwdItem {
   int n_t[NT];   // key tiles that tile t needs
   __device__ __forceinline__ FwdItem(int x, int y, int N, int n_qblk) {
     const int qb = CAUSAL ? (n_qblk - 1 - y) : y;
+    bh = x;
     q_row0 = qb * 128 * NT;
     row_base = x * N;
-    n_valid = (N - q_row0) / 128;
+    n_valid = (N - q_row0 + 127) / 128;  // a tile that runs past N still exists (its tail is masked)
     if (n_valid > NT) n_valid = NT;
     nmax = 0;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      n_t[t] = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : (N / 128)) : 0;
+      n_t[t] = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : ((N + 127) / 128)) : 0;
       nmax = n_t[t] > nmax ? n_t[t] : nmax;
     }
   }
@@ -154,7 +156,7 @@ __device__ __forceinline__ uint32_t pack2_residual(float a, float b, uint32_t& r
 enum : uint32_t {
   W_Q = 1, W_RING_EMPTY = 2, W_RING_FULL = 3, W_P = 4, W_S = 5, W_O = 6, W_DRAIN = 7,
   W_QFREE = 8, W_CLC = 9, W_ITEM = 10, W_OFREE = 11,
-  B_CLC_ID = 20, B_OUT_ROW = 21  // where-codes for FA_DEV_BAD_INDEX
+  B_CLC_ID = 20  // where-code for FA_DEV_BAD_INDEX
 };
 
 template <int D, bool BF16, bool CAUSAL>
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         for (int t = 0; t < w.n_valid; ++t)
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_2d(sQ + t * C::TILE + c * C::CHUNK, &p.tm_q, b_q, c * 64, w.row_base + w.q_row0 + t * 128);
+            tma_load_3d(sQ + t * C::TILE + c * C::CHUNK, &p.tm_q, b_q, c * 64, w.q_row0 + t * 128, w.bh);
         ++n_items;
         const int nload = 2 * w.nmax;
         const int ask_at = nload - 2;  // with the item's last K/V pair
@@ -268,10 +270,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           }
           mbar_arrive_expect_tx(b_full(slot), C::TILE);
           const void* map = (s & 1) ? static_cast<const void*>(&p.tm_v) : static_cast<const void*>(&p.tm_k);
-          const int krow = w.row_base + (s >> 1) * 128;
+          const int krow = (s >> 1) * 128;  // rows past N arrive as zeros
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_2d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow);
+            tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow, w.bh);
           ++seq;
         }
         if (!ok) break;
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     bool ok = true;
     while (ok) {
       const Item w(ix, iy, N, p.n_qblk);
-      const int my_n = (t < w.n_valid) ? (CAUSAL ? (w.q_row0 / 128 + t + 1) : (N / 128)) : 0;  // t is not a constant here
+      const int my_n = (t < w.n_valid) ? (CAUSAL ? (w.q_row0 / 128 + t + 1) : ((N + 127) / 128)) : 0;  // t is not a constant here
       float m_used = 0.f, l = 0.f;
       for (int j = 0; ok && j < my_n; ++j) {
         // warp-uniform outcome: tcgen05.ld/st below are warp-collective
@@ -426,11 +428,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
         }
-        const bool diag = CAUSAL && (j == my_n - 1);
-        if (diag) {
-          // keys past the query's own position do not exist for this row
+        // keys that do not exist for this row: past the query itself (causal, diagonal tile) or past
+        // the end of the sequence (last tile, when N is not a multiple of 128); never all 128 of them
+        int lim = N - j * 128;
+        if (CAUSAL && j == my_n - 1 && lim > r + 1) lim = r + 1;
+        if (__any_sync(0xffffffffu, lim < 128)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = c > r ? -INFINITY : s[c];
+          for (int c = 0; c < 128; ++c) s[c] = c >= lim ? -INFINITY : s[c];
         }
         float ls0 = 0.f, ls1 = 0.f;
         uint32_t pk[64];
@@ -508,12 +512,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         // ---------------------------------------------------------- epilogue of tile t
         ok = __all_sync(0xffffffffu, wait_bar(b_o(t), n_o & 1, p.timeout_ns, abort_flag, W_O));
         ++n_o;
-        const size_t grow = static_cast<size_t>(w.row_base) + w.q_row0 + t * 128 + r;
-        // rows exist only below B*H*N (warp-uniform: the bound is a multiple of 128 rows)
-        if (ok && !__all_sync(0xffffffffu, grow < static_cast<size_t>(gridDim.x) * N)) {
-          if ((threadIdx.x & 31) == 0) report_status(FA_DEV_BAD_INDEX, B_OUT_ROW);
-          ok = false;
-        }
+        const int q_row = w.q_row0 + t * 128 + r;  // within the head
+        const bool row_ok = q_row < N;             // the tile's rows past N are computed, not stored
+        const size_t grow = static_cast<size_t>(w.row_base) + q_row;
         if (ok) {
           tc_fence_after();
           const float inv_l = 1.f / l;
@@ -542,12 +543,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
               lo.y = pack2_residual<BF16>(x[2], x[3], v.y);
               lo.z = pack2_residual<BF16>(x[4], x[5], v.z);
               lo.w = pack2_residual<BF16>(x[6], x[7], v.w);
-              o_row[(c0 >> 3) + g] = v;
-              if (lo_row) lo_row[(c0 >> 3) + g] = lo;
+              if (row_ok) {
+                o_row[(c0 >> 3) + g] = v;
+                if (lo_row) lo_row[(c0 >> 3) + g] = lo;
+              }
             }
           }
           // LSE in natural log: (m_used + log2 l) * ln 2
-          p.lse[grow] = (m_used + log2f(l)) * 0.69314718055994531f;
+          if (row_ok) p.lse[grow] = (m_used + log2f(l)) * 0.69314718055994531f;
         }
       }
       if (!ok) break;

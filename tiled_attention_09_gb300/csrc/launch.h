@@ -43,10 +43,11 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* ws_D;      // [B*H*N]
-  float* ws_lse2;   // [B*H*N]  lse * log2(e)
-  float* ws_dqacc;  // [B*H*N*d]
+  float* ws_D;      // [B*H*Npad]: row (bh, r) at bh * Npad + r, Npad = N rounded up to 64
+  float* ws_lse2;   // [B*H*Npad]  lse * log2(e)
+  float* ws_dqacc;  // [B*H*Npad*d]
   int B, H, N, d;
+  int Npad;  // N rounded up to 64: the per-head row stride of the workspace arrays
   float scale;
   bool causal, bf16;
   uint64_t timeout_ns;
