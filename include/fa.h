@@ -31,8 +31,8 @@
  *    runs past N is zero-filled on load, masked, and not stored); B, H >= 1;
  *    B*H*N' < 2^31 with N' = N rounded up to 128. Anything else:
  *    FA_ERR_UNSUPPORTED, no launch.
- *  - scale: finite and >= 0 (0 gives uniform attention), else
- *    FA_ERR_INVALID_ARG. The pages use scale = d^-1/2.
+ *  - scale: finite and > 0, else FA_ERR_INVALID_ARG. The pages use
+ *    scale = d^-1/2.
  *  - causal != 0: query i attends to keys j <= i.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream). Work is enqueued asynchronously; argument errors are returned
@@ -88,6 +88,42 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
                     int d, float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
+ * Options beyond plain multi-head attention, for fa_fwd_opt / fa_bwd_opt.
+ * Zero-initialise, then set what is needed; a NULL options pointer means all
+ * defaults (then the _opt calls equal fa_fwd_ex / fa_bwd).
+ *  - n_kv_heads: K and V (and dK, dV) have this many heads, [B, n_kv_heads,
+ *    N, d]; query head h reads K/V head h / (H / n_kv_heads) (grouped-query
+ *    attention; 1 is multi-query attention, as in the multi-query kernel of
+ *    page "高级特性：探索PyTorch/XLA的Pallas内核和Flash Attention实现", section
+ *    "Pallas内核：自定义高效计算的关键"). 0 means H. H must be a multiple of
+ *    it (else FA_ERR_UNSUPPORTED); negative: FA_ERR_INVALID_ARG. In the
+ *    backward dK, dV of a K/V head are summed over its H / n_kv_heads query
+ *    heads inside one CTA (no atomics; dk, dv stay bitwise reproducible).
+ *  - kv_len: NULL, or a DEVICE int32 array [B] (4-byte aligned, else
+ *    FA_ERR_ALIGNMENT): in batch b every query sees only keys j < kv_len[b]
+ *    (a key-padding mask; the masking use of an attention bias on page
+ *    "transformer模型详解（十）：FlashAttention优化技术", section "精度与稳定性的平衡").
+ *    Values are clamped to [0, N] on the device. Combined with causal, query
+ *    i sees keys j <= i with j < kv_len[b]. A query that sees no key
+ *    (kv_len[b] = 0) gets O = 0 and LSE = -inf, and contributes zero
+ *    gradients. Key tiles wholly past kv_len[b] are skipped by the forward.
+ *  - o_fp32: nonzero: O is fp32 [B,H,N,d] (the forward writes it so, unrounded;
+ *    the backward reads it so), the mixed-precision output of page
+ *    "在TPU上移植Flash Attention的工程实践与挑战", Example 3 (16-bit inputs and
+ *    products, fp32 result). o_lo must then be NULL (FA_ERR_INVALID_ARG).
+ */
+typedef struct fa_options {
+  int n_kv_heads;
+  const int* kv_len;
+  int o_fp32;
+} fa_options;
+
+/* Forward with options: arguments and results as fa_fwd_ex, k and v with
+ * opt->n_kv_heads heads, o in fp32 when opt->o_fp32. */
+fa_status fa_fwd_opt(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H,
+                     int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 D [B,H,Np], fp32 LSE*log2(e)
  * [B,H,Np] and the fp32 dQ accumulator [B,H,Np,d], each 256-byte aligned,
  * with Np = N rounded up to 64 (each head's rows padded so that every
@@ -118,6 +154,14 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, const void* o_lo, void* workspace, size_t workspace_bytes, int B, int H,
                  int N, int d, float scale, int causal, fa_dtype dtype, void* stream);
+
+/* Backward with options: arguments and results as fa_bwd; k, v, dk, dv with
+ * opt->n_kv_heads heads; o in fp32 when opt->o_fp32; the same kv_len as the
+ * forward that produced o and lse. The workspace is sized by H (query heads). */
+fa_status fa_bwd_opt(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                     void* dq, void* dk, void* dv, const void* o_lo, void* workspace, size_t workspace_bytes, int B,
+                     int H, int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt,
+                     void* stream);
 
 /*
  * fa_bwd for callers that cannot allocate device memory: the workspace is a

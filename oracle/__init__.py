@@ -33,6 +33,17 @@ Readings where the pages are silent (each also listed in the design notes):
 * causal mask: query i attends to keys j <= i (the pages name masking only as
   ``attn_bias``); masked logits are -inf, masked probabilities exactly 0.
 * LSE: natural log of the sum of exp of the scaled logits, per query row.
+* grouped K/V heads (``attention_fwd`` / ``attention_bwd`` only): K and V may
+  have H_kv heads with H a multiple of H_kv; query head h reads K/V head
+  h // (H / H_kv) (page 3, "高级特性：探索PyTorch/XLA的Pallas内核和Flash
+  Attention实现", section "Pallas内核：自定义高效计算的关键", names a multi-query
+  attention kernel: H_kv = 1). The gradient of a shared K/V head is the sum of
+  its query heads' contributions (chain rule for a shared input).
+* key-padding mask (``kv_len``, same two functions): in batch b only keys
+  j < kv_len[b] exist for every query (clamped to [0, N]); the masking use of
+  an attention bias on page 2, section "精度与稳定性的平衡". A row that sees no
+  key has no softmax; read as O = 0, LSE = -inf (the empty sum) and zero
+  gradients.
 * backward: the page-2 sketch calls a block-local ``softmax(s_ij)``; read as
   P_ij = exp(S_ij - LSE_i) with the saved LSE, which is what makes the
   recomputed block equal to the true probabilities. The gradient formulas
@@ -60,51 +71,75 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def head_scores(q, k, scale, causal, row0=0):
+def head_scores(q, k, scale, causal, row0=0, kv_len=None):
     """Scaled logits of one (b, h) head: S = scale * q @ k^T, masked to -inf.
 
     ``q`` holds query rows ``row0 .. row0+len(q)-1`` of the head, ``k`` all keys.
     Page 2, section "Kernel Fusion": scores = q @ k^T (divided by sqrt(d)).
+    Masked: keys after the query (causal) and keys j >= kv_len (key padding).
     """
     s = scale * (q @ k.T)
+    cols = np.arange(k.shape[0])[None, :]
     if causal:
         rows = np.arange(row0, row0 + q.shape[0])[:, None]
-        cols = np.arange(k.shape[0])[None, :]
         s = np.where(cols > rows, -np.inf, s)
+    if kv_len is not None:
+        s = np.where(cols >= kv_len, -np.inf, s)
     return s
 
 
 def _softmax_rows(s):
-    """Row softmax with its log-sum-exp: P = exp(S - LSE), LSE = m + ln(sum exp(S - m))."""
+    """Row softmax with its log-sum-exp: P = exp(S - LSE), LSE = m + ln(sum exp(S - m)).
+
+    A row whose logits are all -inf (no visible key) gets P = 0 and LSE = -inf.
+    """
     m = np.max(s, axis=-1, keepdims=True)
+    empty = np.isneginf(m)
+    m = np.where(empty, 0.0, m)
     e = np.exp(s - m)
     l = np.sum(e, axis=-1, keepdims=True)
-    lse = m + np.log(l)
-    p = np.exp(s - lse)
+    with np.errstate(divide="ignore"):
+        lse = m + np.log(l)
+    p = np.where(empty, 0.0, np.exp(s - np.where(empty, 0.0, lse)))
     return p, lse[..., 0]
 
 
-def attention_fwd(q, k, v, scale, causal=False):
-    """O = softmax(scale * Q K^T [+ causal mask]) V and LSE, per (b, h) head.
+def _kv_head(h, H, Hkv):
+    """K/V head that query head h reads: h // (H / H_kv)."""
+    return h // (H // Hkv)
+
+
+def _key_count(kv_len, b, N):
+    """Keys that exist in batch b: kv_len[b] clamped to [0, N] (all N without a mask)."""
+    if kv_len is None:
+        return None
+    return int(min(max(int(kv_len[b]), 0), N))
+
+
+def attention_fwd(q, k, v, scale, causal=False, kv_len=None):
+    """O = softmax(scale * Q K^T [+ causal mask] [+ key-padding mask]) V and LSE, per (b, h) head.
 
     The definition written out: the full N x N score matrix of each head,
     row softmax, then P @ V (page 2, section "Kernel Fusion", the unfused path).
+    k, v may have H_kv heads (H a multiple of H_kv); kv_len: optional [B] key counts.
     Returns (O [B,H,N,d], LSE [B,H,N]).
     """
     q, k, v = _as64(q), _as64(k), _as64(v)
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     o = np.empty_like(q)
     lse = np.empty((B, H, N))
     for b in range(B):
         for h in range(H):
-            s = head_scores(q[b, h], k[b, h], scale, causal)
+            hk = _kv_head(h, H, Hkv)
+            s = head_scores(q[b, h], k[b, hk], scale, causal, kv_len=_key_count(kv_len, b, N))
             p, l = _softmax_rows(s)
-            o[b, h] = p @ v[b, h]
+            o[b, h] = p @ v[b, hk]
             lse[b, h] = l
     return o, lse
 
 
-def attention_bwd(q, k, v, do, scale, causal=False):
+def attention_bwd(q, k, v, do, scale, causal=False, kv_len=None):
     """Gradients of the forward w.r.t. Q, K, V for upstream dO.
 
     Per head, with P the forward probabilities and O the oracle's own fp64
@@ -112,24 +147,28 @@ def attention_bwd(q, k, v, do, scale, causal=False):
     dQ = scale * dS K;  dK = scale * dS^T Q.
     Page 2, section "Re-computation": the backward rebuilds the scores
     q @ k^T / sqrt(d) and the probabilities instead of storing them; here the
-    whole head is rebuilt at once (no blocking). Returns (dQ, dK, dV).
+    whole head is rebuilt at once (no blocking). With H_kv < H K/V heads, a K/V
+    head's dK and dV are the sums over the query heads that read it.
+    Returns (dQ, dK, dV).
     """
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     dq = np.empty_like(q)
-    dk = np.empty_like(k)
-    dv = np.empty_like(v)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
     for b in range(B):
         for h in range(H):
-            s = head_scores(q[b, h], k[b, h], scale, causal)
+            hk = _kv_head(h, H, Hkv)
+            s = head_scores(q[b, h], k[b, hk], scale, causal, kv_len=_key_count(kv_len, b, N))
             p, _ = _softmax_rows(s)
-            o = p @ v[b, h]
-            dv[b, h] = p.T @ do[b, h]
-            dp = do[b, h] @ v[b, h].T
+            o = p @ v[b, hk]
+            dv[b, hk] += p.T @ do[b, h]
+            dp = do[b, h] @ v[b, hk].T
             D = np.sum(do[b, h] * o, axis=-1, keepdims=True)
             ds = p * (dp - D)
-            dq[b, h] = scale * (ds @ k[b, h])
-            dk[b, h] = scale * (ds.T @ q[b, h])
+            dq[b, h] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h])
     return dq, dk, dv
 
 

@@ -78,6 +78,7 @@ def cancel_tol(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, scal
     matters only where the exact gradient vanishes.
     """
     d = q.shape[-1]
-    absdot = np.einsum("bhik,bhjk->bhij", np.abs(do), np.abs(v)).max()
+    G = do.shape[1] // v.shape[1]  # query heads per K/V head
+    absdot = np.einsum("bhik,bhjk->bhij", np.abs(do), np.repeat(np.abs(v), G, axis=1)).max()
     base = 4 * d * 2.0 ** -24 * scale * absdot
     return {"dQ": base * np.abs(k).max(), "dK": base * np.abs(q).max(), "dV": 0.0}

@@ -49,7 +49,7 @@ def test_status_strings_and_version(L):
     for code, name in _lib.STATUS_NAMES.items():
         assert L.fa_status_string(code).decode() == name
     assert L.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert L.fa_version() == 100
+    assert L.fa_version() == 101
 
 
 def test_workspace_size(L):
@@ -76,6 +76,7 @@ def fwd(L, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=256, d=64, scale=0.125, causal
     (dict(N=0), 2), (dict(N=-5), 2), (dict(d=96), 2), (dict(d=32), 2), (dict(B=0), 2),
     (dict(H=-1), 2), (dict(B=1 << 16, H=1 << 8, N=1 << 8), 2),
     (dict(dtype=7), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-1.0), 1),
+    (dict(scale=0.0), 1),
     (dict(q=P + 8), 3), (dict(o=P + 2), 3), (dict(lse=P + 4), 3),
 ])
 def test_fwd_rejects_bad_arguments(L, kw, code):
@@ -101,6 +102,25 @@ def test_bwd_rejects_bad_arguments(L):
 def test_fwd_ex_rejects_misaligned_residual(L):
     assert L.fa_fwd_ex(V(P), V(P), V(P), V(P), V(P), V(P + 2), 1, 1, 256, 64, 0.125, 0, 0, None) == 3
     assert L.fa_fwd_ex(V(P), V(P), V(P), V(P), V(0), V(P), 1, 1, 256, 64, 0.125, 0, 0, None) == 1
+
+
+def fwd_opt(L, H=4, n_kv_heads=0, kv_len=None, o_fp32=0, o_lo=None):
+    opt = _lib.FAOptions(n_kv_heads, kv_len, o_fp32)
+    return L.fa_fwd_opt(V(P), V(P), V(P), V(P), V(P), V(o_lo), 1, H, 256, 64, 0.125, 0, 0, ctypes.byref(opt), None)
+
+
+def bwd_opt(L, H=4, n_kv_heads=0, kv_len=None, o_fp32=0, o_lo=None):
+    opt = _lib.FAOptions(n_kv_heads, kv_len, o_fp32)
+    return L.fa_bwd_opt(V(P), V(P), V(P), V(P), V(P), V(P), V(P), V(P), V(P), V(o_lo), V(P), 1 << 40, 1, H, 256, 64,
+                        0.125, 0, 0, ctypes.byref(opt), None)
+
+
+@pytest.mark.parametrize("call", [fwd_opt, bwd_opt])
+def test_options_reject_bad_arguments(L, call):
+    assert call(L, n_kv_heads=3) == 2           # 4 query heads cannot share 3 K/V heads evenly
+    assert call(L, n_kv_heads=-1) == 1
+    assert call(L, kv_len=P + 2) == 3           # int32 key counts need 4-byte alignment
+    assert call(L, o_fp32=1, o_lo=P) == 1       # an fp32 O has no rounding residual
 
 
 def test_selftest_rejects_bad_arguments(L):

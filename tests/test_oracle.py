@@ -237,3 +237,112 @@ def test_backward_matches_central_differences(causal, N, d):
             minus[which][idx] -= h
             fd[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
         assert np.abs(fd - grad).max() <= 1e-6 * np.abs(grad).max(), which
+
+
+# ---------------------------------------------------------------- grouped K/V heads, key padding
+def _fd_grads(q, k, v, do, scale, causal, kv_len=None, h=1e-6):
+    """Central differences of L = sum(dO * O) w.r.t. q, k, v, straight from the forward definition."""
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_fwd(qq, kk, vv, scale, causal, kv_len=kv_len)
+        return float(np.sum(do * o))
+
+    out = []
+    args = [q, k, v]
+    for which in range(3):
+        fd = np.zeros_like(args[which])
+        for idx in np.ndindex(fd.shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fd[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        out.append(fd)
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_grouped_heads_equal_repeated_heads(causal, Hkv):
+    """K/V shared by H / H_kv query heads = plain attention on K/V repeated per query head;
+    the shared head's gradient is the sum of the repeated heads' gradients."""
+    B, H, N, d = 2, 4, 11, 8
+    q, do = _rand((B, H, N, d), 40), _rand((B, H, N, d), 41)
+    k, v = _rand((B, Hkv, N, d), 42), _rand((B, Hkv, N, d), 43)
+    G = H // Hkv
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    o, lse = oracle.attention_fwd(q, k, v, 0.3, causal)
+    o_r, lse_r = oracle.attention_fwd(q, kr, vr, 0.3, causal)
+    np.testing.assert_allclose(o, o_r, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_r, atol=1e-14)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.3, causal)
+    dq_r, dk_r, dv_r = oracle.attention_bwd(q, kr, vr, do, 0.3, causal)
+    assert dk.shape == k.shape and dv.shape == v.shape
+    np.testing.assert_allclose(dq, dq_r, atol=1e-13)
+    np.testing.assert_allclose(dk, dk_r.reshape(B, Hkv, G, N, d).sum(axis=2), atol=1e-13)
+    np.testing.assert_allclose(dv, dv_r.reshape(B, Hkv, G, N, d).sum(axis=2), atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads_match_central_differences(causal):
+    B, H, Hkv, N, d = 1, 3, 1, 6, 3
+    q, do = _rand((B, H, N, d), 50), _rand((B, H, N, d), 51)
+    k, v = _rand((B, Hkv, N, d), 52), _rand((B, Hkv, N, d), 53)
+    grads = oracle.attention_bwd(q, k, v, do, 0.6, causal)
+    for g, fd in zip(grads, _fd_grads(q, k, v, do, 0.6, causal)):
+        assert np.abs(fd - g).max() <= 1e-6 * np.abs(g).max()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_padding_equals_truncated_keys(causal):
+    """kv_len[b] = L: the same as attention over the first L keys only; padded keys get zero gradients."""
+    B, H, N, d = 3, 2, 10, 4
+    q, k, v, do = (_rand((B, H, N, d), 60 + s) for s in range(4))
+    kv_len = np.array([10, 4, 7])
+    o, lse = oracle.attention_fwd(q, k, v, 0.5, causal, kv_len=kv_len)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.5, causal, kv_len=kv_len)
+    for b, L in enumerate(kv_len):
+        if causal:
+            # a causal row i < L sees keys 0..i in both problems; rows i >= L see keys 0..L-1
+            qb = q[b:b + 1]
+            ot, lt = oracle.attention_fwd(qb[:, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.5, True)
+            np.testing.assert_allclose(o[b, :, :L], ot[0], atol=1e-14)
+            np.testing.assert_allclose(lse[b, :, :L], lt[0], atol=1e-14)
+            of, lf = oracle.attention_fwd(qb, k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.5, False)
+            np.testing.assert_allclose(o[b, :, L:], of[0, :, L:], atol=1e-14)
+            np.testing.assert_allclose(lse[b, :, L:], lf[0, :, L:], atol=1e-14)
+        else:
+            ot, lt = oracle.attention_fwd(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.5, False)
+            np.testing.assert_allclose(o[b], ot[0], atol=1e-14)
+            np.testing.assert_allclose(lse[b], lt[0], atol=1e-14)
+            gq, gk, gv = oracle.attention_bwd(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], do[b:b + 1], 0.5,
+                                              False)
+            np.testing.assert_allclose(dq[b], gq[0], atol=1e-13)
+            np.testing.assert_allclose(dk[b, :, :L], gk[0], atol=1e-13)
+            np.testing.assert_allclose(dv[b, :, :L], gv[0], atol=1e-13)
+        assert not dk[b, :, L:].any() and not dv[b, :, L:].any()
+
+
+def test_key_padding_matches_central_differences():
+    B, H, N, d = 2, 1, 6, 3
+    q, k, v, do = (_rand((B, H, N, d), 70 + s) for s in range(4))
+    kv_len = np.array([4, 6])
+    for causal in (False, True):
+        grads = oracle.attention_bwd(q, k, v, do, 0.7, causal, kv_len=kv_len)
+        for g, fd in zip(grads, _fd_grads(q, k, v, do, 0.7, causal, kv_len=kv_len)):
+            assert np.abs(fd - g).max() <= 1e-6 * np.abs(g).max()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_no_visible_key_gives_zero_output(causal):
+    B, H, N, d = 2, 2, 5, 4
+    q, k, v, do = (_rand((B, H, N, d), 80 + s) for s in range(4))
+    kv_len = np.array([0, -3])  # clamped to 0
+    o, lse = oracle.attention_fwd(q, k, v, 0.5, causal, kv_len=kv_len)
+    assert not o.any() and np.isneginf(lse).all()
+    for g in oracle.attention_bwd(q, k, v, do, 0.5, causal, kv_len=kv_len):
+        assert not g.any()
+    # kv_len >= N is no mask at all
+    o2, lse2 = oracle.attention_fwd(q, k, v, 0.5, causal, kv_len=np.array([N, N + 7]))
+    o3, lse3 = oracle.attention_fwd(q, k, v, 0.5, causal)
+    np.testing.assert_array_equal(o2, o3)
+    np.testing.assert_array_equal(lse2, lse3)

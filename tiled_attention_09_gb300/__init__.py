@@ -11,7 +11,10 @@ these functions raise if the library is missing or the tensors are not on a
 CUDA device.
 
 Tensors are ``[B, H, N, d]``, contiguous, fp16 or bf16; ``lse`` is fp32
-``[B, H, N]``. ``scale`` defaults to ``d ** -0.5``.
+``[B, H, N]``. ``scale`` defaults to ``d ** -0.5``. Options (``fa_fwd_opt`` /
+``fa_bwd_opt``): ``k``/``v`` may have fewer heads than ``q`` (grouped-query or
+multi-query attention, ``H % H_kv == 0``); ``kv_len`` (int32 ``[B]`` on the
+device) masks keys ``j >= kv_len[b]``; ``out_fp32`` makes O fp32.
 """
 from __future__ import annotations
 
@@ -55,6 +58,28 @@ def _check_qkv(*ts: torch.Tensor):
             raise ValueError("tensors must be contiguous")
 
 
+def _check_kv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
+    """k, v: [B, H_kv, N, d] with H % H_kv == 0, q's dtype and device. Returns H_kv."""
+    _check_qkv(q)
+    _check_qkv(k, v)
+    B, H, N, d = q.shape
+    if k.dim() != 4 or k.shape[0] != B or k.shape[2:] != q.shape[2:] or k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("k, v must be [B, H_kv, N, d] with q's B, N, d, dtype and device")
+    if H % k.shape[1] != 0:
+        raise ValueError(f"H = {H} is not a multiple of H_kv = {k.shape[1]}")
+    return int(k.shape[1])
+
+
+def _options(H, Hkv, kv_len, out_fp32, device):
+    """fa_options for the call, or None when every option has its default."""
+    if Hkv == H and kv_len is None and not out_fp32:
+        return None
+    if kv_len is not None:
+        if kv_len.dtype != torch.int32 or kv_len.device != device or not kv_len.is_contiguous():
+            raise ValueError("kv_len must be a contiguous int32 tensor on q's device")
+    return _lib.FAOptions(Hkv, kv_len.data_ptr() if kv_len is not None else None, int(bool(out_fp32)))
+
+
 def device_status(stream=None):
     """Synchronise and read/clear the kernels' device status word. Returns (code_name, info)."""
     L = _lib.load()
@@ -75,31 +100,54 @@ def workspace_size(B, H, N, d) -> int:
     return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
 
 
-def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, residual=False, o_lo=None):
-    """Forward: returns (o, lse), or (o, lse, o_lo) with residual=True (fa_fwd_ex).
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, residual=False, o_lo=None, kv_len=None,
+        out_fp32=False):
+    """Forward: returns (o, lse), or (o, lse, o_lo) with residual=True (fa_fwd_ex / fa_fwd_opt).
 
     o_lo is the rounding residual of o (O_fp32 - o in the same dtype); pass it
-    to ``bwd`` so that D = rowsum(dO * O) uses O at fp32 accuracy.
+    to ``bwd`` so that D = rowsum(dO * O) uses O at fp32 accuracy. k, v may have
+    fewer heads than q; kv_len masks keys per batch; out_fp32 writes o as fp32
+    (no residual then).
     """
-    _check_qkv(q, k, v)
+    Hkv = _check_kv(q, k, v)
     B, H, N, d = q.shape
+    if out_fp32 and residual:
+        raise ValueError("an fp32 output has no rounding residual")
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
+    if out is None:
+        o = torch.empty(q.shape, device=q.device, dtype=torch.float32) if out_fp32 else torch.empty_like(q)
+    else:
+        o = out
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
     if residual and o_lo is None:
         o_lo = torch.empty_like(q)
     L = _lib.load()
-    code = L.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                       o_lo.data_ptr() if residual else None, B, H, N, d, scale, int(bool(causal)), _DT[q.dtype],
-                       _stream_ptr(q))
-    _lib.check("fa_fwd_ex", code)
-    _after("fa_fwd_ex", q)
+    opt = _options(H, Hkv, kv_len, out_fp32, q.device)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            o_lo.data_ptr() if residual else None, B, H, N, d, scale, int(bool(causal)), _DT[q.dtype])
+    if opt is None:
+        name, code = "fa_fwd_ex", L.fa_fwd_ex(*args, _stream_ptr(q))
+    else:
+        name, code = "fa_fwd_opt", L.fa_fwd_opt(*args, ctypes.byref(opt), _stream_ptr(q))
+    _lib.check(name, code)
+    _after(name, q)
     return (o, lse, o_lo) if residual else (o, lse)
 
 
-def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None, o_lo=None):
-    """Backward: returns (dq, dk, dv). o_lo: the residual from ``fwd(..., residual=True)``, or None."""
-    _check_qkv(q, k, v, o, do)
+def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None, o_lo=None,
+        kv_len=None):
+    """Backward: returns (dq, dk, dv). o_lo: the residual from ``fwd(..., residual=True)``, or None.
+
+    k, v (and dk, dv) may have fewer heads than q; kv_len as given to ``fwd``; o may be fp32.
+    """
+    Hkv = _check_kv(q, k, v)
+    _check_qkv(q, do)
+    out_fp32 = o.dtype == torch.float32
+    if out_fp32:
+        if o.shape != q.shape or o.device != q.device or not o.is_contiguous():
+            raise ValueError("o must be contiguous [B, H, N, d] on q's device")
+    else:
+        _check_qkv(q, o)
     if o_lo is not None:
         _check_qkv(q, o_lo)
     B, H, N, d = q.shape
@@ -111,34 +159,41 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    code = L.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o_lo.data_ptr() if o_lo is not None else None,
-                    workspace.data_ptr(), workspace.numel(), B, H, N, d, scale, int(bool(causal)), _DT[q.dtype],
-                    _stream_ptr(q))
-    _lib.check("fa_bwd", code)
-    _after("fa_bwd", q)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o_lo.data_ptr() if o_lo is not None else None,
+            workspace.data_ptr(), workspace.numel(), B, H, N, d, scale, int(bool(causal)), _DT[q.dtype])
+    opt = _options(H, Hkv, kv_len, out_fp32, q.device)
+    if opt is None:
+        name, code = "fa_bwd", L.fa_bwd(*args, _stream_ptr(q))
+    else:
+        name, code = "fa_bwd_opt", L.fa_bwd_opt(*args, ctypes.byref(opt), _stream_ptr(q))
+    _lib.check(name, code)
+    _after(name, q)
     return dq, dk, dv
 
 
 class _AttentionFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, scale):
+    def forward(ctx, q, k, v, causal, scale, kv_len):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        o, lse, o_lo = fwd(q, k, v, causal, scale, residual=True)
+        o, lse, o_lo = fwd(q, k, v, causal, scale, residual=True, kv_len=kv_len)
         ctx.save_for_backward(q, k, v, o, lse, o_lo)
-        ctx.causal, ctx.scale = causal, scale
+        ctx.causal, ctx.scale, ctx.kv_len = causal, scale, kv_len
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse, o_lo = ctx.saved_tensors
-        dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), ctx.causal, ctx.scale, o_lo=o_lo)
-        return dq, dk, dv, None, None
+        dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), ctx.causal, ctx.scale, o_lo=o_lo, kv_len=ctx.kv_len)
+        return dq, dk, dv, None, None, None
 
 
-def attention(q, k, v, causal=False, scale=None):
-    """Differentiable exact attention over [B, H, N, d] fp16/bf16 CUDA tensors."""
-    return _AttentionFn.apply(q, k, v, causal, scale)
+def attention(q, k, v, causal=False, scale=None, kv_len=None):
+    """Differentiable exact attention over [B, H, N, d] fp16/bf16 CUDA tensors.
+
+    k, v may be [B, H_kv, N, d] (grouped-query / multi-query); kv_len: optional int32 [B] key counts.
+    """
+    return _AttentionFn.apply(q, k, v, causal, scale, kv_len)
 
 
 def selftest_gemm(a, b, n, k, a_mode, b_mode):

@@ -25,14 +25,24 @@ STATUS_NAMES = {
 }
 FA_F16, FA_BF16 = 0, 1
 
+
+class FAOptions(ctypes.Structure):
+    """struct fa_options of include/fa.h."""
+    _fields_ = [("n_kv_heads", c_int), ("kv_len", c_void_p), ("o_fp32", c_int)]
+
+
 # (name, restype, argtypes) for every symbol declared in include/fa.h and include/fa_selftest.h
 SIGNATURES = [
     ("fa_fwd", c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_float, c_int,
                        c_int, c_void_p]),
     ("fa_fwd_ex", c_int, [c_void_p] * 6 + [c_int, c_int, c_int, c_int, c_float, c_int, c_int, c_void_p]),
+    ("fa_fwd_opt", c_int, [c_void_p] * 6 + [c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                            ctypes.POINTER(FAOptions), c_void_p]),
     ("fa_bwd_workspace_size", c_size_t, [c_int, c_int, c_int, c_int]),
     ("fa_bwd", c_int, [c_void_p] * 10 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
                                          c_void_p]),
+    ("fa_bwd_opt", c_int, [c_void_p] * 10 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                             ctypes.POINTER(FAOptions), c_void_p]),
     ("fa_bwd_noalloc", c_int, [c_void_p] * 10 + [c_int, c_int, c_int, c_int, c_float, c_int, c_int, c_void_p]),
     ("fa_bwd_preprocess", c_int, [c_void_p] * 5 + [c_size_t, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     ("fa_bwd_main", c_int, [c_void_p] * 7 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,

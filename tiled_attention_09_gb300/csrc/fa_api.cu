@@ -71,7 +71,7 @@ fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype) {
 }
 
 fa_status check_scale(float scale) {
-  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
@@ -94,6 +94,29 @@ WsLayout ws_layout(int B, int H, int N, int d) {
   return w;
 }
 
+// Options resolved against the shape: K/V heads (0 = H, must divide H), key counts, fp32 O.
+struct Opts {
+  int Hkv;
+  const int* kv_len;
+  bool o_f32;
+};
+fa_status resolve_opts(const fa_options* opt, int H, const void* o_lo, Opts* out) {
+  out->Hkv = H;
+  out->kv_len = nullptr;
+  out->o_f32 = false;
+  if (!opt) return FA_OK;
+  if (opt->n_kv_heads < 0) return FA_ERR_INVALID_ARG;
+  if (opt->n_kv_heads > 0) {
+    if (H % opt->n_kv_heads != 0) return FA_ERR_UNSUPPORTED;
+    out->Hkv = opt->n_kv_heads;
+  }
+  if (opt->kv_len && (reinterpret_cast<uintptr_t>(opt->kv_len) & 3u) != 0) return FA_ERR_ALIGNMENT;
+  out->kv_len = opt->kv_len;
+  out->o_f32 = opt->o_fp32 != 0;
+  if (out->o_f32 && o_lo) return FA_ERR_INVALID_ARG;  // the residual belongs to a 16-bit O
+  return FA_OK;
+}
+
 fa_status bwd_common(fa::BwdArgs* a, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                      float scale, int causal, fa_dtype dtype, void* stream) {
   fa_status s = check_shape(B, H, N, d, dtype);
@@ -108,6 +131,7 @@ fa_status bwd_common(fa::BwdArgs* a, void* workspace, size_t workspace_bytes, in
   a->ws_dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_dq);
   a->B = B;
   a->H = H;
+  a->Hkv = H;
   a->N = N;
   a->Npad = pad_rows(N);
   a->d = d;
@@ -119,11 +143,55 @@ fa_status bwd_common(fa::BwdArgs* a, void* workspace, size_t workspace_bytes, in
   return FA_OK;
 }
 
+fa_status bwd_preprocess_impl(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
+                              size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, const Opts& op,
+                              void* stream) {
+  if (!o || !dO || !lse) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{};
+  fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, 1.0f, 0, dtype, stream);
+  if (s != FA_OK) return s;
+  if (!aligned16(o) || !aligned16(o_lo) || !aligned16(dO) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  a.o = o;
+  a.o_lo = o_lo;
+  a.o_f32 = op.o_f32;
+  a.dO = dO;
+  a.lse = lse;
+  return fa::launch_bwd_preprocess(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, void* dq,
+                        void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                        fa_dtype dtype, const Opts& op, void* stream) {
+  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{};
+  fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
+  if (s != FA_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(dq))
+    return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  const int bq = fa::bwd_query_tile(d);
+  if (bq == 0) return FA_ERR_UNSUPPORTED;
+  const long long heads = static_cast<long long>(B) * H, kv_heads = static_cast<long long>(B) * op.Hkv;
+  if (!make_map(&a.tm_q, q, heads, N, d, a.bf16, bq) || !make_map(&a.tm_do, dO, heads, N, d, a.bf16, bq) ||
+      !make_map(&a.tm_k, k, kv_heads, N, d, a.bf16, 128) || !make_map(&a.tm_v, v, kv_heads, N, d, a.bf16, 128) ||
+      !make_map(&a.tm_dk, dk, kv_heads, N, d, a.bf16, 128) || !make_map(&a.tm_dv, dv, kv_heads, N, d, a.bf16, 128))
+    return FA_ERR_CUDA;
+  a.Hkv = op.Hkv;
+  a.kv_len = op.kv_len;
+  a.dO = dO;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq = dq;  // optional: when given, the dQ conversion is enqueued right after the main kernel
+  return fa::launch_bwd_main(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 101; }
 
 void fa_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns ? ns : 4000000000ull; }
 
@@ -148,26 +216,36 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H, int N,
                     int d, float scale, int causal, fa_dtype dtype, void* stream) {
+  return fa_fwd_opt(q, k, v, o, lse, o_lo, B, H, N, d, scale, causal, dtype, nullptr, stream);
+}
+
+fa_status fa_fwd_opt(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H,
+                     int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   fa_status s = check_shape(B, H, N, d, dtype);
   if (s != FA_OK) return s;
   if ((s = check_scale(scale)) != FA_OK) return s;
+  Opts op;
+  if ((s = resolve_opts(opt, H, o_lo, &op)) != FA_OK) return s;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(o_lo))
     return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
   fa::FwdArgs a;
   const bool bf16 = dtype == FA_BF16;
-  const long long heads = static_cast<long long>(B) * H;
-  if (!make_map(&a.tm_q, q, heads, N, d, bf16, 128) || !make_map(&a.tm_k, k, heads, N, d, bf16, 128) ||
-      !make_map(&a.tm_v, v, heads, N, d, bf16, 128))
+  const long long heads = static_cast<long long>(B) * H, kv_heads = static_cast<long long>(B) * op.Hkv;
+  if (!make_map(&a.tm_q, q, heads, N, d, bf16, 128) || !make_map(&a.tm_k, k, kv_heads, N, d, bf16, 128) ||
+      !make_map(&a.tm_v, v, kv_heads, N, d, bf16, 128))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;
   a.o_lo = o_lo;
+  a.kv_len = op.kv_len;
   a.B = B;
   a.H = H;
+  a.Hkv = op.Hkv;
   a.N = N;
   a.d = d;
+  a.o_f32 = op.o_f32;
   a.scale = scale;
   a.causal = causal != 0;
   a.bf16 = bf16;
@@ -183,42 +261,15 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 fa_status fa_bwd_preprocess(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
                             size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream) {
-  if (!o || !dO || !lse) return FA_ERR_INVALID_ARG;
-  fa::BwdArgs a{};
-  fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, 1.0f, 0, dtype, stream);
-  if (s != FA_OK) return s;
-  if (!aligned16(o) || !aligned16(o_lo) || !aligned16(dO) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
-  if ((s = check_device()) != FA_OK) return s;
-  a.o = o;
-  a.o_lo = o_lo;
-  a.dO = dO;
-  a.lse = lse;
-  return fa::launch_bwd_preprocess(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return bwd_preprocess_impl(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, Opts{H, nullptr, false},
+                             stream);
 }
 
 fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, void* dq,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                       fa_dtype dtype, void* stream) {
-  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
-  fa::BwdArgs a{};
-  fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
-  if (s != FA_OK) return s;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) || !aligned16(dv) ||
-      !aligned16(dq))
-    return FA_ERR_ALIGNMENT;
-  if ((s = check_device()) != FA_OK) return s;
-  const int bq = fa::bwd_query_tile(d);
-  if (bq == 0) return FA_ERR_UNSUPPORTED;
-  const long long heads = static_cast<long long>(B) * H;
-  if (!make_map(&a.tm_q, q, heads, N, d, a.bf16, bq) || !make_map(&a.tm_do, dO, heads, N, d, a.bf16, bq) ||
-      !make_map(&a.tm_k, k, heads, N, d, a.bf16, 128) || !make_map(&a.tm_v, v, heads, N, d, a.bf16, 128) ||
-      !make_map(&a.tm_dk, dk, heads, N, d, a.bf16, 128) || !make_map(&a.tm_dv, dv, heads, N, d, a.bf16, 128))
-    return FA_ERR_CUDA;
-  a.dO = dO;
-  a.dk = dk;
-  a.dv = dv;
-  a.dq = dq;  // optional: when given, the dQ conversion is enqueued right after the main kernel
-  return fa::launch_bwd_main(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return bwd_main_impl(q, k, v, dO, dk, dv, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype,
+                       Opts{H, nullptr, false}, stream);
 }
 
 fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
@@ -236,20 +287,31 @@ fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_by
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, const void* o_lo, void* workspace, size_t workspace_bytes, int B, int H,
                  int N, int d, float scale, int causal, fa_dtype dtype, void* stream) {
+  return fa_bwd_opt(q, k, v, o, dO, lse, dq, dk, dv, o_lo, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                    dtype, nullptr, stream);
+}
+
+fa_status fa_bwd_opt(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                     void* dq, void* dk, void* dv, const void* o_lo, void* workspace, size_t workspace_bytes, int B,
+                     int H, int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt,
+                     void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   // Validate everything before enqueuing anything.
   fa::BwdArgs probe{};
   fa_status s = bwd_common(&probe, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
   if (s != FA_OK) return s;
+  Opts op;
+  if ((s = resolve_opts(opt, H, o_lo, &op)) != FA_OK) return s;
   if (fa::bwd_query_tile(d) == 0) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(o_lo))
     return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
-  if ((s = fa_bwd_preprocess(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK)
+  if ((s = bwd_preprocess_impl(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, op, stream)) != FA_OK)
     return s;
-  // given dq, fa_bwd_main enqueues the dQ conversion right after the main kernel
-  return fa_bwd_main(q, k, v, dO, dk, dv, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
+  // given dq, the main kernel's launch enqueues the dQ conversion right after it
+  return bwd_main_impl(q, k, v, dO, dk, dv, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, op,
+                       stream);
 }
 
 fa_status fa_device_status(void* stream, unsigned int info[4]) {

@@ -23,12 +23,12 @@ cudaError_t launch_pre_t(const BwdArgs& a) {
   if (a.bf16)
     return launch_kernel(fa_bwd_preprocess_kernel<VPR, true>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
                          static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
-                         static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
-                         reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
+                         a.o_f32 ? static_cast<const float4*>(a.o) : nullptr, static_cast<const uint4*>(a.dO),
+                         a.lse, a.ws_D, a.ws_lse2, reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
   return launch_kernel(fa_bwd_preprocess_kernel<VPR, false>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
                        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
-                       static_cast<const uint4*>(a.dO), a.lse, a.ws_D, a.ws_lse2,
-                       reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
+                       a.o_f32 ? static_cast<const float4*>(a.o) : nullptr, static_cast<const uint4*>(a.dO),
+                       a.lse, a.ws_D, a.ws_lse2, reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
 }
 template <int VPR>
 cudaError_t launch_convert_t(const BwdArgs& a) {
@@ -63,6 +63,30 @@ cudaError_t launch_bwd_dq_convert(const BwdArgs& a) {
 }
 
 namespace {
+BwdParams bwd_params(const BwdArgs& a) {
+  BwdParams p;
+  p.tm_q = a.tm_q;
+  p.tm_k = a.tm_k;
+  p.tm_v = a.tm_v;
+  p.tm_do = a.tm_do;
+  p.tm_dk = a.tm_dk;
+  p.tm_dv = a.tm_dv;
+  p.lse2 = a.ws_lse2;
+  p.Dvec = a.ws_D;
+  p.dqacc = a.ws_dqacc;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.kv_len = a.kv_len;
+  p.N = a.N;
+  p.Npad = a.Npad;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.timeout_ns = a.timeout_ns;
+  return p;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_pipe_t(const BwdArgs& a) {
   using C = BwdPipeCfg<D>;
@@ -76,24 +100,8 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
     if (fa_attr.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     checked = 1;
   }
-  BwdParams p;
-  p.tm_q = a.tm_q;
-  p.tm_k = a.tm_k;
-  p.tm_v = a.tm_v;
-  p.tm_do = a.tm_do;
-  p.tm_dk = a.tm_dk;
-  p.tm_dv = a.tm_dv;
-  p.lse2 = a.ws_lse2;
-  p.Dvec = a.ws_D;
-  p.dqacc = a.ws_dqacc;
-  p.dk = a.dk;
-  p.dv = a.dv;
-  p.N = a.N;
-  p.Npad = a.Npad;
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.timeout_ns = a.timeout_ns;
-  dim3 grid(a.B * a.H, (a.N + 127) / 128, 1);  // key blocks; the last may run past N
+  const BwdParams p = bwd_params(a);
+  dim3 grid(a.B * a.Hkv, (a.N + 127) / 128, 1);  // key blocks of each K/V head; the last may run past N
   e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
@@ -104,24 +112,8 @@ cudaError_t launch_d256_t(const BwdArgs& a) {
   auto kern = fa_bwd_d256_kernel<BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  BwdParams p;
-  p.tm_q = a.tm_q;
-  p.tm_k = a.tm_k;
-  p.tm_v = a.tm_v;
-  p.tm_do = a.tm_do;
-  p.tm_dk = a.tm_dk;
-  p.tm_dv = a.tm_dv;
-  p.lse2 = a.ws_lse2;
-  p.Dvec = a.ws_D;
-  p.dqacc = a.ws_dqacc;
-  p.dk = a.dk;
-  p.dv = a.dv;
-  p.N = a.N;
-  p.Npad = a.Npad;
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.timeout_ns = a.timeout_ns;
-  dim3 grid(a.B * a.H, (a.N + 127) / 128, 1);  // key blocks; the last may run past N
+  const BwdParams p = bwd_params(a);
+  dim3 grid(a.B * a.Hkv, (a.N + 127) / 128, 1);  // key blocks of each K/V head; the last may run past N
   e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);

@@ -1,6 +1,7 @@
 // Bandwidth-bound helper kernels of the backward pass (no tensor cores):
 //   K2 preprocess: D_i = sum_k dO_ik * O_ik (fp32; O = o + o_lo when the forward's rounding
-//                  residual o_lo is given), LSE_i * log2(e), dQ accumulator := 0 (padded rows)
+//                  residual o_lo is given, O read as fp32 when the forward wrote it so),
+//                  LSE_i * log2(e), dQ accumulator := 0 (padded rows)
 //   K4 dQ convert: dQ = dtype(scale * dQacc)
 // Each thread owns one 16-byte vector (8 elements) of a row; the d/8 threads of
 // a row sit in one warp and reduce with shuffles. Grid-stride loops keep the
@@ -53,6 +54,7 @@ __device__ __forceinline__ uint32_t pack2f(float lo, float hi) {
 template <int VPR, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __restrict__ o,
                                                                  const uint4* __restrict__ o_lo,
+                                                                 const float4* __restrict__ o32,
                                                                  const uint4* __restrict__ dO,
                                                                  const float* __restrict__ lse, float* __restrict__ D,
                                                                  float* __restrict__ lse2, float4* __restrict__ dqacc,
@@ -67,7 +69,13 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
     if (real) {
       const size_t src = row * VPR + (i % VPR);
       float a[8], b[8];
-      unpack8<BF16>(__ldg(&o[src]), a);
+      if (o32) {  // O given in fp32
+        const float4 x = __ldg(&o32[2 * src]), y = __ldg(&o32[2 * src + 1]);
+        a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+        a[4] = y.x; a[5] = y.y; a[6] = y.z; a[7] = y.w;
+      } else {
+        unpack8<BF16>(__ldg(&o[src]), a);
+      }
       unpack8<BF16>(__ldg(&dO[src]), b);
       if (o_lo) {  // O reconstructed to fp32 accuracy: o + residual
         float rr[8];

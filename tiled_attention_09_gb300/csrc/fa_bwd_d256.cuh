@@ -76,12 +76,13 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int N = p.N;
-  const int bh = blockIdx.x;
+  const int bh = blockIdx.x;  // K/V head (b, h_kv)
   const int key0 = blockIdx.y * 128;
-  const int ws_base = bh * p.Npad;  // row of (b, h, 0) in the workspace's padded rows
+  const BwdGroup grp(bh, p);  // the query heads that share this K/V head, and the batch's key count
   const int it0 = CAUSAL ? (key0 / BQ) : 0;
-  const int n_it = (N + BQ - 1) / BQ - it0;  // query steps per pass (the last may run past N: masked)
-  const int n_g = 2 * n_it;        // steps of both passes: g = h * n_it + it
+  const int n_ith = (N + BQ - 1) / BQ - it0;  // query steps per query head (the last may run past N: masked)
+  const int n_it = grp.G * n_ith;             // query steps per pass, head by head
+  const int n_g = 2 * n_it;                   // steps of both passes: g = h * n_it + it
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
@@ -125,13 +126,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         // second pass also waits for the first pass's epilogue, which staged dV / dK there
         if (g > 0 && !wait_bar(b_qempty, (g - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) break;
         if (g == n_it && !wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_QE)) break;
-        const int q_in = (it0 + it) * BQ;  // within the head; rows past N arrive as zeros
-        const int qrow = ws_base + q_in;    // LSE*log2e / D past N: the head's zero padding, masked
+        int qh, qs;
+        grp.step(it, it0, n_ith, qh, qs);
+        const int q_in = qs * BQ;             // within query head qh; rows past N arrive as zeros
+        const int qrow = qh * p.Npad + q_in;  // LSE*log2e / D past N: the head's zero padding, masked
         mbar_arrive_expect_tx(b_qfull, 2 * C::Q_TILE + 2 * BQ * 4);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfull, c * 64, q_in, bh);
-          tma_load_3d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfull, c * 64, q_in, bh);
+          tma_load_3d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfull, c * 64, q_in, qh);
+          tma_load_3d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfull, c * 64, q_in, qh);
         }
         bulk_load(s0 + C::OFF_LSE, p.lse2 + qrow, BQ * 4, b_qfull);
         bulk_load(s0 + C::OFF_DD, p.Dvec + qrow, BQ * 4, b_qfull);
@@ -221,12 +224,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         tc_fence_after();
         const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
         const float* dd_s = reinterpret_cast<const float*>(smem + C::OFF_DD);
-        const int q0 = (it0 + it) * BQ;  // first query of the tile
+        int qh, qs;
+        grp.step(it, it0, n_ith, qh, qs);
+        const int q0 = qs * BQ;  // first query of the tile
         // masked: column c < kq (key > query, causal), q0 + c >= N (query past the sequence) or the
-        // whole row when the key is past the sequence (zero K row: S = 0, exp(-LSE) need not be finite)
-        const bool need_mask = (CAUSAL && (q0 < key0 + 127)) || (q0 + BQ > N) || (key0 + 128 > N);
+        // whole row when the key does not exist (past N or past the batch's key count: S need not
+        // come from a real key, and exp(-LSE) need not be finite)
+        const bool need_mask = (CAUSAL && (q0 < key0 + 127)) || (q0 + BQ > N) || (key0 + 128 > grp.klen);
         const int kq = CAUSAL ? (key0 + k - q0) : 0;
-        const int qn = key0 + k < N ? N - q0 : 0;
+        const int qn = key0 + k < grp.klen ? N - q0 : 0;
         float pv[64];
         {
           uint32_t u0[32], u1[32];
@@ -305,7 +311,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         mbar_arrive(b_dqfree);
         if (*abort_flag == 0u) {
           // dQ[q][h*128 + t] += dQ^T[t][q]: a warp covers 128 contiguous bytes per query
-          float* dst = p.dqacc + static_cast<size_t>(ws_base + (it0 + it) * BQ) * D + h * DH + t;
+          int qh, qs;
+          grp.step(it, it0, n_ith, qh, qs);
+          float* dst = p.dqacc + static_cast<size_t>(qh * p.Npad + qs * BQ) * D + h * DH + t;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             atomicAdd(dst + c * D, __uint_as_float(u0[c]));

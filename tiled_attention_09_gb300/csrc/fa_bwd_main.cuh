@@ -27,13 +27,42 @@ struct BwdParams {
   const float* lse2;  // [B*H*Npad] LSE * log2(e); row (bh, r) at bh * Npad + r
   const float* Dvec;  // [B*H*Npad] rowsum(dO * O), same rows
   float* dqacc;       // [B*H*Npad, d] fp32, same rows
-  void* dk;           // [B*H*N, d] dtype outputs, written directly by kernels that store from registers
+  void* dk;           // [B*Hkv*N, d] dtype outputs, written directly by kernels that store from registers
   void* dv;
+  const int* kv_len;  // optional [B]: keys j >= kv_len[b] are masked for batch b (key padding)
   int N;
   int Npad;           // N rounded up to 64: the per-head row stride of lse2, Dvec and dqacc
+  int H, Hkv;         // query heads and K/V heads (Hkv divides H; H / Hkv query heads share one K/V head)
   float scale;
   float scale_log2;
   unsigned long long timeout_ns;
+};
+
+// Keys of batch b that exist: min(N, kv_len[b]) (clamped at 0), or N without a key-padding mask.
+__device__ __forceinline__ int bwd_key_count(const BwdParams& p, int b) {
+  if (!p.kv_len) return p.N;
+  const int l = __ldg(p.kv_len + b);
+  return l < 0 ? 0 : (l > p.N ? p.N : l);
+}
+
+// A key block of K/V head x (of the B*Hkv) feeds G = H / Hkv query heads; its query steps run
+// head by head: step `it` is 64-query step it0 + it % n_ith of query head qh0 + it / n_ith.
+struct BwdGroup {
+  int qh0;   // first query head (of the B*H) of the group
+  int G;     // query heads per K/V head
+  int klen;  // keys that exist for this batch (key padding and N)
+  __device__ __forceinline__ BwdGroup(int x, const BwdParams& p) {
+    G = p.H / p.Hkv;
+    const int b = x / p.Hkv;
+    qh0 = b * p.H + (x - b * p.Hkv) * G;
+    klen = bwd_key_count(p, b);
+  }
+  // query head and 64-query step (within the head) of step `it`
+  __device__ __forceinline__ void step(int it, int it0, int n_ith, int& qh, int& qs) const {
+    const int gi = G == 1 ? 0 : it / n_ith;
+    qh = qh0 + gi;
+    qs = it0 + it - gi * n_ith;
+  }
 };
 
 

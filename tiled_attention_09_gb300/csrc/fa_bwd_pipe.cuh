@@ -72,23 +72,25 @@ struct BwdPipeCfg {
   static_assert(SMEM_BYTES <= 232448, "smem budget");
 };
 
-// One work item: the 128-key block y of head x (blockIdx of the CTA launched for it; under
-// causal masking block 0 has the most query steps, so the launch order is longest-first).
+// One work item: the 128-key block y of K/V head x (blockIdx of the CTA launched for it; under
+// causal masking block 0 has the most query steps, so the launch order is longest-first). The
+// block's query steps run over the G query heads that share the K/V head, one head after another.
 template <bool CAUSAL>
 struct BwdItem {
-  int bh;        // head (b, h): the z coordinate of the tensor maps
-  int row_base;  // row of (b, h, 0) in the [B*H*N, d] view of the inputs and outputs
-  int ws_base;   // row of (b, h, 0) in the workspace's padded [B*H*Npad] rows
+  int bh;        // K/V head (b, h_kv): the z coordinate of the K, V maps
+  int row_base;  // row of (b, h_kv, 0) in the [B*Hkv*N, d] view of K, V, dK, dV
   int key0;      // first key of the block
-  int it0;       // first 64-query step (causal: the block's diagonal)
-  int n_it;      // query steps (the last may run past N: its extra queries are masked)
-  __device__ __forceinline__ BwdItem(int x, int y, int N, int Npad) {
+  int it0;       // first 64-query step of each query head (causal: the block's diagonal)
+  int n_ith;     // query steps per query head (the last may run past N: its extra queries are masked)
+  int n_it;      // query steps of the block: G * n_ith
+  BwdGroup grp;  // the query heads of the group and the batch's key count
+  __device__ __forceinline__ BwdItem(int x, int y, const BwdParams& p) : grp(x, p) {
     bh = x;
-    row_base = x * N;
-    ws_base = x * Npad;
+    row_base = x * p.N;
     key0 = y * 128;
     it0 = CAUSAL ? (key0 / 64) : 0;  // 64-query steps
-    n_it = (N + 63) / 64 - it0;
+    n_ith = (p.N + 63) / 64 - it0;
+    n_it = grp.G * n_ith;
   }
 };
 
@@ -205,13 +207,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       auto load_stage = [&](const Item& w, int it) -> bool {
         const uint32_t s = gs % NS, use = gs / NS;
         if (use > 0 && !wait_bar(b_qempty(s), (use - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) return false;
-        const int q_in = (w.it0 + it) * BQ;  // first query of the step within the head
-        const int qrow = w.ws_base + q_in;
+        int qh, qs;
+        w.grp.step(it, w.it0, w.n_ith, qh, qs);
+        const int q_in = qs * BQ;  // first query of the step within query head qh
+        const int qrow = qh * p.Npad + q_in;
         mbar_arrive_expect_tx(b_qfull(s), 2 * C::Q_TILE + 2 * BQ * 4);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(sQ + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_q, b_qfull(s), c * 64, q_in, w.bh);
-          tma_load_3d(sDO + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_do, b_qfull(s), c * 64, q_in, w.bh);
+          tma_load_3d(sQ + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_q, b_qfull(s), c * 64, q_in, qh);
+          tma_load_3d(sDO + s * C::Q_TILE + c * C::Q_CHUNK, &p.tm_do, b_qfull(s), c * 64, q_in, qh);
         }
         // LSE*log2e and D rows past N (a step that runs past the sequence) are the head's padding
         // rows (zeros), and the queries they belong to are masked
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         clc_pending = true;
       };
       while (ok) {
-        const Item w(ix, iy, N, p.Npad);
+        const Item w(ix, iy, p);
         const int pre = w.n_it < 2 ? w.n_it : 2;  // stages issued before the block's K/V can be
         const int ask_at = w.n_it - 2 > 0 ? w.n_it - 2 : 0;
         int it = 0;
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       int nb = 0;       // finished blocks
       bool ok = true;
       while (ok) {
-        const Item w(ix, iy, N, p.Npad);
+        const Item w(ix, iy, p);
         if (!wait_bar(b_kv, nb & 1, p.timeout_ns, abort_flag, WB_KV)) break;
         if (role < 2) {
           if (!score_ready(gs)) break;
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     int nb = 0;
     bool ok = true;
     while (ok) {
-      const Item w(ix, iy, N, p.Npad);
+      const Item w(ix, iy, p);
       for (int it = 0; it < w.n_it; ++it) {
         const uint32_t gq = gs + it, b = gq & 1, s = gq % NS;
         if (!__all_sync(0xffffffffu, wait_bar(b_sdp(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_SDP))) {
@@ -428,13 +432,16 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         const uint32_t tS = tmem + lane_off + C::BUF(b), tDP = tS + 64;
         const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE + s * BQ * 4) + 8 * g;
         const float4* dd4 = reinterpret_cast<const float4*>(smem + C::OFF_DD + s * BQ * 4) + 8 * g;
-        const int q0 = (w.it0 + it) * BQ + 32 * g;  // first query of this group's columns
+        int qh, qs;
+        w.grp.step(it, w.it0, w.n_ith, qh, qs);
+        const int q0 = qs * BQ + 32 * g;  // first query of this group's columns
         // masked: column c < kq (key > query, causal), q0 + c >= N (query past the sequence) or the
-        // whole row when the key is past the sequence (its zero-filled K row gives S = 0, and
-        // exp(-LSE) need not be finite)
-        const bool need_mask = (CAUSAL && (q0 < w.key0 + 127)) || (q0 + 32 > N) || (w.key0 + 128 > N);
+        // whole row when the key does not exist (past the sequence, or past the batch's key count:
+        // a zero-filled K row gives S = 0, and exp(-LSE) need not be finite)
+        const int klen = w.grp.klen;
+        const bool need_mask = (CAUSAL && (q0 < w.key0 + 127)) || (q0 + 32 > N) || (w.key0 + 128 > klen);
         const int kq = CAUSAL ? (w.key0 + k - q0) : 0;
-        const int qn = w.key0 + k < N ? N - q0 : 0;
+        const int qn = w.key0 + k < klen ? N - q0 : 0;
         uint32_t u[32], v[32];
         tmem_ld32_pair(tS + 32 * g, tDP + 32 * g, u, v);  // S^T and dP^T columns in one round trip
         float pv[32];
@@ -525,7 +532,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     int nb = 0;
     bool ok = true;
     while (ok) {
-      const Item w(ix, iy, N, p.Npad);
+      const Item w(ix, iy, p);
       for (int it = 0; it < w.n_it; ++it) {
         const uint32_t gq = gs + it, b = gq & 1;
         const bool full =
@@ -557,8 +564,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
         if (t == 0) {
-          bulk_reduce_add_f32(p.dqacc + static_cast<size_t>(w.ws_base + (w.it0 + it) * BQ) * D, sDQ,
-                              C::DQ_STAGE);
+          int qh, qs;
+          w.grp.step(it, w.it0, w.n_ith, qh, qs);
+          bulk_reduce_add_f32(p.dqacc + static_cast<size_t>(qh * p.Npad + qs * BQ) * D, sDQ, C::DQ_STAGE);
           bulk_commit();
         }
       }

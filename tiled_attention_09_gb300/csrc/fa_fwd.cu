@@ -54,11 +54,14 @@ namespace fa {
 namespace {
 
 struct FwdParams {
-  CUtensorMap tm_q, tm_k, tm_v;
-  uint16_t* o;     // [B*H*N, d] in the input dtype
+  CUtensorMap tm_q, tm_k, tm_v;  // Q over B*H heads; K, V over B*Hkv heads
+  uint16_t* o;     // [B*H*N, d] in the input dtype (nullptr when o32 is given)
+  float* o32;      // optional [B*H*N, d] fp32 output instead of o
   float* lse;      // [B*H*N]
   uint16_t* o_lo;  // optional [B*H*N, d]: dtype(O_fp32 - float(O)), the rounding residual of O
+  const int* kv_len;  // optional [B]: batch b attends only to keys j < kv_len[b] (key padding)
   int N;
+  int H, G;        // query heads; query heads per K/V head
   int n_qblk;
   float scale_log2;
   float rescale_threshold;
@@ -102,15 +105,27 @@ struct FwdCfg {
 // launch order is longest-first).
 template <int NT, bool CAUSAL>
 struct FwdItem {
-  int bh;        // head (b, h): the z coordinate of the tensor maps
+  int bh;        // query head (b, h): the z coordinate of the Q map
+  int bkv;       // its K/V head (b, h / G): the z coordinate of the K and V maps
   int q_row0;    // first query row of the item within the head
   int row_base;  // row of (b, h, 0) in the [B*H*N, d] view
+  int klen;      // keys that exist for this batch: min(N, kv_len[b]), or N
+  int nk;        // key tiles that hold them (at least one: a row with no key gets O = 0, LSE = -inf)
   int n_valid;   // query tiles that exist (the last block can hold one tile fewer)
   int nmax;      // key tiles streamed for the item
   int n_t[NT];   // key tiles that tile t needs
-  __device__ __forceinline__ FwdItem(int x, int y, int N, int n_qblk) {
-    const int qb = CAUSAL ? (n_qblk - 1 - y) : y;
+  __device__ __forceinline__ FwdItem(int x, int y, const FwdParams& p) {
+    const int N = p.N;
+    const int qb = CAUSAL ? (p.n_qblk - 1 - y) : y;
     bh = x;
+    const int b = x / p.H;
+    bkv = b * (p.H / p.G) + (x - b * p.H) / p.G;
+    klen = N;
+    if (p.kv_len) {
+      const int l = __ldg(p.kv_len + b);
+      klen = l < 0 ? 0 : (l > N ? N : l);
+    }
+    nk = klen > 0 ? (klen + 127) / 128 : 1;
     q_row0 = qb * 128 * NT;
     row_base = x * N;
     n_valid = (N - q_row0 + 127) / 128;  // a tile that runs past N still exists (its tail is masked)
@@ -118,9 +133,16 @@ struct FwdItem {
     nmax = 0;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      n_t[t] = (t < n_valid) ? (CAUSAL ? (q_row0 / 128 + t + 1) : ((N + 127) / 128)) : 0;
+      n_t[t] = tiles(t);
       nmax = n_t[t] > nmax ? n_t[t] : nmax;
     }
+  }
+  // key tiles that query tile t needs (computed, not indexed: t need not be a constant)
+  __device__ __forceinline__ int tiles(int t) const {
+    if (t >= n_valid) return 0;
+    if (!CAUSAL) return nk;
+    const int diag = q_row0 / 128 + t + 1;
+    return diag < nk ? diag : nk;
   }
 };
 
@@ -245,7 +267,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       uint32_t clc_phase = 0;
       bool ok = true;
       while (ok) {
-        const Item w(ix, iy, N, p.n_qblk);
+        const Item w(ix, iy, p);
         // Q_t of the previous item is dead once its last S MMA has completed
         if (n_items > 0 && !wait_bar(b_qfree, (n_items - 1) & 1, p.timeout_ns, abort_flag, W_QFREE)) break;
         mbar_arrive_expect_tx(b_q, w.n_valid * C::TILE);
@@ -273,7 +295,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           const int krow = (s >> 1) * 128;  // rows past N arrive as zeros
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow, w.bh);
+            tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow, w.bkv);
           ++seq;
         }
         if (!ok) break;
@@ -327,7 +349,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       int n_items = 0;
       bool ok = true;
       while (ok) {
-        const Item w(ix, iy, N, p.n_qblk);
+        const Item w(ix, iy, p);
         if (!wait_bar(b_q, n_items & 1, p.timeout_ns, abort_flag, W_Q)) break;
         for (int j = 0; ok && j <= w.nmax; ++j) {
           const uint32_t sK = seq + 2 * j, sV = seq + 2 * j - 1;
@@ -410,8 +432,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     int n_items = 0;
     bool ok = true;
     while (ok) {
-      const Item w(ix, iy, N, p.n_qblk);
-      const int my_n = (t < w.n_valid) ? (CAUSAL ? (w.q_row0 / 128 + t + 1) : ((N + 127) / 128)) : 0;  // t is not a constant here
+      const Item w(ix, iy, p);
+      const int my_n = w.tiles(t);
+      const int q_row = w.q_row0 + t * 128 + r;  // within the head
+      // keys this row may see: those that exist, and (causal) none past the query itself
+      const int klim = (CAUSAL && w.klen > q_row + 1) ? q_row + 1 : w.klen;
       float m_used = 0.f, l = 0.f;
       for (int j = 0; ok && j < my_n; ++j) {
         // warp-uniform outcome: tcgen05.ld/st below are warp-collective
@@ -428,10 +453,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
         }
-        // keys that do not exist for this row: past the query itself (causal, diagonal tile) or past
-        // the end of the sequence (last tile, when N is not a multiple of 128); never all 128 of them
-        int lim = N - j * 128;
-        if (CAUSAL && j == my_n - 1 && lim > r + 1) lim = r + 1;
+        // keys this row may not see: past the query itself (causal, diagonal tile), past the end of
+        // the sequence or past the batch's key count (last tiles); all 128 of them only for a row
+        // that sees no key at all (key count 0)
+        const int lim = klim - j * 128;
         if (__any_sync(0xffffffffu, lim < 128)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = c >= lim ? -INFINITY : s[c];
@@ -478,6 +503,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
             mx3 = max3f(mx3, s[c + 6], s[c + 7]);
           }
           m_used = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+          if (m_used == -INFINITY) m_used = 0.f;  // no visible key: every P is 0, l stays 0
           exp_pass(std::false_type{});
         } else {
           // later tiles: exponentiate against the running max and find the new row max on the way;
@@ -512,13 +538,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         // ---------------------------------------------------------- epilogue of tile t
         ok = __all_sync(0xffffffffu, wait_bar(b_o(t), n_o & 1, p.timeout_ns, abort_flag, W_O));
         ++n_o;
-        const int q_row = w.q_row0 + t * 128 + r;  // within the head
-        const bool row_ok = q_row < N;             // the tile's rows past N are computed, not stored
+        const bool row_ok = q_row < N;  // the tile's rows past N are computed, not stored
         const size_t grow = static_cast<size_t>(w.row_base) + q_row;
         if (ok) {
           tc_fence_after();
-          const float inv_l = 1.f / l;
-          uint4* o_row = reinterpret_cast<uint4*>(p.o + grow * D);
+          const float inv_l = l > 0.f ? 1.f / l : 0.f;  // a row with no visible key: O = 0
+          uint4* o_row = p.o32 ? nullptr : reinterpret_cast<uint4*>(p.o + grow * D);
+          float4* o32_row = p.o32 ? reinterpret_cast<float4*>(p.o32 + grow * D) : nullptr;
           uint4* lo_row = p.o_lo ? reinterpret_cast<uint4*>(p.o_lo + grow * D) : nullptr;
           constexpr int EC = D < 128 ? D : 128;  // columns per TMEM round trip
 #pragma unroll 1
@@ -538,6 +564,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
               float x[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(u[8 * g + e]) * inv_l;
+              if (o32_row) {
+                if (row_ok) {
+                  o32_row[2 * ((c0 >> 3) + g)] = make_float4(x[0], x[1], x[2], x[3]);
+                  o32_row[2 * ((c0 >> 3) + g) + 1] = make_float4(x[4], x[5], x[6], x[7]);
+                }
+                continue;
+              }
               uint4 v, lo;
               lo.x = pack2_residual<BF16>(x[0], x[1], v.x);
               lo.y = pack2_residual<BF16>(x[2], x[3], v.y);
@@ -549,7 +582,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
               }
             }
           }
-          // LSE in natural log: (m_used + log2 l) * ln 2
+          // LSE in natural log: (m_used + log2 l) * ln 2 (-inf for a row with no visible key)
           if (row_ok) p.lse[grow] = (m_used + log2f(l)) * 0.69314718055994531f;
         }
       }
@@ -592,10 +625,14 @@ cudaError_t launch_fwd_t(const FwdArgs& a) {
   p.tm_q = a.tm_q;
   p.tm_k = a.tm_k;
   p.tm_v = a.tm_v;
-  p.o = static_cast<uint16_t*>(a.o);
+  p.o = a.o_f32 ? nullptr : static_cast<uint16_t*>(a.o);
+  p.o32 = a.o_f32 ? static_cast<float*>(a.o) : nullptr;
   p.lse = a.lse;
   p.o_lo = static_cast<uint16_t*>(a.o_lo);
+  p.kv_len = a.kv_len;
   p.N = a.N;
+  p.H = a.H;
+  p.G = a.H / a.Hkv;
   p.n_qblk = (a.N + 128 * C::NT - 1) / (128 * C::NT);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.rescale_threshold = 8.0f;

@@ -19,14 +19,16 @@ struct DevStatusHost {
   uint32_t code, where, block, count;
 };
 
-// 2-D tensor maps over the [rows, d] view of a [B,H,N,d] tensor (rows = B*H*N),
-// box {64 elements, box_rows rows}, 128-byte swizzle.
+// 3-D tensor maps over [heads][N][d] (heads = B*H for Q, dO, O; B*Hkv for K, V, dK, dV),
+// box {64 elements, box_rows rows, 1}, 128-byte swizzle.
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // box rows 128
-  void* o;     // [B*H*N, d] output
+  void* o;     // [B*H*N, d] output, in the input dtype or (o_f32) fp32
   float* lse;
   void* o_lo;  // optional rounding residual of O (nullptr: not written)
-  int B, H, N, d;
+  const int* kv_len;  // optional [B] key counts (key-padding mask)
+  int B, H, Hkv, N, d;
+  bool o_f32;
   float scale;
   bool causal, bf16;
   uint64_t timeout_ns;
@@ -36,8 +38,9 @@ struct FwdArgs {
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // q, dO: box rows = query tile; k, v: box rows 128
   CUtensorMap tm_dk, tm_dv;             // box rows 128
-  const void* o;
+  const void* o;      // dtype, or fp32 when o_f32
   const void* o_lo;  // optional rounding residual of O (nullptr: D from o alone)
+  const int* kv_len;  // optional [B] key counts (key-padding mask)
   const void* dO;
   const float* lse;
   void* dq;
@@ -46,8 +49,9 @@ struct BwdArgs {
   float* ws_D;      // [B*H*Npad]: row (bh, r) at bh * Npad + r, Npad = N rounded up to 64
   float* ws_lse2;   // [B*H*Npad]  lse * log2(e)
   float* ws_dqacc;  // [B*H*Npad*d]
-  int B, H, N, d;
+  int B, H, Hkv, N, d;
   int Npad;  // N rounded up to 64: the per-head row stride of the workspace arrays
+  bool o_f32;
   float scale;
   bool causal, bf16;
   uint64_t timeout_ns;
