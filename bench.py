@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle's timed sample")
+    ap.add_argument("--decode", action="store_true",
+                    help="time paged decode attention on the decode points instead (one JSON line each)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
                          "instead of the headline step; one JSON line per point")
@@ -499,11 +501,63 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+DECODE_POINTS = [  # (B, H, Hkv, Mq, d, page_size, ctx)
+    (16, 32, 8, 1, 128, 64, 8192),
+    (1, 32, 8, 1, 128, 64, 65536),
+    (64, 8, 1, 4, 128, 16, 4096),
+    (32, 16, 2, 1, 64, 128, 8192),
+    (8, 64, 8, 2, 128, 256, 16384),
+]
+
+
+def run_decode(args):
+    """One JSON line per paged-decode point: fa_decode (split kernel + merge) timed between two events on the
+    launching stream, L2 flushed before every step, median of the timed steps. HBM-bound: the algorithmic
+    bytes are the sequences' K and V (2 * keys * Hkv * d * 2) plus q in and O out; the fraction divides by
+    the measured copy bandwidth."""
+    import torch
+    import tiled_attention_09_gb300 as fa
+    from tiled_attention_09_gb300.inputs import DecodeWorkload, make_paged_inputs
+    peaks, peak_src = load_peaks()
+    bw = peaks["hbm_gbs"]
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    steps, warmup = max(3, min(args.steps, 30)), max(3, args.warmup)
+    for B, H, Hkv, Mq, d, ps, ctx in DECODE_POINTS:
+        w = DecodeWorkload(B, H, Hkv, Mq, d, ps, ctx // ps, (ctx,) * B, spare=0, poison=False)
+        q, kp, vp, table, cl = (t.to(dev) for t in make_paged_inputs(w))
+        o, lse = fa.decode(q, kp, vp, table, cl)
+        n_split = fa.decode_splits(B, Hkv, ps, w.max_pages)
+        for _ in range(warmup):
+            flush.zero_()
+            fa.decode(q, kp, vp, table, cl, out=o, lse=lse)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            fa.decode(q, kp, vp, table, cl, out=o, lse=lse)
+            e1.record()
+        torch.cuda.synchronize()
+        code, info = fa.device_status()
+        if code != "FA_OK":
+            raise RuntimeError(f"{w.name()}: {code} {info}")
+        t = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+        nbytes = w.kv_bytes() + 2 * q.numel() * 2 + 4 * lse.numel()
+        gbs = nbytes / t / 1e9
+        print(json.dumps({"point": w.name(), "us": 1e6 * t, "n_split": n_split, "ctas": B * Hkv * n_split,
+                          "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_hbm": gbs / bw, "hbm_peak_gbs": bw,
+                          "peak_source": peak_src, "tflops": w.flops() / t / 1e12}), flush=True)
+        del q, kp, vp, table, cl, o, lse
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     if args.warmup < 3:
         args.warmup = 3
-    if args.sweep:
+    if args.decode:
+        run_decode(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -205,6 +205,42 @@ fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_by
                             float scale, fa_dtype dtype, void* stream);
 
 /*
+ * Paged decode attention: Mq new queries per sequence attend to the sequence's
+ * cached keys and values, stored in fixed-size pages (the multi-query paged
+ * attention kernel named on page "高级特性：探索PyTorch/XLA的Pallas内核和Flash
+ * Attention实现", section "Pallas内核：自定义高效计算的关键"); per query the
+ * online softmax of page "transformer模型详解（十）：FlashAttention优化技术",
+ * section "Tiling 分块策略". The key range is cut into n_split splits handled
+ * by different CTAs, each writing partial (O_s, LSE_s) to the workspace, and a
+ * second launch merges them: LSE = ln sum_s exp(LSE_s),
+ * O = sum_s exp(LSE_s - LSE) O_s.
+ *   q        [B, H, Mq, d] dtype: the queries at positions ctx_len[b] - Mq + i
+ *   k_pages, v_pages  [Hkv, n_pages, page_size, d] dtype: the page pool
+ *   page_table  DEVICE int32 [B, max_pages]: key j of sequence b lives in page
+ *            page_table[b][j / page_size], row j % page_size. Entries for pages
+ *            wholly past ctx_len[b] are never read; other entries outside
+ *            [0, n_pages) read as zero keys/values.
+ *   ctx_len  DEVICE int32 [B]: keys of sequence b (clamped to [0, max_pages *
+ *            page_size]); values past it in the last page may hold anything.
+ *   o        [B, H, Mq, d] dtype; lse [B, H, Mq] fp32 (a query that sees no
+ *            key gets O = 0 and LSE = -inf).
+ *   Query head h reads K/V head h / (H / Hkv). causal != 0: query i sees keys
+ *   j <= ctx_len[b] - Mq + i; otherwise all ctx_len[b] keys.
+ * Shapes: d in {64, 128}; page_size a power of two in [16, 256]; H a multiple
+ * of Hkv with (H / Hkv) * Mq <= 128; else FA_ERR_UNSUPPORTED.
+ * n_split <= 0 lets the library choose (fa_decode_splits). workspace: device
+ * memory of fa_decode_workspace_size(...) bytes for the same n_split,
+ * 256-byte aligned. page_table and ctx_len must be 4-byte aligned, the rest
+ * 16-byte aligned. Two launches on `stream`.
+ */
+int fa_decode_splits(int B, int Hkv, int page_size, int max_pages);
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int Mq, int d, int page_size, int max_pages, int n_split);
+fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, const int* page_table, const int* ctx_len,
+                    void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Mq, int d,
+                    int page_size, int n_pages, int max_pages, int n_split, float scale, int causal, fa_dtype dtype,
+                    void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status words of all
  * kernels. FA_OK if no kernel reported anything; FA_ERR_TIMEOUT if a bounded
  * wait expired; FA_ERR_DEVICE_FAULT for a failed device-side check;

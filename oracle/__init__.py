@@ -64,6 +64,8 @@ __all__ = [
     "attention_cols",
     "attention_row_block",
     "head_scores",
+    "paged_attention_fwd",
+    "split_merge",
 ]
 
 
@@ -317,3 +319,66 @@ def attention_row_block(q, k, v, do, scale, causal, b, h, row0, row1):
     D = np.sum(dob * o, axis=-1, keepdims=True)
     ds = p * (dob @ vh.T - D)
     return o, lse, scale * (ds @ kh), scale * (ds.T @ qb), p.T @ dob
+
+
+def paged_attention_fwd(q, k_pages, v_pages, page_table, ctx_len, scale, causal=False):
+    """Decode attention over a paged K/V cache: O [B,H,Mq,d] and LSE [B,H,Mq].
+
+    Page 3, section "Pallas内核：自定义高效计算的关键": a paged multi-query
+    attention kernel. Key j of sequence b is row j % page_size of page
+    page_table[b][j // page_size] of k_pages / v_pages ([H_kv, n_pages,
+    page_size, d]); the sequence has ctx_len[b] keys (clamped to [0, max_pages
+    * page_size]). The Mq queries of q[b, h] sit at positions ctx_len[b] - Mq
+    + i; causal: query i sees keys j <= ctx_len[b] - Mq + i. The keys are
+    gathered into a contiguous sequence and the definition applied to it
+    (scores, row softmax, P @ V); a query with no visible key gets O = 0,
+    LSE = -inf.
+    """
+    q, k_pages, v_pages = _as64(q), _as64(k_pages), _as64(v_pages)
+    B, H, Mq, d = q.shape
+    Hkv, n_pages, ps, _ = k_pages.shape
+    max_pages = page_table.shape[1]
+    o = np.zeros_like(q)
+    lse = np.full((B, H, Mq), -np.inf)
+    for b in range(B):
+        L = int(min(max(int(ctx_len[b]), 0), max_pages * ps))
+        if L == 0:
+            continue
+        keys = np.arange(L)
+        pages = np.asarray(page_table[b])[keys // ps]
+        rows = keys % ps
+        for h in range(H):
+            hk = _kv_head(h, H, Hkv)
+            kb = k_pages[hk, pages, rows]
+            vb = v_pages[hk, pages, rows]
+            s = scale * (q[b, h] @ kb.T)
+            if causal:
+                pos = (L - Mq + np.arange(Mq))[:, None]
+                s = np.where(keys[None, :] > pos, -np.inf, s)
+            p, l = _softmax_rows(s)
+            o[b, h] = p @ vb
+            lse[b, h] = l
+    return o, lse
+
+
+def split_merge(o_parts, lse_parts):
+    """Merge attention results computed over disjoint key ranges.
+
+    Each part s holds, per query row, O_s (normalised over its own keys) and
+    LSE_s. The page-2 online softmax (section "Tiling 分块策略") combines blocks
+    by taking the larger max and rescaling each block's sum and output by
+    exp(m_s - m); in log-sum-exp form that is LSE = ln sum_s exp(LSE_s) and
+    O = sum_s exp(LSE_s - LSE) O_s. Parts with LSE_s = -inf (no key) weigh 0;
+    all of them empty gives O = 0, LSE = -inf. Arrays: o_parts [S, ..., d],
+    lse_parts [S, ...].
+    """
+    o_parts, lse_parts = _as64(o_parts), _as64(lse_parts)
+    m = np.max(lse_parts, axis=0)
+    empty = np.isneginf(m)
+    m0 = np.where(empty, 0.0, m)
+    w = np.exp(lse_parts - m0[None])
+    total = np.sum(w, axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(empty, -np.inf, m0 + np.log(total))
+        o = np.where(empty[..., None], 0.0, np.sum(w[..., None] * o_parts, axis=0) / total[..., None])
+    return o, lse

@@ -36,6 +36,27 @@ def _declared_functions():
     return sorted(names)
 
 
+def _declared_arities():
+    """{function: parameter count} from the headers' declarations."""
+    out = {}
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+        for m in re.finditer(r"\b(?:fa_status|size_t|const char\s*\*|void|int)\s+(fa_\w+)\s*\(([^)]*)\)\s*;", text):
+            params = m.group(2).strip()
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_ctypes_signatures_match_header_arity():
+    ar = _declared_arities()
+    assert "fa_decode" in ar and ar["fa_decode"] == 22
+    for name, _, args in _lib.SIGNATURES:
+        assert len(args) == ar[name], f"{name}: {len(args)} ctypes arguments, {ar[name]} declared"
+
+
 def test_every_declared_symbol_is_exported_and_bound(L):
     names = _declared_functions()
     assert "fa_fwd" in names and "fa_bwd" in names and len(names) >= 10

@@ -346,3 +346,98 @@ def test_no_visible_key_gives_zero_output(causal):
     o3, lse3 = oracle.attention_fwd(q, k, v, 0.5, causal)
     np.testing.assert_array_equal(o2, o3)
     np.testing.assert_array_equal(lse2, lse3)
+
+
+# ---------------------------------------------------------------- paged decode, split merge
+def _paged(B, Hkv, n_pages, ps, max_pages, d, seed):
+    rng = np.random.default_rng(seed)
+    kp = rng.standard_normal((Hkv, n_pages, ps, d))
+    vp = rng.standard_normal((Hkv, n_pages, ps, d))
+    if n_pages >= B * max_pages:  # every sequence its own pages
+        table = rng.permutation(n_pages)[:B * max_pages].reshape(B, max_pages)
+    else:
+        table = np.stack([rng.permutation(n_pages)[:max_pages] for _ in range(B)])
+    return kp, vp, table
+
+
+def _gather(pages, table_b, L):
+    ps = pages.shape[2]
+    j = np.arange(L)
+    return pages[:, table_b[j // ps], j % ps]  # [Hkv, L, d]
+
+
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_paged_decode_with_all_queries_is_causal_attention(Hkv):
+    """Mq = ctx_len: the decode queries are the whole sequence, and causal decode equals causal attention
+    over the gathered sequence (bottom-right alignment meets the ordinary causal mask)."""
+    B, H, ps, d = 2, 4, 4, 8
+    kp, vp, table = _paged(B, Hkv, 12, ps, 5, d, 90)
+    L = 17
+    q = _rand((B, H, L, d), 91)
+    o, lse = oracle.paged_attention_fwd(q, kp, vp, table, np.array([L, L]), 0.4, causal=True)
+    for b in range(B):
+        kb = _gather(kp, table[b], L)[None]
+        vb = _gather(vp, table[b], L)[None]
+        oc, lc = oracle.attention_fwd(q[b:b + 1], kb, vb, 0.4, causal=True)
+        np.testing.assert_allclose(o[b], oc[0], atol=1e-14)
+        np.testing.assert_allclose(lse[b], lc[0], atol=1e-14)
+
+
+def test_paged_decode_page_permutation_invariance():
+    """Moving pages within the pool (and the page table with them) changes nothing; values in pages or rows
+    past ctx_len never matter."""
+    B, H, Hkv, ps, d, n_pages, max_pages = 3, 4, 2, 8, 8, 20, 6
+    kp, vp, table = _paged(B, Hkv, n_pages, ps, max_pages, d, 92)
+    q = _rand((B, H, 3, d), 93)
+    ctx = np.array([41, 8, 0])
+    o, lse = oracle.paged_attention_fwd(q, kp, vp, table, ctx, 0.3, causal=True)
+    perm = np.random.default_rng(94).permutation(n_pages)
+    inv = np.argsort(perm)
+    kp2, vp2 = kp[:, perm], vp[:, perm]  # new page i holds old page perm[i]
+    o2, lse2 = oracle.paged_attention_fwd(q, kp2, vp2, inv[table], ctx, 0.3, causal=True)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    kp3, vp3 = kp.copy(), vp.copy()
+    kp3[:, table[0, 5], 1:] = np.nan  # rows 41.. of sequence 0 (page 5, rows 1..7)
+    vp3[:, table[0, 5], 1:] = np.inf
+    kp3[:, table[1, 1:]] = np.nan     # sequence 1 uses page 0 only
+    o3, lse3 = oracle.paged_attention_fwd(q, kp3, vp3, table, ctx, 0.3, causal=True)
+    np.testing.assert_array_equal(o[:2], o3[:2])
+    assert not o[2].any() and np.isneginf(lse[2]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_merge_recovers_full_attention(causal):
+    """Attention over disjoint key ranges, merged by log-sum-exp weights, equals attention over all keys."""
+    B, H, N, d = 1, 2, 40, 8
+    q, k, v = (_rand((B, H, N, d), 95 + s) for s in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, 0.35, causal)
+    cuts = [0, 7, 8, 30, 40]  # includes a one-key range
+    parts_o, parts_l = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        s = 0.35 * np.einsum("bhid,bhjd->bhij", q, k[:, :, a:b])
+        if causal:
+            s = np.where(np.arange(a, b)[None, None, None, :] > np.arange(N)[None, None, :, None], -np.inf, s)
+        m = s.max(axis=-1, keepdims=True)
+        empty = np.isneginf(m)
+        e = np.where(empty, 0.0, np.exp(s - np.where(empty, 0.0, m)))
+        l = e.sum(axis=-1, keepdims=True)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            parts_o.append(np.where(empty, 0.0, (e @ v[:, :, a:b]) / l))
+            parts_l.append(np.where(empty[..., 0], -np.inf, (m + np.log(l))[..., 0]))
+    om, lm = oracle.split_merge(np.stack(parts_o), np.stack(parts_l))
+    np.testing.assert_allclose(om, o, atol=1e-13)
+    np.testing.assert_allclose(lm, lse, atol=1e-13)
+    oe, le = oracle.split_merge(np.zeros((3, 2, d)), np.full((3, 2), -np.inf))
+    assert not oe.any() and np.isneginf(le).all()
+
+
+def test_paged_decode_grouped_heads_equal_repeated_heads():
+    B, H, Hkv, ps, d = 2, 6, 2, 16, 8
+    kp, vp, table = _paged(B, Hkv, 10, ps, 4, d, 97)
+    q = _rand((B, H, 2, d), 98)
+    ctx = np.array([50, 33])
+    o, lse = oracle.paged_attention_fwd(q, kp, vp, table, ctx, 0.3, causal=False)
+    o2, lse2 = oracle.paged_attention_fwd(q, np.repeat(kp, 3, axis=0), np.repeat(vp, 3, axis=0), table, ctx, 0.3)
+    np.testing.assert_allclose(o, o2, atol=1e-14)
+    np.testing.assert_allclose(lse, lse2, atol=1e-14)

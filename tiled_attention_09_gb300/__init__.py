@@ -27,7 +27,8 @@ import torch
 from . import _lib
 from ._lib import FA_BF16, FA_F16, FAError
 
-__all__ = ["fwd", "bwd", "attention", "workspace_size", "device_status", "FAError", "selftest_gemm", "lib_path"]
+__all__ = ["fwd", "bwd", "attention", "decode", "decode_splits", "workspace_size", "device_status", "FAError",
+           "selftest_gemm", "lib_path"]
 
 _DT = {torch.float16: FA_F16, torch.bfloat16: FA_BF16}
 
@@ -194,6 +195,47 @@ def attention(q, k, v, causal=False, scale=None, kv_len=None):
     k, v may be [B, H_kv, N, d] (grouped-query / multi-query); kv_len: optional int32 [B] key counts.
     """
     return _AttentionFn.apply(q, k, v, causal, scale, kv_len)
+
+
+def decode_splits(B, Hkv, page_size, max_pages) -> int:
+    """Number of key splits fa_decode picks by itself for this shape."""
+    return int(_lib.load().fa_decode_splits(B, Hkv, page_size, max_pages))
+
+
+def decode(q, k_pages, v_pages, page_table, ctx_len, causal=False, scale=None, n_split=0, out=None, lse=None,
+           workspace=None):
+    """Paged decode attention (fa_decode): returns (o [B, H, Mq, d], lse [B, H, Mq]).
+
+    q [B, H, Mq, d]; k_pages, v_pages [Hkv, n_pages, page_size, d] (q's dtype); page_table int32
+    [B, max_pages] and ctx_len int32 [B], all on q's device. n_split <= 0: the library's choice.
+    """
+    _check_qkv(q)
+    _check_qkv(k_pages, v_pages)
+    B, H, Mq, d = q.shape
+    Hkv, n_pages, page_size, dk = k_pages.shape
+    if dk != d or k_pages.dtype != q.dtype or k_pages.device != q.device:
+        raise ValueError("k_pages, v_pages must be [Hkv, n_pages, page_size, d] with q's d, dtype and device")
+    for t in (page_table, ctx_len):
+        if t.dtype != torch.int32 or t.device != q.device or not t.is_contiguous():
+            raise ValueError("page_table and ctx_len must be contiguous int32 tensors on q's device")
+    if page_table.dim() != 2 or page_table.shape[0] != B or ctx_len.shape != (B,):
+        raise ValueError("page_table must be [B, max_pages] and ctx_len [B]")
+    max_pages = page_table.shape[1]
+    scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    L = _lib.load()
+    ws_bytes = int(L.fa_decode_workspace_size(B, H, Hkv, Mq, d, page_size, max_pages, n_split))
+    if ws_bytes == 0:
+        raise ValueError("unsupported decode shape")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Mq), device=q.device, dtype=torch.float32) if lse is None else lse
+    code = L.fa_decode(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), page_table.data_ptr(), ctx_len.data_ptr(),
+                       o.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, Hkv, Mq, d,
+                       page_size, n_pages, max_pages, n_split, scale, int(bool(causal)), _DT[q.dtype], _stream_ptr(q))
+    _lib.check("fa_decode", code)
+    _after("fa_decode", q)
+    return o, lse
 
 
 def selftest_gemm(a, b, n, k, a_mode, b_mode):

@@ -49,6 +49,9 @@ SIGNATURES = [
                                              c_void_p]),
     ("fa_bwd_dq_convert", c_int, [c_void_p, c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int,
                                   c_void_p]),
+    ("fa_decode_splits", c_int, [c_int, c_int, c_int, c_int]),
+    ("fa_decode_workspace_size", c_size_t, [c_int] * 8),
+    ("fa_decode", c_int, [c_void_p] * 7 + [c_void_p, c_size_t] + [c_int] * 9 + [c_float, c_int, c_int, c_void_p]),
     ("fa_device_status", c_int, [c_void_p, ctypes.POINTER(c_uint)]),
     ("fa_status_string", ctypes.c_char_p, [c_int]),
     ("fa_set_wait_timeout_ns", None, [ctypes.c_ulonglong]),

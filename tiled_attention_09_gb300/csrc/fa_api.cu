@@ -49,7 +49,73 @@ bool make_map(CUtensorMap* m, const void* base, long long heads, int N, int d, b
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over [rows][d] of a 16-bit tensor; box = {64 elements, box_rows}; 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int d, bool bf16, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Paged decode shapes: d in {64, 128}; page size a power of two in [16, 256]; the G = H / Hkv heads'
+// Mq queries (G * Mq rows) fit one 128-row tile; cache rows and query rows in 32-bit ints.
+fa_status check_decode_shape(int B, int H, int Hkv, int Mq, int d, int page_size, int n_pages, int max_pages,
+                             fa_dtype dtype) {
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Hkv < 1 || Mq < 1 || n_pages < 1 || max_pages < 1) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (H % Hkv != 0 || (H / Hkv) * Mq > 128) return FA_ERR_UNSUPPORTED;
+  if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(n_pages) * page_size >= (1ll << 31) ||
+      static_cast<long long>(max_pages) * page_size >= (1ll << 31) ||
+      static_cast<long long>(B) * H * Mq + 128 >= (1ll << 31))
+    return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int log2_exact(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+// Splits of the key range: with C = B * Hkv CTAs per split and 152 SMs, pick the count s that
+// minimises waves(C * s) * (tiles per split + 3), the 3 standing for a CTA's fixed cost in tiles.
+int decode_splits(int B, int Hkv, int page_size, int max_pages) {
+  const long long n_tiles = (static_cast<long long>(max_pages) * page_size + 127) / 128;
+  const long long ctas = static_cast<long long>(B) * Hkv;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= 64 && s <= n_tiles; ++s) {
+    const long long waves = (ctas * s + 151) / 152;
+    const long long cost = waves * ((n_tiles + s - 1) / s + 3);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+struct DecWs {
+  size_t off_o, off_lse, total;
+};
+DecWs decode_ws(int B, int H, int Mq, int d, int n_split) {
+  const size_t rows = static_cast<size_t>(B) * H * Mq, parts = 2 * static_cast<size_t>(n_split);
+  DecWs w;
+  w.off_o = 0;
+  w.off_lse = (parts * rows * d * 4 + 255) & ~size_t(255);
+  w.total = w.off_lse + ((parts * rows * 4 + 255) & ~size_t(255));
+  return w;
+}
 
 fa_status check_device() {
   int dev = 0;
@@ -314,18 +380,83 @@ fa_status fa_bwd_opt(const void* q, const void* k, const void* v, const void* o,
                        stream);
 }
 
+int fa_decode_splits(int B, int Hkv, int page_size, int max_pages) {
+  if (B < 1 || Hkv < 1 || page_size < 1 || max_pages < 1) return 0;
+  return decode_splits(B, Hkv, page_size, max_pages);
+}
+
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int Mq, int d, int page_size, int max_pages, int n_split) {
+  if (check_decode_shape(B, H, Hkv, Mq, d, page_size, 1, max_pages, FA_BF16) != FA_OK) return 0;
+  if (n_split <= 0) n_split = decode_splits(B, Hkv, page_size, max_pages);
+  return decode_ws(B, H, Mq, d, n_split).total;
+}
+
+fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, const int* page_table, const int* ctx_len,
+                    void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Mq, int d,
+                    int page_size, int n_pages, int max_pages, int n_split, float scale, int causal, fa_dtype dtype,
+                    void* stream) {
+  if (!q || !k_pages || !v_pages || !page_table || !ctx_len || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status s = check_decode_shape(B, H, Hkv, Mq, d, page_size, n_pages, max_pages, dtype);
+  if (s != FA_OK) return s;
+  if ((s = check_scale(scale)) != FA_OK) return s;
+  if (n_split <= 0) n_split = decode_splits(B, Hkv, page_size, max_pages);
+  const long long n_tiles = (static_cast<long long>(max_pages) * page_size + 127) / 128;
+  if (n_split > n_tiles) n_split = static_cast<int>(n_tiles);
+  const int tiles_per_split = static_cast<int>((n_tiles + n_split - 1) / n_split);
+  n_split = static_cast<int>((n_tiles + tiles_per_split - 1) / tiles_per_split);  // no empty trailing split
+  if (n_split > 65535) return FA_ERR_UNSUPPORTED;
+  const DecWs w = decode_ws(B, H, Mq, d, n_split);
+  if (!workspace) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
+  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(page_table) & 3u) != 0 || (reinterpret_cast<uintptr_t>(ctx_len) & 3u) != 0)
+    return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  fa::DecArgs a;
+  const bool bf16 = dtype == FA_BF16;
+  const int br = page_size < 128 ? page_size : 128;
+  if (!make_map_2d(&a.tm_q, q, static_cast<long long>(B) * H * Mq, d, bf16, 128) ||
+      !make_map(&a.tm_k, k_pages, Hkv, n_pages * page_size, d, bf16, br) ||
+      !make_map(&a.tm_v, v_pages, Hkv, n_pages * page_size, d, bf16, br))
+    return FA_ERR_CUDA;
+  a.page_table = page_table;
+  a.ctx_len = ctx_len;
+  a.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_o);
+  a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse);
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Mq = Mq;
+  a.d = d;
+  a.ps_log2 = log2_exact(page_size);
+  a.max_pages = max_pages;
+  a.n_pages = n_pages;
+  a.tiles_per_split = tiles_per_split;
+  a.n_split = n_split;
+  a.scale = scale;
+  a.causal = causal != 0;
+  a.bf16 = bf16;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return fa::launch_decode(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_device_status(void* stream, unsigned int info[4]) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
-  fa::DevStatusHost a{}, b{};
+  fa::DevStatusHost a{}, b{}, c{};
   if (fa::read_clear_status_fwd(&a, st) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_status_bwd(&b, st) != cudaSuccess) return FA_ERR_CUDA;
-  const fa::DevStatusHost& first = a.code ? a : b;
+  if (fa::read_clear_status_decode(&c, st) != cudaSuccess) return FA_ERR_CUDA;
+  const fa::DevStatusHost& first = a.code ? a : (b.code ? b : c);
   if (info) {
     info[0] = first.code;
     info[1] = first.where;
     info[2] = first.block;
-    info[3] = a.count + b.count;
+    info[3] = a.count + b.count + c.count;
   }
   if (first.code == 1u) return FA_ERR_TIMEOUT;
   if (first.code != 0u) return FA_ERR_DEVICE_FAULT;

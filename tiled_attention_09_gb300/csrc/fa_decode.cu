@@ -1,0 +1,512 @@
+// Paged decode attention for sm_103a: split-key partial attention (K5) and the split merge (K6).
+//
+// Method. A few new queries per sequence (Mq of them, the last Mq positions) attend to a long
+// key/value history kept in fixed-size pages. Page "高级特性：探索PyTorch/XLA的Pallas内核和Flash
+// Attention实现", section "Pallas内核：自定义高效计算的关键", names such a kernel: paged attention
+// for the multi-query case, K/V heads shared by several query heads. The arithmetic per query is
+// the forward's online softmax (page "transformer模型详解（十）：FlashAttention优化技术", section
+// "Tiling 分块策略": per key tile the local max and exponential sum, a rescale of the running sum
+// and output, one normalisation at the end). The key range is cut into splits processed by
+// different CTAs; each produces, per query row, an output O_s normalised by its own sum and its
+// log-sum-exp LSE_s. The merge is the same online-softmax update applied across the splits:
+//   LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+//
+// GB300 design. Decoding reads every cached key and value once, so the kernel is bound by HBM
+// bandwidth, and with G query heads per K/V head each key is used by R = G * Mq query rows. A CTA
+// owns one K/V head of one sequence and one split; its R query rows (the G heads' Mq queries are
+// consecutive rows of q) form one 128-row tile, so the tile's products run on the tensor core
+// (tcgen05.mma, rows past R are never read back) and the per-key cost stays far below the HBM
+// time of a key even for large groups. The CTA runs two independent key streams over its split
+// (even and odd 128-key tiles), each with its own S and O in tensor memory and its own softmax
+// warpgroup, so one stream's exponentials overlap the other's products; the two streams are two
+// partial results for the merge. K/V tiles are gathered page by page with TMA into a ring of
+// shared-memory slots; pages past the sequence's end are not read (zero-filled), and value rows
+// past its end inside the last tile are zeroed before use (a stale page tail may hold non-finite
+// values, and 0 * NaN is NaN in the product).
+// Roles (320 threads): warps 0-3 softmax of stream 0 and warps 4-7 of stream 1 (only the warps
+// that hold rows < R work), warp 8 TMA producer, warp 9 MMA issuer.
+// TMEM: S_t at 128t (fp32 128 x 128; P_t as 16-bit pairs over it), O_t at 256 + d t.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace fa {
+namespace {
+
+struct DecParams {
+  CUtensorMap tm_q;        // [B*H*Mq rows][d], box {64, 128}
+  CUtensorMap tm_k, tm_v;  // [Hkv][P*page_size rows][d], box {64, min(page_size, 128), 1}
+  const int* page_table;   // [B][max_pages]
+  const int* ctx_len;      // [B]
+  float* o_part;           // [n_part][B*H*Mq][d] fp32, each part normalised by its own sum
+  float* lse_part;         // [n_part][B*H*Mq]
+  int H, G, Mq, R;         // query heads, query heads per K/V head, queries per head, rows per CTA
+  int ps_log2;             // log2(page size)
+  int max_pages, n_pages;  // page-table row length, pages in the cache
+  int tiles_per_split;     // 128-key tiles per split
+  int rows_total;          // B*H*Mq
+  int causal;
+  float scale_log2;
+  float rescale_threshold;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct DecCfg {
+  static constexpr int CHUNK = 128 * 128;  // 128 rows x 64 elements x 2 bytes
+  static constexpr int NCH = D / 64;
+  static constexpr int TILE = 128 * D * 2;
+  // ring slots (one K or one V tile each) filling the rest of the 227 KB
+  static constexpr int NS_FIT = (227 * 1024 - 1024 - TILE - 512) / TILE;
+  static constexpr int NS = NS_FIT > 12 ? 12 : NS_FIT;
+  // q, full[NS], empty[NS], s[2], p[2], o[2], drain
+  static constexpr int NBAR = 1 + 2 * NS + 6 + 1;
+  static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
+  static constexpr int SMEM_BYTES = 1024 + TILE + NS * TILE + BAR_BYTES + 16;
+  static constexpr int THREADS = 320;
+  static_assert(NS >= 4, "the ring must hold the MMA issuer's look-ahead");
+  static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
+  static_assert(256 + 2 * D <= 512, "TMEM budget");
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t dpack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+enum : uint32_t { WD_Q = 31, WD_EMPTY = 32, WD_FULL = 33, WD_P = 34, WD_S = 35, WD_O = 36, WD_V = 37, WD_DRAIN = 38 };
+
+// The CTA's split of one sequence: 128-key tiles [lo, lo + n) of the sequence's ceil(ctx / 128),
+// stream t takes tiles lo + t, lo + t + 2, ... (n0 = ceil(n / 2) and n1 = floor(n / 2) of them).
+struct DecWork {
+  int b, hk, ctx, lo, n0, n1;
+  __device__ __forceinline__ DecWork(const DecParams& p) {
+    const int Hkv = p.H / p.G;
+    b = blockIdx.x / Hkv;
+    hk = blockIdx.x - b * Hkv;
+    const int cap = p.max_pages << p.ps_log2;
+    const int c = __ldg(p.ctx_len + b);
+    ctx = c < 0 ? 0 : (c > cap ? cap : c);
+    const int n_tiles = (ctx + 127) / 128;
+    lo = blockIdx.y * p.tiles_per_split;
+    int hi = lo + p.tiles_per_split;
+    hi = hi < n_tiles ? hi : n_tiles;
+    const int n = hi > lo ? hi - lo : 0;
+    n0 = (n + 1) / 2;
+    n1 = n / 2;
+  }
+  __device__ __forceinline__ int tiles(int t) const { return t ? n1 : n0; }
+  // position in the load (and MMA) order of V of stream t's tile j: step m = j + 1 issues, per
+  // stream, V(t, m - 1) then K(t, m); loads before step m (m >= 1) number
+  // min(m, n0) + min(m, n1) + min(m - 1, n0) + min(m - 1, n1)
+  __device__ __forceinline__ uint32_t seq_v(int t, int j) const {
+    const int m = j + 1;
+    int s = min(m, n0) + min(m, n1) + min(m - 1, n0) + min(m - 1, n1);
+    if (t == 1) s += (m <= n0 ? 1 : 0) + (m < n0 ? 1 : 0);
+    return static_cast<uint32_t>(s);
+  }
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant__ DecParams p) {
+  using C = DecCfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sRing = sQ + C::TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE + NS * C::TILE);
+  const uint32_t b_q = smem_u32(&bars[0]);
+  auto b_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto b_empty = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
+  auto b_s = [&](int t) { return smem_u32(&bars[1 + 2 * NS + t]); };
+  auto b_p = [&](int t) { return smem_u32(&bars[3 + 2 * NS + t]); };
+  auto b_o = [&](int t) { return smem_u32(&bars[5 + 2 * NS + t]); };
+  const uint32_t b_drain = smem_u32(&bars[7 + 2 * NS]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::TILE + NS * C::TILE + C::BAR_BYTES);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const DecWork w(p);
+  const int nact = (p.R + 31) / 32;  // softmax warps per stream that hold rows < R
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(b_full(s), 1);
+      mbar_init(b_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(b_s(t), 1);
+      mbar_init(b_p(t), 32 * nact);
+      mbar_init(b_o(t), 1);
+    }
+    mbar_init(b_drain, 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int q_row0 = (w.b * p.H + w.hk * p.G) * p.Mq;  // first of the CTA's R query rows
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(b_q, C::TILE);
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ + c * C::CHUNK, &p.tm_q, b_q, c * 64, q_row0);
+      const int ps = 1 << p.ps_log2;
+      const int br = ps < 128 ? ps : 128;  // rows per TMA box
+      const int oob_row = p.n_pages << p.ps_log2;  // the first row past the cache: the box reads zeros
+      const int* ptab = p.page_table + static_cast<size_t>(w.b) * p.max_pages;
+      uint32_t seq = 0;
+      bool ok = true;
+      // one K or V tile of 128 keys, page by page
+      auto load = [&](const CUtensorMap* map, int kt) -> bool {
+        const uint32_t slot = seq % NS, use = seq / NS;
+        if (use > 0 && !wait_bar(b_empty(slot), (use - 1) & 1, p.timeout_ns, abort_flag, WD_EMPTY)) return false;
+        mbar_arrive_expect_tx(b_full(slot), C::TILE);
+        for (int r0 = 0; r0 < 128; r0 += br) {
+          const int key = kt * 128 + r0;
+          int y = oob_row;
+          if (key < w.ctx) {  // pages wholly past the sequence are not read
+            const int pid = __ldg(ptab + (key >> p.ps_log2));
+            if (pid >= 0 && pid < p.n_pages) y = (pid << p.ps_log2) + (key & (ps - 1));
+          }
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK + r0 * 128, map, b_full(slot), c * 64, y, w.hk);
+        }
+        ++seq;
+        return true;
+      };
+      // the MMA issuer's order: per step j and stream t, V(t, j - 1) then K(t, j)
+      for (int j = 0; ok && j <= w.n0; ++j) {
+        for (int t = 0; ok && t < 2; ++t) {
+          const int nt = w.tiles(t);
+          if (j >= 1 && j <= nt) ok = load(&p.tm_v, w.lo + 2 * (j - 1) + t);
+          if (ok && j < nt) ok = load(&p.tm_k, w.lo + 2 * j + t);
+        }
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      for (uint32_t s = (seq > NS ? seq - NS : 0u); s < seq; ++s)
+        wait_bar(b_full(s % NS), (s / NS) & 1, p.timeout_ns, abort_flag, WD_DRAIN);
+      wait_bar(b_q, 0, p.timeout_ns, abort_flag, WD_DRAIN);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
+      constexpr uint32_t idesc_pv = make_idesc(128, D, BF16, false, true);
+      const uint64_t dq0 = make_sdesc(sQ, 16, 1024);           // Q, K-major
+      const uint64_t dk0 = make_sdesc(sRing, 16, 1024);        // K in a ring slot, K-major
+      const uint64_t dv0 = make_sdesc(sRing, C::CHUNK, 1024);  // V in a ring slot, MN-major
+      uint32_t seq = 0;
+      bool ok = wait_bar(b_q, 0, p.timeout_ns, abort_flag, WD_Q);
+      for (int j = 0; ok && j <= w.n0; ++j) {
+        for (int t = 0; ok && t < 2; ++t) {
+          const int nt = w.tiles(t);
+          if (j >= 1 && j <= nt) {
+            // O_t += P_t(j - 1) V(t, j - 1)
+            const uint32_t sv = seq++;
+            if (!wait_bar(b_full(sv % NS), (sv / NS) & 1, p.timeout_ns, abort_flag, WD_FULL) ||
+                !wait_bar(b_p(t), (j - 1) & 1, p.timeout_ns, abort_flag, WD_P)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dv = dv0 + static_cast<uint64_t>(((sv % NS) * C::TILE) >> 4);
+            const uint32_t tO = tmem + 256 + D * t, tP = tmem + 128 * t;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 16 rows of V = 2048 bytes
+              mma_ts(tO, tP + k * 8, dv + static_cast<uint64_t>(k * (2048 >> 4)), idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+            mma_commit(b_empty(sv % NS));
+            if (j == nt) mma_commit(b_o(t));
+          }
+          if (j < nt) {
+            // S_t(j) = Q K(t, j)^T; its commit also covers O_t's update above
+            const uint32_t sk = seq++;
+            if (!wait_bar(b_full(sk % NS), (sk / NS) & 1, p.timeout_ns, abort_flag, WD_FULL)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dk = dk0 + static_cast<uint64_t>(((sk % NS) * C::TILE) >> 4);
+            const uint32_t tS = tmem + 128 * t;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {  // 16 head dims per MMA
+              const uint64_t off = static_cast<uint64_t>(((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4);
+              mma_ss(tS, dq0 + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
+            }
+            mma_commit(b_s(t));
+            mma_commit(b_empty(sk % NS));
+          }
+        }
+      }
+      mma_commit(b_drain);
+      wait_bar(b_drain, 0, p.timeout_ns, abort_flag, WD_DRAIN);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  } else if ((warp & 3) < nact) {
+    // ------------------------------------------------------------ softmax + epilogue of stream t
+    const int t = warp >> 2;
+    const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 128 * t;
+    const uint32_t tO = tmem + lane_off + 256 + D * t;
+    const float sl2 = p.scale_log2;
+    const int nt = w.tiles(t);
+    // keys this row may see: the sequence's, and (causal) none after the query's own position
+    // ctx - Mq + i, i = r % Mq
+    int klim = w.ctx;
+    if (p.causal) klim = w.ctx - p.Mq + (r % p.Mq) + 1;
+    float m_used = 0.f, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      if (!__all_sync(0xffffffffu, wait_bar(b_s(t), j & 1, p.timeout_ns, abort_flag, WD_S))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kt = w.lo + 2 * j + t;
+      float s[128];
+      {
+        uint32_t u[128];
+        tmem_ld128(tS, u);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
+      }
+      const int lim = klim - kt * 128;
+      if (__any_sync(0xffffffffu, lim < 128)) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = c >= lim ? -INFINITY : s[c];
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+        mx0 = max3f(mx0, s[c + 0], s[c + 1]);
+        mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+        mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+        mx3 = max3f(mx3, s[c + 6], s[c + 7]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      if (j == 0) {
+        m_used = m_tile == -INFINITY ? 0.f : m_tile;  // no visible key yet: every P is 0
+      } else {
+        // lazy rescale: the running max moves only when the row max grows past the threshold;
+        // the commit that announced S_t(j) also covers P_t(j - 1) V, so O_t is quiescent
+        const bool rescale = m_tile > m_used + p.rescale_threshold;
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float alpha = rescale ? ex2_approx(m_used - m_tile) : 1.f;
+          if (rescale) {
+            m_used = m_tile;
+            l *= alpha;
+          }
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tO + 32 * c, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(tO + 32 * c, u);
+          }
+        }
+      }
+      uint32_t pk[64];
+      float ls0 = 0.f, ls1 = 0.f;
+      const float neg_m = -m_used;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
+        const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
+        ls0 += p0;
+        ls1 += p1;
+        pk[c >> 1] = dpack2<BF16>(p0, p1);
+      }
+      l += ls0 + ls1;
+      // The sequence's last tile: value rows past its end may come from a stale page tail; zero them
+      // (after their copy has landed) so that P = 0 there cannot meet a non-finite value.
+      const int valid = w.ctx - kt * 128;
+      if (valid < 128) {
+        const uint32_t sv = w.seq_v(t, j);
+        if (!__all_sync(0xffffffffu, wait_bar(b_full(sv % NS), (sv / NS) & 1, p.timeout_ns, abort_flag, WD_V))) {
+          ok = false;
+          break;
+        }
+        uint8_t* vt = smem + C::TILE + (sv % NS) * C::TILE;
+        for (int row = valid + (r & 31) + 32 * (warp & 3); row < 128; row += 32 * nact) {
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c) {
+            uint4* z = reinterpret_cast<uint4*>(vt + c * C::CHUNK + row * 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) z[u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();  // visible to the tensor core before P is announced
+      }
+      tmem_st64(tS, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(b_p(t));
+    }
+    // ---------------------------------------------------------- epilogue: this stream's partial result
+    const int part = 2 * blockIdx.y + t;
+    const bool row_ok = r < p.R;
+    const size_t grow = static_cast<size_t>(part) * p.rows_total + q_row0 + r;
+    float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D);
+    if (ok && nt > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(b_o(t), 0, p.timeout_ns, abort_flag, WD_O));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t u[64];
+          tmem_ld64(tO + c0, u);
+          if (row_ok) {
+#pragma unroll
+            for (int g = 0; g < 16; ++g)
+              dst[(c0 >> 2) + g] = make_float4(__uint_as_float(u[4 * g]) * inv_l, __uint_as_float(u[4 * g + 1]) * inv_l,
+                                               __uint_as_float(u[4 * g + 2]) * inv_l,
+                                               __uint_as_float(u[4 * g + 3]) * inv_l);
+          }
+        }
+        if (row_ok) p.lse_part[grow] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    } else if (ok && row_ok) {  // no tile in this stream: an empty partial
+#pragma unroll 4
+      for (int g = 0; g < D / 4; ++g) dst[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+      p.lse_part[grow] = -INFINITY;
+    }
+    tc_fence_before();
+    __syncthreads();
+  } else {
+    // ------------------------------------------------------------ softmax warps without rows < R
+    __syncthreads();
+  }
+}
+
+// LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s, rounded to the dtype; a row whose parts
+// are all empty gets O = 0 and LSE = -inf. VPR threads per row, 8 columns each.
+template <int VPR, bool BF16>
+__global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float4* __restrict__ o_part,
+                                                              const float* __restrict__ lse_part, uint4* __restrict__ o,
+                                                              float* __restrict__ lse, int rows, int n_part) {
+  const size_t n_vec = static_cast<size_t>(rows) * VPR;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
+    const size_t row = i / VPR;
+    const int cv = static_cast<int>(i % VPR);
+    float m = -INFINITY;
+    for (int s = 0; s < n_part; ++s) m = fmaxf(m, __ldg(lse_part + static_cast<size_t>(s) * rows + row));
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < n_part; ++s) {
+        const float ls = __ldg(lse_part + static_cast<size_t>(s) * rows + row);
+        if (ls == -INFINITY) continue;
+        const float wgt = __expf(ls - m);
+        wsum += wgt;
+        const float4* src = o_part + (static_cast<size_t>(s) * rows + row) * (VPR * 2) + 2 * cv;
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        acc[0] = fmaf(wgt, a.x, acc[0]);
+        acc[1] = fmaf(wgt, a.y, acc[1]);
+        acc[2] = fmaf(wgt, a.z, acc[2]);
+        acc[3] = fmaf(wgt, a.w, acc[3]);
+        acc[4] = fmaf(wgt, b.x, acc[4]);
+        acc[5] = fmaf(wgt, b.y, acc[5]);
+        acc[6] = fmaf(wgt, b.z, acc[6]);
+        acc[7] = fmaf(wgt, b.w, acc[7]);
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    o[i] = make_uint4(dpack2<BF16>(acc[0] * inv, acc[1] * inv), dpack2<BF16>(acc[2] * inv, acc[3] * inv),
+                      dpack2<BF16>(acc[4] * inv, acc[5] * inv), dpack2<BF16>(acc[6] * inv, acc[7] * inv));
+    if (cv == 0) lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_decode_t(const DecArgs& a) {
+  using C = DecCfg<D>;
+  auto kern = fa_decode_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  DecParams p;
+  p.tm_q = a.tm_q;
+  p.tm_k = a.tm_k;
+  p.tm_v = a.tm_v;
+  p.page_table = a.page_table;
+  p.ctx_len = a.ctx_len;
+  p.o_part = a.ws_o;
+  p.lse_part = a.ws_lse;
+  p.H = a.H;
+  p.G = a.H / a.Hkv;
+  p.Mq = a.Mq;
+  p.R = p.G * a.Mq;
+  p.ps_log2 = a.ps_log2;
+  p.max_pages = a.max_pages;
+  p.n_pages = a.n_pages;
+  p.tiles_per_split = a.tiles_per_split;
+  p.rows_total = a.B * a.H * a.Mq;
+  p.causal = a.causal ? 1 : 0;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.rescale_threshold = 8.0f;
+  p.timeout_ns = a.timeout_ns;
+  e = launch_kernel(kern, dim3(a.B * a.Hkv, a.n_split, 1), dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  if (e != cudaSuccess) return e;
+  const size_t n_vec = static_cast<size_t>(p.rows_total) * (D / 8);
+  size_t blocks = (n_vec + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  return launch_kernel(fa_decode_merge_kernel<D / 8, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                       a.stream, reinterpret_cast<const float4*>(a.ws_o), static_cast<const float*>(a.ws_lse),
+                       static_cast<uint4*>(a.o), a.lse, p.rows_total, 2 * a.n_split);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecArgs& a) {
+  if (a.d == 128) return a.bf16 ? launch_decode_t<128, true>(a) : launch_decode_t<128, false>(a);
+  if (a.d == 64) return a.bf16 ? launch_decode_t<64, true>(a) : launch_decode_t<64, false>(a);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_clear_status_decode(DevStatusHost* out, cudaStream_t s) {
+  DevStatus zero{0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(DevStatus), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (out->code != 0 || out->count != 0)
+    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(DevStatus), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
+}  // namespace fa

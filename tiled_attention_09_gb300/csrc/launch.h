@@ -58,6 +58,25 @@ struct BwdArgs {
   cudaStream_t stream;
 };
 
+// Paged decode: q [B*H*Mq, d] (2-D map, box rows 128); k, v pages [Hkv][n_pages*page_size][d]
+// (3-D maps, box rows min(page_size, 128)); partial results in the workspace.
+struct DecArgs {
+  CUtensorMap tm_q, tm_k, tm_v;
+  const int* page_table;  // [B][max_pages]
+  const int* ctx_len;     // [B]
+  float* ws_o;            // [2*n_split][B*H*Mq][d]
+  float* ws_lse;          // [2*n_split][B*H*Mq]
+  void* o;                // [B*H*Mq, d] dtype
+  float* lse;             // [B*H*Mq]
+  int B, H, Hkv, Mq, d;
+  int ps_log2, max_pages, n_pages;
+  int tiles_per_split, n_split;
+  float scale;
+  bool causal, bf16;
+  uint64_t timeout_ns;
+  cudaStream_t stream;
+};
+
 // Query-tile height of the backward main kernel for head dimension d (0 = unsupported).
 inline int bwd_query_tile(int d) { return (d == 64 || d == 128 || d == 256) ? 64 : 0; }
 
@@ -68,5 +87,7 @@ cudaError_t launch_bwd_dq_convert(const BwdArgs& a);
 
 cudaError_t read_clear_status_fwd(DevStatusHost* out, cudaStream_t s);
 cudaError_t read_clear_status_bwd(DevStatusHost* out, cudaStream_t s);
+cudaError_t launch_decode(const DecArgs& a);
+cudaError_t read_clear_status_decode(DevStatusHost* out, cudaStream_t s);
 
 }  // namespace fa

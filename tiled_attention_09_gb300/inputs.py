@@ -123,3 +123,71 @@ def sample_cols(N: int, n: int = 64, seed: int = 1):
     perm = np.random.Generator(np.random.PCG64(seed + 1000)).permutation(N).tolist()
     extra = [c for c in perm if c not in fixed][: max(0, n - len(fixed))]
     return sorted(fixed | set(extra))
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One paged-decode problem: Mq new queries per sequence over a paged K/V pool.
+
+    ``ctx`` gives each sequence's cached length. The pool holds ``B * max_pages`` pages plus
+    ``spare`` pages no sequence uses; each sequence owns ``max_pages`` distinct pages in a random
+    order (so neighbouring keys live in scattered pages).
+    """
+
+    B: int
+    H: int
+    Hkv: int
+    Mq: int
+    d: int
+    page_size: int
+    max_pages: int
+    ctx: tuple
+    dtype: str = "bf16"
+    causal: bool = False
+    spare: int = 3
+    seed: int = 0
+    poison: bool = True  # rows past a sequence's end (in its own pages) hold NaN, as a stale cache may
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def n_pages(self) -> int:
+        return self.B * self.max_pages + self.spare
+
+    def kv_bytes(self) -> int:
+        """Bytes of K and V the sequences' keys occupy (what one decode step must read)."""
+        keys = sum(min(max(c, 0), self.max_pages * self.page_size) for c in self.ctx)
+        return 2 * keys * self.Hkv * self.d * 2
+
+    def flops(self) -> float:
+        keys = sum(min(max(c, 0), self.max_pages * self.page_size) for c in self.ctx)
+        return 4.0 * keys * self.H * self.Mq * self.d
+
+    def name(self) -> str:
+        ctx = str(self.ctx[0]) if len(set(self.ctx)) == 1 else "-".join(map(str, self.ctx))
+        return (f"B{self.B}_H{self.H}_Hkv{self.Hkv}_Mq{self.Mq}_d{self.d}_ps{self.page_size}_"
+                f"ctx{ctx}_{self.dtype}_{'causal' if self.causal else 'full'}")
+
+
+def make_paged_inputs(w: DecodeWorkload):
+    """q [B,H,Mq,d], k_pages, v_pages [Hkv,n_pages,page_size,d] (w.dtype), page_table int32 [B,max_pages],
+    ctx_len int32 [B], all CPU tensors. PCG64(seed): q, k_pages, v_pages as float32 standard normals, then
+    the page assignment as one permutation of the pool."""
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    q = rng.standard_normal((w.B, w.H, w.Mq, w.d), dtype=np.float32)
+    kp = rng.standard_normal((w.Hkv, w.n_pages, w.page_size, w.d), dtype=np.float32)
+    vp = rng.standard_normal((w.Hkv, w.n_pages, w.page_size, w.d), dtype=np.float32)
+    table = rng.permutation(w.n_pages)[: w.B * w.max_pages].reshape(w.B, w.max_pages).astype(np.int32)
+    ctx = np.asarray(w.ctx, dtype=np.int32)
+    if w.poison:
+        for b in range(w.B):
+            L = int(min(max(ctx[b], 0), w.max_pages * w.page_size))
+            for j in range(L, w.max_pages * w.page_size):
+                pg, row = table[b, j // w.page_size], j % w.page_size
+                kp[:, pg, row] = np.nan
+                vp[:, pg, row] = np.nan
+    dt = DTYPES[w.dtype]
+    return (torch.from_numpy(q).to(dt), torch.from_numpy(kp).to(dt), torch.from_numpy(vp).to(dt),
+            torch.from_numpy(table), torch.from_numpy(ctx))
