@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work in the oracle's timed sample")
     ap.add_argument("--decode", action="store_true",
                     help="time paged decode attention on the decode points instead (one JSON line each)")
+    ap.add_argument("--decode-point", type=int, default=-1, help="with --decode: only this point (0-based)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
                          "instead of the headline step; one JSON line per point")
@@ -512,30 +513,47 @@ DECODE_POINTS = [  # (B, H, Hkv, Mq, d, page_size, ctx)
 
 def run_decode(args):
     """One JSON line per paged-decode point: fa_decode (split kernel + merge) timed between two events on the
-    launching stream, L2 flushed before every step, median of the timed steps. HBM-bound: the algorithmic
-    bytes are the sequences' K and V (2 * keys * Hkv * d * 2) plus q in and O out; the fraction divides by
-    the measured copy bandwidth."""
+    launching stream, L2 flushed before every step, median of the timed steps. The C function is called
+    with prepared arguments (no Python-side checks or allocation), so the host enqueues it while the L2
+    flush still runs and the events time the device work. HBM-bound: the algorithmic bytes are the
+    sequences' K and V (2 * keys * Hkv * d * 2) plus q in and O out; the fraction divides by the measured
+    copy bandwidth."""
     import torch
     import tiled_attention_09_gb300 as fa
+    from tiled_attention_09_gb300 import _lib
     from tiled_attention_09_gb300.inputs import DecodeWorkload, make_paged_inputs
     peaks, peak_src = load_peaks()
     bw = peaks["hbm_gbs"]
     dev = torch.device("cuda", 0)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     steps, warmup = max(3, min(args.steps, 30)), max(3, args.warmup)
-    for B, H, Hkv, Mq, d, ps, ctx in DECODE_POINTS:
+    points = DECODE_POINTS if args.decode_point < 0 else [DECODE_POINTS[args.decode_point]]
+    for B, H, Hkv, Mq, d, ps, ctx in points:
         w = DecodeWorkload(B, H, Hkv, Mq, d, ps, ctx // ps, (ctx,) * B, spare=0, poison=False)
         q, kp, vp, table, cl = (t.to(dev) for t in make_paged_inputs(w))
         o, lse = fa.decode(q, kp, vp, table, cl)
         n_split = fa.decode_splits(B, Hkv, ps, w.max_pages)
+        L = _lib.load()
+        ws = torch.empty(int(L.fa_decode_workspace_size(B, H, Hkv, Mq, d, ps, w.max_pages, 0)), dtype=torch.uint8,
+                         device=dev)
+        stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+        args = (q.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(), cl.data_ptr(), o.data_ptr(),
+                lse.data_ptr(), ws.data_ptr(), ws.numel(), B, H, Hkv, Mq, d, ps, w.n_pages, w.max_pages, 0, w.scale,
+                0, 1, stream)
+
+        def call():
+            rc = L.fa_decode(*args)
+            if rc != 0:
+                raise RuntimeError(f"fa_decode returned {rc}")
+
         for _ in range(warmup):
             flush.zero_()
-            fa.decode(q, kp, vp, table, cl, out=o, lse=lse)
+            call()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for e0, e1 in evs:
             flush.zero_()
             e0.record()
-            fa.decode(q, kp, vp, table, cl, out=o, lse=lse)
+            call()
             e1.record()
         torch.cuda.synchronize()
         code, info = fa.device_status()

@@ -211,7 +211,7 @@ fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_by
  * Attention实现", section "Pallas内核：自定义高效计算的关键"); per query the
  * online softmax of page "transformer模型详解（十）：FlashAttention优化技术",
  * section "Tiling 分块策略". The key range is cut into n_split splits handled
- * by different CTAs, each writing partial (O_s, LSE_s) to the workspace, and a
+ * by different CTAs, each writing a partial (O_s, LSE_s) to the workspace, and a
  * second launch merges them: LSE = ln sum_s exp(LSE_s),
  * O = sum_s exp(LSE_s - LSE) O_s.
  *   q        [B, H, Mq, d] dtype: the queries at positions ctx_len[b] - Mq + i

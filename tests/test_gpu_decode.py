@@ -3,7 +3,7 @@
 Cases cover grouped-query and multi-query heads (up to 128 query rows per K/V head), one and several
 queries per sequence with the causal end alignment, page sizes 16 to 256, sequence lengths that end
 inside a page, a sequence shorter than its query count and an empty one, and explicit split counts
-(including one split per CTA pair and more splits than tiles). Rows past each sequence's end inside its
+(including a single split with long key streams, and more splits than tiles). Rows past each sequence's end inside its
 pages hold NaN, as a stale cache may: they must never reach the result.
 """
 import numpy as np
@@ -27,6 +27,9 @@ CASES = [
     (DecodeWorkload(2, 2, 2, 2, 64, 128, 3, (1, 384), causal=True), 0),
     (DecodeWorkload(2, 4, 1, 3, 64, 32, 9, (200, 129), dtype="fp16", causal=True), 50),
     (DecodeWorkload(4, 8, 8, 1, 64, 16, 64, (1024, 1, 513, 1023)), 0),
+    # long key streams in one split (tens of tiles per stream, each ring reused many times)
+    (DecodeWorkload(2, 8, 2, 1, 128, 64, 128, (8192, 8000)), 1),
+    (DecodeWorkload(2, 16, 2, 2, 64, 128, 64, (8192, 7777), causal=True), 1),
 ]
 
 

@@ -109,7 +109,7 @@ struct DecWs {
   size_t off_o, off_lse, total;
 };
 DecWs decode_ws(int B, int H, int Mq, int d, int n_split) {
-  const size_t rows = static_cast<size_t>(B) * H * Mq, parts = 2 * static_cast<size_t>(n_split);
+  const size_t rows = static_cast<size_t>(B) * H * Mq, parts = static_cast<size_t>(n_split);
   DecWs w;
   w.off_o = 0;
   w.off_lse = (parts * rows * d * 4 + 255) & ~size_t(255);

@@ -15,17 +15,20 @@
 // bandwidth, and with G query heads per K/V head each key is used by R = G * Mq query rows. A CTA
 // owns one K/V head of one sequence and one split; its R query rows (the G heads' Mq queries are
 // consecutive rows of q) form one 128-row tile, so the tile's products run on the tensor core
-// (tcgen05.mma, rows past R are never read back) and the per-key cost stays far below the HBM
-// time of a key even for large groups. The CTA runs two independent key streams over its split
-// (even and odd 128-key tiles), each with its own S and O in tensor memory and its own softmax
-// warpgroup, so one stream's exponentials overlap the other's products; the two streams are two
-// partial results for the merge. K/V tiles are gathered page by page with TMA into a ring of
-// shared-memory slots; pages past the sequence's end are not read (zero-filled), and value rows
-// past its end inside the last tile are zeroed before use (a stale page tail may hold non-finite
-// values, and 0 * NaN is NaN in the product).
-// Roles (320 threads): warps 0-3 softmax of stream 0 and warps 4-7 of stream 1 (only the warps
-// that hold rows < R work), warp 8 TMA producer, warp 9 MMA issuer.
-// TMEM: S_t at 128t (fp32 128 x 128; P_t as 16-bit pairs over it), O_t at 256 + d t.
+// (tcgen05.mma, rows past R are never read back). One thread issues a tcgen05.mma only every
+// ~150 cycles, so the products of a key tile are split between two issuing warps: S(j) = Q K(j)^T
+// into one of two TMEM buffers (j & 1), and O += P(j) V(j) with P(j) read from that buffer. The
+// S issuer computes S(j + 1) while the softmax warps turn S(j) into P(j) and while O += P(j - 1)
+// V(j - 1) runs, and waits only before reusing a buffer (its previous P must have been read). The
+// softmax's lazy rescale of O waits for the previous P V only when a row's max has grown.
+// K and V tiles are gathered page by page with TMA into two rings of shared-memory slots, the K
+// ring consumed in order by the S issuer and the V ring by the P V issuer (one in-order consumer
+// per ring keeps a slot's full-barrier parity unambiguous). Pages past the sequence's end are not
+// read (zero-filled), and value rows past its end inside the last tile are zeroed before use (a
+// stale page tail may hold non-finite values, and 0 * NaN is NaN in the product).
+// Roles (224 threads): warps 0-3 softmax (only the warps holding rows < R work), warp 4 TMA
+// producer, warp 5 the S issuer (and TMEM owner), warp 6 the P V issuer.
+// TMEM: S buffers at 0 and 128 (fp32 128 x 128; P as 16-bit pairs over them), O at 256.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,8 +44,8 @@ struct DecParams {
   CUtensorMap tm_k, tm_v;  // [Hkv][P*page_size rows][d], box {64, min(page_size, 128), 1}
   const int* page_table;   // [B][max_pages]
   const int* ctx_len;      // [B]
-  float* o_part;           // [n_part][B*H*Mq][d] fp32, each part normalised by its own sum
-  float* lse_part;         // [n_part][B*H*Mq]
+  float* o_part;           // [n_split][B*H*Mq][d] fp32, each split's part normalised by its own sum
+  float* lse_part;         // [n_split][B*H*Mq]
   int H, G, Mq, R;         // query heads, query heads per K/V head, queries per head, rows per CTA
   int ps_log2;             // log2(page size)
   int max_pages, n_pages;  // page-table row length, pages in the cache
@@ -59,17 +62,17 @@ struct DecCfg {
   static constexpr int CHUNK = 128 * 128;  // 128 rows x 64 elements x 2 bytes
   static constexpr int NCH = D / 64;
   static constexpr int TILE = 128 * D * 2;
-  // ring slots (one K or one V tile each) filling the rest of the 227 KB
+  // ring slots (one K or one V tile each) filling the rest of the 227 KB, half for K, half for V
   static constexpr int NS_FIT = (227 * 1024 - 1024 - TILE - 512) / TILE;
-  static constexpr int NS = NS_FIT > 12 ? 12 : NS_FIT;
-  // q, full[NS], empty[NS], s[2], p[2], o[2], drain
-  static constexpr int NBAR = 1 + 2 * NS + 6 + 1;
+  static constexpr int NSR = (NS_FIT > 12 ? 12 : NS_FIT) / 2;  // slots per ring
+  // q, kfull[NSR], kempty[NSR], vfull[NSR], vempty[NSR], sfull[2], pfull[2], pvdone[2], odone, drain[2]
+  static constexpr int NBAR = 1 + 4 * NSR + 6 + 1 + 2;
   static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
-  static constexpr int SMEM_BYTES = 1024 + TILE + NS * TILE + BAR_BYTES + 16;
-  static constexpr int THREADS = 320;
-  static_assert(NS >= 4, "the ring must hold the MMA issuer's look-ahead");
+  static constexpr int SMEM_BYTES = 1024 + TILE + 2 * NSR * TILE + BAR_BYTES + 16;
+  static constexpr int THREADS = 224;
+  static_assert(NSR >= 2, "a ring must hold the tile in use and the next one");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
-  static_assert(256 + 2 * D <= 512, "TMEM budget");
+  static_assert(256 + D <= 512, "TMEM budget");
 };
 
 template <bool BF16>
@@ -83,12 +86,13 @@ __device__ __forceinline__ uint32_t dpack2(float lo, float hi) {
   }
 }
 
-enum : uint32_t { WD_Q = 31, WD_EMPTY = 32, WD_FULL = 33, WD_P = 34, WD_S = 35, WD_O = 36, WD_V = 37, WD_DRAIN = 38 };
+enum : uint32_t {
+  WD_Q = 31, WD_EMPTY = 32, WD_FULL = 33, WD_P = 34, WD_S = 35, WD_O = 36, WD_V = 37, WD_DRAIN = 38, WD_PV = 39
+};
 
-// The CTA's split of one sequence: 128-key tiles [lo, lo + n) of the sequence's ceil(ctx / 128),
-// stream t takes tiles lo + t, lo + t + 2, ... (n0 = ceil(n / 2) and n1 = floor(n / 2) of them).
+// The CTA's split of one sequence: 128-key tiles [lo, lo + n) of the sequence's ceil(ctx / 128).
 struct DecWork {
-  int b, hk, ctx, lo, n0, n1;
+  int b, hk, ctx, lo, n;
   __device__ __forceinline__ DecWork(const DecParams& p) {
     const int Hkv = p.H / p.G;
     b = blockIdx.x / Hkv;
@@ -100,62 +104,57 @@ struct DecWork {
     lo = blockIdx.y * p.tiles_per_split;
     int hi = lo + p.tiles_per_split;
     hi = hi < n_tiles ? hi : n_tiles;
-    const int n = hi > lo ? hi - lo : 0;
-    n0 = (n + 1) / 2;
-    n1 = n / 2;
-  }
-  __device__ __forceinline__ int tiles(int t) const { return t ? n1 : n0; }
-  // position in the load (and MMA) order of V of stream t's tile j: step m = j + 1 issues, per
-  // stream, V(t, m - 1) then K(t, m); loads before step m (m >= 1) number
-  // min(m, n0) + min(m, n1) + min(m - 1, n0) + min(m - 1, n1)
-  __device__ __forceinline__ uint32_t seq_v(int t, int j) const {
-    const int m = j + 1;
-    int s = min(m, n0) + min(m, n1) + min(m - 1, n0) + min(m - 1, n1);
-    if (t == 1) s += (m <= n0 ? 1 : 0) + (m < n0 ? 1 : 0);
-    return static_cast<uint32_t>(s);
+    n = hi > lo ? hi - lo : 0;
   }
 };
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant__ DecParams p) {
   using C = DecCfg<D>;
-  constexpr int NS = C::NS;
+  constexpr int NSR = C::NSR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);
-  const uint32_t sRing = sQ + C::TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE + NS * C::TILE);
+  const uint32_t sK = sQ + C::TILE;              // K ring
+  const uint32_t sV = sK + NSR * C::TILE;        // V ring
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE + 2 * NSR * C::TILE);
   const uint32_t b_q = smem_u32(&bars[0]);
-  auto b_full = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto b_empty = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
-  auto b_s = [&](int t) { return smem_u32(&bars[1 + 2 * NS + t]); };
-  auto b_p = [&](int t) { return smem_u32(&bars[3 + 2 * NS + t]); };
-  auto b_o = [&](int t) { return smem_u32(&bars[5 + 2 * NS + t]); };
-  const uint32_t b_drain = smem_u32(&bars[7 + 2 * NS]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::TILE + NS * C::TILE + C::BAR_BYTES);
+  auto b_kfull = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto b_kempty = [&](int s) { return smem_u32(&bars[1 + NSR + s]); };
+  auto b_vfull = [&](int s) { return smem_u32(&bars[1 + 2 * NSR + s]); };
+  auto b_vempty = [&](int s) { return smem_u32(&bars[1 + 3 * NSR + s]); };
+  auto b_sfull = [&](int b) { return smem_u32(&bars[1 + 4 * NSR + b]); };
+  auto b_pfull = [&](int b) { return smem_u32(&bars[3 + 4 * NSR + b]); };
+  auto b_pvdone = [&](int b) { return smem_u32(&bars[5 + 4 * NSR + b]); };
+  const uint32_t b_odone = smem_u32(&bars[7 + 4 * NSR]);
+  auto b_drain = [&](int i) { return smem_u32(&bars[8 + 4 * NSR + i]); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::TILE + 2 * NSR * C::TILE + C::BAR_BYTES);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
   const DecWork w(p);
-  const int nact = (p.R + 31) / 32;  // softmax warps per stream that hold rows < R
+  const int nact = (p.R + 31) / 32;  // softmax warps that hold rows < R
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(b_full(s), 1);
-      mbar_init(b_empty(s), 1);
+    for (int s = 0; s < NSR; ++s) {
+      mbar_init(b_kfull(s), 1);
+      mbar_init(b_kempty(s), 1);
+      mbar_init(b_vfull(s), 1);
+      mbar_init(b_vempty(s), 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(b_s(t), 1);
-      mbar_init(b_p(t), 32 * nact);
-      mbar_init(b_o(t), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(b_sfull(b), 1);
+      mbar_init(b_pfull(b), 32 * nact);
+      mbar_init(b_pvdone(b), 1);
+      mbar_init(b_drain(b), 1);
     }
-    mbar_init(b_drain, 1);
+    mbar_init(b_odone, 1);
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
   }
-  if (warp == 9) {
+  if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -164,8 +163,9 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int q_row0 = (w.b * p.H + w.hk * p.G) * p.Mq;  // first of the CTA's R query rows
+  const int n = w.n;
 
-  if (warp == 8) {
+  if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
       tma_prefetch_desc(&p.tm_q);
@@ -175,16 +175,15 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ + c * C::CHUNK, &p.tm_q, b_q, c * 64, q_row0);
       const int ps = 1 << p.ps_log2;
-      const int br = ps < 128 ? ps : 128;  // rows per TMA box
-      const int oob_row = p.n_pages << p.ps_log2;  // the first row past the cache: the box reads zeros
+      const int br = ps < 128 ? ps : 128;           // rows per TMA box
+      const int oob_row = p.n_pages << p.ps_log2;   // the first row past the cache: the box reads zeros
       const int* ptab = p.page_table + static_cast<size_t>(w.b) * p.max_pages;
-      uint32_t seq = 0;
-      bool ok = true;
-      // one K or V tile of 128 keys, page by page
-      auto load = [&](const CUtensorMap* map, int kt) -> bool {
-        const uint32_t slot = seq % NS, use = seq / NS;
-        if (use > 0 && !wait_bar(b_empty(slot), (use - 1) & 1, p.timeout_ns, abort_flag, WD_EMPTY)) return false;
-        mbar_arrive_expect_tx(b_full(slot), C::TILE);
+      // tile j of the split into ring slot j % NSR, page by page
+      auto load = [&](uint32_t ring, uint32_t full, uint32_t empty, const CUtensorMap* map, int j) -> bool {
+        const int slot = j % NSR, use = j / NSR;
+        if (use > 0 && !wait_bar(empty + 8 * slot, (use - 1) & 1, p.timeout_ns, abort_flag, WD_EMPTY)) return false;
+        mbar_arrive_expect_tx(full + 8 * slot, C::TILE);
+        const int kt = w.lo + j;
         for (int r0 = 0; r0 < 128; r0 += br) {
           const int key = kt * 128 + r0;
           int y = oob_row;
@@ -194,107 +193,100 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
           }
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK + r0 * 128, map, b_full(slot), c * 64, y, w.hk);
+            tma_load_3d(ring + slot * C::TILE + c * C::CHUNK + r0 * 128, map, full + 8 * slot, c * 64, y, w.hk);
         }
-        ++seq;
         return true;
       };
-      // the MMA issuer's order: per step j and stream t, V(t, j - 1) then K(t, j)
-      for (int j = 0; ok && j <= w.n0; ++j) {
-        for (int t = 0; ok && t < 2; ++t) {
-          const int nt = w.tiles(t);
-          if (j >= 1 && j <= nt) ok = load(&p.tm_v, w.lo + 2 * (j - 1) + t);
-          if (ok && j < nt) ok = load(&p.tm_k, w.lo + 2 * j + t);
-        }
-      }
+      int j = 0;
+      for (; j < n; ++j)
+        if (!load(sK, b_kfull(0), b_kempty(0), &p.tm_k, j) || !load(sV, b_vfull(0), b_vempty(0), &p.tm_v, j)) break;
       // Drain: every issued copy has landed before the CTA may exit.
-      for (uint32_t s = (seq > NS ? seq - NS : 0u); s < seq; ++s)
-        wait_bar(b_full(s % NS), (s / NS) & 1, p.timeout_ns, abort_flag, WD_DRAIN);
+      for (int i = (j > NSR ? j - NSR : 0); i < j; ++i) {
+        wait_bar(b_kfull(i % NSR), (i / NSR) & 1, p.timeout_ns, abort_flag, WD_DRAIN);
+        wait_bar(b_vfull(i % NSR), (i / NSR) & 1, p.timeout_ns, abort_flag, WD_DRAIN);
+      }
       wait_bar(b_q, 0, p.timeout_ns, abort_flag, WD_DRAIN);
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ S issuer: S(j) = Q K(j)^T into buffer j & 1
     if (elect_one()) {
       constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
-      constexpr uint32_t idesc_pv = make_idesc(128, D, BF16, false, true);
-      const uint64_t dq0 = make_sdesc(sQ, 16, 1024);           // Q, K-major
-      const uint64_t dk0 = make_sdesc(sRing, 16, 1024);        // K in a ring slot, K-major
-      const uint64_t dv0 = make_sdesc(sRing, C::CHUNK, 1024);  // V in a ring slot, MN-major
-      uint32_t seq = 0;
+      const uint64_t dq0 = make_sdesc(sQ, 16, 1024);  // Q, K-major
+      const uint64_t dk0 = make_sdesc(sK, 16, 1024);  // K ring slot, K-major
       bool ok = wait_bar(b_q, 0, p.timeout_ns, abort_flag, WD_Q);
-      for (int j = 0; ok && j <= w.n0; ++j) {
-        for (int t = 0; ok && t < 2; ++t) {
-          const int nt = w.tiles(t);
-          if (j >= 1 && j <= nt) {
-            // O_t += P_t(j - 1) V(t, j - 1)
-            const uint32_t sv = seq++;
-            if (!wait_bar(b_full(sv % NS), (sv / NS) & 1, p.timeout_ns, abort_flag, WD_FULL) ||
-                !wait_bar(b_p(t), (j - 1) & 1, p.timeout_ns, abort_flag, WD_P)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t dv = dv0 + static_cast<uint64_t>(((sv % NS) * C::TILE) >> 4);
-            const uint32_t tO = tmem + 256 + D * t, tP = tmem + 128 * t;
+      for (int j = 0; ok && j < n; ++j) {
+        const int slot = j % NSR, b = j & 1;
+        if (!wait_bar(b_kfull(slot), (j / NSR) & 1, p.timeout_ns, abort_flag, WD_FULL)) break;
+        // the buffer still holds P(j - 2) until O += P(j - 2) V(j - 2) has read it
+        if (j >= 2 && !wait_bar(b_pvdone(b), ((j - 2) >> 1) & 1, p.timeout_ns, abort_flag, WD_PV)) break;
+        tc_fence_after();
+        const uint64_t dk = dk0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 16 rows of V = 2048 bytes
-              mma_ts(tO, tP + k * 8, dv + static_cast<uint64_t>(k * (2048 >> 4)), idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
-            mma_commit(b_empty(sv % NS));
-            if (j == nt) mma_commit(b_o(t));
-          }
-          if (j < nt) {
-            // S_t(j) = Q K(t, j)^T; its commit also covers O_t's update above
-            const uint32_t sk = seq++;
-            if (!wait_bar(b_full(sk % NS), (sk / NS) & 1, p.timeout_ns, abort_flag, WD_FULL)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t dk = dk0 + static_cast<uint64_t>(((sk % NS) * C::TILE) >> 4);
-            const uint32_t tS = tmem + 128 * t;
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {  // 16 head dims per MMA
-              const uint64_t off = static_cast<uint64_t>(((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4);
-              mma_ss(tS, dq0 + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
-            }
-            mma_commit(b_s(t));
-            mma_commit(b_empty(sk % NS));
-          }
+        for (int k = 0; k < D / 16; ++k) {  // 16 head dims per MMA
+          const uint64_t off = static_cast<uint64_t>(((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4);
+          mma_ss(tmem + 128 * b, dq0 + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
         }
+        mma_commit(b_sfull(b));
+        mma_commit(b_kempty(slot));
       }
-      mma_commit(b_drain);
-      wait_bar(b_drain, 0, p.timeout_ns, abort_flag, WD_DRAIN);
+      mma_commit(b_drain(0));
+      wait_bar(b_drain(0), 0, p.timeout_ns, abort_flag, WD_DRAIN);
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
-  } else if ((warp & 3) < nact) {
-    // ------------------------------------------------------------ softmax + epilogue of stream t
-    const int t = warp >> 2;
-    const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + 128 * t;
-    const uint32_t tO = tmem + lane_off + 256 + D * t;
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ P V issuer: O += P(j) V(j)
+    if (elect_one()) {
+      constexpr uint32_t idesc_pv = make_idesc(128, D, BF16, false, true);
+      const uint64_t dv0 = make_sdesc(sV, C::CHUNK, 1024);  // V ring slot, MN-major
+      for (int j = 0; j < n; ++j) {
+        const int slot = j % NSR, b = j & 1;
+        if (!wait_bar(b_pfull(b), (j >> 1) & 1, p.timeout_ns, abort_flag, WD_P) ||
+            !wait_bar(b_vfull(slot), (j / NSR) & 1, p.timeout_ns, abort_flag, WD_FULL))
+          break;
+        tc_fence_after();
+        const uint64_t dv = dv0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 16 rows of V = 2048 bytes
+          mma_ts(tmem + 256, tmem + 128 * b + k * 8, dv + static_cast<uint64_t>(k * (2048 >> 4)), idesc_pv,
+                 (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit(b_pvdone(b));
+        mma_commit(b_vempty(slot));
+        if (j == n - 1) mma_commit(b_odone);
+      }
+      mma_commit(b_drain(1));
+      wait_bar(b_drain(1), 0, p.timeout_ns, abort_flag, WD_DRAIN);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+  } else if (warp < nact) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int r = threadIdx.x;  // query row of the CTA (0 .. R-1 are real) == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_off + 256;
     const float sl2 = p.scale_log2;
-    const int nt = w.tiles(t);
     // keys this row may see: the sequence's, and (causal) none after the query's own position
     // ctx - Mq + i, i = r % Mq
     int klim = w.ctx;
     if (p.causal) klim = w.ctx - p.Mq + (r % p.Mq) + 1;
     float m_used = 0.f, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bar(b_s(t), j & 1, p.timeout_ns, abort_flag, WD_S))) {
+    for (int j = 0; j < n; ++j) {
+      const int b = j & 1;
+      const uint32_t tS = tmem + lane_off + 128 * b;
+      if (!__all_sync(0xffffffffu, wait_bar(b_sfull(b), (j >> 1) & 1, p.timeout_ns, abort_flag, WD_S))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int kt = w.lo + 2 * j + t;
+      const int kt = w.lo + j;
       float s[128];
       {
         uint32_t u[128];
@@ -307,22 +299,29 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = c >= lim ? -INFINITY : s[c];
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        mx0 = max3f(mx0, s[c + 0], s[c + 1]);
-        mx1 = max3f(mx1, s[c + 2], s[c + 3]);
-        mx2 = max3f(mx2, s[c + 4], s[c + 5]);
-        mx3 = max3f(mx3, s[c + 6], s[c + 7]);
+      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; c += 16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = max3f(mx[e], s[c + 2 * e], s[c + 2 * e + 1]);
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_tile =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
       if (j == 0) {
         m_used = m_tile == -INFINITY ? 0.f : m_tile;  // no visible key yet: every P is 0
       } else {
-        // lazy rescale: the running max moves only when the row max grows past the threshold;
-        // the commit that announced S_t(j) also covers P_t(j - 1) V, so O_t is quiescent
+        // lazy rescale: the running max moves only when the row max grows past the threshold; O must
+        // then be quiescent, i.e. O += P(j - 1) V(j - 1) complete
         const bool rescale = m_tile > m_used + p.rescale_threshold;
         if (__any_sync(0xffffffffu, rescale)) {
+          if (!__all_sync(0xffffffffu,
+                          wait_bar(b_pvdone((j - 1) & 1), ((j - 1) >> 1) & 1, p.timeout_ns, abort_flag, WD_PV))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const float alpha = rescale ? ex2_approx(m_used - m_tile) : 1.f;
           if (rescale) {
             m_used = m_tile;
@@ -339,28 +338,31 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
         }
       }
       uint32_t pk[64];
-      float ls0 = 0.f, ls1 = 0.f;
+      float ls[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ls[e] = 0.f;
       const float neg_m = -m_used;
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
         const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
         const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
-        ls0 += p0;
-        ls1 += p1;
+        ls[(c >> 1) & 7] += p0 + p1;
         pk[c >> 1] = dpack2<BF16>(p0, p1);
       }
-      l += ls0 + ls1;
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       // The sequence's last tile: value rows past its end may come from a stale page tail; zero them
-      // (after their copy has landed) so that P = 0 there cannot meet a non-finite value.
+      // (after their copy has landed) so that P = 0 there cannot meet a non-finite value. V(j) is load
+      // j of the V ring; the slot's previous load (j - NSR <= j - 2) was consumed by O += P V before
+      // S(j) could be issued, so the parity names this load's phase.
       const int valid = w.ctx - kt * 128;
       if (valid < 128) {
-        const uint32_t sv = w.seq_v(t, j);
-        if (!__all_sync(0xffffffffu, wait_bar(b_full(sv % NS), (sv / NS) & 1, p.timeout_ns, abort_flag, WD_V))) {
+        const int slot = j % NSR;
+        if (!__all_sync(0xffffffffu, wait_bar(b_vfull(slot), (j / NSR) & 1, p.timeout_ns, abort_flag, WD_V))) {
           ok = false;
           break;
         }
-        uint8_t* vt = smem + C::TILE + (sv % NS) * C::TILE;
-        for (int row = valid + (r & 31) + 32 * (warp & 3); row < 128; row += 32 * nact) {
+        uint8_t* vt = smem + C::TILE + (NSR + slot) * C::TILE;
+        for (int row = valid + r; row < 128; row += 32 * nact) {
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c) {
             uint4* z = reinterpret_cast<uint4*>(vt + c * C::CHUNK + row * 128);
@@ -373,15 +375,14 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
       tmem_st64(tS, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(b_p(t));
+      mbar_arrive(b_pfull(b));
     }
-    // ---------------------------------------------------------- epilogue: this stream's partial result
-    const int part = 2 * blockIdx.y + t;
+    // ---------------------------------------------------------- epilogue: the split's partial result
     const bool row_ok = r < p.R;
-    const size_t grow = static_cast<size_t>(part) * p.rows_total + q_row0 + r;
+    const size_t grow = static_cast<size_t>(blockIdx.y) * p.rows_total + q_row0 + r;
     float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D);
-    if (ok && nt > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(b_o(t), 0, p.timeout_ns, abort_flag, WD_O));
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(b_odone, 0, p.timeout_ns, abort_flag, WD_O));
       if (ok) {
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
         }
         if (row_ok) p.lse_part[grow] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
-    } else if (ok && row_ok) {  // no tile in this stream: an empty partial
+    } else if (ok && row_ok) {  // no tile in this split for the sequence: an empty partial
 #pragma unroll 4
       for (int g = 0; g < D / 4; ++g) dst[g] = make_float4(0.f, 0.f, 0.f, 0.f);
       p.lse_part[grow] = -INFINITY;
@@ -413,7 +414,8 @@ __global__ void __launch_bounds__(320, 1) fa_decode_kernel(const __grid_constant
 }
 
 // LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s, rounded to the dtype; a row whose parts
-// are all empty gets O = 0 and LSE = -inf. VPR threads per row, 8 columns each.
+// are all empty gets O = 0 and LSE = -inf. VPR threads per row, 8 columns each. The loops over the
+// parts are unrolled so that their loads are in flight together (an empty part weighs exp(-inf) = 0).
 template <int VPR, bool BF16>
 __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float4* __restrict__ o_part,
                                                               const float* __restrict__ lse_part, uint4* __restrict__ o,
@@ -424,26 +426,25 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float4* __re
     const size_t row = i / VPR;
     const int cv = static_cast<int>(i % VPR);
     float m = -INFINITY;
+#pragma unroll 8
     for (int s = 0; s < n_part; ++s) m = fmaxf(m, __ldg(lse_part + static_cast<size_t>(s) * rows + row));
+    const float m0 = m == -INFINITY ? 0.f : m;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float wsum = 0.f;
-    if (m != -INFINITY) {
-      for (int s = 0; s < n_part; ++s) {
-        const float ls = __ldg(lse_part + static_cast<size_t>(s) * rows + row);
-        if (ls == -INFINITY) continue;
-        const float wgt = __expf(ls - m);
-        wsum += wgt;
-        const float4* src = o_part + (static_cast<size_t>(s) * rows + row) * (VPR * 2) + 2 * cv;
-        const float4 a = __ldg(src), b = __ldg(src + 1);
-        acc[0] = fmaf(wgt, a.x, acc[0]);
-        acc[1] = fmaf(wgt, a.y, acc[1]);
-        acc[2] = fmaf(wgt, a.z, acc[2]);
-        acc[3] = fmaf(wgt, a.w, acc[3]);
-        acc[4] = fmaf(wgt, b.x, acc[4]);
-        acc[5] = fmaf(wgt, b.y, acc[5]);
-        acc[6] = fmaf(wgt, b.z, acc[6]);
-        acc[7] = fmaf(wgt, b.w, acc[7]);
-      }
+#pragma unroll 4
+    for (int s = 0; s < n_part; ++s) {
+      const float wgt = __expf(__ldg(lse_part + static_cast<size_t>(s) * rows + row) - m0);
+      const float4* src = o_part + (static_cast<size_t>(s) * rows + row) * (VPR * 2) + 2 * cv;
+      const float4 a = __ldg(src), b = __ldg(src + 1);
+      wsum += wgt;
+      acc[0] = fmaf(wgt, a.x, acc[0]);
+      acc[1] = fmaf(wgt, a.y, acc[1]);
+      acc[2] = fmaf(wgt, a.z, acc[2]);
+      acc[3] = fmaf(wgt, a.w, acc[3]);
+      acc[4] = fmaf(wgt, b.x, acc[4]);
+      acc[5] = fmaf(wgt, b.y, acc[5]);
+      acc[6] = fmaf(wgt, b.z, acc[6]);
+      acc[7] = fmaf(wgt, b.w, acc[7]);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     o[i] = make_uint4(dpack2<BF16>(acc[0] * inv, acc[1] * inv), dpack2<BF16>(acc[2] * inv, acc[3] * inv),
@@ -486,7 +487,7 @@ cudaError_t launch_decode_t(const DecArgs& a) {
   if (blocks > 152 * 16) blocks = 152 * 16;
   return launch_kernel(fa_decode_merge_kernel<D / 8, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
                        a.stream, reinterpret_cast<const float4*>(a.ws_o), static_cast<const float*>(a.ws_lse),
-                       static_cast<uint4*>(a.o), a.lse, p.rows_total, 2 * a.n_split);
+                       static_cast<uint4*>(a.o), a.lse, p.rows_total, a.n_split);
 }
 
 }  // namespace

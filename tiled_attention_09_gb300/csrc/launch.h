@@ -64,8 +64,8 @@ struct DecArgs {
   CUtensorMap tm_q, tm_k, tm_v;
   const int* page_table;  // [B][max_pages]
   const int* ctx_len;     // [B]
-  float* ws_o;            // [2*n_split][B*H*Mq][d]
-  float* ws_lse;          // [2*n_split][B*H*Mq]
+  float* ws_o;            // [n_split][B*H*Mq][d]
+  float* ws_lse;          // [n_split][B*H*Mq]
   void* o;                // [B*H*Mq, d] dtype
   float* lse;             // [B*H*Mq]
   int B, H, Hkv, Mq, d;
