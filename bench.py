@@ -8,7 +8,7 @@ FLOPs follow the metric's own count: forward 4*B*H*N^2*d halved when causal,
 backward 2.5x that; value = 3.5*F_fwd / (t_fwd + t_bwd).
 
 Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
-barrier and torch.cuda.synchronize(); the L2 cache is flushed (a 256 MiB write)
+barrier and torch.cuda.synchronize(); the L2 cache is flushed (a 256 MiB write, then a 256 MiB read)
 before each step, outside the CUDA-event-timed interval of that step. A step is
 timed between two events (fa_fwd_ex, fa_bwd through the C ABI), so the kernels
 keep their programmatic dependent launch; per-kernel times (kernels_ms and the
@@ -258,6 +258,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+class L2Flush:
+    """Evicts the L2 cache between timed steps: a write of a buffer larger than L2, then a read of a second
+    one, so that the dirty lines the write leaves behind are written back here, outside the timed interval,
+    and the step starts from a cold, clean L2."""
+
+    def __init__(self, torch, dev, mib=256):
+        n = mib * 1024 * 1024 // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.ones(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.sink)
+
+
 def run_native(args):
     import torch
     import tiled_attention_09_gb300 as fa
@@ -286,7 +303,7 @@ def run_native(args):
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     ws_bytes = int(L.fa_bwd_workspace_size(B, H, N, d))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
     scale = w.scale
@@ -321,7 +338,7 @@ def run_native(args):
     o_lo = torch.empty_like(qd)
     dptrs = [t.data_ptr() for t in (qd, kd, vd, o, lse, dod, dq, dk, dv, o_lo)]
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         launch(dptrs)
     torch.cuda.synchronize()
     code, info = fa.device_status(stream.cuda_stream)
@@ -338,11 +355,11 @@ def run_native(args):
         dist.barrier()
     torch.cuda.synchronize()
     for s in range(args.steps):
-        flush.zero_()
+        flush()
         launch(dptrs, evs[s])
     torch.cuda.synchronize()
     for s in range(K2):
-        flush.zero_()
+        flush()
         launch_phases(dptrs, pevs[s])
     torch.cuda.synchronize()
     if dist:
@@ -415,7 +432,7 @@ def run_native(args):
         "ms_per_step": 1e3 * total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name(), "B": B, "H": H, "N": N, "d": d, "causal": True, "seed": 0,
-                   "l2": "flushed before every step (256 MiB write, outside the timed interval)",
+                   "l2": "flushed before every step (256 MiB write, then a 256 MiB read of another buffer so the write-back is not charged to the step; outside the timed interval)",
                    "timing": "value: whole step between two events; kernels_ms/roofline: a second pass of "
                              f"{K2} steps with events between kernels",
                    "parallelism": f"weak: {world} independent replica(s)"},
@@ -448,7 +465,7 @@ def run_sweep(args):
     peaks, peak_src = load_peaks()
     peak, bw = peaks["bf16_tflops"], peaks["hbm_gbs"]
     dev = torch.device("cuda", 0)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     steps, warmup = max(3, min(args.steps, 20)), max(3, args.warmup)
     for d in (64, 128, 256):
         for N in (512, 1024, 2048, 4096, 8192, 16384):
@@ -471,12 +488,12 @@ def run_sweep(args):
                     times = {}
                     for name, fn in (("fwd", fwd), ("fwd_bwd", step)):
                         for _ in range(warmup):
-                            flush.zero_()
+                            flush()
                             fn()
                         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                                for _ in range(steps)]
                         for e0, e1 in evs:
-                            flush.zero_()
+                            flush()
                             e0.record()
                             fn()
                             e1.record()
@@ -525,7 +542,7 @@ def run_decode(args):
     peaks, peak_src = load_peaks()
     bw = peaks["hbm_gbs"]
     dev = torch.device("cuda", 0)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)  # ~80 us of device work: longer than the host takes to enqueue the call
     steps, warmup = max(3, min(args.steps, 30)), max(3, args.warmup)
     points = DECODE_POINTS if args.decode_point < 0 else [DECODE_POINTS[args.decode_point]]
     for B, H, Hkv, Mq, d, ps, ctx in points:
@@ -547,13 +564,16 @@ def run_decode(args):
                 raise RuntimeError(f"fa_decode returned {rc}")
 
         for _ in range(warmup):
-            flush.zero_()
+            flush()
             call()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        host = []
         for e0, e1 in evs:
-            flush.zero_()
+            flush()
             e0.record()
+            h0 = time.perf_counter()
             call()
+            host.append(time.perf_counter() - h0)
             e1.record()
         torch.cuda.synchronize()
         code, info = fa.device_status()
@@ -562,7 +582,8 @@ def run_decode(args):
         t = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
         nbytes = w.kv_bytes() + 2 * q.numel() * 2 + 4 * lse.numel()
         gbs = nbytes / t / 1e9
-        print(json.dumps({"point": w.name(), "us": 1e6 * t, "n_split": n_split, "ctas": B * Hkv * n_split,
+        print(json.dumps({"point": w.name(), "us": 1e6 * t, "host_us": 1e6 * statistics.median(host),
+                          "n_split": n_split, "ctas": B * Hkv * n_split,
                           "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_hbm": gbs / bw, "hbm_peak_gbs": bw,
                           "peak_source": peak_src, "tflops": w.flops() / t / 1e12}), flush=True)
         del q, kp, vp, table, cl, o, lse

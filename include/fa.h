@@ -228,10 +228,12 @@ fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_by
  *   j <= ctx_len[b] - Mq + i; otherwise all ctx_len[b] keys.
  * Shapes: d in {64, 128}; page_size a power of two in [16, 256]; H a multiple
  * of Hkv with (H / Hkv) * Mq <= 128; else FA_ERR_UNSUPPORTED.
- * n_split <= 0 lets the library choose (fa_decode_splits). workspace: device
+ * n_split <= 0 lets the library choose (fa_decode_splits); at most 64 (larger
+ * values are capped), and with one split the kernel writes o and lse itself
+ * (no merge launch). workspace: device
  * memory of fa_decode_workspace_size(...) bytes for the same n_split,
  * 256-byte aligned. page_table and ctx_len must be 4-byte aligned, the rest
- * 16-byte aligned. Two launches on `stream`.
+ * 16-byte aligned. One or two launches on `stream`.
  */
 int fa_decode_splits(int B, int Hkv, int page_size, int max_pages);
 size_t fa_decode_workspace_size(int B, int H, int Hkv, int Mq, int d, int page_size, int max_pages, int n_split);

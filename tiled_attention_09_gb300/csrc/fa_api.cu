@@ -388,6 +388,7 @@ int fa_decode_splits(int B, int Hkv, int page_size, int max_pages) {
 size_t fa_decode_workspace_size(int B, int H, int Hkv, int Mq, int d, int page_size, int max_pages, int n_split) {
   if (check_decode_shape(B, H, Hkv, Mq, d, page_size, 1, max_pages, FA_BF16) != FA_OK) return 0;
   if (n_split <= 0) n_split = decode_splits(B, Hkv, page_size, max_pages);
+  if (n_split > 64) n_split = 64;
   return decode_ws(B, H, Mq, d, n_split).total;
 }
 
@@ -400,11 +401,11 @@ fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, con
   if (s != FA_OK) return s;
   if ((s = check_scale(scale)) != FA_OK) return s;
   if (n_split <= 0) n_split = decode_splits(B, Hkv, page_size, max_pages);
+  if (n_split > 64) n_split = 64;
   const long long n_tiles = (static_cast<long long>(max_pages) * page_size + 127) / 128;
   if (n_split > n_tiles) n_split = static_cast<int>(n_tiles);
   const int tiles_per_split = static_cast<int>((n_tiles + n_split - 1) / n_split);
   n_split = static_cast<int>((n_tiles + tiles_per_split - 1) / tiles_per_split);  // no empty trailing split
-  if (n_split > 65535) return FA_ERR_UNSUPPORTED;
   const DecWs w = decode_ws(B, H, Mq, d, n_split);
   if (!workspace) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;

@@ -87,10 +87,10 @@ BwdParams bwd_params(const BwdArgs& a) {
   return p;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool GRP>
 cudaError_t launch_pipe_t(const BwdArgs& a) {
   using C = BwdPipeCfg<D>;
-  auto kern = fa_bwd_pipe_kernel<D, BF16, CAUSAL>;
+  auto kern = fa_bwd_pipe_kernel<D, BF16, CAUSAL, GRP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   static int checked = 0;  // 1: the compiled register count matches the kernel's register split
@@ -118,6 +118,16 @@ cudaError_t launch_d256_t(const BwdArgs& a) {
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
 }
+template <int D>
+cudaError_t launch_pipe_d(const BwdArgs& a) {
+  const bool grp = a.Hkv != a.H || a.kv_len != nullptr;  // the general form only where it is needed
+  if (a.bf16) {
+    if (a.causal) return grp ? launch_pipe_t<D, true, true, true>(a) : launch_pipe_t<D, true, true, false>(a);
+    return grp ? launch_pipe_t<D, true, false, true>(a) : launch_pipe_t<D, true, false, false>(a);
+  }
+  if (a.causal) return grp ? launch_pipe_t<D, false, true, true>(a) : launch_pipe_t<D, false, true, false>(a);
+  return grp ? launch_pipe_t<D, false, false, true>(a) : launch_pipe_t<D, false, false, false>(a);
+}
 }  // namespace
 
 cudaError_t launch_bwd_main(const BwdArgs& a) {
@@ -125,14 +135,8 @@ cudaError_t launch_bwd_main(const BwdArgs& a) {
     if (a.bf16) return a.causal ? launch_d256_t<true, true>(a) : launch_d256_t<true, false>(a);
     return a.causal ? launch_d256_t<false, true>(a) : launch_d256_t<false, false>(a);
   }
-  if (a.d == 128) {  // software-pipelined, persistent kernel
-    if (a.bf16) return a.causal ? launch_pipe_t<128, true, true>(a) : launch_pipe_t<128, true, false>(a);
-    return a.causal ? launch_pipe_t<128, false, true>(a) : launch_pipe_t<128, false, false>(a);
-  }
-  if (a.d == 64) {  // the same kernel, K^T zero-padded to 128 rows for dQ^T
-    if (a.bf16) return a.causal ? launch_pipe_t<64, true, true>(a) : launch_pipe_t<64, true, false>(a);
-    return a.causal ? launch_pipe_t<64, false, true>(a) : launch_pipe_t<64, false, false>(a);
-  }
+  if (a.d == 128) return launch_pipe_d<128>(a);  // software-pipelined, persistent kernel
+  if (a.d == 64) return launch_pipe_d<64>(a);    // the same kernel, K^T zero-padded to 128 rows for dQ^T
   return cudaErrorNotSupported;
 }
 

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
   const int N = p.N;
   const int bh = blockIdx.x;  // K/V head (b, h_kv)
   const int key0 = blockIdx.y * 128;
-  const BwdGroup grp(bh, p);  // the query heads that share this K/V head, and the batch's key count
+  const BwdGroup<true> grp(bh, p);  // the query heads that share this K/V head, and the batch's key count
   const int it0 = CAUSAL ? (key0 / BQ) : 0;
   const int n_ith = (N + BQ - 1) / BQ - it0;  // query steps per query head (the last may run past N: masked)
   const int n_it = grp.G * n_ith;             // query steps per pass, head by head

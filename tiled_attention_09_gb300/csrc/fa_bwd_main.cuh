@@ -47,21 +47,35 @@ __device__ __forceinline__ int bwd_key_count(const BwdParams& p, int b) {
 
 // A key block of K/V head x (of the B*Hkv) feeds G = H / Hkv query heads; its query steps run
 // head by head: step `it` is 64-query step it0 + it % n_ith of query head qh0 + it / n_ith.
+// GRP = false is plain multi-head attention without a key-padding mask (G = 1, every key exists),
+// with all of that known at compile time.
+template <bool GRP>
 struct BwdGroup {
   int qh0;   // first query head (of the B*H) of the group
   int G;     // query heads per K/V head
   int klen;  // keys that exist for this batch (key padding and N)
   __device__ __forceinline__ BwdGroup(int x, const BwdParams& p) {
-    G = p.H / p.Hkv;
-    const int b = x / p.Hkv;
-    qh0 = b * p.H + (x - b * p.Hkv) * G;
-    klen = bwd_key_count(p, b);
+    if constexpr (GRP) {
+      G = p.H / p.Hkv;
+      const int b = x / p.Hkv;
+      qh0 = b * p.H + (x - b * p.Hkv) * G;
+      klen = bwd_key_count(p, b);
+    } else {
+      G = 1;
+      qh0 = x;
+      klen = p.N;
+    }
   }
   // query head and 64-query step (within the head) of step `it`
   __device__ __forceinline__ void step(int it, int it0, int n_ith, int& qh, int& qs) const {
-    const int gi = G == 1 ? 0 : it / n_ith;
-    qh = qh0 + gi;
-    qs = it0 + it - gi * n_ith;
+    if constexpr (!GRP) {
+      qh = qh0;
+      qs = it0 + it;
+    } else {
+      const int gi = G == 1 ? 0 : it / n_ith;
+      qh = qh0 + gi;
+      qs = it0 + it - gi * n_ith;
+    }
   }
 };
 

@@ -75,7 +75,7 @@ struct BwdPipeCfg {
 // One work item: the 128-key block y of K/V head x (blockIdx of the CTA launched for it; under
 // causal masking block 0 has the most query steps, so the launch order is longest-first). The
 // block's query steps run over the G query heads that share the K/V head, one head after another.
-template <bool CAUSAL>
+template <bool CAUSAL, bool GRP>
 struct BwdItem {
   int bh;        // K/V head (b, h_kv): the z coordinate of the K, V maps
   int row_base;  // row of (b, h_kv, 0) in the [B*Hkv*N, d] view of K, V, dK, dV
@@ -83,7 +83,7 @@ struct BwdItem {
   int it0;       // first 64-query step of each query head (causal: the block's diagonal)
   int n_ith;     // query steps per query head (the last may run past N: its extra queries are masked)
   int n_it;      // query steps of the block: G * n_ith
-  BwdGroup grp;  // the query heads of the group and the batch's key count
+  BwdGroup<GRP> grp;  // the query heads of the group and the batch's key count
   __device__ __forceinline__ BwdItem(int x, int y, const BwdParams& p) : grp(x, p) {
     bh = x;
     row_base = x * p.N;
@@ -94,10 +94,11 @@ struct BwdItem {
   }
 };
 
-template <int D_, bool BF16, bool CAUSAL>
+// GRP: grouped K/V heads or a key-padding mask (the general form); false for plain multi-head attention
+template <int D_, bool BF16, bool CAUSAL, bool GRP>
 __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdPipeCfg<D_>;
-  using Item = BwdItem<CAUSAL>;
+  using Item = BwdItem<CAUSAL, GRP>;
   constexpr int BQ = C::BQ, D = C::D, NS = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -46,6 +46,9 @@ struct DecParams {
   const int* ctx_len;      // [B]
   float* o_part;           // [n_split][B*H*Mq][d] fp32, each split's part normalised by its own sum
   float* lse_part;         // [n_split][B*H*Mq]
+  void* o_final;           // with one split: O [B*H*Mq][d] dtype and LSE written here directly
+  float* lse_final;
+  int direct;              // one split: no partials, no merge
   int H, G, Mq, R;         // query heads, query heads per K/V head, queries per head, rows per CTA
   int ps_log2;             // log2(page size)
   int max_pages, n_pages;  // page-table row length, pages in the cache
@@ -166,41 +169,49 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
   const int n = w.n;
 
   if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (elect_one()) {
+    // ------------------------------------------------------------ producer (the whole warp)
+    // A 128-key tile is 128 / min(page_size, 128) page boxes per 64-column chunk; lane l issues box
+    // l / NCH, chunk l % NCH, after looking up its own page, so small pages cost one round of loads.
+    const int lane = threadIdx.x & 31;
+    const int ps = 1 << p.ps_log2;
+    const int br = ps < 128 ? ps : 128;           // rows per TMA box
+    const int nbox = (128 / br) * C::NCH;         // boxes per tile (at most 16)
+    const int oob_row = p.n_pages << p.ps_log2;   // the first row past the cache: the box reads zeros
+    const int* ptab = p.page_table + static_cast<size_t>(w.b) * p.max_pages;
+    const int r0 = (lane / C::NCH) * br, cc = lane % C::NCH;  // this lane's box: first row, chunk
+    if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       mbar_arrive_expect_tx(b_q, C::TILE);
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ + c * C::CHUNK, &p.tm_q, b_q, c * 64, q_row0);
-      const int ps = 1 << p.ps_log2;
-      const int br = ps < 128 ? ps : 128;           // rows per TMA box
-      const int oob_row = p.n_pages << p.ps_log2;   // the first row past the cache: the box reads zeros
-      const int* ptab = p.page_table + static_cast<size_t>(w.b) * p.max_pages;
-      // tile j of the split into ring slot j % NSR, page by page
-      auto load = [&](uint32_t ring, uint32_t full, uint32_t empty, const CUtensorMap* map, int j) -> bool {
-        const int slot = j % NSR, use = j / NSR;
-        if (use > 0 && !wait_bar(empty + 8 * slot, (use - 1) & 1, p.timeout_ns, abort_flag, WD_EMPTY)) return false;
-        mbar_arrive_expect_tx(full + 8 * slot, C::TILE);
-        const int kt = w.lo + j;
-        for (int r0 = 0; r0 < 128; r0 += br) {
-          const int key = kt * 128 + r0;
-          int y = oob_row;
-          if (key < w.ctx) {  // pages wholly past the sequence are not read
-            const int pid = __ldg(ptab + (key >> p.ps_log2));
-            if (pid >= 0 && pid < p.n_pages) y = (pid << p.ps_log2) + (key & (ps - 1));
-          }
-#pragma unroll
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(ring + slot * C::TILE + c * C::CHUNK + r0 * 128, map, full + 8 * slot, c * 64, y, w.hk);
+    }
+    // tile j of the split into ring slot j % NSR
+    auto load = [&](uint32_t ring, uint32_t full, uint32_t empty, const CUtensorMap* map, int j) -> bool {
+      const int slot = j % NSR, use = j / NSR;
+      bool ok = true;
+      if (lane == 0) {
+        if (use > 0) ok = wait_bar(empty + 8 * slot, (use - 1) & 1, p.timeout_ns, abort_flag, WD_EMPTY);
+        if (ok) mbar_arrive_expect_tx(full + 8 * slot, C::TILE);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      if (lane < nbox) {
+        const int key = (w.lo + j) * 128 + r0;
+        int y = oob_row;
+        if (key < w.ctx) {  // pages wholly past the sequence are not read
+          const int pid = __ldg(ptab + (key >> p.ps_log2));
+          if (pid >= 0 && pid < p.n_pages) y = (pid << p.ps_log2) + (key & (ps - 1));
         }
-        return true;
-      };
-      int j = 0;
-      for (; j < n; ++j)
-        if (!load(sK, b_kfull(0), b_kempty(0), &p.tm_k, j) || !load(sV, b_vfull(0), b_vempty(0), &p.tm_v, j)) break;
-      // Drain: every issued copy has landed before the CTA may exit.
+        tma_load_3d(ring + slot * C::TILE + cc * C::CHUNK + r0 * 128, map, full + 8 * slot, cc * 64, y, w.hk);
+      }
+      return true;
+    };
+    int j = 0;
+    for (; j < n; ++j)
+      if (!load(sK, b_kfull(0), b_kempty(0), &p.tm_k, j) || !load(sV, b_vfull(0), b_vempty(0), &p.tm_v, j)) break;
+    // Drain: every issued copy has landed before the CTA may exit.
+    if (lane == 0) {
       for (int i = (j > NSR ? j - NSR : 0); i < j; ++i) {
         wait_bar(b_kfull(i % NSR), (i / NSR) & 1, p.timeout_ns, abort_flag, WD_DRAIN);
         wait_bar(b_vfull(i % NSR), (i / NSR) & 1, p.timeout_ns, abort_flag, WD_DRAIN);
@@ -378,7 +389,42 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
       mbar_arrive(b_pfull(b));
     }
     // ---------------------------------------------------------- epilogue: the split's partial result
+    // (with a single split, the final O in the dtype and LSE)
     const bool row_ok = r < p.R;
+    if (p.direct) {
+      const size_t grow = static_cast<size_t>(q_row0) + r;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o_final) + grow * D);
+      bool have = false;
+      if (ok && n > 0) {
+        ok = __all_sync(0xffffffffu, wait_bar(b_odone, 0, p.timeout_ns, abort_flag, WD_O));
+        have = ok;
+      }
+      if (have) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t u[64];
+          tmem_ld64(tO + c0, u);
+          if (row_ok) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const float* x = reinterpret_cast<const float*>(u + 8 * g);
+              dst[(c0 >> 3) + g] = make_uint4(dpack2<BF16>(x[0] * inv_l, x[1] * inv_l), dpack2<BF16>(x[2] * inv_l, x[3] * inv_l),
+                                              dpack2<BF16>(x[4] * inv_l, x[5] * inv_l), dpack2<BF16>(x[6] * inv_l, x[7] * inv_l));
+            }
+          }
+        }
+        if (row_ok) p.lse_final[grow] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      } else if (ok && row_ok) {  // no key at all: O = 0, LSE = -inf
+#pragma unroll 4
+        for (int g = 0; g < D / 8; ++g) dst[g] = make_uint4(0u, 0u, 0u, 0u);
+        p.lse_final[grow] = -INFINITY;
+      }
+      tc_fence_before();
+      __syncthreads();
+      return;
+    }
     const size_t grow = static_cast<size_t>(blockIdx.y) * p.rows_total + q_row0 + r;
     float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D);
     if (ok && n > 0) {
@@ -414,41 +460,57 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
 }
 
 // LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s, rounded to the dtype; a row whose parts
-// are all empty gets O = 0 and LSE = -inf. VPR threads per row, 8 columns each. The loops over the
-// parts are unrolled so that their loads are in flight together (an empty part weighs exp(-inf) = 0).
+// are all empty gets O = 0 and LSE = -inf. One block per row: thread (s, cv) loads part s's 8 columns
+// cv*8 .. cv*8+7 (all parts' loads in flight at once), then the weighted values are summed over the
+// parts in shared memory. blockDim = VPR * NPP, NPP a power of two >= n_part.
 template <int VPR, bool BF16>
-__global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float4* __restrict__ o_part,
-                                                              const float* __restrict__ lse_part, uint4* __restrict__ o,
-                                                              float* __restrict__ lse, int rows, int n_part) {
-  const size_t n_vec = static_cast<size_t>(rows) * VPR;
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
-    const size_t row = i / VPR;
-    const int cv = static_cast<int>(i % VPR);
-    float m = -INFINITY;
-#pragma unroll 8
-    for (int s = 0; s < n_part; ++s) m = fmaxf(m, __ldg(lse_part + static_cast<size_t>(s) * rows + row));
-    const float m0 = m == -INFINITY ? 0.f : m;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float wsum = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < n_part; ++s) {
-      const float wgt = __expf(__ldg(lse_part + static_cast<size_t>(s) * rows + row) - m0);
-      const float4* src = o_part + (static_cast<size_t>(s) * rows + row) * (VPR * 2) + 2 * cv;
-      const float4 a = __ldg(src), b = __ldg(src + 1);
-      wsum += wgt;
-      acc[0] = fmaf(wgt, a.x, acc[0]);
-      acc[1] = fmaf(wgt, a.y, acc[1]);
-      acc[2] = fmaf(wgt, a.z, acc[2]);
-      acc[3] = fmaf(wgt, a.w, acc[3]);
-      acc[4] = fmaf(wgt, b.x, acc[4]);
-      acc[5] = fmaf(wgt, b.y, acc[5]);
-      acc[6] = fmaf(wgt, b.z, acc[6]);
-      acc[7] = fmaf(wgt, b.w, acc[7]);
+__global__ void __launch_bounds__(1024) fa_decode_merge_kernel(const float4* __restrict__ o_part,
+                                                               const float* __restrict__ lse_part,
+                                                               uint4* __restrict__ o, float* __restrict__ lse, int rows,
+                                                               int n_part) {
+  extern __shared__ float sm[];
+  const int npp = blockDim.x / VPR;
+  float* s_lse = sm;        // [npp]
+  float* s_val = sm + npp;  // [npp][VPR][9]: 8 weighted values and the weight
+  const size_t row = blockIdx.x;
+  const int s = threadIdx.x / VPR, cv = threadIdx.x % VPR;
+  float ls = -INFINITY;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (s < n_part) {
+    ls = __ldg(lse_part + static_cast<size_t>(s) * rows + row);
+    const float4* src = o_part + (static_cast<size_t>(s) * rows + row) * (VPR * 2) + 2 * cv;
+    a = __ldg(src);
+    b = __ldg(src + 1);
+  }
+  if (cv == 0) s_lse[s] = ls;
+  __syncthreads();
+  float m = -INFINITY;
+  for (int t = 0; t < n_part; ++t) m = fmaxf(m, s_lse[t]);
+  const float wgt = __expf(ls - (m == -INFINITY ? 0.f : m));  // 0 for an empty part (or no part)
+  float* v = s_val + (s * VPR + cv) * 9;
+  v[0] = wgt * a.x;
+  v[1] = wgt * a.y;
+  v[2] = wgt * a.z;
+  v[3] = wgt * a.w;
+  v[4] = wgt * b.x;
+  v[5] = wgt * b.y;
+  v[6] = wgt * b.z;
+  v[7] = wgt * b.w;
+  v[8] = wgt;
+  __syncthreads();
+  for (int half = npp / 2; half > 0; half >>= 1) {
+    if (s < half) {
+      const float* u = s_val + ((s + half) * VPR + cv) * 9;
+#pragma unroll
+      for (int k = 0; k < 9; ++k) v[k] += u[k];
     }
+    __syncthreads();
+  }
+  if (s == 0) {
+    const float wsum = v[8];
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    o[i] = make_uint4(dpack2<BF16>(acc[0] * inv, acc[1] * inv), dpack2<BF16>(acc[2] * inv, acc[3] * inv),
-                      dpack2<BF16>(acc[4] * inv, acc[5] * inv), dpack2<BF16>(acc[6] * inv, acc[7] * inv));
+    o[row * VPR + cv] = make_uint4(dpack2<BF16>(v[0] * inv, v[1] * inv), dpack2<BF16>(v[2] * inv, v[3] * inv),
+                                   dpack2<BF16>(v[4] * inv, v[5] * inv), dpack2<BF16>(v[6] * inv, v[7] * inv));
     if (cv == 0) lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
   }
 }
@@ -457,8 +519,15 @@ template <int D, bool BF16>
 cudaError_t launch_decode_t(const DecArgs& a) {
   using C = DecCfg<D>;
   auto kern = fa_decode_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  static int attr_set = -1;  // the device whose function attribute was set (decode steps are host-latency bound)
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (attr_set != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = dev;
+  }
   DecParams p;
   p.tm_q = a.tm_q;
   p.tm_k = a.tm_k;
@@ -467,6 +536,9 @@ cudaError_t launch_decode_t(const DecArgs& a) {
   p.ctx_len = a.ctx_len;
   p.o_part = a.ws_o;
   p.lse_part = a.ws_lse;
+  p.o_final = a.o;
+  p.lse_final = a.lse;
+  p.direct = a.n_split == 1 ? 1 : 0;
   p.H = a.H;
   p.G = a.H / a.Hkv;
   p.Mq = a.Mq;
@@ -482,11 +554,13 @@ cudaError_t launch_decode_t(const DecArgs& a) {
   p.timeout_ns = a.timeout_ns;
   e = launch_kernel(kern, dim3(a.B * a.Hkv, a.n_split, 1), dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess) return e;
-  const size_t n_vec = static_cast<size_t>(p.rows_total) * (D / 8);
-  size_t blocks = (n_vec + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  return launch_kernel(fa_decode_merge_kernel<D / 8, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
-                       a.stream, reinterpret_cast<const float4*>(a.ws_o), static_cast<const float*>(a.ws_lse),
+  if (p.direct) return cudaSuccess;
+  int npp = 1;
+  while (npp < a.n_split) npp <<= 1;
+  const int threads = npp * (D / 8);  // n_split <= 64 (host check): at most 1024 threads
+  const size_t smem = static_cast<size_t>(npp) * (1 + (D / 8) * 9) * sizeof(float);
+  return launch_kernel(fa_decode_merge_kernel<D / 8, BF16>, dim3(static_cast<unsigned>(p.rows_total)), dim3(threads),
+                       smem, a.stream, reinterpret_cast<const float4*>(a.ws_o), static_cast<const float*>(a.ws_lse),
                        static_cast<uint4*>(a.o), a.lse, p.rows_total, a.n_split);
 }
 
