@@ -381,32 +381,65 @@ def run_native(args):
     K = args.steps
     value = world * step_flops * K / total / 1e12
 
-    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region.
+    # Every step copies its own Q, K, V, dO in and its O, LSE, dQ, dK, dV out; the copies of neighbouring
+    # steps overlap the current step's kernels (an input stream, the compute stream, an output stream, two
+    # sets of device buffers), as a serving or training loop would run them.
     hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
-    ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
-    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv, hlse))
+    dsets, hsets = [], []
+    for b in range(2):
+        ins = [torch.empty_like(t) for t in (qd, kd, vd, dod)]
+        outs = [torch.empty_like(qd), torch.empty((B, H, N), device=dev, dtype=torch.float32), torch.empty_like(qd),
+                torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)]  # o, lse, o_lo, dq, dk, dv
+        dsets.append((ins, outs))
+        hsets.append([torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (outs[0], outs[1], outs[3], outs[4],
+                                                                                outs[5])])
+    d2h = sum(t.numel() * t.element_size() for t in hsets[0])
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    started = [False, False]
 
-    def e2e_step():
-        for src, dst in ((hq, qd), (hk, kd), (hv, vd), (hdo, dod)):
-            dst.copy_(src, non_blocking=True)
-        o_, lse_, lo_ = fa.fwd(qd, kd, vd, causal=True, out=o, lse=lse, residual=True, o_lo=o_lo)
-        fa.bwd(qd, kd, vd, o_, lse_, dod, causal=True, workspace=ws, dq=dq, dk=dk, dv=dv, o_lo=lo_)
-        for src, dst in ((o, ho), (dq, hdq), (dk, hdk), (dv, hdv), (lse, hlse)):
-            dst.copy_(src, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        (qi, ki, vi, doi), (o_, lse_, lo_, dq_, dk_, dv_) = dsets[b]
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(comp_done[b])  # step i - 2 has finished reading this input set
+            for src, dst in ((hq, qi), (hk, ki), (hv, vi), (hdo, doi)):
+                dst.copy_(src, non_blocking=True)
+            in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        if started[b]:
+            stream.wait_event(out_done[b])  # step i - 2's outputs have been read back
+        fa.fwd(qi, ki, vi, causal=True, out=o_, lse=lse_, residual=True, o_lo=lo_)
+        fa.bwd(qi, ki, vi, o_, lse_, doi, causal=True, workspace=ws, dq=dq_, dk=dk_, dv=dv_, o_lo=lo_)
+        comp_done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            for src, dst in zip((o_, lse_, dq_, dk_, dv_), hsets[b]):
+                dst.copy_(src, non_blocking=True)
+            out_done[b].record(s_out)
+        started[b] = True
 
-    for _ in range(max(3, args.warmup // 2)):
-        e2e_step()
+    for i in range(max(3, args.warmup // 2)):
+        e2e_step(i)
     torch.cuda.synchronize()
+    started[0] = started[1] = False
     e2e_steps = max(3, min(K, 50))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     ev0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    s_in.wait_event(ev0)
+    s_out.wait_event(ev0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
     ev1.record(stream)
     torch.cuda.synchronize()
     t_e2e = ev0.elapsed_time(ev1) / 1e3
