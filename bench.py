@@ -558,6 +558,7 @@ DECODE_POINTS = [  # (B, H, Hkv, Mq, d, page_size, ctx)
     (64, 8, 1, 4, 128, 16, 4096),
     (32, 16, 2, 1, 64, 128, 8192),
     (8, 64, 8, 2, 128, 256, 16384),
+    (8, 32, 8, 1, 256, 64, 8192),
 ]
 
 
@@ -582,7 +583,7 @@ def run_decode(args):
         w = DecodeWorkload(B, H, Hkv, Mq, d, ps, ctx // ps, (ctx,) * B, spare=0, poison=False)
         q, kp, vp, table, cl = (t.to(dev) for t in make_paged_inputs(w))
         o, lse = fa.decode(q, kp, vp, table, cl)
-        n_split = fa.decode_splits(B, Hkv, ps, w.max_pages)
+        n_split = fa.decode_splits(B, Hkv, d, ps, w.max_pages)
         L = _lib.load()
         ws = torch.empty(int(L.fa_decode_workspace_size(B, H, Hkv, Mq, d, ps, w.max_pages, 0)), dtype=torch.uint8,
                          device=dev)

@@ -226,16 +226,16 @@ fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_by
  *            key gets O = 0 and LSE = -inf).
  *   Query head h reads K/V head h / (H / Hkv). causal != 0: query i sees keys
  *   j <= ctx_len[b] - Mq + i; otherwise all ctx_len[b] keys.
- * Shapes: d in {64, 128}; page_size a power of two in [16, 256]; H a multiple
- * of Hkv with (H / Hkv) * Mq <= 128; else FA_ERR_UNSUPPORTED.
- * n_split <= 0 lets the library choose (fa_decode_splits); at most 64 (larger
- * values are capped), and with one split the kernel writes o and lse itself
- * (no merge launch). workspace: device
+ * Shapes: d in {64, 128, 256}; page_size a power of two in [16, 256]; H a
+ * multiple of Hkv with (H / Hkv) * Mq <= 128; else FA_ERR_UNSUPPORTED.
+ * n_split <= 0 lets the library choose (fa_decode_splits); at most 64 (32 for
+ * d = 256; larger values are capped), and with one split the kernel writes o
+ * and lse itself (no merge launch). workspace: device
  * memory of fa_decode_workspace_size(...) bytes for the same n_split,
  * 256-byte aligned. page_table and ctx_len must be 4-byte aligned, the rest
  * 16-byte aligned. One or two launches on `stream`.
  */
-int fa_decode_splits(int B, int Hkv, int page_size, int max_pages);
+int fa_decode_splits(int B, int Hkv, int d, int page_size, int max_pages);
 size_t fa_decode_workspace_size(int B, int H, int Hkv, int Mq, int d, int page_size, int max_pages, int n_split);
 fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, const int* page_table, const int* ctx_len,
                     void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Mq, int d,

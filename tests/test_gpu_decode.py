@@ -30,6 +30,11 @@ CASES = [
     # long key streams in one split (tens of tiles per stream, each ring reused many times)
     (DecodeWorkload(2, 8, 2, 1, 128, 64, 128, (8192, 8000)), 1),
     (DecodeWorkload(2, 16, 2, 2, 64, 128, 64, (8192, 7777), causal=True), 1),
+    # d = 256: 64-key tiles
+    (DecodeWorkload(2, 8, 2, 1, 256, 64, 20, (1000, 77)), 0),
+    (DecodeWorkload(3, 4, 1, 4, 256, 16, 40, (640, 3, 0), dtype="fp16", causal=True), 0),
+    (DecodeWorkload(1, 16, 4, 2, 256, 256, 12, (3000,)), 1),
+    (DecodeWorkload(1, 16, 4, 2, 256, 256, 12, (3000,), causal=True), 40),
 ]
 
 
@@ -49,6 +54,22 @@ def test_decode_matches_oracle(case):
     assert np.isneginf(l_gpu[empty]).all() and (to64(o)[empty] == 0).all()
     if (~empty).any():
         check_lse(l_gpu[~empty], lse_ref[~empty])
+
+
+def test_decode_never_reads_page_table_entries_past_the_sequence():
+    """Page-table entries for pages wholly past ctx_len are never read: garbage there changes nothing."""
+    w = DecodeWorkload(3, 8, 2, 2, 128, 32, 16, (100, 33, 512), causal=True)
+    q, kp, vp, table, ctx = make_paged_inputs(w)
+    bad = table.clone()
+    for b in range(w.B):
+        used = (int(ctx[b]) + w.page_size - 1) // w.page_size
+        bad[b, used:] = torch.tensor([-7, 1 << 30, -1] * w.max_pages, dtype=torch.int32)[: w.max_pages - used]
+    args = [t.cuda() for t in (q, kp, vp)]
+    o1, l1 = fa.decode(*args, table.cuda(), ctx.cuda(), causal=True)
+    o2, l2 = fa.decode(*args, bad.cuda(), ctx.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert fa.device_status()[0] == "FA_OK"
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_decode_split_count_does_not_change_the_result_much():

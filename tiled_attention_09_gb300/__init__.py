@@ -197,9 +197,9 @@ def attention(q, k, v, causal=False, scale=None, kv_len=None):
     return _AttentionFn.apply(q, k, v, causal, scale, kv_len)
 
 
-def decode_splits(B, Hkv, page_size, max_pages) -> int:
+def decode_splits(B, Hkv, d, page_size, max_pages) -> int:
     """Number of key splits fa_decode picks by itself for this shape."""
-    return int(_lib.load().fa_decode_splits(B, Hkv, page_size, max_pages))
+    return int(_lib.load().fa_decode_splits(B, Hkv, d, page_size, max_pages))
 
 
 def decode(q, k_pages, v_pages, page_table, ctx_len, causal=False, scale=None, n_split=0, out=None, lse=None,

@@ -49,7 +49,7 @@ SIGNATURES = [
                                              c_void_p]),
     ("fa_bwd_dq_convert", c_int, [c_void_p, c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int,
                                   c_void_p]),
-    ("fa_decode_splits", c_int, [c_int, c_int, c_int, c_int]),
+    ("fa_decode_splits", c_int, [c_int] * 5),
     ("fa_decode_workspace_size", c_size_t, [c_int] * 8),
     ("fa_decode", c_int, [c_void_p] * 7 + [c_void_p, c_size_t] + [c_int] * 9 + [c_float, c_int, c_int, c_void_p]),
     ("fa_device_status", c_int, [c_void_p, ctypes.POINTER(c_uint)]),

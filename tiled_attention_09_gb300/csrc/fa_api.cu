@@ -65,13 +65,13 @@ bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int d, bool b
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Paged decode shapes: d in {64, 128}; page size a power of two in [16, 256]; the G = H / Hkv heads'
-// Mq queries (G * Mq rows) fit one 128-row tile; cache rows and query rows in 32-bit ints.
+// Paged decode shapes: d in {64, 128, 256}; page size a power of two in [16, 256]; the G = H / Hkv
+// heads' Mq queries (G * Mq rows) fit one 128-row tile; cache rows and query rows in 32-bit ints.
 fa_status check_decode_shape(int B, int H, int Hkv, int Mq, int d, int page_size, int n_pages, int max_pages,
                              fa_dtype dtype) {
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Hkv < 1 || Mq < 1 || n_pages < 1 || max_pages < 1) return FA_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (H % Hkv != 0 || (H / Hkv) * Mq > 128) return FA_ERR_UNSUPPORTED;
   if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(n_pages) * page_size >= (1ll << 31) ||
@@ -87,14 +87,20 @@ int log2_exact(int x) {
   return l;
 }
 
+// Keys per decode tile (the kernel's BK) and the most splits the merge takes (its block is
+// splits x d / 8 threads, at most 1024).
+int decode_tile_keys(int d) { return d == 256 ? 64 : 128; }
+int decode_max_splits(int d) { return d == 256 ? 32 : 64; }
+
 // Splits of the key range: with C = B * Hkv CTAs per split and 152 SMs, pick the count s that
 // minimises waves(C * s) * (tiles per split + 3), the 3 standing for a CTA's fixed cost in tiles.
-int decode_splits(int B, int Hkv, int page_size, int max_pages) {
-  const long long n_tiles = (static_cast<long long>(max_pages) * page_size + 127) / 128;
+int decode_splits(int B, int Hkv, int d, int page_size, int max_pages) {
+  const int bk = decode_tile_keys(d);
+  const long long n_tiles = (static_cast<long long>(max_pages) * page_size + bk - 1) / bk;
   const long long ctas = static_cast<long long>(B) * Hkv;
   int best = 1;
   long long best_cost = -1;
-  for (int s = 1; s <= 64 && s <= n_tiles; ++s) {
+  for (int s = 1; s <= decode_max_splits(d) && s <= n_tiles; ++s) {
     const long long waves = (ctas * s + 151) / 152;
     const long long cost = waves * ((n_tiles + s - 1) / s + 3);
     if (best_cost < 0 || cost < best_cost) {
@@ -380,15 +386,15 @@ fa_status fa_bwd_opt(const void* q, const void* k, const void* v, const void* o,
                        stream);
 }
 
-int fa_decode_splits(int B, int Hkv, int page_size, int max_pages) {
-  if (B < 1 || Hkv < 1 || page_size < 1 || max_pages < 1) return 0;
-  return decode_splits(B, Hkv, page_size, max_pages);
+int fa_decode_splits(int B, int Hkv, int d, int page_size, int max_pages) {
+  if (B < 1 || Hkv < 1 || page_size < 1 || max_pages < 1 || (d != 64 && d != 128 && d != 256)) return 0;
+  return decode_splits(B, Hkv, d, page_size, max_pages);
 }
 
 size_t fa_decode_workspace_size(int B, int H, int Hkv, int Mq, int d, int page_size, int max_pages, int n_split) {
   if (check_decode_shape(B, H, Hkv, Mq, d, page_size, 1, max_pages, FA_BF16) != FA_OK) return 0;
-  if (n_split <= 0) n_split = decode_splits(B, Hkv, page_size, max_pages);
-  if (n_split > 64) n_split = 64;
+  if (n_split <= 0) n_split = decode_splits(B, Hkv, d, page_size, max_pages);
+  if (n_split > decode_max_splits(d)) n_split = decode_max_splits(d);
   return decode_ws(B, H, Mq, d, n_split).total;
 }
 
@@ -400,9 +406,10 @@ fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, con
   fa_status s = check_decode_shape(B, H, Hkv, Mq, d, page_size, n_pages, max_pages, dtype);
   if (s != FA_OK) return s;
   if ((s = check_scale(scale)) != FA_OK) return s;
-  if (n_split <= 0) n_split = decode_splits(B, Hkv, page_size, max_pages);
-  if (n_split > 64) n_split = 64;
-  const long long n_tiles = (static_cast<long long>(max_pages) * page_size + 127) / 128;
+  if (n_split <= 0) n_split = decode_splits(B, Hkv, d, page_size, max_pages);
+  if (n_split > decode_max_splits(d)) n_split = decode_max_splits(d);
+  const int bk = decode_tile_keys(d);
+  const long long n_tiles = (static_cast<long long>(max_pages) * page_size + bk - 1) / bk;
   if (n_split > n_tiles) n_split = static_cast<int>(n_tiles);
   const int tiles_per_split = static_cast<int>((n_tiles + n_split - 1) / n_split);
   n_split = static_cast<int>((n_tiles + tiles_per_split - 1) / tiles_per_split);  // no empty trailing split
@@ -416,7 +423,7 @@ fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, con
   if ((s = check_device()) != FA_OK) return s;
   fa::DecArgs a;
   const bool bf16 = dtype == FA_BF16;
-  const int br = page_size < 128 ? page_size : 128;
+  const int br = page_size < bk ? page_size : bk;
   if (!make_map_2d(&a.tm_q, q, static_cast<long long>(B) * H * Mq, d, bf16, 128) ||
       !make_map(&a.tm_k, k_pages, Hkv, n_pages * page_size, d, bf16, br) ||
       !make_map(&a.tm_v, v_pages, Hkv, n_pages * page_size, d, bf16, br))

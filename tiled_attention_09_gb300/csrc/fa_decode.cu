@@ -28,7 +28,9 @@
 // stale page tail may hold non-finite values, and 0 * NaN is NaN in the product).
 // Roles (224 threads): warps 0-3 softmax (only the warps holding rows < R work), warp 4 TMA
 // producer, warp 5 the S issuer (and TMEM owner), warp 6 the P V issuer.
-// TMEM: S buffers at 0 and 128 (fp32 128 x 128; P as 16-bit pairs over them), O at 256.
+// Tiles hold BK = 128 keys (64 for d = 256, whose 64 KB Q tile leaves room for two 32 KB slots per
+// ring only at that height).
+// TMEM: S buffers at 0 and 128 (fp32 128 x BK; P as 16-bit pairs over them), O at 256 (d columns).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -62,20 +64,23 @@ struct DecParams {
 
 template <int D>
 struct DecCfg {
-  static constexpr int CHUNK = 128 * 128;  // 128 rows x 64 elements x 2 bytes
+  static constexpr int BK = D == 256 ? 64 : 128;   // keys per tile (d = 256: 64, so that two slots per ring fit)
+  static constexpr int QCHUNK = 128 * 128;         // Q: 128 rows x 64 elements x 2 bytes
+  static constexpr int CHUNK = BK * 128;           // K or V: BK rows x 64 elements x 2 bytes
   static constexpr int NCH = D / 64;
-  static constexpr int TILE = 128 * D * 2;
+  static constexpr int QTILE = 128 * D * 2;
+  static constexpr int TILE = BK * D * 2;          // one K or one V tile
   // ring slots (one K or one V tile each) filling the rest of the 227 KB, half for K, half for V
-  static constexpr int NS_FIT = (227 * 1024 - 1024 - TILE - 512) / TILE;
+  static constexpr int NS_FIT = (227 * 1024 - 1024 - QTILE - 512) / TILE;
   static constexpr int NSR = (NS_FIT > 12 ? 12 : NS_FIT) / 2;  // slots per ring
   // q, kfull[NSR], kempty[NSR], vfull[NSR], vempty[NSR], sfull[2], pfull[2], pvdone[2], odone, drain[2]
   static constexpr int NBAR = 1 + 4 * NSR + 6 + 1 + 2;
   static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
-  static constexpr int SMEM_BYTES = 1024 + TILE + 2 * NSR * TILE + BAR_BYTES + 16;
+  static constexpr int SMEM_BYTES = 1024 + QTILE + 2 * NSR * TILE + BAR_BYTES + 16;
   static constexpr int THREADS = 224;
   static_assert(NSR >= 2, "a ring must hold the tile in use and the next one");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
-  static_assert(256 + D <= 512, "TMEM budget");
+  static_assert(256 + D <= 512, "TMEM budget");  // S buffers at 0 and 128 (BK columns each), O at 256
 };
 
 template <bool BF16>
@@ -93,7 +98,8 @@ enum : uint32_t {
   WD_Q = 31, WD_EMPTY = 32, WD_FULL = 33, WD_P = 34, WD_S = 35, WD_O = 36, WD_V = 37, WD_DRAIN = 38, WD_PV = 39
 };
 
-// The CTA's split of one sequence: 128-key tiles [lo, lo + n) of the sequence's ceil(ctx / 128).
+// The CTA's split of one sequence: BK-key tiles [lo, lo + n) of the sequence's ceil(ctx / BK).
+template <int BK>
 struct DecWork {
   int b, hk, ctx, lo, n;
   __device__ __forceinline__ DecWork(const DecParams& p) {
@@ -103,7 +109,7 @@ struct DecWork {
     const int cap = p.max_pages << p.ps_log2;
     const int c = __ldg(p.ctx_len + b);
     ctx = c < 0 ? 0 : (c > cap ? cap : c);
-    const int n_tiles = (ctx + 127) / 128;
+    const int n_tiles = (ctx + BK - 1) / BK;
     lo = blockIdx.y * p.tiles_per_split;
     int hi = lo + p.tiles_per_split;
     hi = hi < n_tiles ? hi : n_tiles;
@@ -114,13 +120,13 @@ struct DecWork {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant__ DecParams p) {
   using C = DecCfg<D>;
-  constexpr int NSR = C::NSR;
+  constexpr int NSR = C::NSR, BK = C::BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK = sQ + C::TILE;              // K ring
+  const uint32_t sK = sQ + C::QTILE;             // K ring
   const uint32_t sV = sK + NSR * C::TILE;        // V ring
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE + 2 * NSR * C::TILE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::QTILE + 2 * NSR * C::TILE);
   const uint32_t b_q = smem_u32(&bars[0]);
   auto b_kfull = [&](int s) { return smem_u32(&bars[1 + s]); };
   auto b_kempty = [&](int s) { return smem_u32(&bars[1 + NSR + s]); };
@@ -131,11 +137,11 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
   auto b_pvdone = [&](int b) { return smem_u32(&bars[5 + 4 * NSR + b]); };
   const uint32_t b_odone = smem_u32(&bars[7 + 4 * NSR]);
   auto b_drain = [&](int i) { return smem_u32(&bars[8 + 4 * NSR + i]); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::TILE + 2 * NSR * C::TILE + C::BAR_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::QTILE + 2 * NSR * C::TILE + C::BAR_BYTES);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
-  const DecWork w(p);
+  const DecWork<BK> w(p);
   const int nact = (p.R + 31) / 32;  // softmax warps that hold rows < R
 
   if (threadIdx.x == 0) {
@@ -170,12 +176,12 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer (the whole warp)
-    // A 128-key tile is 128 / min(page_size, 128) page boxes per 64-column chunk; lane l issues box
+    // A BK-key tile is BK / min(page_size, BK) page boxes per 64-column chunk; lane l issues box
     // l / NCH, chunk l % NCH, after looking up its own page, so small pages cost one round of loads.
     const int lane = threadIdx.x & 31;
     const int ps = 1 << p.ps_log2;
-    const int br = ps < 128 ? ps : 128;           // rows per TMA box
-    const int nbox = (128 / br) * C::NCH;         // boxes per tile (at most 16)
+    const int br = ps < BK ? ps : BK;             // rows per TMA box
+    const int nbox = (BK / br) * C::NCH;          // boxes per tile (at most 16)
     const int oob_row = p.n_pages << p.ps_log2;   // the first row past the cache: the box reads zeros
     const int* ptab = p.page_table + static_cast<size_t>(w.b) * p.max_pages;
     const int r0 = (lane / C::NCH) * br, cc = lane % C::NCH;  // this lane's box: first row, chunk
@@ -183,9 +189,9 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(b_q, C::TILE);
+      mbar_arrive_expect_tx(b_q, C::QTILE);
 #pragma unroll
-      for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ + c * C::CHUNK, &p.tm_q, b_q, c * 64, q_row0);
+      for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ + c * C::QCHUNK, &p.tm_q, b_q, c * 64, q_row0);
     }
     // tile j of the split into ring slot j % NSR
     auto load = [&](uint32_t ring, uint32_t full, uint32_t empty, const CUtensorMap* map, int j) -> bool {
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       if (lane < nbox) {
-        const int key = (w.lo + j) * 128 + r0;
+        const int key = (w.lo + j) * BK + r0;
         int y = oob_row;
         if (key < w.ctx) {  // pages wholly past the sequence are not read
           const int pid = __ldg(ptab + (key >> p.ps_log2));
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
   } else if (warp == 5) {
     // ------------------------------------------------------------ S issuer: S(j) = Q K(j)^T into buffer j & 1
     if (elect_one()) {
-      constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
+      constexpr uint32_t idesc_s = make_idesc(128, BK, BF16, false, false);
       const uint64_t dq0 = make_sdesc(sQ, 16, 1024);  // Q, K-major
       const uint64_t dk0 = make_sdesc(sK, 16, 1024);  // K ring slot, K-major
       bool ok = wait_bar(b_q, 0, p.timeout_ns, abort_flag, WD_Q);
@@ -237,8 +243,9 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
         const uint64_t dk = dk0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {  // 16 head dims per MMA
-          const uint64_t off = static_cast<uint64_t>(((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4);
-          mma_ss(tmem + 128 * b, dq0 + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
+          const uint64_t qo = static_cast<uint64_t>(((k >> 2) * C::QCHUNK + (k & 3) * 32) >> 4);
+          const uint64_t ko = static_cast<uint64_t>(((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4);
+          mma_ss(tmem + 128 * b, dq0 + qo, dk + ko, idesc_s, k > 0 ? 1u : 0u);
         }
         mma_commit(b_sfull(b));
         mma_commit(b_kempty(slot));
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
         tc_fence_after();
         const uint64_t dv = dv0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 16 rows of V = 2048 bytes
+        for (int k = 0; k < BK / 16; ++k)  // 16 keys per MMA: 16 rows of V = 2048 bytes
           mma_ts(tmem + 256, tmem + 128 * b + k * 8, dv + static_cast<uint64_t>(k * (2048 >> 4)), idesc_pv,
                  (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(b_pvdone(b));
@@ -298,23 +305,26 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
       }
       tc_fence_after();
       const int kt = w.lo + j;
-      float s[128];
+      float s[BK];
       {
-        uint32_t u[128];
-        tmem_ld128(tS, u);
+        uint32_t u[BK];
+        if constexpr (BK == 128)
+          tmem_ld128(tS, u);
+        else
+          tmem_ld64(tS, u);
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
+        for (int i = 0; i < BK; ++i) s[i] = __uint_as_float(u[i]);
       }
-      const int lim = klim - kt * 128;
-      if (__any_sync(0xffffffffu, lim < 128)) {
+      const int lim = klim - kt * BK;
+      if (__any_sync(0xffffffffu, lim < BK)) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = c >= lim ? -INFINITY : s[c];
+        for (int c = 0; c < BK; ++c) s[c] = c >= lim ? -INFINITY : s[c];
       }
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; c += 16) {
+      for (int c = 0; c < BK; c += 16) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx[e] = max3f(mx[e], s[c + 2 * e], s[c + 2 * e + 1]);
       }
@@ -348,13 +358,13 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
           }
         }
       }
-      uint32_t pk[64];
+      uint32_t pk[BK / 2];
       float ls[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ls[e] = 0.f;
       const float neg_m = -m_used;
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
+      for (int c = 0; c < BK; c += 2) {
         const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
         const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
         ls[(c >> 1) & 7] += p0 + p1;
@@ -365,15 +375,15 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
       // (after their copy has landed) so that P = 0 there cannot meet a non-finite value. V(j) is load
       // j of the V ring; the slot's previous load (j - NSR <= j - 2) was consumed by O += P V before
       // S(j) could be issued, so the parity names this load's phase.
-      const int valid = w.ctx - kt * 128;
-      if (valid < 128) {
+      const int valid = w.ctx - kt * BK;
+      if (valid < BK) {
         const int slot = j % NSR;
         if (!__all_sync(0xffffffffu, wait_bar(b_vfull(slot), (j / NSR) & 1, p.timeout_ns, abort_flag, WD_V))) {
           ok = false;
           break;
         }
-        uint8_t* vt = smem + C::TILE + (NSR + slot) * C::TILE;
-        for (int row = valid + r; row < 128; row += 32 * nact) {
+        uint8_t* vt = smem + C::QTILE + (NSR + slot) * C::TILE;
+        for (int row = valid + r; row < BK; row += 32 * nact) {
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c) {
             uint4* z = reinterpret_cast<uint4*>(vt + c * C::CHUNK + row * 128);
@@ -383,7 +393,10 @@ __global__ void __launch_bounds__(224, 1) fa_decode_kernel(const __grid_constant
         }
         fence_proxy_async_smem();  // visible to the tensor core before P is announced
       }
-      tmem_st64(tS, pk);
+      if constexpr (BK == 128)
+        tmem_st64(tS, pk);
+      else
+        tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(b_pfull(b));
@@ -567,6 +580,7 @@ cudaError_t launch_decode_t(const DecArgs& a) {
 }  // namespace
 
 cudaError_t launch_decode(const DecArgs& a) {
+  if (a.d == 256) return a.bf16 ? launch_decode_t<256, true>(a) : launch_decode_t<256, false>(a);
   if (a.d == 128) return a.bf16 ? launch_decode_t<128, true>(a) : launch_decode_t<128, false>(a);
   if (a.d == 64) return a.bf16 ? launch_decode_t<64, true>(a) : launch_decode_t<64, false>(a);
   return cudaErrorInvalidValue;
