@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -33,10 +34,55 @@ EncodeTiledFn get_encode_fn() {
 
 unsigned long long g_timeout_ns = 4000000000ull;
 
+// Tensor maps are pure functions of (base, shape, box, type); encoding one is host work on every call,
+// so each host thread keeps the last few it built (direct-mapped by a hash of the key).
+struct MapKey {
+  const void* base;
+  long long dim2;
+  int dim1, d, box_rows, rank;
+  bool bf16;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && dim2 == o.dim2 && dim1 == o.dim1 && d == o.d && box_rows == o.box_rows &&
+           rank == o.rank && bf16 == o.bf16;
+  }
+};
+struct MapSlot {
+  MapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kMapCache = 64;
+thread_local MapSlot t_maps[kMapCache];
+
+MapSlot& map_slot(const MapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+  h ^= static_cast<uint64_t>(k.dim2) * 0xC2B2AE3D27D4EB4Full;
+  h ^= (static_cast<uint64_t>(k.dim1) << 20) ^ (static_cast<uint64_t>(k.d) << 8) ^
+       (static_cast<uint64_t>(k.box_rows) << 40) ^ (static_cast<uint64_t>(k.rank) << 56) ^ (k.bf16 ? 1u : 0u);
+  h ^= h >> 29;
+  return t_maps[h % kMapCache];
+}
+
+bool cached(CUtensorMap* m, const MapKey& k) {
+  MapSlot& s = map_slot(k);
+  if (!s.valid || !(s.key == k)) return false;
+  *m = s.map;
+  return true;
+}
+
+void remember(const CUtensorMap& m, const MapKey& k) {
+  MapSlot& s = map_slot(k);
+  s.key = k;
+  s.map = m;
+  s.valid = true;
+}
+
 // 3-D map over a [heads][N][d] row-major 16-bit tensor (heads = B*H); box = {64 elements, box_rows, 1};
 // 128-byte swizzle. Rows past N are outside a head, so a tile that runs past the end of a sequence
 // is zero-filled by the hardware instead of reading the next head's rows.
 bool make_map(CUtensorMap* m, const void* base, long long heads, int N, int d, bool bf16, int box_rows) {
+  const MapKey key{base, heads, N, d, box_rows, 3, bf16};
+  if (cached(m, key)) return true;
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(heads)};
@@ -46,11 +92,15 @@ bool make_map(CUtensorMap* m, const void* base, long long heads, int N, int d, b
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  remember(*m, key);
+  return true;
 }
 
 // 2-D map over [rows][d] of a 16-bit tensor; box = {64 elements, box_rows}; 128-byte swizzle.
 bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int d, bool bf16, int box_rows) {
+  const MapKey key{base, rows, 0, d, box_rows, 2, bf16};
+  if (cached(m, key)) return true;
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
@@ -60,7 +110,9 @@ bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int d, bool b
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  remember(*m, key);
+  return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -126,11 +178,19 @@ DecWs decode_ws(int B, int H, int Mq, int d, int n_split) {
 fa_status check_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  // 0 unknown, 1 a compute capability 10.3 device, 2 another device (the answer never changes)
+  static std::atomic<unsigned char> known[64];
+  if (dev >= 0 && dev < 64) {
+    const unsigned char k = known[dev].load(std::memory_order_relaxed);
+    if (k == 1) return FA_OK;
+    if (k == 2) return FA_ERR_UNSUPPORTED;
+  }
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
-  return FA_OK;
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < 64) known[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
+  return ok ? FA_OK : FA_ERR_UNSUPPORTED;
 }
 
 fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype) {

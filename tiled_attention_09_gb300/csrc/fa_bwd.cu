@@ -91,7 +91,8 @@ template <int D, bool BF16, bool CAUSAL, bool GRP>
 cudaError_t launch_pipe_t(const BwdArgs& a) {
   using C = BwdPipeCfg<D>;
   auto kern = fa_bwd_pipe_kernel<D, BF16, CAUSAL, GRP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   static int checked = 0;  // 1: the compiled register count matches the kernel's register split
   if (!checked) {
@@ -110,7 +111,8 @@ template <bool BF16, bool CAUSAL>
 cudaError_t launch_d256_t(const BwdArgs& a) {
   using C = BwdD256Cfg;
   auto kern = fa_bwd_d256_kernel<BF16, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const BwdParams p = bwd_params(a);
   dim3 grid(a.B * a.Hkv, (a.N + 127) / 128, 1);  // key blocks of each K/V head; the last may run past N

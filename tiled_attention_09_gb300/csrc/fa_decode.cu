@@ -532,15 +532,9 @@ template <int D, bool BF16>
 cudaError_t launch_decode_t(const DecArgs& a) {
   using C = DecCfg<D>;
   auto kern = fa_decode_kernel<D, BF16>;
-  cudaError_t e = cudaSuccess;
-  static int attr_set = -1;  // the device whose function attribute was set (decode steps are host-latency bound)
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if (attr_set != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = dev;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
   DecParams p;
   p.tm_q = a.tm_q;
   p.tm_k = a.tm_k;

@@ -610,7 +610,8 @@ template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   if constexpr (C::NT == 2) {
     static int checked = 0;  // 1: the compiled register count matches the split

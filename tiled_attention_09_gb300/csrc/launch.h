@@ -3,9 +3,23 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace fa {
+
+// Raises a kernel's dynamic shared-memory limit once per device: cudaFuncSetAttribute costs host
+// time on every call, and decode steps are short enough for that to show.
+inline cudaError_t smem_attr_once(const void* kern, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Plain stream-ordered launch, returning the launch error.
 template <typename... KArgs, typename... Args>
