@@ -46,6 +46,15 @@ fa_status fa_selftest_gemm(const void* a, const void* b, float* d, int n, int k,
 fa_status fa_selftest_mma_rate(int n, int a_tmem, int n_acc, int reps, int blocks, unsigned long long* cycles,
                                void* stream);
 
+/*
+ * Failure-detection self-test: one kernel waits (bounded, like every wait in
+ * the library) on an mbarrier phase that nothing completes. After timeout_ns
+ * (1e3 .. 1e9, else FA_ERR_INVALID_ARG) it records a timeout in the device
+ * status word and returns; fa_device_status then reports FA_ERR_TIMEOUT with
+ * info[1] = 90, and the context stays usable. Nothing traps or hangs.
+ */
+fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

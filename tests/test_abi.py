@@ -158,3 +158,40 @@ def test_python_layer_requires_cuda_tensors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fwd(q, q, q)
+
+
+def test_wait_timeout_selftest_rejects_bad_limits(L):
+    assert L.fa_selftest_wait_timeout(10, None) == 1           # below 1 us
+    assert L.fa_selftest_wait_timeout(2_000_000_000, None) == 1  # above 1 s
+
+
+def test_decode_split_choice_and_workspace(L):
+    # the library's split count for a shape, and the workspace it implies
+    s = L.fa_decode_splits(1, 8, 128, 64, 1024)
+    assert 1 <= s <= 64
+    assert L.fa_decode_splits(1, 8, 256, 64, 1024) <= 32
+    assert L.fa_decode_splits(19, 8, 128, 64, 128) == 1  # 152 CTAs fill the GPU once: no split
+    assert L.fa_decode_splits(1, 8, 96, 64, 16) == 0      # unsupported head dimension
+    r256 = lambda x: (x + 255) // 256 * 256
+    rows = 2 * 16 * 1
+    for n_split in (1, 3):
+        assert L.fa_decode_workspace_size(2, 16, 4, 1, 128, 64, 32, n_split) == \
+            r256(n_split * rows * 128 * 4) + r256(n_split * rows * 4)
+    assert L.fa_decode_workspace_size(2, 16, 4, 1, 128, 64, 32, 500) == r256(64 * rows * 128 * 4) + r256(64 * rows * 4)
+    assert L.fa_decode_workspace_size(2, 16, 3, 1, 128, 64, 32, 1) == 0   # 16 query heads on 3 K/V heads
+    assert L.fa_decode_workspace_size(2, 16, 1, 9, 128, 64, 32, 1) == 0   # 16 heads x 9 queries > 128 rows
+    assert L.fa_decode_workspace_size(2, 16, 4, 1, 128, 48, 32, 1) == 0   # page size not a power of two
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(page_table=0), 1), (dict(ctx_len=0), 1), (dict(d=96), 2), (dict(page_size=8), 2),
+    (dict(H=16, Hkv=3), 2), (dict(scale=0.0), 1), (dict(ws=0), 4), (dict(ws=P + 64), 3), (dict(ws_bytes=16), 4),
+    (dict(page_table=P + 2), 3), (dict(q=P + 8), 3),
+])
+def test_decode_rejects_bad_arguments(L, kw, code):
+    a = dict(q=P, kp=P, vp=P, page_table=P, ctx_len=P, o=P, lse=P, ws=P, ws_bytes=1 << 40, B=2, H=16, Hkv=4, Mq=1,
+             d=128, page_size=64, n_pages=64, max_pages=32, n_split=0, scale=0.125, causal=0, dtype=1)
+    a.update(kw)
+    assert L.fa_decode(V(a["q"]), V(a["kp"]), V(a["vp"]), V(a["page_table"]), V(a["ctx_len"]), V(a["o"]), V(a["lse"]),
+                       V(a["ws"]), a["ws_bytes"], a["B"], a["H"], a["Hkv"], a["Mq"], a["d"], a["page_size"],
+                       a["n_pages"], a["max_pages"], a["n_split"], a["scale"], a["causal"], a["dtype"], None) == code

@@ -515,16 +515,17 @@ fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, con
 fa_status fa_device_status(void* stream, unsigned int info[4]) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
-  fa::DevStatusHost a{}, b{}, c{};
+  fa::DevStatusHost a{}, b{}, c{}, t{};
   if (fa::read_clear_status_fwd(&a, st) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_status_bwd(&b, st) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_status_decode(&c, st) != cudaSuccess) return FA_ERR_CUDA;
-  const fa::DevStatusHost& first = a.code ? a : (b.code ? b : c);
+  if (fa::read_clear_status_selftest(&t, st) != cudaSuccess) return FA_ERR_CUDA;
+  const fa::DevStatusHost& first = a.code ? a : (b.code ? b : (c.code ? c : t));
   if (info) {
     info[0] = first.code;
     info[1] = first.where;
     info[2] = first.block;
-    info[3] = a.count + b.count + c.count;
+    info[3] = a.count + b.count + c.count + t.count;
   }
   if (first.code == 1u) return FA_ERR_TIMEOUT;
   if (first.code != 0u) return FA_ERR_DEVICE_FAULT;

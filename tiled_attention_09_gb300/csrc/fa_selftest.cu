@@ -13,6 +13,7 @@
 #include "../../include/fa.h"
 #include "../../include/fa_selftest.h"
 #include "common.cuh"
+#include "launch.h"
 
 namespace fa {
 namespace {
@@ -290,5 +291,50 @@ extern "C" fa_status fa_selftest_mma_rate(int n, int a_tmem, int n_acc, int reps
     return FA_ERR_CUDA;
   fa_mma_rate_kernel<<<blocks, 128, MR_SMEM, static_cast<cudaStream_t>(stream)>>>(n, a_tmem ? 1 : 0, n_acc, tmem_mode, reps, cycles,
                                                                                  2000000000ull);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// A wait that nothing completes: one thread waits on an mbarrier phase that no thread or copy will
+// ever finish. The bounded wait gives up after timeout_ns, records FA_DEV_TIMEOUT (where-code 90) in
+// this translation unit's status word and the kernel returns: nothing else is in flight, so the
+// context stays usable. This is how every kernel of the library reports a wait that ran out.
+namespace fa {
+namespace {
+constexpr uint32_t WT_WHERE = 90;
+__global__ void __launch_bounds__(32, 1) fa_wait_timeout_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    mbar_fence_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) wait_bar(smem_u32(&bar), 0, timeout_ns, &abort_flag, WT_WHERE);
+  __syncwarp();
+}
+}  // namespace
+
+cudaError_t read_clear_status_selftest(DevStatusHost* out, cudaStream_t s) {
+  DevStatus zero{0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(DevStatus), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (out->code != 0 || out->count != 0)
+    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(DevStatus), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+}  // namespace fa
+
+extern "C" fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return FA_ERR_INVALID_ARG;  // 1 us .. 1 s
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  fa::fa_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -103,5 +103,6 @@ cudaError_t read_clear_status_fwd(DevStatusHost* out, cudaStream_t s);
 cudaError_t read_clear_status_bwd(DevStatusHost* out, cudaStream_t s);
 cudaError_t launch_decode(const DecArgs& a);
 cudaError_t read_clear_status_decode(DevStatusHost* out, cudaStream_t s);
+cudaError_t read_clear_status_selftest(DevStatusHost* out, cudaStream_t s);
 
 }  // namespace fa
