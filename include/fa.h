@@ -247,7 +247,10 @@ fa_status fa_decode(const void* q, const void* k_pages, const void* v_pages, con
  * kernels. FA_OK if no kernel reported anything; FA_ERR_TIMEOUT if a bounded
  * wait expired; FA_ERR_DEVICE_FAULT for a failed device-side check;
  * FA_ERR_CUDA if the synchronisation itself failed.
- * If `info` is non-NULL it receives {code, where, block, count} of the first report.
+ * If `info` is non-NULL it receives {code, where, block, count} of the first report:
+ * code 1 = a bounded wait ran out, 2 = a failed index check; `where` names the
+ * wait or check (1-20 forward, 31-39 decode, 41-59 backward, 90-99 self-tests);
+ * `block` is the linear CTA index; `count` the number of reports.
  */
 fa_status fa_device_status(void* stream, unsigned int info[4]);
 

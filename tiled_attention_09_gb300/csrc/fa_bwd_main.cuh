@@ -91,9 +91,10 @@ __device__ __forceinline__ uint32_t bpack2(float lo, float hi) {
   }
 }
 
+// where-codes of the backward's waits and checks (40-59; the forward uses 1-20, decode 31-39)
 enum : uint32_t {
-  WB_KV = 11, WB_QE = 12, WB_QF = 13, WB_SDP = 14, WB_DS = 15, WB_DQF = 16, WB_DQFREE = 17, WB_DONE = 18, WB_DRAIN = 19,
-  WB_ITEM = 20, WB_CLC = 21
+  WB_KV = 41, WB_QE = 42, WB_QF = 43, WB_SDP = 44, WB_DS = 45, WB_DQF = 46, WB_DQFREE = 47, WB_DONE = 48, WB_DRAIN = 49,
+  WB_ITEM = 50, WB_CLC = 51
 };
 
 // Write one 128 x d accumulator (thread = row, TMEM lane) as dtype into a 128-byte-swizzled
