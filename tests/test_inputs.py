@@ -9,7 +9,8 @@ import hashlib
 import pytest
 import torch
 
-from tiled_attention_09_gb300.inputs import CAUSAL_4K_STRESS, SMALL, Workload, make_inputs, sample_cols, sample_rows
+from tiled_attention_09_gb300.inputs import (CAUSAL_4K_STRESS, SMALL, DecodeWorkload, Workload, make_inputs,
+                                          make_paged_inputs, sample_cols, sample_rows)
 
 FINGERPRINTS = {
     SMALL: "6c040eb1f28fd935eb783d32eda74b6d",
@@ -40,3 +41,31 @@ def test_sample_recipes():
     assert len(rows) == 64 and rows == sorted(set(rows)) and {0, 1, 127, 128, 129, 2048, 4095} <= set(rows)
     cols = sample_cols(4096)
     assert len(cols) == 64 and {0, 2048, 4095} <= set(cols)
+
+
+PAGED_FINGERPRINTS = {
+    DecodeWorkload(2, 8, 2, 1, 128, 64, 20, (1000, 77)): "cc7e3b7e76506a8d2ccfe1e8f1c6e841",
+    DecodeWorkload(3, 4, 1, 4, 256, 16, 40, (640, 3, 0), dtype="fp16", causal=True): "d24a171155d1deaa1ab2370bc9369d41",
+}
+
+
+@pytest.mark.parametrize("w", list(PAGED_FINGERPRINTS), ids=lambda w: w.name())
+def test_paged_input_fingerprint(w):
+    q, kp, vp, table, ctx = make_paged_inputs(w)
+    assert q.shape == (w.B, w.H, w.Mq, w.d) and kp.shape == (w.Hkv, w.n_pages, w.page_size, w.d) == vp.shape
+    assert table.shape == (w.B, w.max_pages) and table.dtype == torch.int32 and ctx.dtype == torch.int32
+    # every sequence owns distinct pages of the pool
+    assert len(set(table.flatten().tolist())) == w.B * w.max_pages
+    h = hashlib.sha256()
+    for x in (q, kp, vp, table, ctx):
+        h.update((x.view(torch.int16) if x.dtype in (torch.bfloat16, torch.float16) else x).numpy().tobytes())
+    assert h.hexdigest()[:32] == PAGED_FINGERPRINTS[w]
+
+
+def test_paged_inputs_poison_only_rows_past_each_sequence():
+    w = DecodeWorkload(2, 4, 2, 1, 64, 16, 5, (33, 80))
+    q, kp, vp, table, ctx = make_paged_inputs(w)
+    for b in range(w.B):
+        for j in range(w.max_pages * w.page_size):
+            row = kp[:, table[b, j // w.page_size], j % w.page_size].float()
+            assert bool(torch.isnan(row).all()) == (j >= int(ctx[b]))
