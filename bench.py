@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="time paged decode attention on the decode points instead (one JSON line each)")
     ap.add_argument("--decode-point", type=int, default=-1, help="with --decode: only this point (0-based)")
+    ap.add_argument("--shape", default="", help="B,H,N,d: time this bf16 causal shape instead (profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
                          "instead of the headline step; one JSON line per point")
@@ -224,11 +225,10 @@ def cpu_cores():
 
 def run_reference(args):
     """Reference arm: the fp64 CPU oracle on a bounded sample of the same workload per step."""
-    from tiled_attention_09_gb300.inputs import CAUSAL_4K
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    w = CAUSAL_4K
+    w = bench_workload(args)
     smp = OracleSampler(w)
     smp.run(64)
     # size the per-step sample so warm-up + timed steps stay within ~2.5 minutes
@@ -275,16 +275,46 @@ class L2Flush:
         self.torch.sum(self.r, dim=0, out=self.sink)
 
 
+def bench_workload(args):
+    """The timed workload: B2 H12 N4096 d128 bf16 causal, or --shape B,H,N,d (bf16, causal) for profiling
+    other sizes with the same step."""
+    from tiled_attention_09_gb300.inputs import CAUSAL_4K, Workload
+    if not getattr(args, "shape", ""):
+        return CAUSAL_4K
+    B, H, N, d = (int(x) for x in args.shape.split(","))
+    return Workload(B, H, N, d, "bf16", True)
+
+
+def measure_ex2_rate(torch, L, dev, reps=4096):
+    """Exponentials per second of the whole GPU (fa_selftest_ex2_rate on 2 CTAs per SM, median of 5 timed
+    launches after one warm-up): the peak of the softmax's secondary roofline."""
+    blocks = 2 * torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.zeros(blocks, dtype=torch.float32, device=dev)
+    sp = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    times = []
+    for i in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if L.fa_selftest_ex2_rate(reps, blocks, ctypes.c_void_p(sink.data_ptr()), sp) != 0:
+            return None
+        e1.record()
+        torch.cuda.synchronize()
+        if i > 0:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    return blocks * 512 * 8 * reps / statistics.median(times)
+
+
 def run_native(args):
     import torch
     import tiled_attention_09_gb300 as fa
     from tiled_attention_09_gb300 import _lib
-    from tiled_attention_09_gb300.inputs import CAUSAL_4K, make_inputs
+    from tiled_attention_09_gb300.inputs import make_inputs
 
     world, rank, local, dist = dist_setup(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = CAUSAL_4K
+    w = bench_workload(args)
+    roof_kernel = ROOFLINE_KERNEL if w.d != 256 else "fa_bwd_d256_kernel"
     B, H, N, d = w.B, w.H, w.N, w.d
     F = w.fwd_flops()
     step_flops = 3.5 * F
@@ -459,7 +489,16 @@ def run_native(args):
     achieved = main_flops / main_avg / 1e12
     peak = peaks["bf16_tflops"]
     fwd_avg = t_fwd
-    traffic = recorded_traffic(ROOFLINE_KERNEL)
+    traffic = None if args.shape else recorded_traffic(roof_kernel)  # recorded for the bench workload only
+    # secondary roofline of the softmax: exponentials (B*H*N^2, halved when causal: the FLOP count's
+    # convention) per second in the forward and in the backward main kernel (which rebuilds P)
+    ex2_peak = measure_ex2_rate(torch, L, dev)
+    exps = B * H * N * N / 2
+    exp_roof = None
+    if ex2_peak:
+        exp_roof = {"unit": "exp/s", "peak": ex2_peak, "peak_source": "measured (fa_selftest_ex2_rate)",
+                    "fa_fwd_kernel": {"achieved": exps / fwd_avg, "frac": exps / fwd_avg / ex2_peak},
+                    roof_kernel: {"achieved": exps / main_avg, "frac": exps / main_avg / ex2_peak}}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -471,12 +510,13 @@ def run_native(args):
                    "parallelism": f"weak: {world} independent replica(s)"},
         "pct_of_peak": value / (world * peak), "peak_tflops": peak, "peak_source": f"{peak_src} (bf16 burst)",
         "kernels_ms": {"fa_fwd_kernel": 1e3 * fwd_avg, "fa_bwd_preprocess_kernel": 1e3 * t_pre,
-                       ROOFLINE_KERNEL: 1e3 * main_avg, "fa_bwd_dq_convert_kernel": 1e3 * t_conv},
+                       roof_kernel: 1e3 * main_avg, "fa_bwd_dq_convert_kernel": 1e3 * t_conv},
         "fwd_tflops": F / fwd_avg / 1e12,
         "bwd_tflops": 2.5 * F / (t_pre + t_main + t_conv) / 1e12,
-        "roofline": {"kernel": ROOFLINE_KERNEL, "bound": "tensor", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": roof_kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 burst"},
+        "exp_roofline": exp_roof,
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 4 * K,

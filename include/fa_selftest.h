@@ -55,6 +55,15 @@ fa_status fa_selftest_mma_rate(int n, int a_tmem, int n_acc, int reps, int block
  */
 fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
 
+/*
+ * Exponential-unit rate microbenchmark (the secondary roofline of the softmax):
+ * `blocks` CTAs of 512 threads each run 8 independent chains of `reps`
+ * dependent ex2.approx.f32, i.e. blocks * 512 * 8 * reps exponentials; the
+ * caller times the launch. sink: DEVICE float[blocks], zeroed by the caller
+ * (receives the chains' sums). 1 <= reps <= 2^20, 1 <= blocks <= 65535.
+ */
+fa_status fa_selftest_ex2_rate(int reps, int blocks, float* sink, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -53,3 +53,25 @@ def test_mma_rate_microbenchmark(n, a_tmem, n_acc):
     flop_per_clk = 2 * 128 * n * 16 / per_mma
     print(f"MMA rate n={n} a_tmem={a_tmem} n_acc={n_acc}: {per_mma:.1f} cycles/instr, {flop_per_clk:.0f} FLOP/clk/SM")
     assert per_mma >= n / 2 * 0.95  # nominal 8192 dense bf16 FLOP/clk/SM
+
+
+def test_ex2_rate_microbenchmark():
+    """Exponentials per second of the whole GPU: finite results, and a rate between 1e12/s and the
+    nominal 32 per clock per SM at 2.1 GHz."""
+    import ctypes
+    from tiled_attention_09_gb300 import _lib
+    L = _lib.load()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.zeros(2 * sms, dtype=torch.float32, device="cuda")
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.fa_selftest_ex2_rate(64, 2 * sms, ctypes.c_void_p(sink.data_ptr()), st) == 0  # warm-up
+    reps = 4096
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    assert L.fa_selftest_ex2_rate(reps, 2 * sms, ctypes.c_void_p(sink.data_ptr()), st) == 0
+    e1.record()
+    torch.cuda.synchronize()
+    rate = 2 * sms * 512 * 8 * reps / (e0.elapsed_time(e1) / 1e3)
+    print(f"ex2 rate {rate / 1e12:.2f} T/s = {rate / sms / 2.07e9:.1f} per clock per SM at 2.07 GHz")
+    assert torch.isfinite(sink).all()
+    assert 1e12 < rate < 32 * sms * 2.1e9

@@ -59,6 +59,7 @@ SIGNATURES = [
     ("fa_selftest_mma_rate", c_int, [c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     ("fa_selftest_gemm", c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     ("fa_selftest_wait_timeout", c_int, [ctypes.c_ulonglong, c_void_p]),
+    ("fa_selftest_ex2_rate", c_int, [c_int, c_int, c_void_p, c_void_p]),
 ]
 
 _lock = threading.Lock()

@@ -338,3 +338,39 @@ extern "C" fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, voi
   fa::fa_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+// Exponential-unit rate microbenchmark: every thread runs 8 independent chains of `reps` dependent
+// ex2.approx.f32 (x <- 2^x - 1.5 keeps x in [-1, 0]), so the special-function units, not latency,
+// set the pace once enough warps are resident. The sum of the chains goes to sink[block] so that
+// nothing is optimised away. Timed by the caller (events around the launch).
+namespace fa {
+namespace {
+__global__ void __launch_bounds__(512) fa_ex2_rate_kernel(int reps, float* sink) {
+  float x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = -0.125f * static_cast<float>(c + 1) - 1e-6f * static_cast<float>(threadIdx.x);
+#pragma unroll 1
+  for (int r = 0; r < reps; ++r) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = ex2_approx(x[c]) - 1.5f;
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) s += x[c];
+  s += __shfl_xor_sync(0xffffffffu, s, 16);
+  if ((threadIdx.x & 31) == 0) atomicAdd(sink + blockIdx.x, s);
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_selftest_ex2_rate(int reps, int blocks, float* sink, void* stream) {
+  if (!sink) return FA_ERR_INVALID_ARG;
+  if (reps < 1 || reps > (1 << 20) || blocks < 1 || blocks > 65535) return FA_ERR_UNSUPPORTED;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  fa::fa_ex2_rate_kernel<<<blocks, 512, 0, static_cast<cudaStream_t>(stream)>>>(reps, sink);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
