@@ -479,6 +479,33 @@ def run_native(args):
         t_e2e = tt.item()
     e2e_value = world * step_flops * e2e_steps / t_e2e / 1e12
 
+    # The same copies alone, in and out at once on the same two streams: the time the host link needs per
+    # step, so that e2e can be read against max(this, the device step time).
+    def copies_only(b):
+        (qi, ki, vi, doi), (o_, lse_, lo_, dq_, dk_, dv_) = dsets[b]
+        with torch.cuda.stream(s_in):
+            for src, dst in ((hq, qi), (hk, ki), (hv, vi), (hdo, doi)):
+                dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for src, dst in zip((o_, lse_, dq_, dk_, dv_), hsets[b]):
+                dst.copy_(src, non_blocking=True)
+
+    copies_only(0)
+    torch.cuda.synchronize()
+    n_copy = 10
+    ev0.record(stream)
+    s_in.wait_event(ev0)
+    s_out.wait_event(ev0)
+    for i in range(n_copy):
+        copies_only(i % 2)
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_copy = ev0.elapsed_time(ev1) / 1e3 / n_copy
+    t_e2e_step = t_e2e / e2e_steps
+    e2e_bound = max(t_copy, total / K)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -518,7 +545,12 @@ def run_native(args):
                      "peak_source": f"{peak_src} bf16 burst"},
         "exp_roofline": exp_roof,
         "clocks": clk,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": 1e3 * t_e2e_step,
+                "copies_alone_ms_per_step": 1e3 * t_copy,
+                "h2d_gbs_concurrent": h2d / t_copy / 1e9, "d2h_gbs_concurrent": d2h / t_copy / 1e9,
+                "bound": "host copies" if t_copy > total / K else "device step",
+                "frac_of_bound": e2e_bound / t_e2e_step},
         "gpu_launches": 4 * K,
         "cpu_baseline": cpu,
     }

@@ -29,8 +29,9 @@
  *    (a TMA requirement), else FA_ERR_ALIGNMENT.
  *  - Supported shapes: d in {64, 128, 256}; any N >= 1 (a last tile that
  *    runs past N is zero-filled on load, masked, and not stored); B, H >= 1;
- *    B*H*N' < 2^31 with N' = N rounded up to 128. Anything else:
- *    FA_ERR_UNSUPPORTED, no launch.
+ *    B*H*N' < 2^31 with N' = N rounded up to 128; N <= 65535*128 =
+ *    8,388,480 (one backward CTA column per 128-key block, and a grid's y
+ *    extent is at most 65535). Anything else: FA_ERR_UNSUPPORTED, no launch.
  *  - scale: finite and > 0, else FA_ERR_INVALID_ARG. The pages use
  *    scale = d^-1/2.
  *  - causal != 0: query i attends to keys j <= i.

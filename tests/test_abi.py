@@ -95,7 +95,7 @@ def fwd(L, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=256, d=64, scale=0.125, causal
 @pytest.mark.parametrize("kw,code", [
     (dict(q=0), 1), (dict(lse=0), 1),
     (dict(N=0), 2), (dict(N=-5), 2), (dict(d=96), 2), (dict(d=32), 2), (dict(B=0), 2),
-    (dict(H=-1), 2), (dict(B=1 << 16, H=1 << 8, N=1 << 8), 2),
+    (dict(H=-1), 2), (dict(B=1 << 16, H=1 << 8, N=1 << 8), 2), (dict(N=65535 * 128 + 1), 2),
     (dict(dtype=7), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-1.0), 1),
     (dict(scale=0.0), 1),
     (dict(q=P + 8), 3), (dict(o=P + 2), 3), (dict(lse=P + 4), 3),
@@ -114,6 +114,7 @@ def test_bwd_rejects_bad_arguments(L):
     assert bwd(L, ws_bytes=10) == 4
     assert bwd(L, ws=P + 16) == 3   # workspace must be 256-byte aligned
     assert bwd(L, N=0) == 2
+    assert bwd(L, N=65535 * 128 + 1) == 2  # more 128-key blocks than a grid's y extent
     assert bwd(L, scale=float("nan")) == 1
     assert bwd(L, dq=0) == 1
     assert bwd(L, dq=P + 4) == 3

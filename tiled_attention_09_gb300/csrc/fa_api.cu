@@ -193,12 +193,16 @@ fa_status check_device() {
   return ok ? FA_OK : FA_ERR_UNSUPPORTED;
 }
 
+constexpr int kMaxKeyBlocks = 65535;
+
 fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype) {
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   // row indices (including the backward workspace's per-head padding) stay in 32-bit ints
   if (static_cast<long long>(B) * H * ((N + 127) / 128 * 128) >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  // the backward launches its 128-key blocks along the grid's y dimension (at most 65535)
+  if ((N + 127) / 128 > kMaxKeyBlocks) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 

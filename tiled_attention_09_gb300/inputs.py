@@ -104,6 +104,21 @@ def make_inputs(w: Workload):
     return cast_inputs(w, make_inputs_fp32(w))
 
 
+def make_inputs_device(w: Workload, device, n_kv_heads: int | None = None):
+    """q [B,H,N,d] and k, v, do drawn on ``device`` for tensors too large to draw on the host in seconds.
+
+    ``torch.randn`` with a ``torch.Generator`` on the device, seeded with ``w.seed``, in the order Q, K,
+    V, dO, directly in ``w.torch_dtype``; k and v have ``n_kv_heads`` heads (default H). The values
+    depend on the device and the torch build, so a consumer copies back whatever it checks: the oracle
+    then reads exactly the values the CUDA path read.
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    hkv = w.H if n_kv_heads is None else n_kv_heads
+    shapes = ((w.B, w.H, w.N, w.d), (w.B, hkv, w.N, w.d), (w.B, hkv, w.N, w.d), (w.B, w.H, w.N, w.d))
+    return tuple(torch.randn(s, generator=g, device=device, dtype=w.torch_dtype) for s in shapes)
+
+
 def sample_rows(N: int, n_random: int = 57, seed: int = 1):
     """Query rows checked when the full oracle is too slow.
 
