@@ -10,14 +10,14 @@ backward 2.5x that; value = 3.5*F_fwd / (t_fwd + t_bwd).
 Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
 barrier and torch.cuda.synchronize(); the L2 cache is flushed (a 256 MiB write, then a 256 MiB read)
 before each step, outside the CUDA-event-timed interval of that step. A step is
-timed between two events (fa_fwd_ex, fa_bwd through the C ABI), so the kernels
-keep their programmatic dependent launch; per-kernel times (kernels_ms and the
+timed between two events (fa_fwd_ex, fa_bwd through the C ABI); per-kernel times (kernels_ms and the
 roofline's launch duration) come from a second pass of min(K, 50) steps with an
 event between every two kernels. The max over ranks is reported; under torchrun
 every rank runs the same workload on its own GPU (weak scaling, no data-path
 collective).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       python bench.py --decode | --sweep | --shape B,H,N,d | --oracle-timing | --sdpa
 """
 from __future__ import annotations
 
@@ -59,6 +59,14 @@ def parse():
                     help="time paged decode attention on the decode points instead (one JSON line each)")
     ap.add_argument("--decode-point", type=int, default=-1, help="with --decode: only this point (0-based)")
     ap.add_argument("--shape", default="", help="B,H,N,d: time this bf16 causal shape instead (profiling)")
+    ap.add_argument("--oracle-timing", action="store_true",
+                    help="time the fp64 CPU oracle on the host cores: the small, pages and causal-4k workloads in "
+                         "full (forward and backward apart, the small one also single-threaded), the 32k one on "
+                         "sampled rows; one JSON line each, no GPU")
+    ap.add_argument("--oracle-single", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sdpa", action="store_true",
+                    help="context only: time torch's scaled_dot_product_attention (each backend that runs) "
+                         "forward+backward on the headline workload, one JSON line")
     ap.add_argument("--sweep", action="store_true",
                     help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
                          "instead of the headline step; one JSON line per point")
@@ -696,10 +704,134 @@ def run_decode(args):
         torch.cuda.empty_cache()
 
 
+def cpu_model():
+    """The host CPU's name from /proc/cpuinfo (x86 "model name"; Arm "CPU part" code), else the machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+        for key in ("model name", "Model", "CPU part"):
+            for line in info:
+                if line.split(":")[0].strip() == key:
+                    return f"{key}: {line.split(':', 1)[1].strip()} ({platform.machine()})"
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def run_oracle_timing(args):
+    """The fp64 oracle as it stands (numpy, BLAS threads = host cores), timed on the host: the small
+    (B1 H2 N256 d64), pages (B2 H12 N1024 d64) and causal 4k (B2 H12 N4096 d128) workloads in full,
+    forward and backward timed apart; the small one again with one BLAS thread (a child process, since
+    the thread count is fixed when numpy loads); the 32k workload (B1 H8 N32768 d128) on the sampled
+    query rows the parity tests check (O, LSE and dQ of those rows). GFLOP/s use the metric's count
+    (forward 4BHN^2d, halved when causal; backward 2.5x), or for sampled rows 8 d (visible keys) a row."""
+    import numpy as np
+    import oracle
+    from tiled_attention_09_gb300.inputs import CAUSAL_4K, LONG_32K, PAGES_SHAPE, SMALL, make_inputs, sample_rows
+    cores, cpu = cpu_cores(), cpu_model()
+    f64 = lambda t: t.double().numpy()
+
+    def full(label, w):
+        q, k, v, do = (f64(t) for t in make_inputs(w))
+        t0 = time.perf_counter()
+        oracle.attention_fwd(q, k, v, w.scale, w.causal)
+        t_f = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, w.scale, w.causal)
+        t_b = time.perf_counter() - t0
+        F = w.fwd_flops()
+        print(json.dumps({"oracle_timing": label, "workload": w.name(), "mode": "full", "threads": cores,
+                          "cpu": cpu, "fwd_s": t_f, "bwd_s": t_b, "fwd_gflops": F / t_f / 1e9,
+                          "bwd_gflops": 2.5 * F / t_b / 1e9}), flush=True)
+
+    if args.oracle_single:
+        full("small, 1 thread", SMALL)
+        return
+    for label, w in (("small", SMALL), ("pages", PAGES_SHAPE), ("causal 4k", CAUSAL_4K)):
+        full(label, w)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-timing", "--oracle-single"], env=env,
+                   check=True)
+    w = LONG_32K
+    q, k, v, do = (f64(t) for t in make_inputs(w))
+    rows = np.asarray(sample_rows(w.N))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, do, w.scale, w.causal, rows)
+    dt = time.perf_counter() - t0
+    visible = (rows + 1).sum() if w.causal else len(rows) * w.N
+    flops = w.B * w.H * 8.0 * w.d * visible
+    print(json.dumps({"oracle_timing": "long 32k", "workload": w.name(), "mode": "sampled rows",
+                      "rows_per_head": int(len(rows)), "heads": w.B * w.H, "threads": cores, "cpu": cpu,
+                      "s": dt, "gflops": flops / dt / 1e9}), flush=True)
+
+
+def run_sdpa(args):
+    """Context, not a target: torch.nn.functional.scaled_dot_product_attention, forward then backward
+    with the same dO, on the headline workload, timed like the headline step (L2 flushed before every
+    step, CUDA events around it); each backend torch offers is tried on its own and reported with its
+    TFLOP/s (metric's FLOP count) or the error it raised. The library is only run."""
+    import torch
+    import torch.nn.functional as F
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    from tiled_attention_09_gb300.inputs import make_inputs
+    w = bench_workload(args)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    q, k, v = (t.requires_grad_() for t in (q, k, v))
+    flush = L2Flush(torch, dev)
+    steps, warmup = max(3, min(args.steps, 50)), max(3, args.warmup)
+    flops = 3.5 * w.fwd_flops()
+    res = {}
+    for name, be in (("cudnn", SDPBackend.CUDNN_ATTENTION), ("flash", SDPBackend.FLASH_ATTENTION),
+                     ("efficient", SDPBackend.EFFICIENT_ATTENTION)):
+        try:
+            with sdpa_kernel([be]):
+                def step():
+                    q.grad = k.grad = v.grad = None
+                    o = F.scaled_dot_product_attention(q, k, v, is_causal=w.causal, scale=w.scale)
+                    o.backward(do)
+
+                def fwd_only():
+                    with torch.no_grad():
+                        F.scaled_dot_product_attention(q, k, v, is_causal=w.causal, scale=w.scale)
+
+                times = []
+                for fn in (step, fwd_only):
+                    for _ in range(warmup):
+                        flush()
+                        fn()
+                    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                           for _ in range(steps)]
+                    for e0, e1 in evs:
+                        flush()
+                        e0.record()
+                        fn()
+                        e1.record()
+                    torch.cuda.synchronize()
+                    times.append(statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3)
+            t, t_f = times
+            res[name] = {"ms_per_step": 1e3 * t, "tflops": flops / t / 1e12, "fwd_ms": 1e3 * t_f,
+                         "fwd_tflops": w.fwd_flops() / t_f / 1e12}
+        except Exception as e:  # a backend that does not run on this GPU or shape
+            torch.cuda.synchronize()
+            res[name] = {"error": f"{type(e).__name__}: {str(e).splitlines()[0][:160] if str(e) else ''}"}
+    print(json.dumps({"impl": "torch scaled_dot_product_attention (context)", "torch": torch.__version__,
+                      "workload": w.name(), "steps": steps, "warmup": warmup,
+                      "timing": "median step between two events, L2 flushed before each step", "backends": res}),
+          flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3:
         args.warmup = 3
+    if args.oracle_timing:
+        run_oracle_timing(args)
+        return
+    if args.sdpa:
+        run_sdpa(args)
+        return
     if args.decode:
         run_decode(args)
     elif args.sweep:
