@@ -66,18 +66,35 @@ def _check_kv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
     B, H, N, d = q.shape
     if k.dim() != 4 or k.shape[0] != B or k.shape[2:] != q.shape[2:] or k.dtype != q.dtype or k.device != q.device:
         raise ValueError("k, v must be [B, H_kv, N, d] with q's B, N, d, dtype and device")
-    if H % k.shape[1] != 0:
+    if k.shape[1] < 1 or H % k.shape[1] != 0:
         raise ValueError(f"H = {H} is not a multiple of H_kv = {k.shape[1]}")
     return int(k.shape[1])
 
 
-def _options(H, Hkv, kv_len, out_fp32, device):
+def _check_buf(t: torch.Tensor, shape, dtype, device, name: str):
+    """A caller-supplied output or input buffer: the kernels get only its pointer, so its shape, dtype,
+    device and layout are checked here (a wrong one would be read or written past its end)."""
+    if (not isinstance(t, torch.Tensor) or tuple(t.shape) != tuple(shape) or t.dtype != dtype
+            or t.device != device or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+
+
+def _check_workspace(t: torch.Tensor, need: int, device) -> int:
+    """A caller-supplied workspace: contiguous, on the device, at least ``need`` bytes. Returns its bytes."""
+    if not isinstance(t, torch.Tensor) or t.device != device or not t.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+    nbytes = t.numel() * t.element_size()
+    if nbytes < need:
+        raise ValueError(f"workspace holds {nbytes} bytes, {need} needed")
+    return nbytes
+
+
+def _options(B, H, Hkv, kv_len, out_fp32, device):
     """fa_options for the call, or None when every option has its default."""
     if Hkv == H and kv_len is None and not out_fp32:
         return None
     if kv_len is not None:
-        if kv_len.dtype != torch.int32 or kv_len.device != device or not kv_len.is_contiguous():
-            raise ValueError("kv_len must be a contiguous int32 tensor on q's device")
+        _check_buf(kv_len, (B,), torch.int32, device, "kv_len")
     return _lib.FAOptions(Hkv, kv_len.data_ptr() if kv_len is not None else None, int(bool(out_fp32)))
 
 
@@ -115,15 +132,23 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, residual=False, o
     if out_fp32 and residual:
         raise ValueError("an fp32 output has no rounding residual")
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    o_dtype = torch.float32 if out_fp32 else q.dtype
     if out is None:
-        o = torch.empty(q.shape, device=q.device, dtype=torch.float32) if out_fp32 else torch.empty_like(q)
+        o = torch.empty(q.shape, device=q.device, dtype=o_dtype)
     else:
+        _check_buf(out, q.shape, o_dtype, q.device, "out")
         o = out
-    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
-    if residual and o_lo is None:
-        o_lo = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    else:
+        _check_buf(lse, (B, H, N), torch.float32, q.device, "lse")
+    if residual:
+        if o_lo is None:
+            o_lo = torch.empty_like(q)
+        else:
+            _check_buf(o_lo, q.shape, q.dtype, q.device, "o_lo")
     L = _lib.load()
-    opt = _options(H, Hkv, kv_len, out_fp32, q.device)
+    opt = _options(B, H, Hkv, kv_len, out_fp32, q.device)
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
             o_lo.data_ptr() if residual else None, B, H, N, d, scale, int(bool(causal)), _DT[q.dtype])
     if opt is None:
@@ -152,18 +177,24 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     if o_lo is not None:
         _check_qkv(q, o_lo)
     B, H, N, d = q.shape
+    _check_buf(lse, (B, H, N), torch.float32, q.device, "lse")
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
     L = _lib.load()
     ws_bytes = int(L.fa_bwd_workspace_size(B, H, N, d))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    else:
+        ws_bytes = _check_workspace(workspace, ws_bytes, q.device)
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t is not None:
+            _check_buf(t, like.shape, like.dtype, like.device, name)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o_lo.data_ptr() if o_lo is not None else None,
-            workspace.data_ptr(), workspace.numel(), B, H, N, d, scale, int(bool(causal)), _DT[q.dtype])
-    opt = _options(H, Hkv, kv_len, out_fp32, q.device)
+            workspace.data_ptr(), ws_bytes, B, H, N, d, scale, int(bool(causal)), _DT[q.dtype])
+    opt = _options(B, H, Hkv, kv_len, out_fp32, q.device)
     if opt is None:
         name, code = "fa_bwd", L.fa_bwd(*args, _stream_ptr(q))
     else:
@@ -212,6 +243,8 @@ def decode(q, k_pages, v_pages, page_table, ctx_len, causal=False, scale=None, n
     _check_qkv(q)
     _check_qkv(k_pages, v_pages)
     B, H, Mq, d = q.shape
+    if k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages, v_pages must both be [Hkv, n_pages, page_size, d]")
     Hkv, n_pages, page_size, dk = k_pages.shape
     if dk != d or k_pages.dtype != q.dtype or k_pages.device != q.device:
         raise ValueError("k_pages, v_pages must be [Hkv, n_pages, page_size, d] with q's d, dtype and device")
@@ -228,10 +261,19 @@ def decode(q, k_pages, v_pages, page_table, ctx_len, causal=False, scale=None, n
         raise ValueError("unsupported decode shape")
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    o = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, Mq), device=q.device, dtype=torch.float32) if lse is None else lse
+    else:
+        ws_bytes = _check_workspace(workspace, ws_bytes, q.device)
+    if out is None:
+        o = torch.empty_like(q)
+    else:
+        _check_buf(out, q.shape, q.dtype, q.device, "out")
+        o = out
+    if lse is None:
+        lse = torch.empty((B, H, Mq), device=q.device, dtype=torch.float32)
+    else:
+        _check_buf(lse, (B, H, Mq), torch.float32, q.device, "lse")
     code = L.fa_decode(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), page_table.data_ptr(), ctx_len.data_ptr(),
-                       o.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, Hkv, Mq, d,
+                       o.data_ptr(), lse.data_ptr(), workspace.data_ptr(), ws_bytes, B, H, Hkv, Mq, d,
                        page_size, n_pages, max_pages, n_split, scale, int(bool(causal)), _DT[q.dtype], _stream_ptr(q))
     _lib.check("fa_decode", code)
     _after("fa_decode", q)
@@ -240,6 +282,10 @@ def decode(q, k_pages, v_pages, page_table, ctx_len, causal=False, scale=None, n
 
 def selftest_gemm(a, b, n, k, a_mode, b_mode):
     """Tensor-core operand self-test (see include/fa_selftest.h). Returns d [128, n] fp32."""
+    for name, t, need in (("a", a, 128 * k), ("b", b, n * k)):
+        if t.device.type != "cuda" or t.dtype not in _DT or t.dtype != a.dtype or not t.is_contiguous() \
+                or t.numel() < need:
+            raise ValueError(f"{name} must be a contiguous fp16/bf16 CUDA tensor of at least {need} elements")
     L = _lib.load()
     d = torch.empty((128, n), device=a.device, dtype=torch.float32)
     code = L.fa_selftest_gemm(a.data_ptr(), b.data_ptr(), d.data_ptr(), n, k, a_mode, b_mode, _DT[a.dtype],
