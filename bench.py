@@ -25,7 +25,6 @@ import argparse
 import ctypes
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
