@@ -3,7 +3,9 @@
 Each case rewrites one line of an oracle function (a plausible slip: a flipped mask, a dropped term,
 a wrong index or sign), installs the mutant in the oracle module for the duration of the case, and
 runs the pins that concern that function: at least one of them must fail. This shows the pins in
-tests/test_oracle.py are tied to the arithmetic, not to whatever the oracle happens to compute.
+tests/test_oracle.py are tied to the arithmetic, not to whatever the oracle happens to compute. The
+comparison with torch's float64 attention (tests/test_oracle_vs_library.py) must catch every mutation of
+a function it covers as well.
 """
 import inspect
 import textwrap
@@ -12,6 +14,7 @@ import pytest
 
 import oracle
 import test_oracle as pins
+import test_oracle_vs_library as lib
 
 # (name, oracle function, original text, mutated text, pins that must catch it)
 MUTATIONS = [
@@ -67,3 +70,29 @@ def test_planted_mistake_fails_a_pin(monkeypatch, what, fn, original, mutated, c
         except (AssertionError, ValueError, IndexError, FloatingPointError):
             caught += 1
     assert caught >= 1, f"no pin catches: {what}"
+
+
+# The same planted mistakes against the library comparison alone (tests/test_oracle_vs_library.py): every
+# mutation of a function that comparison covers must fail it too. The LSE base and the split merge are
+# outside it (the library returns neither), so they are left to the pins above.
+LIBRARY_CATCHERS = {
+    "flipped causal mask": (lib.test_matches_library_attention, {"causal": True, "N": 77, "d": 32}),
+    "dropped D in dS": (lib.test_matches_library_attention, {"causal": False, "N": 77, "d": 32}),
+    "missing scale in dQ": (lib.test_matches_library_attention, {"causal": True, "N": 77, "d": 32}),
+    "untransposed P in dV": (lib.test_matches_library_attention, {"causal": False, "N": 77, "d": 32}),
+    "dK sign": (lib.test_matches_library_attention, {"causal": True, "N": 77, "d": 32}),
+    "grouped heads read the wrong K/V head": (lib.test_grouped_heads_match_library, {"Hkv": 2, "causal": False}),
+    "key padding off by one": (lib.test_key_padding_matches_library, {"causal": False}),
+    "page row index": (lib.test_paged_decode_matches_library, {"causal": False}),
+    "decode causal alignment": (lib.test_paged_decode_matches_library, {"causal": True}),
+}
+
+
+@pytest.mark.parametrize("what,fn,original,mutated", [m[:4] for m in MUTATIONS if m[0] in LIBRARY_CATCHERS],
+                         ids=[m[0] for m in MUTATIONS if m[0] in LIBRARY_CATCHERS])
+def test_planted_mistake_fails_the_library_comparison(monkeypatch, what, fn, original, mutated):
+    pin, kwargs = LIBRARY_CATCHERS[what]
+    pin(**kwargs)  # passes on the real oracle
+    monkeypatch.setattr(oracle, fn, _mutant(fn, original, mutated))
+    with pytest.raises((AssertionError, ValueError, IndexError, FloatingPointError)):
+        pin(**kwargs)
