@@ -176,10 +176,18 @@ fa_status fa_bwd_opt(const void* q, const void* k, const void* v, const void* o,
  *  - problems whose fa_bwd_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
  *    (64 MiB; for d = 128 that is B*H*N up to about 129,000 rows) return
  *    FA_ERR_WORKSPACE with nothing enqueued;
- *  - every device that calls it keeps its own 64 MiB copy of the array for as
- *    long as the library stays loaded;
- *  - the first call on a device looks up the array's device address (with that
- *    device current); make that first call before any stream capture;
+ *  - the array is device memory of the library's own module, one 64 MiB copy
+ *    per CUDA context. Under lazy module loading (the CUDA default) a context
+ *    gets its copy at the first fa_bwd_noalloc call made in it: that first
+ *    call loads the module and so allocates the 64 MiB (through the driver).
+ *    Make it at set-up time, outside the path that must not allocate and
+ *    before any stream capture. Under CUDA_MODULE_LOADING=EAGER every context
+ *    that loads the library gets its copy when the context is created, whether
+ *    or not it ever calls this entry point. The copy lasts as long as the
+ *    context;
+ *  - every call looks up the current device's copy (a host-side lookup once
+ *    the module is loaded), so a context re-created after cudaDeviceReset is
+ *    served from its own new copy;
  *  - all calls share the array: calls whose GPU work can overlap (different
  *    streams without ordering) race on it and must be serialised by the caller.
  * Calls no cudaMalloc/cudaFree and no allocating library routine.

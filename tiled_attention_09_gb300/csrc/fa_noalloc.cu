@@ -10,11 +10,20 @@
 // synchronise). Such callers still hand over the inputs and outputs they own;
 // only the scratch space comes from here.
 //
-// The array lives as long as the library is loaded, on every device that uses
-// this entry point (FA_NOALLOC_SCRATCH_BYTES = 64 MiB each). In host code its
-// name is not a device address, so the first call on each device looks the
-// address up with cudaGetSymbolAddress while that device is current and caches
-// it; make that first call before any stream capture. All calls share the one
+// The array is device memory of this file's own module. Under lazy module
+// loading (the CUDA default) a context gets its copy when the module is loaded
+// there, which is the first fa_bwd_noalloc call in that context: that call
+// allocates the FA_NOALLOC_SCRATCH_BYTES (64 MiB) through the driver's module
+// loader, so it belongs at set-up time, outside the path that must not
+// allocate and before any stream capture. Under CUDA_MODULE_LOADING=EAGER every
+// context that loads the library gets the copy when the context is created,
+// whether or not it ever calls this entry point. Either way the copy lasts as
+// long as the context. In host code the array's name is not a device address:
+// every call looks up the current device's copy with cudaGetSymbolAddress
+// (with that device current), a host-side lookup once the module is loaded.
+// Looking it up on every call, rather than caching it per device, keeps the
+// address right when a context is re-created (after cudaDeviceReset the module
+// is loaded again and the array can sit elsewhere). All calls share the one
 // array: two calls whose work can overlap on the GPU (different streams, no
 // ordering between them) race on it. Nothing in it has to start at zero: the
 // preprocess kernel writes D and LSE*log2e in full and zeroes the dQ
@@ -22,7 +31,6 @@
 #include <cuda_runtime.h>
 
 #include <cstddef>
-#include <mutex>
 
 #include "../../include/fa.h"
 
@@ -30,27 +38,18 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_fa_bwd_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the current device's copy of the scratch array (looked up once per device).
+// Device address of the current device's copy of the scratch array, looked up on every call.
 fa_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return FA_ERR_CUDA;
   if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fa_bwd_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fa_bwd_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+  *out = p;
   return FA_OK;
 }
 
