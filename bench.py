@@ -14,9 +14,11 @@ timed between two events (fa_fwd_ex, fa_bwd through the C ABI); per-kernel times
 roofline's launch duration) come from a second pass of min(K, 50) steps with an
 event between every two kernels. The max over ranks is reported; under torchrun
 every rank runs the same workload on its own GPU (weak scaling, no data-path
-collective).
+collective), or with --shard heads its contiguous range of the job's B*H heads
+(strong scaling: value = the whole job's FLOPs over the slowest rank's time;
+heads are independent, so there is still no data-path collective).
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--shard replicas|heads]
        python bench.py --decode | --sweep | --shape B,H,N,d | --oracle-timing | --sdpa
 """
 from __future__ import annotations
@@ -36,6 +38,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's published dense (no 2:4 sparsity) bf16 tensor-core peak of one GB300 GPU, TFLOP/s
+PUBLISHED_DENSE_BF16_TFLOPS = 2250.0
 METRIC = "attention fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense tensor peak"
 _CSRC = "tiled_attention_09_gb300/csrc/"
 # sources each timed kernel is built from: a recorded ncu traffic figure is used only while these are unchanged
@@ -66,6 +70,9 @@ def parse():
     ap.add_argument("--sdpa", action="store_true",
                     help="context only: time torch's scaled_dot_product_attention (each backend that runs) "
                          "forward+backward on the headline workload, one JSON line")
+    ap.add_argument("--shard", default="replicas", choices=["replicas", "heads"],
+                    help="under torchrun: every rank runs the whole workload (replicas, weak scaling) or its "
+                         "contiguous range of the job's B*H heads (heads, strong scaling, no data-path collective)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
                          "instead of the headline step; one JSON line per point")
@@ -323,8 +330,16 @@ def run_native(args):
     w = bench_workload(args)
     roof_kernel = ROOFLINE_KERNEL if w.d != 256 else "fa_bwd_d256_kernel"
     B, H, N, d = w.B, w.H, w.N, w.d
-    F = w.fwd_flops()
+    sharded = args.shard == "heads" and world > 1
+    job_heads = B * H
+    if sharded:  # this rank's contiguous range of the job's heads, as a B' = 1, H' = count problem
+        from tiled_attention_09_gb300.shard import head_ranges
+        h0, nh = head_ranges(job_heads, world)[rank]
+        if nh == 0:
+            raise SystemExit(f"rank {rank}: no heads left for this rank ({job_heads} heads, {world} ranks)")
+    F = w.fwd_flops() * ((nh / job_heads) if sharded else 1.0)  # forward FLOPs of this rank's share
     step_flops = 3.5 * F
+    job_step_flops = 3.5 * w.fwd_flops() if sharded else world * step_flops
 
     # CPU baseline first (rank 0, N=1 only), before the GPU work starts
     cpu = None
@@ -334,6 +349,10 @@ def run_native(args):
 
     L = _lib.load()
     q, k, v, do = make_inputs(w)
+    if sharded:
+        from tiled_attention_09_gb300.shard import head_slice
+        q, k, v, do = (head_slice(t, h0, nh).contiguous() for t in (q, k, v, do))
+        B, H = 1, nh
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
@@ -416,7 +435,7 @@ def run_native(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total = tt.item()
     K = args.steps
-    value = world * step_flops * K / total / 1e12
+    value = job_step_flops * K / total / 1e12
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region.
     # Every step copies its own Q, K, V, dO in and its O, LSE, dQ, dK, dV out; the copies of neighbouring
@@ -484,7 +503,7 @@ def run_native(args):
         tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_e2e = tt.item()
-    e2e_value = world * step_flops * e2e_steps / t_e2e / 1e12
+    e2e_value = job_step_flops * e2e_steps / t_e2e / 1e12
 
     # The same copies alone, in and out at once on the same two streams: the time the host link needs per
     # step, so that e2e can be read against max(this, the device step time).
@@ -535,14 +554,20 @@ def run_native(args):
                     roof_kernel: {"achieved": exps / main_avg, "frac": exps / main_avg / ex2_peak}}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": 1e3 * total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": 1e3 * total / K, "higher_is_better": True, "scaling": "strong" if sharded else "weak",
+        "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name(), "B": B, "H": H, "N": N, "d": d, "causal": True, "seed": 0,
                    "l2": "flushed before every step (256 MiB write, then a 256 MiB read of another buffer so the write-back is not charged to the step; outside the timed interval)",
                    "timing": "value: whole step between two events; kernels_ms/roofline: a second pass of "
                              f"{K2} steps with events between kernels",
-                   "parallelism": f"weak: {world} independent replica(s)"},
+                   "parallelism": (f"heads: {job_heads} heads in contiguous ranges over {world} rank(s), no "
+                                   "data-path collective" if sharded else f"weak: {world} independent replica(s)")},
         "pct_of_peak": value / (world * peak), "peak_tflops": peak, "peak_source": f"{peak_src} (bf16 burst)",
+        "pct_of_published_peak": value / (world * PUBLISHED_DENSE_BF16_TFLOPS),
+        "published_peak_tflops": PUBLISHED_DENSE_BF16_TFLOPS,
+        "published_peak_source": "NVIDIA's GB300 dense bf16 tensor-core figure, 2.25 PFLOP/s per GPU (its "
+                                 "larger per-system figures assume 2:4 sparsity)",
         "kernels_ms": {"fa_fwd_kernel": 1e3 * fwd_avg, "fa_bwd_preprocess_kernel": 1e3 * t_pre,
                        roof_kernel: 1e3 * main_avg, "fa_bwd_dq_convert_kernel": 1e3 * t_conv},
         "fwd_tflops": F / fwd_avg / 1e12,
