@@ -7,8 +7,18 @@ Tolerance reading (fixed before any kernel ran; derivation in the design notes):
   output to fp16/bf16, and u_dtype * (P|V|)_i bounds the error of rounding the
   probabilities P to the input dtype before the P.V tensor-core product
   (u_bf16 = 2^-8, u_fp16 = 2^-11; (P|V|)_i is the oracle's attention output
-  with |V| in place of V). The literal max-abs error and the share of elements
-  inside 2e-3 + half_ulp are reported alongside.
+  with |V| in place of V). That is the per-element cap.
+* O, the literal bound 2e-3 + half_ulp: the elements outside it are counted and
+  that count is bounded by what an ideal kernel with the same rounding steps
+  gives on the same inputs (ideal_kernel_o: fp32 scores, exact exponentials,
+  P rounded to the dtype, fp32 sums, output rounded to the dtype). The GPU's
+  rounding of P and of its sums is another, equally valid realisation of those
+  same steps, so its count is allowed 3x the ideal kernel's plus 8 elements:
+  n_outside_gpu <= 3 * n_outside_ideal + 8. Where the ideal kernel has none
+  outside (every fp16 configuration and most bf16 ones), at most 8 elements of
+  the whole tensor may be. The literal max-abs error, the share inside the
+  literal bound and both counts are recorded for every check and printed at the
+  end of the pytest run.
 * LSE: |LSE_gpu - LSE_orc| <= 2e-3 (fp32 output).
 * dQ, dK, dV: max|g_gpu - g_orc| <= 1e-2 * max|g_orc|, per tensor. Where the exact
   gradient is zero (a single key: the softmax is the constant 1, so dQ = dK = 0
@@ -40,16 +50,96 @@ def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def check_o(o_gpu: np.ndarray, o_ref: np.ndarray, pv_abs: np.ndarray, dtype: str, what: str = "O"):
+# (what, max_abs, share inside 2e-3 + half-ulp, elements outside, ideal kernel's outside, allowed, elements)
+O_STATS: list = []
+
+
+def round16(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round to fp16 / bf16 (round to nearest even) and back to fp32."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16 if dtype == "bf16" else torch.float16).float().numpy()
+
+
+def ideal_kernel_o(q, k, v, scale, dtype, causal=False, kv_len=None, rows=None, q_offset=0):
+    """O as an ideal fused kernel with the same rounding steps would produce it (fp32 arithmetic).
+
+    Per head: S = scale * q k^T in fp32 from the exact 16-bit inputs; masked entries -inf (key j is
+    visible to query row r when j < kv_len[b] and, causal, j <= r + q_offset); P = exp(S - rowmax) in
+    fp32 and its fp32 row sum l; P rounded to the dtype for the product with V (fp32 sums); O = (P V) / l
+    (0 for a row with no visible key) rounded to the dtype. Only the count of its elements outside the
+    literal bound is used (it scales what the GPU is allowed); the reference values stay the oracle's.
+    q: [B, H, M, d], k, v: [B, H_kv, Nk, d] (float64 holding 16-bit values); rows: query rows (default all).
+    """
+    B, H, M, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    G = H // Hkv
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    out = np.empty((B, H, len(rows), d), dtype=np.float64)
+    j = np.arange(Nk)[None, :]
+    for b in range(B):
+        klen = Nk if kv_len is None else int(min(max(int(kv_len[b]), 0), Nk))
+        vis = np.broadcast_to(j < klen, (len(rows), Nk))
+        if causal:
+            vis = vis & (j <= rows[:, None] + q_offset)
+        for h in range(H):
+            qq = q[b, h, rows].astype(np.float32)
+            kk = k[b, h // G].astype(np.float32)
+            vv = v[b, h // G].astype(np.float32)
+            s = (qq @ kk.T) * np.float32(scale)
+            s = np.where(vis, s, np.float32(-np.inf))
+            m = s.max(axis=1, keepdims=True)
+            m = np.where(np.isfinite(m), m, np.float32(0.0))
+            p = np.exp(s - m).astype(np.float32)
+            l = p.sum(axis=1, keepdims=True, dtype=np.float32)
+            o = (round16(p, dtype) @ vv) / np.where(l > 0, l, np.float32(1.0))
+            out[b, h] = round16(np.where(l > 0, o, np.float32(0.0)), dtype)
+    return out
+
+
+def ideal_decode_o(q64, kp64, vp64, table, ctx, scale, dtype, causal):
+    """The ideal kernel's O per sequence: its keys gathered through the page table (entries outside the
+    pool read as zero keys and values), its queries at positions ctx - Mq ... ctx - 1."""
+    B, Mq = q64.shape[0], q64.shape[2]
+    Hkv, n_pages, ps, d = kp64.shape
+    out = np.zeros(q64.shape)
+    for b in range(B):
+        c = int(min(max(int(ctx[b]), 0), table.shape[1] * ps))
+        if c == 0:
+            continue  # no key: O = 0
+        j = np.arange(c)
+        pg, r = table[b, j // ps], j % ps
+        ok = (pg >= 0) & (pg < n_pages)
+        gather = lambda pool: np.where(ok[None, :, None], pool[:, np.clip(pg, 0, n_pages - 1), r], 0.0)[None]
+        out[b:b + 1] = ideal_kernel_o(q64[b:b + 1], gather(kp64), gather(vp64), scale, dtype, causal,
+                                      kv_len=[c], q_offset=c - Mq)
+    return out
+
+
+def check_o(o_gpu: np.ndarray, o_ref: np.ndarray, pv_abs: np.ndarray, dtype: str, what: str = "O",
+            ideal: np.ndarray = None):
+    """Per-element cap (stated bound + output rounding + P rounding), and, given the ideal kernel's
+    output on the same inputs, a bound on the count of elements outside the literal 2e-3 + half-ulp."""
     err = np.abs(o_gpu - o_ref)
     tol = o_tolerance(o_ref, pv_abs, dtype)
     bad = err > tol
-    literal = float(np.mean(err <= 2e-3 + half_ulp(o_ref, dtype)))
+    literal_tol = 2e-3 + half_ulp(o_ref, dtype)
+    n_out = int((err > literal_tol).sum())
     assert np.isfinite(o_gpu).all(), f"{what}: non-finite values"
     assert not bad.any(), (
         f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; max err {err.max():.3e}; "
         f"worst excess {(err - tol).max():.3e}")
-    return {"max_abs": float(err.max()), "within_2e-3+half_ulp": literal}
+    stats = {"max_abs": float(err.max()), "within_2e-3+half_ulp": 1.0 - n_out / err.size, "outside": n_out}
+    if ideal is not None:
+        n_ideal = int((np.abs(ideal - o_ref) > literal_tol).sum())
+        allowed = 3 * n_ideal + 8
+        stats.update(ideal_outside=n_ideal, allowed=allowed)
+        O_STATS.append((what, stats["max_abs"], stats["within_2e-3+half_ulp"], n_out, n_ideal, allowed, err.size))
+        assert n_out <= allowed, (
+            f"{what}: {n_out} of {err.size} elements outside 2e-3 + half-ulp; the ideal kernel has {n_ideal} "
+            f"(allowed {allowed}); max err {err.max():.3e}")
+    else:
+        O_STATS.append((what, stats["max_abs"], stats["within_2e-3+half_ulp"], n_out, None, None, err.size))
+    return stats
 
 
 def check_lse(lse_gpu: np.ndarray, lse_ref: np.ndarray, what: str = "LSE"):

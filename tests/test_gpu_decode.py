@@ -13,7 +13,7 @@ import torch
 import oracle
 import tiled_attention_09_gb300 as fa
 from tiled_attention_09_gb300.inputs import DecodeWorkload, make_paged_inputs
-from helpers import check_lse, check_o, to64
+from helpers import check_lse, check_o, ideal_decode_o, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,8 @@ def test_decode_matches_oracle(case):
     q64, kp64, vp64 = to64(q), to64(kp), to64(vp)
     o_ref, lse_ref = oracle.paged_attention_fwd(q64, kp64, vp64, table.numpy(), ctx.numpy(), w.scale, w.causal)
     pv_abs, _ = oracle.paged_attention_fwd(q64, kp64, np.abs(vp64), table.numpy(), ctx.numpy(), w.scale, w.causal)
-    check_o(to64(o), o_ref, pv_abs, w.dtype)
+    check_o(to64(o), o_ref, pv_abs, w.dtype, f"O decode {w.name()} split{n_split}",
+            ideal=ideal_decode_o(q64, kp64, vp64, table.numpy(), ctx.numpy(), w.scale, w.dtype, w.causal))
     l_gpu, empty = to64(lse), np.isneginf(lse_ref)
     assert np.isneginf(l_gpu[empty]).all() and (to64(o)[empty] == 0).all()
     if (~empty).any():

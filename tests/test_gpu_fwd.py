@@ -14,7 +14,7 @@ import oracle
 import tiled_attention_09_gb300 as fa
 from tiled_attention_09_gb300.inputs import (CAUSAL_4K, CAUSAL_4K_STRESS, LONG_32K, PAGES_SHAPE, SMALL, Workload,
                                              make_inputs, sample_rows)
-from helpers import check_lse, check_o, to64
+from helpers import check_lse, check_o, ideal_kernel_o, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,8 @@ def test_fwd_full_oracle(w):
     q64, k64, v64 = to64(q), to64(k), to64(v)
     o_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, w.scale, w.causal)
     pv_abs, _ = oracle.attention_fwd(q64, k64, np.abs(v64), w.scale, w.causal)
-    check_o(to64(o), o_ref, pv_abs, w.dtype)
+    check_o(to64(o), o_ref, pv_abs, w.dtype, f"O fwd {w.name()}",
+            ideal=ideal_kernel_o(q64, k64, v64, w.scale, w.dtype, w.causal))
     check_lse(to64(lse), lse_ref)
 
 
@@ -61,7 +62,8 @@ def test_fwd_sampled_rows(w):
     q64, k64, v64 = to64(q), to64(k), to64(v)
     o_ref, lse_ref, _ = oracle.attention_rows(q64, k64, v64, np.zeros_like(q64), w.scale, w.causal, rows)
     pv_abs, _, _ = oracle.attention_rows(q64, k64, np.abs(v64), np.zeros_like(q64), w.scale, w.causal, rows)
-    check_o(o_g, o_ref, pv_abs, w.dtype)
+    check_o(o_g, o_ref, pv_abs, w.dtype, f"O fwd {w.name()} sampled rows",
+            ideal=ideal_kernel_o(q64, k64, v64, w.scale, w.dtype, w.causal, rows=rows))
     check_lse(lse_g, lse_ref)
 
 
@@ -83,7 +85,8 @@ def test_fwd_closed_form_q_zero(causal, d):
         want = np.broadcast_to(v64.mean(axis=2, keepdims=True), v64.shape)
         want_lse = np.full((B, H, N), math.log(N))
     # P is exactly uniform (exp2(0) = 1), so only output rounding and fp32 sums remain
-    check_o(to64(o), want, np.zeros_like(want), "bf16")
+    check_o(to64(o), want, np.zeros_like(want), "bf16", f"O fwd Q=0 d{d} causal{int(causal)}",
+            ideal=ideal_kernel_o(to64(q), to64(k), v64, d ** -0.5, "bf16", causal))
     check_lse(to64(lse), want_lse)
 
 
@@ -95,7 +98,8 @@ def test_fwd_closed_form_constant_v_and_row0():
     o, _ = run_fwd(q, k, torch.ones_like(q), True)
     # V = 1: O = 1 up to the P-rounding term u*(P|V|) = 2^-8 and output rounding
     ones = np.ones(o.shape)
-    check_o(to64(o), ones, ones, "bf16")
+    check_o(to64(o), ones, ones, "bf16", "O fwd V=1",
+            ideal=ideal_kernel_o(to64(q), to64(k), ones, d ** -0.5, "bf16", True))
     v = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16)
     o, lse = run_fwd(q, k, v, True)
     # causal row 0 sees key 0 only: O_0 = V_0 exactly, LSE_0 = scale q0.k0

@@ -12,7 +12,7 @@ import torch
 import oracle
 import tiled_attention_09_gb300 as fa
 from tiled_attention_09_gb300.inputs import Workload, make_inputs
-from helpers import cancel_tol, check_grad, check_lse, check_o, to64
+from helpers import cancel_tol, check_grad, check_lse, check_o, ideal_kernel_o, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,8 @@ def test_options_fwd_bwd(case):
     kl64 = None if kv_len is None else kv_len.numpy()
     o_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, w.scale, w.causal, kv_len=kl64)
     pv_abs, _ = oracle.attention_fwd(q64, k64, np.abs(v64), w.scale, w.causal, kv_len=kl64)
-    check_o(to64(o), o_ref, pv_abs, w.dtype)
+    check_o(to64(o), o_ref, pv_abs, w.dtype, f"O fwd {_name(case)}",
+            ideal=ideal_kernel_o(q64, k64, v64, w.scale, w.dtype, w.causal, kv_len=kl64))
     _check_lse_masked(to64(lse), lse_ref)
     ref = oracle.attention_bwd(q64, k64, v64, do64, w.scale, w.causal, kv_len=kl64)
     floor = cancel_tol(q64, k64, v64, do64, w.scale)
