@@ -47,6 +47,27 @@ fa_status fa_selftest_mma_rate(int n, int a_tmem, int n_acc, int reps, int block
                                void* stream);
 
 /*
+ * Tensor-core operand-pattern microbenchmark: like fa_selftest_mma_rate, but
+ * with the operand pattern of the attention kernels. Each CTA fills its shared
+ * memory with random 16-bit values; `issuers` threads (1 to 4, lane 0 of warps
+ * 0..3, each with its own accumulators) each issue `reps` products of K = 128
+ * (8 tcgen05.mma of M = 128, N = n, K = 16, the first of each overwriting its
+ * accumulator), alternating between two distinct A tiles and two distinct B
+ * tiles. a_tmem = 1 takes A from tensor memory (then a_mn must be 0); a_mn /
+ * b_mn = 1 lay A / B out MN-major instead of K-major (128-byte swizzle either
+ * way). mode 0: product after product (all SS, or all TS with a_tmem); mode
+ * 1: an SS and a TS product in turn, as the forward issues S = Q K^T and
+ * O += P V (needs a_tmem); mode 2: two SS products interleaved instruction by
+ * instruction into two accumulators (each rep then holds 16 instructions).
+ * cycles: DEVICE array of 4 * blocks entries; entry 4*block + i receives
+ * issuer i's clock64 cycles from its first issue to the completion of its last
+ * instruction. n in {64, 128, 256}; the issuers' accumulators must fit in
+ * tensor memory (else FA_ERR_UNSUPPORTED).
+ */
+fa_status fa_selftest_mma_pattern(int n, int a_tmem, int a_mn, int b_mn, int issuers, int mode, int reps, int blocks,
+                                  unsigned long long* cycles, void* stream);
+
+/*
  * Failure-detection self-test: one kernel waits (bounded, like every wait in
  * the library) on an mbarrier phase that nothing completes. After timeout_ns
  * (1e3 .. 1e9, else FA_ERR_INVALID_ARG) it records a timeout in the device

@@ -75,3 +75,43 @@ def test_ex2_rate_microbenchmark():
     print(f"ex2 rate {rate / 1e12:.2f} T/s = {rate / sms / 2.07e9:.1f} per clock per SM at 2.07 GHz")
     assert torch.isfinite(sink).all()
     assert 1e12 < rate < 32 * sms * 2.1e9
+
+
+PATTERNS = [  # (n, a_tmem, a_mn, b_mn, issuers, mode): the shapes and operand forms of the attention kernels
+    (64, 0, 0, 0, 1, 0), (128, 0, 0, 0, 1, 0), (256, 0, 0, 0, 1, 0), (64, 1, 0, 0, 1, 0), (128, 1, 0, 0, 1, 0),
+    (256, 1, 0, 0, 1, 0), (128, 1, 0, 1, 1, 0), (64, 0, 1, 1, 1, 0), (128, 0, 1, 1, 1, 0), (128, 0, 0, 1, 1, 0),
+    (64, 0, 0, 0, 2, 0), (128, 0, 0, 0, 2, 0), (128, 1, 0, 1, 2, 0),
+    (64, 0, 0, 0, 4, 0), (128, 0, 0, 0, 4, 0), (128, 0, 1, 1, 4, 0), (64, 1, 0, 0, 4, 0), (64, 1, 0, 1, 4, 0),
+    (128, 1, 0, 0, 1, 1), (64, 1, 0, 1, 2, 1), (64, 1, 0, 0, 1, 1),
+    (64, 0, 0, 0, 1, 2), (128, 0, 0, 0, 1, 2), (128, 0, 0, 0, 2, 2),
+]
+
+
+@pytest.mark.parametrize("n,a_tmem,a_mn,b_mn,issuers,mode", PATTERNS)
+def test_mma_pattern_microbenchmark(n, a_tmem, a_mn, b_mn, issuers, mode):
+    """Cycles per tcgen05.mma with distinct random operand tiles: never faster than the nominal
+    dense rate; prints the shared-memory operand bytes the tensor core read per cycle."""
+    import ctypes
+    from tiled_attention_09_gb300 import _lib
+    L = _lib.load()
+    blocks = torch.cuda.get_device_properties(0).multi_processor_count
+    reps = 1024
+    cyc = torch.zeros(4 * blocks, dtype=torch.int64, device="cuda")
+    code = L.fa_selftest_mma_pattern(n, a_tmem, a_mn, b_mn, issuers, mode, reps, blocks,
+                                     ctypes.c_void_p(cyc.data_ptr()),
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    torch.cuda.synchronize()
+    assert fa.device_status()[0] == "FA_OK"
+    span = cyc.view(blocks, 4)[:, :issuers].amax(dim=1).double().median().item()
+    n_mma = 8 * reps * issuers * (2 if mode == 2 else 1)
+    per_mma = span / n_mma  # cycles of the SM per instruction, all issuers together
+    a_bytes = 128 * 16 * 2
+    if mode == 1:
+        smem_bytes = a_bytes / 2 + n * 16 * 2  # half the instructions read A from shared memory
+    else:
+        smem_bytes = (0 if a_tmem else a_bytes) + n * 16 * 2
+    print(f"MMA pattern n={n} a_tmem={a_tmem} a_mn={a_mn} b_mn={b_mn} issuers={issuers} mode={mode}: "
+          f"{per_mma:.1f} cycles/instr, {2 * 128 * n * 16 / per_mma:.0f} FLOP/clk/SM, "
+          f"{smem_bytes / per_mma:.0f} operand B/clk")
+    assert per_mma >= n / 2 * 0.95

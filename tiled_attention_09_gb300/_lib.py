@@ -57,6 +57,7 @@ SIGNATURES = [
     ("fa_set_wait_timeout_ns", None, [ctypes.c_ulonglong]),
     ("fa_version", c_int, []),
     ("fa_selftest_mma_rate", c_int, [c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
+    ("fa_selftest_mma_pattern", c_int, [c_int] * 8 + [c_void_p, c_void_p]),
     ("fa_selftest_gemm", c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     ("fa_selftest_wait_timeout", c_int, [ctypes.c_ulonglong, c_void_p]),
     ("fa_selftest_ex2_rate", c_int, [c_int, c_int, c_void_p, c_void_p]),

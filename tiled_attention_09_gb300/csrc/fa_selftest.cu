@@ -294,6 +294,166 @@ extern "C" fa_status fa_selftest_mma_rate(int n, int a_tmem, int n_acc, int reps
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- MMA operand-pattern microbenchmark
+// Like the issue-rate test, but with the operand pattern of the attention kernels: random 16-bit
+// data, two distinct B tiles (and two distinct A tiles) used in turn, whole K = 128 products (8
+// instructions, the first overwriting the accumulator), K-major or MN-major operands, A from shared
+// memory or from TMEM, and 1 to 4 issuing threads (lane 0 of warps 0..3), each with its own
+// accumulators. Modes:
+//   0  one K = 128 product after another, each into the next of the issuer's accumulators (all SS,
+//      or all TS with a_tmem);
+//   1  the forward's pattern: an SS product (S = Q K^T) and a TS product (O += P V) in turn, into two
+//      accumulators (needs a_tmem for the TS operand);
+//   2  two SS products interleaved instruction by instruction into two accumulators (two
+//      independent accumulation chains in flight from one thread).
+// An SS instruction reads 128 x 16 (A) + n x 16 (B) 16-bit elements from shared memory, a TS
+// instruction only the B part.
+namespace fa {
+namespace {
+constexpr int MP_A_TILE = 2 * 16384;   // 128 rows x 128 K elements (two 64-wide chunks)
+constexpr int MP_B_TILE = 2 * 32768;   // up to 256 rows x 128 K elements
+constexpr int MP_SMEM = 1024 + 2 * MP_A_TILE + 2 * MP_B_TILE + 128;
+
+__global__ void __launch_bounds__(128, 1) fa_mma_pattern_kernel(int n, int a_tmem, int a_mn, int b_mn, int issuers,
+                                                                int mode, int n_buf, int reps,
+                                                                unsigned long long* out,
+                                                                unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA = smem_u32(smem), sB = sA + 2 * MP_A_TILE;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * MP_A_TILE + 2 * MP_B_TILE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const int warp = threadIdx.x >> 5;
+  // random bf16 in about (-1, 1): a hash of the element index, exponent fixed at 2^-1
+  uint32_t* w = reinterpret_cast<uint32_t*>(smem);
+  for (int i = threadIdx.x; i < (2 * MP_A_TILE + 2 * MP_B_TILE) / 4; i += 128) {
+    uint32_t h = static_cast<uint32_t>(i) * 2654435761u + 0x9E3779B9u * static_cast<uint32_t>(blockIdx.x);
+    h ^= h >> 15;
+    h *= 2246822519u;
+    h ^= h >> 13;
+    w[i] = (h & 0x807F807Fu) | 0x3F003F00u;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(bar + i), 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t a_col = 448;  // A operand in TMEM: 128 lanes x 128 K elements as 64 packed columns
+  if (a_tmem) {
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0x3F003F00u ^ ((threadIdx.x * 7u + i * 13u) & 0x007F007Fu);
+    tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + a_col, z);
+    tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + a_col + 32, z);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int lane = threadIdx.x & 31;
+  if (warp < issuers && lane == 0) {
+    const uint32_t idesc = make_idesc(128, n, true, a_mn != 0, b_mn != 0);
+    const uint32_t idesc_ts = make_idesc(128, n, true, false, b_mn != 0);
+    // K-major: rows of 128 bytes (64 K elements), 8-row groups 1024 bytes apart, a K step of 16 is
+    // 32 bytes inside the row, the second 64-wide K chunk a whole chunk further on.
+    // MN-major: rows are K indices of 64 M/N elements; LBO = distance between 64-wide M/N chunks,
+    // a K step of 16 is 16 rows (2048 bytes).
+    const uint32_t a_chunk = 128 * 128, b_chunk = static_cast<uint32_t>(n) * 128;
+    const uint64_t da = a_mn ? make_sdesc(sA, 128 * 128, 1024) : make_sdesc(sA, 16, 1024);
+    const uint64_t db = b_mn ? make_sdesc(sB, 128 * 128, 1024) : make_sdesc(sB, 16, 1024);
+    const uint32_t acc0 = tmem + static_cast<uint32_t>(warp * n_buf * n);
+    auto ss = [&](uint32_t d, uint32_t tile, int kk) {
+      const uint32_t oa = a_mn ? kk * 2048u : (kk >> 2) * a_chunk + (kk & 3) * 32u;
+      const uint32_t ob = b_mn ? kk * 2048u : (kk >> 2) * b_chunk + (kk & 3) * 32u;
+      mma_ss(d, da + (static_cast<uint64_t>(tile * MP_A_TILE + oa) >> 4),
+             db + (static_cast<uint64_t>(tile * MP_B_TILE + ob) >> 4), idesc, kk > 0 ? 1u : 0u);
+    };
+    auto ts = [&](uint32_t d, uint32_t tile, int kk) {
+      const uint32_t ob = b_mn ? kk * 2048u : (kk >> 2) * b_chunk + (kk & 3) * 32u;
+      mma_ts(d, tmem + a_col + kk * 8, db + (static_cast<uint64_t>(tile * MP_B_TILE + ob) >> 4), idesc_ts,
+             kk > 0 ? 1u : 0u);
+    };
+    const long long t0 = clock64();
+    for (int r = 0; r < reps; ++r) {
+      const uint32_t tile = static_cast<uint32_t>(r & 1);
+      if (mode == 0) {
+        const uint32_t d = acc0 + static_cast<uint32_t>((r % n_buf) * n);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          if (a_tmem)
+            ts(d, tile, kk);
+          else
+            ss(d, tile, kk);
+        }
+      } else if (mode == 1) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          if (r & 1)
+            ts(acc0 + n, tile, kk);
+          else
+            ss(acc0, tile, kk);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          ss(acc0, tile, kk);
+          ss(acc0 + n, tile ^ 1u, kk);
+        }
+      }
+    }
+    const uint32_t mybar = smem_u32(bar + warp);
+    mma_commit(mybar);
+    wait_bar(mybar, 0, timeout_ns, abort_flag, 98);
+    out[blockIdx.x * 4 + warp] = static_cast<unsigned long long>(clock64() - t0);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_selftest_mma_pattern(int n, int a_tmem, int a_mn, int b_mn, int issuers, int mode, int reps,
+                                             int blocks, unsigned long long* cycles, void* stream) {
+  using namespace fa;
+  if (!cycles) return FA_ERR_INVALID_ARG;
+  if (!(n == 64 || n == 128 || n == 256) || issuers < 1 || issuers > 4 || mode < 0 || mode > 2 || reps < 1 ||
+      reps > (1 << 20) || blocks < 1 || blocks > 4096)
+    return FA_ERR_UNSUPPORTED;
+  if (a_tmem && a_mn) return FA_ERR_UNSUPPORTED;  // a TMEM operand has no major-ness choice
+  if (mode == 1 && !a_tmem) return FA_ERR_UNSUPPORTED;  // the TS products need the TMEM operand
+  // accumulators per issuer: mode 0 two where they fit (else one), modes 1 and 2 exactly two; all of
+  // them next to the TMEM A operand (columns 448..511) when there is one
+  const int room = a_tmem ? 448 : 512;
+  int n_buf = mode == 0 ? ((issuers * 2 * n <= room) ? 2 : 1) : 2;
+  if (issuers * n_buf * n > room) return FA_ERR_UNSUPPORTED;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(fa_mma_pattern_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MP_SMEM) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  fa_mma_pattern_kernel<<<blocks, 128, MP_SMEM, static_cast<cudaStream_t>(stream)>>>(
+      n, a_tmem ? 1 : 0, a_mn ? 1 : 0, b_mn ? 1 : 0, issuers, mode, n_buf, reps, cycles, 2000000000ull);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 // A wait that nothing completes: one thread waits on an mbarrier phase that no thread or copy will
 // ever finish. The bounded wait gives up after timeout_ns, records FA_DEV_TIMEOUT (where-code 90) in
 // this translation unit's status word and the kernel returns: nothing else is in flight, so the
