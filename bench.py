@@ -70,13 +70,29 @@ def parse():
     ap.add_argument("--sdpa", action="store_true",
                     help="context only: time torch's scaled_dot_product_attention (each backend that runs) "
                          "forward+backward on the headline workload, one JSON line")
+    ap.add_argument("--dq-mode", default="default", choices=["default", "accumulate", "separate"],
+                    help="how the backward forms dQ: the library's choice, fp32 partial tiles reduced into the "
+                         "workspace, or the separate query-major pass (d = 64, 128)")
     ap.add_argument("--shard", default="replicas", choices=["replicas", "heads"],
                     help="under torchrun: every rank runs the whole workload (replicas, weak scaling) or its "
                          "contiguous range of the job's B*H heads (heads, strong scaling, no data-path collective)")
+    ap.add_argument("--sweep-bf16", action="store_true", help="with --sweep: bf16 points only")
     ap.add_argument("--sweep", action="store_true",
                     help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
                          "instead of the headline step; one JSON line per point")
     return ap.parse_args()
+
+
+def dq_separate(L, mode, d, causal):
+    """Whether the backward forms dQ with the separate pass for this mode, head dimension and mask."""
+    opt = _lib_options(mode)
+    return bool(L.fa_bwd_uses_dq_pass(d, int(causal), ctypes.byref(opt)))
+
+
+def _lib_options(mode):
+    import tiled_attention_09_gb300 as fa
+    from tiled_attention_09_gb300 import _lib
+    return _lib.FAOptions(0, None, 0, fa.DQ_MODES[mode])
 
 
 def load_peaks():
@@ -365,30 +381,40 @@ def run_native(args):
     scale = w.scale
     DT = _lib.FA_BF16
 
+    opt = _lib.FAOptions(0, None, 0, fa.DQ_MODES[args.dq_mode])
+    optp = ctypes.byref(opt)
+    sep = dq_separate(L, args.dq_mode, d, True)
+
     def launch(ptrs, evs=None):
-        """One step through the public entry points (fa_fwd_ex, fa_bwd); evs: [start, end] events or None."""
+        """One step through the public entry points (fa_fwd_ex, fa_bwd_opt); evs: [start, end] events or None."""
         qp, kp, vp, op, lp, dop, dqp, dkp, dvp, lop = ptrs
         if evs:
             evs[0].record(stream)
         _lib.check("fa_fwd_ex", L.fa_fwd_ex(qp, kp, vp, op, lp, lop, B, H, N, d, scale, 1, DT, sp))
-        _lib.check("fa_bwd", L.fa_bwd(qp, kp, vp, op, dop, lp, dqp, dkp, dvp, lop, ws.data_ptr(), ws_bytes, B, H, N, d,
-                                      scale, 1, DT, sp))
+        _lib.check("fa_bwd_opt", L.fa_bwd_opt(qp, kp, vp, op, dop, lp, dqp, dkp, dvp, lop, ws.data_ptr(), ws_bytes, B,
+                                              H, N, d, scale, 1, DT, optp, sp))
         if evs:
             evs[1].record(stream)
 
     def launch_phases(ptrs, evs):
         """The same step as its four kernels with an event between each (per-kernel times; an event between
-        two kernels can keep the second from starting early, so this pass is not the step time)."""
+        two kernels can keep the second from starting early, so this pass is not the step time). The last
+        kernel is the dQ conversion, or the separate dQ pass."""
         qp, kp, vp, op, lp, dop, dqp, dkp, dvp, lop = ptrs
         evs[0].record(stream)
         _lib.check("fa_fwd_ex", L.fa_fwd_ex(qp, kp, vp, op, lp, lop, B, H, N, d, scale, 1, DT, sp))
         evs[1].record(stream)
-        _lib.check("pre", L.fa_bwd_preprocess(op, lop, dop, lp, ws.data_ptr(), ws_bytes, B, H, N, d, DT, sp))
+        _lib.check("pre", L.fa_bwd_preprocess_opt(op, lop, dop, lp, ws.data_ptr(), ws_bytes, B, H, N, d, 1, DT, optp,
+                                                  sp))
         evs[2].record(stream)
-        _lib.check("main", L.fa_bwd_main(qp, kp, vp, dop, dkp, dvp, None, ws.data_ptr(), ws_bytes, B, H, N, d, scale,
-                                         1, DT, sp))
+        _lib.check("main", L.fa_bwd_main_opt(qp, kp, vp, dop, dkp, dvp, None, ws.data_ptr(), ws_bytes, B, H, N, d,
+                                             scale, 1, DT, optp, sp))
         evs[3].record(stream)
-        _lib.check("conv", L.fa_bwd_dq_convert(dqp, ws.data_ptr(), ws_bytes, B, H, N, d, scale, DT, sp))
+        if sep:
+            _lib.check("dq", L.fa_bwd_dq_pass(qp, kp, vp, dop, dqp, ws.data_ptr(), ws_bytes, B, H, N, d, scale, 1, DT,
+                                              optp, sp))
+        else:
+            _lib.check("conv", L.fa_bwd_dq_convert(dqp, ws.data_ptr(), ws_bytes, B, H, N, d, scale, DT, sp))
         evs[4].record(stream)
 
     o_lo = torch.empty_like(qd)
@@ -471,7 +497,8 @@ def run_native(args):
         if started[b]:
             stream.wait_event(out_done[b])  # step i - 2's outputs have been read back
         fa.fwd(qi, ki, vi, causal=True, out=o_, lse=lse_, residual=True, o_lo=lo_)
-        fa.bwd(qi, ki, vi, o_, lse_, doi, causal=True, workspace=ws, dq=dq_, dk=dk_, dv=dv_, o_lo=lo_)
+        fa.bwd(qi, ki, vi, o_, lse_, doi, causal=True, workspace=ws, dq=dq_, dk=dk_, dv=dv_, o_lo=lo_,
+               dq_mode=args.dq_mode)
         comp_done[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -558,6 +585,7 @@ def run_native(args):
         "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name(), "B": B, "H": H, "N": N, "d": d, "causal": True, "seed": 0,
+                   "dq": "separate pass" if sep else "accumulated (bulk reductions)",
                    "l2": "flushed before every step (256 MiB write, then a 256 MiB read of another buffer so the write-back is not charged to the step; outside the timed interval)",
                    "timing": "value: whole step between two events; kernels_ms/roofline: a second pass of "
                              f"{K2} steps with events between kernels",
@@ -569,7 +597,8 @@ def run_native(args):
         "published_peak_source": "NVIDIA's GB300 dense bf16 tensor-core figure, 2.25 PFLOP/s per GPU (its "
                                  "larger per-system figures assume 2:4 sparsity)",
         "kernels_ms": {"fa_fwd_kernel": 1e3 * fwd_avg, "fa_bwd_preprocess_kernel": 1e3 * t_pre,
-                       roof_kernel: 1e3 * main_avg, "fa_bwd_dq_convert_kernel": 1e3 * t_conv},
+                       roof_kernel: 1e3 * main_avg,
+                       ("fa_bwd_dq_kernel" if sep else "fa_bwd_dq_convert_kernel"): 1e3 * t_conv},
         "fwd_tflops": F / fwd_avg / 1e12,
         "bwd_tflops": 2.5 * F / (t_pre + t_main + t_conv) / 1e12,
         "roofline": {"kernel": roof_kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
@@ -599,15 +628,18 @@ def run_sweep(args):
     import torch
     import tiled_attention_09_gb300 as fa
     from tiled_attention_09_gb300.inputs import Workload, cast_inputs, make_inputs_fp32
+    from tiled_attention_09_gb300 import _lib
+    L = _lib.load()
     peaks, peak_src = load_peaks()
     peak, bw = peaks["bf16_tflops"], peaks["hbm_gbs"]
     dev = torch.device("cuda", 0)
     flush = L2Flush(torch, dev)
     steps, warmup = max(3, min(args.steps, 20)), max(3, args.warmup)
+    dtypes = ("bf16",) if args.sweep_bf16 else ("bf16", "fp16")
     for d in (64, 128, 256):
         for N in (512, 1024, 2048, 4096, 8192, 16384):
             fp32 = make_inputs_fp32(Workload(2, 12, N, d, "bf16", True))
-            for dtype in ("bf16", "fp16"):
+            for dtype in dtypes:
                 for causal in (True, False):
                     w = Workload(2, 12, N, d, dtype, causal)
                     q, k, v, do = (t.to(dev) for t in cast_inputs(w, fp32))
@@ -618,12 +650,18 @@ def run_sweep(args):
                     def fwd():
                         fa.fwd(q, k, v, causal=causal, out=o, lse=lse, residual=True, o_lo=o_lo)
 
-                    def step():
+                    def step(mode):
                         fwd()
-                        fa.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws, dq=dq, dk=dk, dv=dv, o_lo=o_lo)
+                        fa.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws, dq=dq, dk=dk, dv=dv, o_lo=o_lo,
+                               dq_mode=mode)
 
+                    # both ways of forming dQ where the separate pass exists (d = 64, 128); the point's
+                    # fwd_bwd is the library's default choice
+                    modes = ("accumulate", "separate") if d in (64, 128) else ("accumulate",)
+                    default = "separate" if dq_separate(L, "default", d, causal) else "accumulate"
                     times = {}
-                    for name, fn in (("fwd", fwd), ("fwd_bwd", step)):
+                    fns = [("fwd", fwd)] + [(f"fwd_bwd_{m}", (lambda m=m: step(m))) for m in modes]
+                    for name, fn in fns:
                         for _ in range(warmup):
                             flush()
                             fn()
@@ -643,8 +681,11 @@ def run_sweep(args):
                     heads = w.B * w.H
                     bytes_fwd = heads * (4 * N * d * 2 + 4 * N)  # Q, K, V in, O out; LSE
                     bytes_bwd = heads * (8 * N * d * 2 + 8 * N)  # Q, K, V, dO in; dQ, dK, dV out (+ O); LSE, D
-                    line = {"point": w.name(), "N": N, "d": d, "dtype": dtype, "causal": causal}
-                    for name, flops, nbytes in (("fwd", F, bytes_fwd), ("fwd_bwd", 3.5 * F, bytes_fwd + bytes_bwd)):
+                    line = {"point": w.name(), "N": N, "d": d, "dtype": dtype, "causal": causal, "dq_default": default}
+                    times["fwd_bwd"] = times[f"fwd_bwd_{default}"]
+                    for name, flops, nbytes in [("fwd", F, bytes_fwd)] + [
+                            (f"fwd_bwd{x}", 3.5 * F, bytes_fwd + bytes_bwd)
+                            for x in [""] + [f"_{m}" for m in modes]]:
                         tf = flops / times[name] / 1e12
                         attainable = min(peak, bw * 1e9 * flops / nbytes / 1e12)
                         line[name] = {"ms": 1e3 * times[name], "tflops": tf, "pct_of_peak": tf / peak,

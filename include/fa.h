@@ -112,11 +112,27 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
  *    the backward reads it so), the mixed-precision output of page
  *    "在TPU上移植Flash Attention的工程实践与挑战", Example 3 (16-bit inputs and
  *    products, fp32 result). o_lo must then be NULL (FA_ERR_INVALID_ARG).
+ *  - dq_mode (backward only): how dQ = scale * dS K is formed (page
+ *    "transformer模型详解（十）：FlashAttention优化技术", section "Re-computation
+ *    而非缓存", accumulates dq across the K/V block loop).
+ *      FA_DQ_ACCUMULATE: the key-major main kernel adds fp32 partial tiles into
+ *        the workspace's dQ accumulator (bulk reductions), and a conversion pass
+ *        scales and rounds it; dq's summation order depends on scheduling.
+ *      FA_DQ_SEPARATE: the main kernel computes dK, dV only; a query-major pass
+ *        recomputes S and dP per 128 x 128 tile and keeps dQ in tensor memory
+ *        (no accumulator, no zeroing, dq bitwise reproducible); d = 64 and 128
+ *        only (else FA_ERR_UNSUPPORTED).
+ *      FA_DQ_DEFAULT (0): the library picks the faster of the two for the
+ *        head dimension and mask, as measured on GB300 (the table is in the
+ *        design notes).
+ *    Other values: FA_ERR_INVALID_ARG.
  */
+enum { FA_DQ_DEFAULT = 0, FA_DQ_ACCUMULATE = 1, FA_DQ_SEPARATE = 2 };
 typedef struct fa_options {
   int n_kv_heads;
   const int* kv_len;
   int o_fp32;
+  int dq_mode;
 } fa_options;
 
 /* Forward with options: arguments and results as fa_fwd_ex, k and v with
@@ -125,10 +141,36 @@ fa_status fa_fwd_opt(const void* q, const void* k, const void* v, void* o, float
                      int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt, void* stream);
 
 /*
+ * Forward with the key range of each query block split over several CTAs
+ * (page "transformer模型详解（十）：FlashAttention优化技术", section "Tiling
+ * 分块策略": the running max and sum of the online softmax are updated block by
+ * block, so disjoint key ranges can be reduced apart and joined afterwards).
+ * Each of the kv_splits ranges writes a normalised fp32 partial O_s and LSE_s
+ * to the workspace; a second launch joins them, LSE = ln sum_s e^(LSE_s),
+ * O = sum_s e^(LSE_s - LSE) O_s, and writes o (with o_lo when given, or fp32
+ * with opt->o_fp32) and lse, with the same meaning as fa_fwd_opt. It pays where
+ * the grid would otherwise leave SMs idle (few heads, short sequences).
+ *  - kv_splits: 1 = no split (exactly fa_fwd_opt; workspace unused); 2..16 =
+ *    that many ranges; 0 = the library's choice, fa_fwd_kv_splits(); above 16:
+ *    FA_ERR_UNSUPPORTED.
+ *  - workspace: device memory of fa_fwd_workspace_size(B,H,N,d,kv_splits)
+ *    bytes, 256-byte aligned, caller-owned (contents on entry do not matter);
+ *    may be NULL when kv_splits resolves to 1.
+ * fa_fwd_workspace_size returns 0 for kv_splits < 2 (no workspace) and for
+ * unsupported shapes.
+ */
+fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H,
+                       int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt, int kv_splits,
+                       void* workspace, size_t workspace_bytes, void* stream);
+int fa_fwd_kv_splits(int B, int H, int N, int d, int causal);
+size_t fa_fwd_workspace_size(int B, int H, int N, int d, int kv_splits);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 D [B,H,Np], fp32 LSE*log2(e)
  * [B,H,Np] and the fp32 dQ accumulator [B,H,Np,d], each 256-byte aligned,
- * with Np = N rounded up to 64 (each head's rows padded so that every
- * 64-query step of the main kernel starts aligned and stays in its head).
+ * with Np = N rounded up to 128 (each head's rows padded so that every query
+ * step or tile of the backward starts aligned and stays in its head). The
+ * separate dQ pass leaves the accumulator untouched.
  * Returns 0 for unsupported shapes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -212,6 +254,30 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* d
                       fa_dtype dtype, void* stream);
 fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                             float scale, fa_dtype dtype, void* stream);
+
+/*
+ * The phases with options (opt as for fa_bwd_opt; NULL = defaults). With the
+ * separate dQ pass (opt->dq_mode, or the library's choice): fa_bwd_preprocess_opt
+ * does not zero the dQ accumulator; fa_bwd_main_opt computes dK and dV only and,
+ * given dq, enqueues fa_bwd_dq_pass right after; fa_bwd_dq_pass is that pass on
+ * its own: it reads D and LSE*log2e from the workspace (written by the
+ * preprocess of the same call sequence) and writes dq [B,H,N,d] in full.
+ * fa_bwd_opt is fa_bwd_preprocess_opt then fa_bwd_main_opt with dq given.
+ */
+fa_status fa_bwd_preprocess_opt(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
+                                size_t workspace_bytes, int B, int H, int N, int d, int causal, fa_dtype dtype,
+                                const fa_options* opt, void* stream);
+fa_status fa_bwd_main_opt(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, void* dq,
+                          void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                          fa_dtype dtype, const fa_options* opt, void* stream);
+fa_status fa_bwd_dq_pass(const void* q, const void* k, const void* v, const void* dO, void* dq, void* workspace,
+                         size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                         const fa_options* opt, void* stream);
+
+/* 1 if a backward with this head dimension, mask and options forms dQ with
+ * the separate pass (then dq is bitwise reproducible), 0 if it accumulates it
+ * (or the combination is not supported). opt may be NULL. */
+int fa_bwd_uses_dq_pass(int d, int causal, const fa_options* opt);
 
 /*
  * Paged decode attention: Mq new queries per sequence attend to the sequence's

@@ -70,7 +70,7 @@ def test_status_strings_and_version(L):
     for code, name in _lib.STATUS_NAMES.items():
         assert L.fa_status_string(code).decode() == name
     assert L.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert L.fa_version() == 101
+    assert L.fa_version() == 102
 
 
 def test_workspace_size(L):
@@ -196,3 +196,21 @@ def test_decode_rejects_bad_arguments(L, kw, code):
     assert L.fa_decode(V(a["q"]), V(a["kp"]), V(a["vp"]), V(a["page_table"]), V(a["ctx_len"]), V(a["o"]), V(a["lse"]),
                        V(a["ws"]), a["ws_bytes"], a["B"], a["H"], a["Hkv"], a["Mq"], a["d"], a["page_size"],
                        a["n_pages"], a["max_pages"], a["n_split"], a["scale"], a["causal"], a["dtype"], None) == code
+
+
+def test_split_forward_workspace_and_choice(L):
+    """Host-side sizing of the split-key forward: partial O [S][B*H*N][d] and LSE [S][B*H*N], fp32, each
+    256-byte aligned; none for one range; the library splits only grids of fewer than two CTAs per SM."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    B, H, N, d, S = 2, 3, 300, 128, 4
+    rows = B * H * N * S
+    assert L.fa_fwd_workspace_size(B, H, N, d, S) == r256(rows * d * 4) + r256(rows * 4)
+    assert L.fa_fwd_workspace_size(B, H, N, d, 1) == 0 and L.fa_fwd_workspace_size(B, H, N, d, 17) == 0
+    assert L.fa_fwd_workspace_size(1, 1, 0, 64, 2) == 0
+    assert L.fa_fwd_kv_splits(2, 12, 4096, 128, 1) == 1  # 384 CTAs already
+    assert L.fa_fwd_kv_splits(1, 2, 1024, 128, 1) > 1     # 8 CTAs
+    assert L.fa_fwd_kv_splits(1, 1, 128, 64, 0) == 1      # one key tile: nothing to split
+    for args in ((1, 2, 1024, 128, 1), (1, 4, 8192, 64, 0), (4, 8, 2048, 256, 1)):
+        s = L.fa_fwd_kv_splits(*args)
+        assert 1 <= s <= 16 and (s & (s - 1)) == 0
+

@@ -89,13 +89,19 @@ def _check_workspace(t: torch.Tensor, need: int, device) -> int:
     return nbytes
 
 
-def _options(B, H, Hkv, kv_len, out_fp32, device):
+DQ_MODES = {"default": 0, "accumulate": 1, "separate": 2}
+
+
+def _options(B, H, Hkv, kv_len, out_fp32, device, dq_mode="default"):
     """fa_options for the call, or None when every option has its default."""
-    if Hkv == H and kv_len is None and not out_fp32:
+    if dq_mode not in DQ_MODES:
+        raise ValueError(f"dq_mode must be one of {sorted(DQ_MODES)}")
+    if Hkv == H and kv_len is None and not out_fp32 and dq_mode == "default":
         return None
     if kv_len is not None:
         _check_buf(kv_len, (B,), torch.int32, device, "kv_len")
-    return _lib.FAOptions(Hkv, kv_len.data_ptr() if kv_len is not None else None, int(bool(out_fp32)))
+    return _lib.FAOptions(Hkv, kv_len.data_ptr() if kv_len is not None else None, int(bool(out_fp32)),
+                          DQ_MODES[dq_mode])
 
 
 def device_status(stream=None):
@@ -119,13 +125,15 @@ def workspace_size(B, H, N, d) -> int:
 
 
 def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, residual=False, o_lo=None, kv_len=None,
-        out_fp32=False):
+        out_fp32=False, kv_splits=1, workspace=None):
     """Forward: returns (o, lse), or (o, lse, o_lo) with residual=True (fa_fwd_ex / fa_fwd_opt).
 
     o_lo is the rounding residual of o (O_fp32 - o in the same dtype); pass it
     to ``bwd`` so that D = rowsum(dO * O) uses O at fp32 accuracy. k, v may have
     fewer heads than q; kv_len masks keys per batch; out_fp32 writes o as fp32
-    (no residual then).
+    (no residual then). kv_splits > 1 splits each query block's key range over
+    that many CTAs, joined by a merge launch (fa_fwd_split; 0 = the library's
+    choice); workspace: optional caller buffer for the partial outputs.
     """
     Hkv = _check_kv(q, k, v)
     B, H, N, d = q.shape
@@ -151,7 +159,17 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, residual=False, o
     opt = _options(B, H, Hkv, kv_len, out_fp32, q.device)
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
             o_lo.data_ptr() if residual else None, B, H, N, d, scale, int(bool(causal)), _DT[q.dtype])
-    if opt is None:
+    splits = int(kv_splits) if kv_splits else int(L.fa_fwd_kv_splits(B, H, N, d, int(bool(causal))))
+    if splits > 1:
+        ws_bytes = int(L.fa_fwd_workspace_size(B, H, N, d, splits))
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+        else:
+            ws_bytes = _check_workspace(workspace, ws_bytes, q.device)
+        opt = opt if opt is not None else _lib.FAOptions(0, None, 0, 0)
+        name, code = "fa_fwd_split", L.fa_fwd_split(*args, ctypes.byref(opt), splits, workspace.data_ptr(), ws_bytes,
+                                                     _stream_ptr(q))
+    elif opt is None:
         name, code = "fa_fwd_ex", L.fa_fwd_ex(*args, _stream_ptr(q))
     else:
         name, code = "fa_fwd_opt", L.fa_fwd_opt(*args, ctypes.byref(opt), _stream_ptr(q))
@@ -161,10 +179,12 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, residual=False, o
 
 
 def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None, o_lo=None,
-        kv_len=None):
+        kv_len=None, dq_mode="default"):
     """Backward: returns (dq, dk, dv). o_lo: the residual from ``fwd(..., residual=True)``, or None.
 
     k, v (and dk, dv) may have fewer heads than q; kv_len as given to ``fwd``; o may be fp32.
+    dq_mode: "accumulate" (fp32 partial tiles reduced into the workspace), "separate" (a query-major
+    pass that keeps dQ in tensor memory; d = 64 and 128) or "default" (the library's choice).
     """
     Hkv = _check_kv(q, k, v)
     _check_qkv(q, do)
@@ -194,7 +214,7 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o_lo.data_ptr() if o_lo is not None else None,
             workspace.data_ptr(), ws_bytes, B, H, N, d, scale, int(bool(causal)), _DT[q.dtype])
-    opt = _options(B, H, Hkv, kv_len, out_fp32, q.device)
+    opt = _options(B, H, Hkv, kv_len, out_fp32, q.device, dq_mode)
     if opt is None:
         name, code = "fa_bwd", L.fa_bwd(*args, _stream_ptr(q))
     else:

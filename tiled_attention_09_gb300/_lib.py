@@ -28,7 +28,7 @@ FA_F16, FA_BF16 = 0, 1
 
 class FAOptions(ctypes.Structure):
     """struct fa_options of include/fa.h."""
-    _fields_ = [("n_kv_heads", c_int), ("kv_len", c_void_p), ("o_fp32", c_int)]
+    _fields_ = [("n_kv_heads", c_int), ("kv_len", c_void_p), ("o_fp32", c_int), ("dq_mode", c_int)]
 
 
 # (name, restype, argtypes) for every symbol declared in include/fa.h and include/fa_selftest.h
@@ -39,6 +39,10 @@ SIGNATURES = [
     ("fa_fwd_opt", c_int, [c_void_p] * 6 + [c_int, c_int, c_int, c_int, c_float, c_int, c_int,
                                             ctypes.POINTER(FAOptions), c_void_p]),
     ("fa_bwd_workspace_size", c_size_t, [c_int, c_int, c_int, c_int]),
+    ("fa_fwd_split", c_int, [c_void_p] * 6 + [c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                              ctypes.POINTER(FAOptions), c_int, c_void_p, c_size_t, c_void_p]),
+    ("fa_fwd_kv_splits", c_int, [c_int] * 5),
+    ("fa_fwd_workspace_size", c_size_t, [c_int] * 5),
     ("fa_bwd", c_int, [c_void_p] * 10 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
                                          c_void_p]),
     ("fa_bwd_opt", c_int, [c_void_p] * 10 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
@@ -49,6 +53,13 @@ SIGNATURES = [
                                              c_void_p]),
     ("fa_bwd_dq_convert", c_int, [c_void_p, c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int,
                                   c_void_p]),
+    ("fa_bwd_preprocess_opt", c_int, [c_void_p] * 5 + [c_size_t] + [c_int] * 6 + [ctypes.POINTER(FAOptions),
+                                                                                 c_void_p]),
+    ("fa_bwd_main_opt", c_int, [c_void_p] * 7 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int,
+                                                 c_int, ctypes.POINTER(FAOptions), c_void_p]),
+    ("fa_bwd_uses_dq_pass", c_int, [c_int, c_int, ctypes.POINTER(FAOptions)]),
+    ("fa_bwd_dq_pass", c_int, [c_void_p] * 6 + [c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                                ctypes.POINTER(FAOptions), c_void_p]),
     ("fa_decode_splits", c_int, [c_int] * 5),
     ("fa_decode_workspace_size", c_size_t, [c_int] * 8),
     ("fa_decode", c_int, [c_void_p] * 7 + [c_void_p, c_size_t] + [c_int] * 9 + [c_float, c_int, c_int, c_void_p]),

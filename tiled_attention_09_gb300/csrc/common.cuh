@@ -35,15 +35,18 @@ __device__ __forceinline__ void report_status(uint32_t code, uint32_t where) {
 
 // Wait until the phase with the given parity of mbarrier `bar` has completed.
 // Returns false (after recording a timeout, or seeing another role's abort) if
-// it did not complete before `timeout_ns`.
+// it did not complete before `timeout_ns`. After one immediate test the thread
+// sleeps in the barrier (up to kWaitSleepNs per try, woken when the phase
+// completes) instead of spinning, so waiting warps do not take issue slots from
+// the warps they share a sub-partition with; the abort flag and the deadline are
+// checked between tries.
+constexpr uint32_t kWaitSleepNs = 200000;
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                          volatile uint32_t* abort_flag, uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       report_status(FA_DEV_TIMEOUT, where);

@@ -194,6 +194,32 @@ fa_status check_device() {
 }
 
 constexpr int kMaxKeyBlocks = 65535;
+constexpr int kMaxKvSplits = 16;
+
+// Split-key forward: partial outputs [S][B*H*N][d] fp32 and their LSEs [S][B*H*N], each 256-byte aligned.
+struct FwdWs {
+  size_t off_o, off_lse, total;
+};
+FwdWs fwd_ws(int B, int H, int N, int d, int S) {
+  const size_t rows = static_cast<size_t>(B) * H * N * S;
+  FwdWs w;
+  w.off_o = 0;
+  w.off_lse = (rows * d * 4 + 255) & ~size_t(255);
+  w.total = w.off_lse + ((rows * 4 + 255) & ~size_t(255));
+  return w;
+}
+
+// The library's split count: one CTA per (query block, key range) and 152 SMs; split the key range
+// only while the grid has fewer than two CTAs per SM, and keep at least two key tiles per range
+// (about one, on average, under a causal mask).
+int fwd_kv_splits(int B, int H, int N, int d, bool causal) {
+  const long long qblk_rows = d <= 128 ? 256 : 128;
+  const long long items = static_cast<long long>(B) * H * ((N + qblk_rows - 1) / qblk_rows);
+  const long long key_tiles = (N + 127) / 128;
+  int s = 1;
+  while (s < kMaxKvSplits && items * s < 2 * 152 && (causal ? key_tiles : 2 * key_tiles) >= 4 * s) s *= 2;
+  return s;
+}
 
 fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype) {
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
@@ -216,10 +242,11 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t off_D, off_lse2, off_dq, total;
 };
-// Each head's rows are padded to Npad = N rounded up to 64: every 64-query step of the backward
-// then starts 256-byte aligned (bulk copies need 16) and the last, partial step of a sequence
-// reads LSE*log2e and D of its own (zeroed, masked) padding rows and adds zero dQ partials there.
-int pad_rows(int N) { return (N + 63) / 64 * 64; }
+// Each head's rows are padded to Npad = N rounded up to 128: every 64-query step of the main
+// kernel and every 128-row query tile of the separate dQ pass then starts 256-byte aligned (bulk
+// copies need 16) and stays in its head; the last, partial step or tile of a sequence reads
+// LSE*log2e and D of its own (zeroed, masked) padding rows and adds zero dQ partials there.
+int pad_rows(int N) { return (N + 127) / 128 * 128; }
 WsLayout ws_layout(int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * pad_rows(N);
   WsLayout w;
@@ -230,17 +257,22 @@ WsLayout ws_layout(int B, int H, int N, int d) {
   return w;
 }
 
-// Options resolved against the shape: K/V heads (0 = H, must divide H), key counts, fp32 O.
+// Options resolved against the shape: K/V heads (0 = H, must divide H), key counts, fp32 O, how dQ
+// is computed.
 struct Opts {
   int Hkv;
   const int* kv_len;
   bool o_f32;
+  int dq_mode;  // FA_DQ_DEFAULT, FA_DQ_ACCUMULATE or FA_DQ_SEPARATE
 };
 fa_status resolve_opts(const fa_options* opt, int H, const void* o_lo, Opts* out) {
   out->Hkv = H;
   out->kv_len = nullptr;
   out->o_f32 = false;
+  out->dq_mode = FA_DQ_DEFAULT;
   if (!opt) return FA_OK;
+  if (opt->dq_mode < FA_DQ_DEFAULT || opt->dq_mode > FA_DQ_SEPARATE) return FA_ERR_INVALID_ARG;
+  out->dq_mode = opt->dq_mode;
   if (opt->n_kv_heads < 0) return FA_ERR_INVALID_ARG;
   if (opt->n_kv_heads > 0) {
     if (H % opt->n_kv_heads != 0) return FA_ERR_UNSUPPORTED;
@@ -250,6 +282,23 @@ fa_status resolve_opts(const fa_options* opt, int H, const void* o_lo, Opts* out
   out->kv_len = opt->kv_len;
   out->o_f32 = opt->o_fp32 != 0;
   if (out->o_f32 && o_lo) return FA_ERR_INVALID_ARG;  // the residual belongs to a 16-bit O
+  return FA_OK;
+}
+
+// Whether dQ comes from the separate query-major pass: asked for explicitly (d = 64 or 128 only), or
+// the library's choice, which follows the measured speed of the two paths per (d, mask).
+fa_status dq_pass_for(const Opts& op, int d, bool causal, bool* out) {
+  if (op.dq_mode == FA_DQ_SEPARATE) {
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    *out = true;
+    return FA_OK;
+  }
+  if (op.dq_mode == FA_DQ_ACCUMULATE || d == 256) {
+    *out = false;
+    return FA_OK;
+  }
+  (void)causal;
+  *out = false;
   return FA_OK;
 }
 
@@ -280,14 +329,15 @@ fa_status bwd_common(fa::BwdArgs* a, void* workspace, size_t workspace_bytes, in
 }
 
 fa_status bwd_preprocess_impl(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
-                              size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, const Opts& op,
-                              void* stream) {
+                              size_t workspace_bytes, int B, int H, int N, int d, int causal, fa_dtype dtype,
+                              const Opts& op, void* stream) {
   if (!o || !dO || !lse) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a{};
   fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, 1.0f, 0, dtype, stream);
   if (s != FA_OK) return s;
   if (!aligned16(o) || !aligned16(o_lo) || !aligned16(dO) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
+  if ((s = dq_pass_for(op, d, causal, &a.dq_pass)) != FA_OK) return s;
   a.o = o;
   a.o_lo = o_lo;
   a.o_f32 = op.o_f32;
@@ -307,6 +357,7 @@ fa_status bwd_main_impl(const void* q, const void* k, const void* v, const void*
       !aligned16(dq))
     return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
+  if ((s = dq_pass_for(op, d, causal != 0, &a.dq_pass)) != FA_OK) return s;
   const int bq = fa::bwd_query_tile(d);
   if (bq == 0) return FA_ERR_UNSUPPORTED;
   const long long heads = static_cast<long long>(B) * H, kv_heads = static_cast<long long>(B) * op.Hkv;
@@ -319,15 +370,37 @@ fa_status bwd_main_impl(const void* q, const void* k, const void* v, const void*
   a.dO = dO;
   a.dk = dk;
   a.dv = dv;
-  a.dq = dq;  // optional: when given, the dQ conversion is enqueued right after the main kernel
+  a.dq = dq;  // optional: when given, the dQ conversion (or the dQ pass) is enqueued right after the main kernel
   return fa::launch_bwd_main(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status bwd_dq_pass_impl(const void* q, const void* k, const void* v, const void* dO, void* dq, void* workspace,
+                           size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                           const Opts& op, void* stream) {
+  if (!q || !k || !v || !dO || !dq) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  fa::BwdArgs a{};
+  fa_status s = bwd_common(&a, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream);
+  if (s != FA_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq)) return FA_ERR_ALIGNMENT;
+  if ((s = check_device()) != FA_OK) return s;
+  const long long heads = static_cast<long long>(B) * H, kv_heads = static_cast<long long>(B) * op.Hkv;
+  const int bq = fa::bwd_query_tile(d);
+  if (!make_map(&a.tm_q, q, heads, N, d, a.bf16, bq) || !make_map(&a.tm_do, dO, heads, N, d, a.bf16, bq) ||
+      !make_map(&a.tm_k, k, kv_heads, N, d, a.bf16, 128) || !make_map(&a.tm_v, v, kv_heads, N, d, a.bf16, 128))
+    return FA_ERR_CUDA;
+  a.Hkv = op.Hkv;
+  a.kv_len = op.kv_len;
+  a.dq_pass = true;
+  a.dq = dq;
+  return fa::launch_bwd_dq_pass(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
 
 extern "C" {
 
-int fa_version(void) { return 101; }
+int fa_version(void) { return 102; }
 
 void fa_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns ? ns : 4000000000ull; }
 
@@ -357,6 +430,22 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
 fa_status fa_fwd_opt(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H,
                      int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt, void* stream) {
+  return fa_fwd_split(q, k, v, o, lse, o_lo, B, H, N, d, scale, causal, dtype, opt, 1, nullptr, 0, stream);
+}
+
+int fa_fwd_kv_splits(int B, int H, int N, int d, int causal) {
+  if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
+  return fwd_kv_splits(B, H, N, d, causal != 0);
+}
+
+size_t fa_fwd_workspace_size(int B, int H, int N, int d, int kv_splits) {
+  if (check_shape(B, H, N, d, FA_BF16) != FA_OK || kv_splits < 2 || kv_splits > kMaxKvSplits) return 0;
+  return fwd_ws(B, H, N, d, kv_splits).total;
+}
+
+fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H,
+                       int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt, int kv_splits,
+                       void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   fa_status s = check_shape(B, H, N, d, dtype);
   if (s != FA_OK) return s;
@@ -372,6 +461,19 @@ fa_status fa_fwd_opt(const void* q, const void* k, const void* v, void* o, float
   if (!make_map(&a.tm_q, q, heads, N, d, bf16, 128) || !make_map(&a.tm_k, k, kv_heads, N, d, bf16, 128) ||
       !make_map(&a.tm_v, v, kv_heads, N, d, bf16, 128))
     return FA_ERR_CUDA;
+  if (kv_splits <= 0) kv_splits = fwd_kv_splits(B, H, N, d, causal != 0);
+  if (kv_splits > kMaxKvSplits) return FA_ERR_UNSUPPORTED;
+  a.kv_splits = kv_splits;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
+  if (kv_splits > 1) {
+    const FwdWs w = fwd_ws(B, H, N, d, kv_splits);
+    if (!workspace) return FA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
+    if (workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+    a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_o);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse);
+  }
   a.o = o;
   a.lse = lse;
   a.o_lo = o_lo;
@@ -397,15 +499,51 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 fa_status fa_bwd_preprocess(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
                             size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream) {
-  return bwd_preprocess_impl(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, Opts{H, nullptr, false},
-                             stream);
+  return bwd_preprocess_impl(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, 0, dtype,
+                             Opts{H, nullptr, false, FA_DQ_ACCUMULATE}, stream);
+}
+
+fa_status fa_bwd_preprocess_opt(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
+                                size_t workspace_bytes, int B, int H, int N, int d, int causal, fa_dtype dtype,
+                                const fa_options* opt, void* stream) {
+  Opts op;
+  fa_status s = resolve_opts(opt, H, o_lo, &op);
+  if (s != FA_OK) return s;
+  return bwd_preprocess_impl(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, causal, dtype, op, stream);
 }
 
 fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, void* dq,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                       fa_dtype dtype, void* stream) {
   return bwd_main_impl(q, k, v, dO, dk, dv, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype,
-                       Opts{H, nullptr, false}, stream);
+                       Opts{H, nullptr, false, FA_DQ_ACCUMULATE}, stream);
+}
+
+fa_status fa_bwd_main_opt(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, void* dq,
+                          void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                          fa_dtype dtype, const fa_options* opt, void* stream) {
+  Opts op;
+  fa_status s = resolve_opts(opt, H, nullptr, &op);
+  if (s != FA_OK) return s;
+  return bwd_main_impl(q, k, v, dO, dk, dv, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, op,
+                       stream);
+}
+
+int fa_bwd_uses_dq_pass(int d, int causal, const fa_options* opt) {
+  Opts op{1, nullptr, false, opt ? opt->dq_mode : FA_DQ_DEFAULT};
+  if (op.dq_mode < FA_DQ_DEFAULT || op.dq_mode > FA_DQ_SEPARATE) return 0;
+  bool pass = false;
+  if (dq_pass_for(op, d, causal != 0, &pass) != FA_OK) return 0;
+  return pass ? 1 : 0;
+}
+
+fa_status fa_bwd_dq_pass(const void* q, const void* k, const void* v, const void* dO, void* dq, void* workspace,
+                         size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                         const fa_options* opt, void* stream) {
+  Opts op;
+  fa_status s = resolve_opts(opt, H, nullptr, &op);
+  if (s != FA_OK) return s;
+  return bwd_dq_pass_impl(q, k, v, dO, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, op, stream);
 }
 
 fa_status fa_bwd_dq_convert(void* dq, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
@@ -443,7 +581,10 @@ fa_status fa_bwd_opt(const void* q, const void* k, const void* v, const void* o,
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(o_lo))
     return FA_ERR_ALIGNMENT;
   if ((s = check_device()) != FA_OK) return s;
-  if ((s = bwd_preprocess_impl(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, dtype, op, stream)) != FA_OK)
+  bool dq_pass = false;
+  if ((s = dq_pass_for(op, d, causal != 0, &dq_pass)) != FA_OK) return s;
+  if ((s = bwd_preprocess_impl(o, o_lo, dO, lse, workspace, workspace_bytes, B, H, N, d, causal, dtype, op, stream)) !=
+      FA_OK)
     return s;
   // given dq, the main kernel's launch enqueues the dQ conversion right after it
   return bwd_main_impl(q, k, v, dO, dk, dv, dq, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, op,

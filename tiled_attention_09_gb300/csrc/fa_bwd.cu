@@ -6,6 +6,7 @@
 #include "fa_bwd_main.cuh"
 #include "fa_bwd_d256.cuh"
 #include "fa_bwd_pipe.cuh"
+#include "fa_bwd_dq.cuh"
 #include "launch.h"
 
 namespace fa {
@@ -20,15 +21,16 @@ int grid_for(size_t n_vec) {
 template <int VPR>
 cudaError_t launch_pre_t(const BwdArgs& a) {
   const size_t n_vec_pad = static_cast<size_t>(a.B) * a.H * a.Npad * VPR;
+  float4* dqacc = a.dq_pass ? nullptr : reinterpret_cast<float4*>(a.ws_dqacc);  // the pass needs no accumulator
   if (a.bf16)
     return launch_kernel(fa_bwd_preprocess_kernel<VPR, true>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
                          static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
                          a.o_f32 ? static_cast<const float4*>(a.o) : nullptr, static_cast<const uint4*>(a.dO),
-                         a.lse, a.ws_D, a.ws_lse2, reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
+                         a.lse, a.ws_D, a.ws_lse2, dqacc, a.N, a.Npad, n_vec_pad);
   return launch_kernel(fa_bwd_preprocess_kernel<VPR, false>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
                        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
                        a.o_f32 ? static_cast<const float4*>(a.o) : nullptr, static_cast<const uint4*>(a.dO),
-                       a.lse, a.ws_D, a.ws_lse2, reinterpret_cast<float4*>(a.ws_dqacc), a.N, a.Npad, n_vec_pad);
+                       a.lse, a.ws_D, a.ws_lse2, dqacc, a.N, a.Npad, n_vec_pad);
 }
 template <int VPR>
 cudaError_t launch_convert_t(const BwdArgs& a) {
@@ -74,6 +76,7 @@ BwdParams bwd_params(const BwdArgs& a) {
   p.lse2 = a.ws_lse2;
   p.Dvec = a.ws_D;
   p.dqacc = a.ws_dqacc;
+  p.dq = a.dq;
   p.dk = a.dk;
   p.dv = a.dv;
   p.kv_len = a.kv_len;
@@ -88,9 +91,21 @@ BwdParams bwd_params(const BwdArgs& a) {
 }
 
 template <int D, bool BF16, bool CAUSAL, bool GRP>
+cudaError_t launch_dq_t(const BwdArgs& a) {
+  using C = BwdDqCfg<D>;
+  auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL, GRP>;
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
+  const BwdParams p = bwd_params(a);
+  dim3 grid(a.B * a.H, (a.N + 127) / 128, 1);  // 128-row query tiles of each query head
+  return launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+}
+
+template <int D, bool BF16, bool CAUSAL, bool GRP, bool DQACC>
 cudaError_t launch_pipe_t(const BwdArgs& a) {
   using C = BwdPipeCfg<D>;
-  auto kern = fa_bwd_pipe_kernel<D, BF16, CAUSAL, GRP>;
+  auto kern = fa_bwd_pipe_kernel<D, BF16, CAUSAL, GRP, DQACC>;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
@@ -105,7 +120,7 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
   dim3 grid(a.B * a.Hkv, (a.N + 127) / 128, 1);  // key blocks of each K/V head; the last may run past N
   e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
-  return launch_bwd_dq_convert(a);
+  return DQACC ? launch_bwd_dq_convert(a) : launch_bwd_dq_pass(a);
 }
 template <bool BF16, bool CAUSAL>
 cudaError_t launch_d256_t(const BwdArgs& a) {
@@ -120,17 +135,39 @@ cudaError_t launch_d256_t(const BwdArgs& a) {
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return launch_bwd_dq_convert(a);
 }
-template <int D>
-cudaError_t launch_pipe_d(const BwdArgs& a) {
+template <int D, bool DQACC>
+cudaError_t launch_pipe_dm(const BwdArgs& a) {
   const bool grp = a.Hkv != a.H || a.kv_len != nullptr;  // the general form only where it is needed
   if (a.bf16) {
-    if (a.causal) return grp ? launch_pipe_t<D, true, true, true>(a) : launch_pipe_t<D, true, true, false>(a);
-    return grp ? launch_pipe_t<D, true, false, true>(a) : launch_pipe_t<D, true, false, false>(a);
+    if (a.causal)
+      return grp ? launch_pipe_t<D, true, true, true, DQACC>(a) : launch_pipe_t<D, true, true, false, DQACC>(a);
+    return grp ? launch_pipe_t<D, true, false, true, DQACC>(a) : launch_pipe_t<D, true, false, false, DQACC>(a);
   }
-  if (a.causal) return grp ? launch_pipe_t<D, false, true, true>(a) : launch_pipe_t<D, false, true, false>(a);
-  return grp ? launch_pipe_t<D, false, false, true>(a) : launch_pipe_t<D, false, false, false>(a);
+  if (a.causal)
+    return grp ? launch_pipe_t<D, false, true, true, DQACC>(a) : launch_pipe_t<D, false, true, false, DQACC>(a);
+  return grp ? launch_pipe_t<D, false, false, true, DQACC>(a) : launch_pipe_t<D, false, false, false, DQACC>(a);
+}
+template <int D>
+cudaError_t launch_pipe_d(const BwdArgs& a) {
+  return a.dq_pass ? launch_pipe_dm<D, false>(a) : launch_pipe_dm<D, true>(a);
+}
+template <int D>
+cudaError_t launch_dq_d(const BwdArgs& a) {
+  const bool grp = a.Hkv != a.H || a.kv_len != nullptr;
+  if (a.bf16) {
+    if (a.causal) return grp ? launch_dq_t<D, true, true, true>(a) : launch_dq_t<D, true, true, false>(a);
+    return grp ? launch_dq_t<D, true, false, true>(a) : launch_dq_t<D, true, false, false>(a);
+  }
+  if (a.causal) return grp ? launch_dq_t<D, false, true, true>(a) : launch_dq_t<D, false, true, false>(a);
+  return grp ? launch_dq_t<D, false, false, true>(a) : launch_dq_t<D, false, false, false>(a);
 }
 }  // namespace
+
+cudaError_t launch_bwd_dq_pass(const BwdArgs& a) {
+  if (a.d == 128) return launch_dq_d<128>(a);
+  if (a.d == 64) return launch_dq_d<64>(a);
+  return cudaErrorNotSupported;  // d = 256 accumulates dQ in its main kernel
+}
 
 cudaError_t launch_bwd_main(const BwdArgs& a) {
   if (a.d == 256) {  // head-dimension split: two passes per key block

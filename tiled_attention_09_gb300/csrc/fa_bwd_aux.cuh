@@ -1,7 +1,8 @@
 // Bandwidth-bound helper kernels of the backward pass (no tensor cores):
 //   K2 preprocess: D_i = sum_k dO_ik * O_ik (fp32; O = o + o_lo when the forward's rounding
 //                  residual o_lo is given, O read as fp32 when the forward wrote it so),
-//                  LSE_i * log2(e), dQ accumulator := 0 (padded rows)
+//                  LSE_i * log2(e), dQ accumulator := 0 (padded rows; not when dQ comes from
+//                  the separate pass, which needs no accumulator)
 //   K4 dQ convert: dQ = dtype(scale * dQacc)
 // Each thread owns one 16-byte vector (8 elements) of a row; the d/8 threads of
 // a row sit in one warp and reduce with shuffles. Grid-stride loops keep the
@@ -47,8 +48,8 @@ __device__ __forceinline__ uint32_t pack2f(float lo, float hi) {
 }
 
 // Workspace rows are padded per head: row (bh, r) of D, LSE*log2e and the dQ accumulator sits at
-// bh * Npad + r with Npad = N rounded up to 64, so every 64-query step of the backward starts
-// 256-byte aligned (a bulk copy needs 16) and stays inside its own head. Padding rows hold D = 0 and
+// bh * Npad + r with Npad = N rounded up to 128, so every query step (64 rows) or query tile (128
+// rows) of the backward starts 256-byte aligned (a bulk copy needs 16) and stays inside its own head. Padding rows hold D = 0 and
 // LSE*log2e = 0 (finite: a masked query still multiplies them by zero).
 // VPR = vectors (of 8 elements) per row = d / 8, a power of two <= 32.
 template <int VPR, bool BF16>
@@ -89,9 +90,11 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
     // every lane of a row's VPR-lane group takes the same branch (rows never straddle a group)
 #pragma unroll
     for (int off = VPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, VPR);
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    dqacc[2 * i] = z;
-    dqacc[2 * i + 1] = z;
+    if (dqacc) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      dqacc[2 * i] = z;
+      dqacc[2 * i + 1] = z;
+    }
     if ((i % VPR) == 0) {
       D[row_pad] = acc;
       lse2[row_pad] = real ? lse[row] * 1.4426950408889634f : 0.f;

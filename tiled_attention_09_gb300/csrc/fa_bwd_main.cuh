@@ -24,14 +24,15 @@ namespace fa {
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;
-  const float* lse2;  // [B*H*Npad] LSE * log2(e); row (bh, r) at bh * Npad + r
+  const float* lse2;  // [B*H*Npad] LSE * log2(e); row (bh, r) at bh * Npad + r (Npad = N rounded up to 128)
   const float* Dvec;  // [B*H*Npad] rowsum(dO * O), same rows
-  float* dqacc;       // [B*H*Npad, d] fp32, same rows
+  float* dqacc;       // [B*H*Npad, d] fp32, same rows (the accumulating dQ path)
+  void* dq;           // [B*H*N, d] dtype output, written directly by the separate dQ pass
   void* dk;           // [B*Hkv*N, d] dtype outputs, written directly by kernels that store from registers
   void* dv;
   const int* kv_len;  // optional [B]: keys j >= kv_len[b] are masked for batch b (key padding)
   int N;
-  int Npad;           // N rounded up to 64: the per-head row stride of lse2, Dvec and dqacc
+  int Npad;           // N rounded up to 128: the per-head row stride of lse2, Dvec and dqacc
   int H, Hkv;         // query heads and K/V heads (Hkv divides H; H / Hkv query heads share one K/V head)
   float scale;
   float scale_log2;

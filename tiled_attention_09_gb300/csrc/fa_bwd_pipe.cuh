@@ -26,6 +26,10 @@
 // groups that each own 32 of the tile's 64 query columns; warps 8-11 dQ
 // read-out and the dK epilogue; warp 12 TMA producer; warps 13-15 MMA issuers
 // (S^T + dV, dP^T + dK, dQ^T), since one thread cannot issue fast enough.
+// DQACC = false is the kernel for the separate dQ pass (fa_bwd_dq.cuh): it
+// computes dK and dV only, so no dQ^T product, no dS^T tile in shared memory and
+// no read-out; a buffer is then refilled as soon as the same issuer's dV / dK of
+// two steps before (issued earlier by that thread, executed in order) have read it.
 #pragma once
 #include "fa_bwd_main.cuh"
 
@@ -94,8 +98,9 @@ struct BwdItem {
   }
 };
 
-// GRP: grouped K/V heads or a key-padding mask (the general form); false for plain multi-head attention
-template <int D_, bool BF16, bool CAUSAL, bool GRP>
+// GRP: grouped K/V heads or a key-padding mask (the general form); false for plain multi-head attention.
+// DQACC: dQ partials accumulated here (true) or left to the separate dQ pass (false).
+template <int D_, bool BF16, bool CAUSAL, bool GRP, bool DQACC>
 __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdPipeCfg<D_>;
   using Item = BwdItem<CAUSAL, GRP>;
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       // A: the buffer of step g still holds dQ^T(g - 2) until warps 8-11 have read it out
       auto score_ready = [&](uint32_t g) -> bool {
         if (!wait_bar(b_qfull(g % NS), (g / NS) & 1, p.timeout_ns, abort_flag, WB_QF)) return false;
-        if (role == 0 && g >= 2 &&
+        if (DQACC && role == 0 && g >= 2 &&
             !wait_bar(b_dqfree(g & 1), ((g >> 1) - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE))
           return false;
         return true;
@@ -370,9 +375,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
               mma_ts(tmem + acc_col, tb + (kk >> 1) * 32 + (kk & 1) * 8, dOQ_mn + so + ((kk * 2048) >> 4),
                      idesc_acc, kk > 0 ? 1u : acc0);
             mma_commit(b_qempty(s));
-            if (role == 0) mma_commit(b_dvdone(b));
+            if (DQACC && role == 0) mma_commit(b_dvdone(b));
           }
-        } else {
+        } else if constexpr (DQACC) {
           // C: dQ^T(g) = K^T dS^T(g) over S^T(g)'s columns (M = d, N = 64 queries, K = 128 keys)
           for (int it = 0; ok && it < w.n_it; ++it) {
             const uint32_t g = gs + it, b = g & 1;
@@ -473,13 +478,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
                                         pv[4 * c4 + 3] * (__uint_as_float(v[4 * c4 + 3]) - dd.w));
         }
         tmem_st16(tDP + 32 * g, pk);
-        // dS^T row k, queries 32g .. 32g+31: 16-byte units 4g .. 4g+3 of the 128-byte swizzled row
-        uint8_t* row = smem + C::OFF_DS + b * C::DS_TILE + k * 128;
+        if constexpr (DQACC) {
+          // dS^T row k, queries 32g .. 32g+31: 16-byte units 4g .. 4g+3 of the 128-byte swizzled row
+          uint8_t* row = smem + C::OFF_DS + b * C::DS_TILE + k * 128;
 #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4)
-          *reinterpret_cast<uint4*>(row + (((4 * g + u4) ^ (k & 7)) << 4)) =
-              make_uint4(pk[4 * u4], pk[4 * u4 + 1], pk[4 * u4 + 2], pk[4 * u4 + 3]);
-        fence_proxy_async_smem();
+          for (int u4 = 0; u4 < 4; ++u4)
+            *reinterpret_cast<uint4*>(row + (((4 * g + u4) ^ (k & 7)) << 4)) =
+                make_uint4(pk[4 * u4], pk[4 * u4 + 1], pk[4 * u4 + 2], pk[4 * u4 + 3]);
+          fence_proxy_async_smem();
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_ds(b));
@@ -534,7 +541,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     bool ok = true;
     while (ok) {
       const Item w(ix, iy, p);
-      for (int it = 0; it < w.n_it; ++it) {
+      for (int it = 0; DQACC && it < w.n_it; ++it) {
         const uint32_t gq = gs + it, b = gq & 1;
         const bool full =
             __all_sync(0xffffffffu, wait_bar(b_dqfull(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_DQF));

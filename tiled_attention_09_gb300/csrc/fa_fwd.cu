@@ -39,7 +39,12 @@
 // exponentiates against the current m and finds the new row max in the same
 // pass; only a row whose max grew past the threshold rescales O and repeats the
 // pass. The final O / l and LSE use the same m, so the result is exact up to
-// rounding.
+// rounding. With a lazy max, the largest probability of a key tile is 2^delta
+// (0 < delta <= 8) rather than exactly 1, and its rounding to the dtype for the
+// P V product would not cancel in acc / l: for a nearly one-hot row that is an
+// error of up to half an ulp of P times |V|. So O is divided by l plus the
+// rounding error of each tile's largest probability (one exponential per row
+// and tile), which gives a one-hot row its V row again; the LSE keeps l.
 // Causal: tiles above the diagonal are never loaded or computed; the
 // diagonal tile masks keys > query inside the softmax.
 #include <cuda.h>
@@ -60,6 +65,10 @@ struct FwdParams {
   float* lse;      // [B*H*N]
   uint16_t* o_lo;  // optional [B*H*N, d]: dtype(O_fp32 - float(O)), the rounding residual of O
   const int* kv_len;  // optional [B]: batch b attends only to keys j < kv_len[b] (key padding)
+  float* part_o;      // split keys (kv_splits > 1): [kv_splits][B*H*N, d] fp32 partial O, each normalised
+  float* part_lse;    // [kv_splits][B*H*N] natural-log LSE of each part (-inf: the part saw no key)
+  long long part_rows;  // B*H*N
+  int kv_splits;      // CTAs that share one query block's key range (1: no split)
   int N;
   int H, G;        // query heads; query heads per K/V head
   int n_qblk;
@@ -100,10 +109,13 @@ struct FwdCfg {
 };
 
 // One work item: NT consecutive query tiles of one (b, h) head, named by the
-// blockIdx of the CTA that was launched for it (x = head, y = launch rank; under
-// causal masking rank 0 is the last and heaviest query block, so the hardware's
-// launch order is longest-first).
-template <int NT, bool CAUSAL>
+// blockIdx of the CTA that was launched for it (x = head, y = launch rank x key
+// split; under causal masking rank 0 is the last and heaviest query block, so the
+// hardware's launch order is longest-first). With split keys (kv_splits = S > 1)
+// the item is one of S contiguous ranges of the block's key tiles, [kt0, kt1):
+// each range writes its own normalised partial O and LSE and a merge pass joins
+// them by the online-softmax rule (O = sum_s e^(LSE_s - LSE) O_s).
+template <int NT, bool CAUSAL, bool SPLIT>
 struct FwdItem {
   int bh;        // query head (b, h): the z coordinate of the Q map
   int bkv;       // its K/V head (b, h / G): the z coordinate of the K and V maps
@@ -114,9 +126,14 @@ struct FwdItem {
   int n_valid;   // query tiles that exist (the last block can hold one tile fewer)
   int nmax;      // key tiles streamed for the item
   int n_t[NT];   // key tiles that tile t needs
+  int kt0, kt1;  // the item's range of key tiles (all of them without a split)
+  int sp;        // which of the kv_splits ranges (0 without a split)
   __device__ __forceinline__ FwdItem(int x, int y, const FwdParams& p) {
     const int N = p.N;
-    const int qb = CAUSAL ? (p.n_qblk - 1 - y) : y;
+    const int S = SPLIT ? p.kv_splits : 1;
+    const int rank = SPLIT ? y / S : y;
+    sp = SPLIT ? y - rank * S : 0;
+    const int qb = CAUSAL ? (p.n_qblk - 1 - rank) : rank;
     bh = x;
     const int b = x / p.H;
     bkv = b * (p.H / p.G) + (x - b * p.H) / p.G;
@@ -130,19 +147,35 @@ struct FwdItem {
     row_base = x * N;
     n_valid = (N - q_row0 + 127) / 128;  // a tile that runs past N still exists (its tail is masked)
     if (n_valid > NT) n_valid = NT;
+    kt0 = 0;
+    kt1 = 1 << 30;
+    if constexpr (SPLIT) {
+      int full = 0;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) full = tiles(t) > full ? tiles(t) : full;
+      const int per = (full + S - 1) / S;
+      kt0 = sp * per;
+      kt1 = kt0 + per < full ? kt0 + per : full;
+    }
     nmax = 0;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      n_t[t] = tiles(t);
+      n_t[t] = tiles_in_range(t);
       nmax = n_t[t] > nmax ? n_t[t] : nmax;
     }
   }
-  // key tiles that query tile t needs (computed, not indexed: t need not be a constant)
+  // key tiles that query tile t needs from key tile 0 on (computed, not indexed: t need not be a constant)
   __device__ __forceinline__ int tiles(int t) const {
     if (t >= n_valid) return 0;
     if (!CAUSAL) return nk;
     const int diag = q_row0 / 128 + t + 1;
     return diag < nk ? diag : nk;
+  }
+  // key tiles of the item's range [kt0, kt1) that query tile t needs
+  __device__ __forceinline__ int tiles_in_range(int t) const {
+    if constexpr (!SPLIT) return tiles(t);
+    const int end = tiles(t) < kt1 ? tiles(t) : kt1;
+    return end > kt0 ? end - kt0 : 0;
   }
 };
 
@@ -154,6 +187,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   } else {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// x rounded to the dtype (round to nearest even) and back to fp32.
+template <bool BF16>
+__device__ __forceinline__ float round_dtype(float x) {
+  if constexpr (BF16) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+  } else {
+    return __half2float(__float2half_rn(x));
   }
 }
 
@@ -181,10 +224,12 @@ enum : uint32_t {
   B_CLC_ID = 20  // where-code for FA_DEV_BAD_INDEX
 };
 
-template <int D, bool BF16, bool CAUSAL>
+// SPLIT: the item is one of kv_splits ranges of its block's key tiles and writes a partial O and LSE
+// (a separate instantiation, so the plain forward carries none of it).
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
-  using Item = FwdItem<C::NT, CAUSAL>;
+  using Item = FwdItem<C::NT, CAUSAL, SPLIT>;
   constexpr int NT = C::NT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -277,7 +322,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
             tma_load_3d(sQ + t * C::TILE + c * C::CHUNK, &p.tm_q, b_q, c * 64, w.q_row0 + t * 128, w.bh);
         ++n_items;
         const int nload = 2 * w.nmax;
-        const int ask_at = nload - 2;  // with the item's last K/V pair
+        const int ask_at = nload >= 2 ? nload - 2 : 0;  // with the item's last K/V pair (at once if it has none)
+        if (SPLIT && nload == 0 && clc_live) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(b_clc, 16);
+          clc_try_cancel(clc_resp, b_clc);
+          clc_pending = true;
+        }
         for (int s = 0; s < nload; ++s) {
           if (s == ask_at && clc_live) {
             fence_proxy_async_smem();  // earlier generic reads of the answer slot come first
@@ -292,7 +343,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           }
           mbar_arrive_expect_tx(b_full(slot), C::TILE);
           const void* map = (s & 1) ? static_cast<const void*>(&p.tm_v) : static_cast<const void*>(&p.tm_k);
-          const int krow = (s >> 1) * 128;  // rows past N arrive as zeros
+          const int krow = ((SPLIT ? w.kt0 : 0) + (s >> 1)) * 128;  // rows past N arrive as zeros
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, map, b_full(slot), c * 64, krow, w.bkv);
@@ -399,6 +450,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           if (j > 0) mma_commit(b_empty(sV % C::NS));
         }
         if (!ok) break;
+        if (SPLIT && w.nmax == 0) mma_commit(b_qfree);  // an empty key range: nothing reads Q
         seq += 2 * w.nmax;
         const int qi = n_items++;
         if (!wait_bar(b_item_full(qi & 1), (qi >> 1) & 1, p.timeout_ns, abort_flag, W_ITEM)) break;
@@ -433,11 +485,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     bool ok = true;
     while (ok) {
       const Item w(ix, iy, p);
-      const int my_n = w.tiles(t);
+      const int my_n = w.tiles_in_range(t);  // computed: t is not a compile-time index
       const int q_row = w.q_row0 + t * 128 + r;  // within the head
       // keys this row may see: those that exist, and (causal) none past the query itself
       const int klim = (CAUSAL && w.klen > q_row + 1) ? q_row + 1 : w.klen;
       float m_used = 0.f, l = 0.f;
+      float l_fix = 0.f;  // sum over tiles of round(p_max) - p_max, the rounding of each tile's largest P
       for (int j = 0; ok && j < my_n; ++j) {
         // warp-uniform outcome: tcgen05.ld/st below are warp-collective
         if (!__all_sync(0xffffffffu, wait_bar(b_s(t), n_s & 1, p.timeout_ns, abort_flag, W_S))) {
@@ -456,7 +509,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         // keys this row may not see: past the query itself (causal, diagonal tile), past the end of
         // the sequence or past the batch's key count (last tiles); all 128 of them only for a row
         // that sees no key at all (key count 0)
-        const int lim = klim - j * 128;
+        const int lim = klim - ((SPLIT ? w.kt0 : 0) + j) * 128;
         if (__any_sync(0xffffffffu, lim < 128)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = c >= lim ? -INFINITY : s[c];
@@ -508,13 +561,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         } else {
           // later tiles: exponentiate against the running max and find the new row max on the way;
           // only a row whose max grew by more than the threshold redoes the pass
-          const float m_new = exp_pass(std::true_type{}) + m_used;
+          const float x_max = exp_pass(std::true_type{});  // the tile's largest exponent against m_used
+          const float m_new = x_max + m_used;
           const bool rescale = m_new > m_used + p.rescale_threshold;
           if (__any_sync(0xffffffffu, rescale)) {
             const float alpha = rescale ? ex2_approx(m_used - m_new) : 1.f;
             if (rescale) {
               m_used = m_new;
               l *= alpha;
+              l_fix *= alpha;
             }
             // the commit that announced S_t(j) also covers P_t(j-1) V: O_t is quiescent
 #pragma unroll 1
@@ -526,6 +581,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
               tmem_st32(tO + 32 * c, u);
             }
             exp_pass(std::false_type{});
+          }
+          // a row that moved its max has P = 1 exactly at the tile's maximum; a row whose tile maximum
+          // stayed at or below m_used holds no row-dominant weight in this tile; the rest have their
+          // largest P = 2^x_max (0 < x_max <= 8), as the pass computed it
+          if (!rescale && x_max > 0.f) {
+            const float p_max = ex2_approx(x_max);
+            l_fix += round_dtype<BF16>(p_max) - p_max;
           }
         }
         l += ls0 + ls1;
@@ -542,10 +604,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         const size_t grow = static_cast<size_t>(w.row_base) + q_row;
         if (ok) {
           tc_fence_after();
-          const float inv_l = l > 0.f ? 1.f / l : 0.f;  // a row with no visible key: O = 0
-          uint4* o_row = p.o32 ? nullptr : reinterpret_cast<uint4*>(p.o + grow * D);
-          float4* o32_row = p.o32 ? reinterpret_cast<float4*>(p.o32 + grow * D) : nullptr;
-          uint4* lo_row = p.o_lo ? reinterpret_cast<uint4*>(p.o_lo + grow * D) : nullptr;
+          const float l_o = l + l_fix;  // the sum of the weights that P V used, to fp32 accuracy
+          const float inv_l = l_o > 0.f ? 1.f / l_o : 0.f;  // a row with no visible key: O = 0
+          // a split key range writes its normalised partial O in fp32 (and its LSE) for the merge
+          constexpr bool part = SPLIT;
+          const size_t prow = static_cast<size_t>(w.sp) * p.part_rows + grow;
+          uint4* o_row = (p.o32 || part) ? nullptr : reinterpret_cast<uint4*>(p.o + grow * D);
+          float4* o32_row = part ? reinterpret_cast<float4*>(p.part_o + prow * D)
+                                 : (p.o32 ? reinterpret_cast<float4*>(p.o32 + grow * D) : nullptr);
+          uint4* lo_row = (p.o_lo && !part) ? reinterpret_cast<uint4*>(p.o_lo + grow * D) : nullptr;
           constexpr int EC = D < 128 ? D : 128;  // columns per TMEM round trip
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += EC) {
@@ -583,8 +650,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
             }
           }
           // LSE in natural log: (m_used + log2 l) * ln 2 (-inf for a row with no visible key)
-          if (row_ok) p.lse[grow] = (m_used + log2f(l)) * 0.69314718055994531f;
+          if (row_ok) (part ? p.part_lse + prow : p.lse + grow)[0] = (m_used + log2f(l)) * 0.69314718055994531f;
         }
+      } else if (SPLIT && ok && q_row < N) {
+        // a split key range that holds none of this tile's keys: an empty part (weight 0 in the merge)
+        const size_t prow = static_cast<size_t>(w.sp) * p.part_rows + static_cast<size_t>(w.row_base) + q_row;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll 4
+        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.part_lse[prow] = -INFINITY;
       }
       if (!ok) break;
       const int qi = n_items++;
@@ -606,10 +680,70 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+// Joins the split key ranges of a query row (the online-softmax update of page
+// "transformer模型详解（十）：FlashAttention优化技术", section "Tiling 分块策略", applied
+// across ranges): LSE = ln sum_s e^(LSE_s), O = sum_s e^(LSE_s - LSE) O_s; a part
+// with LSE_s = -inf weighs 0, and a row whose parts are all empty gets O = 0,
+// LSE = -inf. One warp per row, lane l holding columns 4l .. 4l+3 (+128 for
+// d = 256); O is written in the dtype (with its rounding residual when o_lo is
+// given) or in fp32.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restrict__ part_o,
+                                                            const float* __restrict__ part_lse, long long rows,
+                                                            int n_split, uint16_t* o, uint16_t* o_lo, float* o32,
+                                                            float* lse) {
+  constexpr int V = D / 128 > 0 ? D / 128 : 1;  // float4 vectors per lane (d = 64: half the lanes)
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    float m = -INFINITY;
+    for (int s = 0; s < n_split; ++s) m = fmaxf(m, __ldg(part_lse + s * rows + row));
+    float acc[4 * V] = {};
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < n_split; ++s) {
+        const float ls = __ldg(part_lse + s * rows + row);
+        if (ls == -INFINITY) continue;
+        const float wgt = __expf(ls - m);
+        wsum += wgt;
+        const float4* src = reinterpret_cast<const float4*>(part_o + (s * rows + row) * D);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          if (D == 64 && lane >= 16) break;
+          const float4 x = __ldg(src + lane + 32 * v);
+          acc[4 * v] += wgt * x.x;
+          acc[4 * v + 1] += wgt * x.y;
+          acc[4 * v + 2] += wgt * x.z;
+          acc[4 * v + 3] += wgt * x.w;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      if (D == 64 && lane >= 16) break;
+      const float x0 = acc[4 * v] * inv, x1 = acc[4 * v + 1] * inv, x2 = acc[4 * v + 2] * inv,
+                  x3 = acc[4 * v + 3] * inv;
+      const long long e = row * D + 4 * (lane + 32 * v);
+      if (o32) {
+        *reinterpret_cast<float4*>(o32 + e) = make_float4(x0, x1, x2, x3);
+      } else {
+        uint2 r, lo;
+        lo.x = pack2_residual<BF16>(x0, x1, r.x);
+        lo.y = pack2_residual<BF16>(x2, x3, r.y);
+        *reinterpret_cast<uint2*>(o + e) = r;
+        if (o_lo) *reinterpret_cast<uint2*>(o_lo + e) = lo;
+      }
+    }
+    if (lane == 0) lse[row] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 cudaError_t launch_fwd_t(const FwdArgs& a) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
@@ -631,6 +765,10 @@ cudaError_t launch_fwd_t(const FwdArgs& a) {
   p.lse = a.lse;
   p.o_lo = static_cast<uint16_t*>(a.o_lo);
   p.kv_len = a.kv_len;
+  p.kv_splits = a.kv_splits > 1 ? a.kv_splits : 1;
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  p.part_rows = static_cast<long long>(a.B) * a.H * a.N;
   p.N = a.N;
   p.H = a.H;
   p.G = a.H / a.Hkv;
@@ -638,21 +776,33 @@ cudaError_t launch_fwd_t(const FwdArgs& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.rescale_threshold = 8.0f;
   p.timeout_ns = a.timeout_ns;
-  dim3 grid(a.B * a.H, p.n_qblk, 1);
-  return launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  dim3 grid(a.B * a.H, p.n_qblk * p.kv_splits, 1);
+  e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
+  if (e != cudaSuccess || p.kv_splits == 1) return e;
+  const long long blocks_needed = (p.part_rows + 7) / 8;  // 8 rows (warps) per block
+  const int blocks = static_cast<int>(blocks_needed < 152 * 16 ? blocks_needed : 152 * 16);
+  return launch_kernel(fa_fwd_merge_kernel<D, BF16>, dim3(blocks), dim3(256), 0, a.stream,
+                       static_cast<const float*>(a.part_o), static_cast<const float*>(a.part_lse), p.part_rows,
+                       p.kv_splits, p.o, p.o_lo, p.o32, a.lse);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a) {
-#define FA_FWD_CASE(D_)                                                                    \
-  if (a.d == D_) {                                                                         \
-    if (a.bf16) return a.causal ? launch_fwd_t<D_, true, true>(a) : launch_fwd_t<D_, true, false>(a); \
-    return a.causal ? launch_fwd_t<D_, false, true>(a) : launch_fwd_t<D_, false, false>(a);          \
+#define FA_FWD_CASE(D_, S_)                                                                          \
+  if (a.d == D_) {                                                                                   \
+    if (a.bf16) return a.causal ? launch_fwd_t<D_, true, true, S_>(a) : launch_fwd_t<D_, true, false, S_>(a); \
+    return a.causal ? launch_fwd_t<D_, false, true, S_>(a) : launch_fwd_t<D_, false, false, S_>(a);          \
   }
-  FA_FWD_CASE(64)
-  FA_FWD_CASE(128)
-  FA_FWD_CASE(256)
+  if (a.kv_splits > 1) {
+    FA_FWD_CASE(64, true)
+    FA_FWD_CASE(128, true)
+    FA_FWD_CASE(256, true)
+  } else {
+    FA_FWD_CASE(64, false)
+    FA_FWD_CASE(128, false)
+    FA_FWD_CASE(256, false)
+  }
 #undef FA_FWD_CASE
   return cudaErrorInvalidValue;
 }

@@ -41,6 +41,9 @@ struct FwdArgs {
   float* lse;
   void* o_lo;  // optional rounding residual of O (nullptr: not written)
   const int* kv_len;  // optional [B] key counts (key-padding mask)
+  int kv_splits;      // CTAs per query block's key range (1: no split)
+  float* part_o;      // kv_splits > 1: [kv_splits][B*H*N][d] fp32 partial outputs
+  float* part_lse;    // kv_splits > 1: [kv_splits][B*H*N] their LSEs
   int B, H, Hkv, N, d;
   bool o_f32;
   float scale;
@@ -60,11 +63,12 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* ws_D;      // [B*H*Npad]: row (bh, r) at bh * Npad + r, Npad = N rounded up to 64
+  float* ws_D;      // [B*H*Npad]: row (bh, r) at bh * Npad + r, Npad = N rounded up to 128
   float* ws_lse2;   // [B*H*Npad]  lse * log2(e)
   float* ws_dqacc;  // [B*H*Npad*d]
   int B, H, Hkv, N, d;
-  int Npad;  // N rounded up to 64: the per-head row stride of the workspace arrays
+  int Npad;  // N rounded up to 128: the per-head row stride of the workspace arrays
+  bool dq_pass;  // dQ by the separate query-major pass (no accumulator) instead of accumulation
   bool o_f32;
   float scale;
   bool causal, bf16;
@@ -98,6 +102,7 @@ cudaError_t launch_fwd(const FwdArgs& a);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a);
 cudaError_t launch_bwd_main(const BwdArgs& a);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a);
+cudaError_t launch_bwd_dq_pass(const BwdArgs& a);
 
 cudaError_t read_clear_status_fwd(DevStatusHost* out, cudaStream_t s);
 cudaError_t read_clear_status_bwd(DevStatusHost* out, cudaStream_t s);
