@@ -46,6 +46,7 @@ _CSRC = "tiled_attention_09_gb300/csrc/"
 KERNEL_SOURCES = {
     "fa_bwd_pipe_kernel": [_CSRC + f for f in ("fa_bwd_pipe.cuh", "fa_bwd_main.cuh", "ptx.cuh", "common.cuh")],
     "fa_fwd_kernel": [_CSRC + f for f in ("fa_fwd.cu", "ptx.cuh", "common.cuh")],
+    "fa_bwd_dq_kernel": [_CSRC + f for f in ("fa_bwd_dq.cuh", "fa_bwd_main.cuh", "ptx.cuh", "common.cuh")],
 }
 ROOFLINE_KERNEL = "fa_bwd_pipe_kernel"  # the step's dominant kernel (d = 128 backward)
 
@@ -650,6 +651,15 @@ def run_sweep(args):
                     def fwd():
                         fa.fwd(q, k, v, causal=causal, out=o, lse=lse, residual=True, o_lo=o_lo)
 
+                    # the split-key forward where the library would split this grid (kv_splits = 0)
+                    n_split = int(L.fa_fwd_kv_splits(w.B, w.H, N, d, int(causal)))
+                    fws = (torch.empty(int(L.fa_fwd_workspace_size(w.B, w.H, N, d, n_split)), dtype=torch.uint8,
+                                       device=dev) if n_split > 1 else None)
+
+                    def fwd_split():
+                        fa.fwd(q, k, v, causal=causal, out=o, lse=lse, residual=True, o_lo=o_lo, kv_splits=n_split,
+                               workspace=fws)
+
                     def step(mode):
                         fwd()
                         fa.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws, dq=dq, dk=dk, dv=dv, o_lo=o_lo,
@@ -661,6 +671,8 @@ def run_sweep(args):
                     default = "separate" if dq_separate(L, "default", d, causal) else "accumulate"
                     times = {}
                     fns = [("fwd", fwd)] + [(f"fwd_bwd_{m}", (lambda m=m: step(m))) for m in modes]
+                    if n_split > 1:
+                        fns.append(("fwd_split", fwd_split))
                     for name, fn in fns:
                         for _ in range(warmup):
                             flush()
@@ -683,9 +695,11 @@ def run_sweep(args):
                     bytes_bwd = heads * (8 * N * d * 2 + 8 * N)  # Q, K, V, dO in; dQ, dK, dV out (+ O); LSE, D
                     line = {"point": w.name(), "N": N, "d": d, "dtype": dtype, "causal": causal, "dq_default": default}
                     times["fwd_bwd"] = times[f"fwd_bwd_{default}"]
+                    line["fwd_kv_splits"] = n_split
                     for name, flops, nbytes in [("fwd", F, bytes_fwd)] + [
                             (f"fwd_bwd{x}", 3.5 * F, bytes_fwd + bytes_bwd)
-                            for x in [""] + [f"_{m}" for m in modes]]:
+                            for x in [""] + [f"_{m}" for m in modes]] + (
+                            [("fwd_split", F, bytes_fwd)] if n_split > 1 else []):
                         tf = flops / times[name] / 1e12
                         attainable = min(peak, bw * 1e9 * flops / nbytes / 1e12)
                         line[name] = {"ms": 1e3 * times[name], "tflops": tf, "pct_of_peak": tf / peak,
@@ -693,7 +707,7 @@ def run_sweep(args):
                     line["peak_tflops"] = peak
                     line["peak_source"] = peak_src
                     print(json.dumps(line), flush=True)
-                    del q, k, v, do, o, lse, o_lo, ws, dq, dk, dv
+                    del q, k, v, do, o, lse, o_lo, ws, dq, dk, dv, fws
             torch.cuda.empty_cache()
 
 

@@ -24,7 +24,9 @@
 // Roles (12 warps): warps 0-7 elementwise (two groups of 64 key columns) and the dQ
 // epilogue (each group half the head dimension), warp 8 TMA producer and work scheduler
 // (cluster launch control takes over CTAs that have not started, as in the forward),
-// warp 9 MMA issuer, warps 10-11 idle.
+// warps 9, 10, 11 the MMA issuers of S, dP and dQ: one thread issues an MMA only every
+// ~90-110 cycles, so a single issuer of the tile's 24 products would take about 2500
+// cycles against 1536 of arithmetic.
 #pragma once
 #include "fa_bwd_main.cuh"
 
@@ -44,8 +46,8 @@ struct BwdDqCfg {
   static constexpr int OFF_DD = OFF_LSE + 2 * BQ * 4;  // 2 items x 128 floats
   static constexpr int OFF_BAR = OFF_DD + 2 * BQ * 4;
   // bars: q_full, q_free, kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], s_full[2], ds_ready[2],
-  // dq_done[2], dp_full, dp_free, dq_final, dq_read, clc, item_full[2], item_empty[2], drain
-  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 6 + 4 + 1 + 4 + 1;
+  // dq_done[2], dp_full, dp_free, dq_final, dq_read, clc, item_full[2], item_empty[2], drain[3]
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 6 + 4 + 1 + 4 + 3;
   static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES + 16 + 16 + 16;
   static constexpr int THREADS = 384;
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
   const uint32_t b_clc = smem_u32(&bars[B0 + 10]);
   auto b_item_full = [&](int i) { return smem_u32(&bars[B0 + 11 + i]); };
   auto b_item_empty = [&](int i) { return smem_u32(&bars[B0 + 13 + i]); };
-  const uint32_t b_drain = smem_u32(&bars[B0 + 15]);
+  auto b_drain = [&](int i) { return smem_u32(&bars[B0 + 15 + i]); };
   const uint32_t clc_resp = smem_u32(aux + C::BAR_BYTES);
   volatile int* items = reinterpret_cast<volatile int*>(aux + C::BAR_BYTES + 16);  // [2][2]: x, y (x < 0: none)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + C::BAR_BYTES + 32);
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
-    mbar_init(b_qfree, 1);
+    mbar_init(b_qfree, 2);  // the S issuer after its item's last S, the dP issuer after its last dP
     for (int s = 0; s < NSK; ++s) {
       mbar_init(b_kfull(s), 1);
       mbar_init(b_kempty(s), 1);
@@ -146,9 +148,9 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
     mbar_init(b_clc, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_item_full(i), 1);
-      mbar_init(b_item_empty(i), 1 + 8);  // the MMA thread and one lane per elementwise warp
+      mbar_init(b_item_empty(i), 3 + 8);  // the three MMA threads and one lane per elementwise warp
     }
-    mbar_init(b_drain, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(b_drain(i), 1);
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -266,8 +268,9 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 9) {
+    // ------------------------------------------------------------ MMA issuers: 9 = S, 10 = dP, 11 = dQ
+    const int role = warp - 9;
     if (elect_one()) {
       constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
       constexpr uint32_t idesc_dq = make_idesc(128, D, BF16, false, true);
@@ -321,8 +324,10 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
       // dQ += dS(j) K_j: A = packed dS from the S buffer (keys 16kk.. at column 64 (kk / 4) + 8 (kk % 4)),
       // B = K_j MN-major (M = 128 queries, N = d, K = 128 keys)
       auto issue_dq = [&](int j, bool first) -> bool {
-        const uint32_t b = ndq & 1, ks = (kseq + j) % NSK;
+        const uint32_t b = ndq & 1, ks = (kseq + j) % NSK, ku = (kseq + j) / NSK;
         if (!wait_bar(b_dsready(b), (ndq >> 1) & 1, p.timeout_ns, abort_flag, WQ_DS)) return false;
+        // K_j landed long before (S(j) read it); this thread acquires the copy for its own products
+        if (!wait_bar(b_kfull(ks), ku & 1, p.timeout_ns, abort_flag, WQ_KV)) return false;
         // the first product of an item overwrites the accumulator: the previous epilogue has read it
         if (first && n_items > 0 && !wait_bar(b_dqread, (n_items - 1) & 1, p.timeout_ns, abort_flag, WQ_DQ))
           return false;
@@ -337,21 +342,23 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
         ++ndq;
         return true;
       };
+      // S(j) waits for its K tile and, from the third tile on, for dQ(j - 2) (its buffer held dS(j - 2));
+      // dP(j) for its V tile and for the elementwise warps to have read dP(j - 1); dQ(j) for dS(j).
       while (ok) {
         const Item w(ix, iy, p);
         const int nt = w.ntile;
-        if (!wait_bar(b_qfull, n_items & 1, p.timeout_ns, abort_flag, WQ_Q)) break;
-        if (nt > 0) ok = issue_s(0) && issue_dp(0);
-        if (ok && nt > 1) ok = issue_s(1);
+        if (role < 2 && !wait_bar(b_qfull, n_items & 1, p.timeout_ns, abort_flag, WQ_Q)) break;
         for (int j = 0; ok && j < nt; ++j) {
-          if (j + 1 < nt && !issue_dp(j + 1)) ok = false;
-          if (ok && j == nt - 1) mma_commit(b_qfree);  // every S and dP of the item has been issued
-          if (ok && !issue_dq(j, j == 0)) ok = false;
-          if (ok && j + 2 < nt && !issue_s(j + 2)) ok = false;
+          if (role == 0)
+            ok = issue_s(j);
+          else if (role == 1)
+            ok = issue_dp(j);
+          else
+            ok = issue_dq(j, j == 0);
         }
         if (!ok) break;
-        if (nt == 0) mma_commit(b_qfree);
-        mma_commit(b_dqfinal);  // the item's dQ is complete (an item with no key tile: nothing to wait for)
+        if (role < 2) mma_commit(b_qfree);  // every S (dP) of the item has been issued
+        if (role == 2) mma_commit(b_dqfinal);  // the item's dQ is complete (no key tile: nothing to wait for)
         kseq += nt;
         vseq += nt;
         const int qi = n_items++;
@@ -363,14 +370,16 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
         iy = ny;
       }
       // Drain: all issued MMAs complete before teardown.
-      mma_commit(b_drain);
-      wait_bar(b_drain, 0, p.timeout_ns, abort_flag, WQ_DRAIN);
+      mma_commit(b_drain(role));
+      wait_bar(b_drain(role), 0, p.timeout_ns, abort_flag, WQ_DRAIN);
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();  // every role is done with TMEM
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if (warp == 9) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
   } else if (warp < 8) {
     // ------------------------------------------------------------ elementwise: dS; dQ epilogue
     const int grp = warp >> 2;        // key columns 64 grp .. 64 grp + 63 of each tile
@@ -473,9 +482,6 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
       iy = ny;
     }
     tc_fence_before();
-    __syncthreads();
-  } else {
-    // ------------------------------------------------------------ idle warps
     __syncthreads();
   }
 }
