@@ -78,6 +78,9 @@ def parse():
                     help="under torchrun: every rank runs the whole workload (replicas, weak scaling) or its "
                          "contiguous range of the job's B*H heads (heads, strong scaling, no data-path collective)")
     ap.add_argument("--sweep-bf16", action="store_true", help="with --sweep: bf16 points only")
+    ap.add_argument("--split-sweep", action="store_true",
+                    help="time the forward on grids with few heads and long rows at 1, 2, 4 and 8 key ranges per "
+                         "query block and at the library's choice; one JSON line per shape")
     ap.add_argument("--sweep", action="store_true",
                     help="time every sweep point (B2 H12, d 64/128/256, N 512-16384, both dtypes and masks) "
                          "instead of the headline step; one JSON line per point")
@@ -711,6 +714,60 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+SPLIT_POINTS = [  # (B, H, N, d, causal): few query blocks, each with a long key range
+    (1, 1, 4096, 128, True), (1, 1, 8192, 128, True), (1, 1, 16384, 128, True), (1, 1, 32768, 128, True),
+    (1, 2, 16384, 128, True), (1, 1, 8192, 128, False), (1, 4, 4096, 128, True), (1, 1, 16384, 64, True),
+    (1, 1, 8192, 256, True), (2, 2, 8192, 128, True), (2, 12, 4096, 128, True),
+]
+
+
+def run_split_sweep(args):
+    """One JSON line per SPLIT_POINTS shape (bf16): the forward's median time at kv_splits 1, 2, 4, 8 (each
+    between two events on the launching stream, L2 flushed before every call) and the library's choice."""
+    import torch
+    import tiled_attention_09_gb300 as fa
+    from tiled_attention_09_gb300.inputs import Workload, make_inputs
+    from tiled_attention_09_gb300 import _lib
+    L = _lib.load()
+    dev = torch.device("cuda", 0)
+    flush = L2Flush(torch, dev)
+    steps, warmup = max(3, min(args.steps, 20)), max(3, args.warmup)
+    for B, H, N, d, causal in SPLIT_POINTS:
+        w = Workload(B, H, N, d, "bf16", causal)
+        q, k, v, _ = (t.to(dev) for t in make_inputs(w))
+        o, lse = torch.empty_like(q), torch.empty(B, H, N, device=dev)
+        us = {}
+        for n_split in (1, 2, 4, 8):
+            ws = (torch.empty(int(L.fa_fwd_workspace_size(B, H, N, d, n_split)), dtype=torch.uint8, device=dev)
+                  if n_split > 1 else None)
+
+            def call():
+                fa.fwd(q, k, v, causal=causal, out=o, lse=lse, kv_splits=n_split, workspace=ws)
+
+            for _ in range(warmup):
+                flush()
+                call()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for e0, e1 in evs:
+                flush()
+                e0.record()
+                call()
+                e1.record()
+            torch.cuda.synchronize()
+            us[n_split] = 1e3 * statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+        code, info = fa.device_status()
+        if code != "FA_OK":
+            raise RuntimeError(f"{w.name()}: {code} {info}")
+        best = min(us, key=us.get)
+        choice = int(L.fa_fwd_kv_splits(B, H, N, d, int(causal)))
+        print(json.dumps({"point": w.name(), "us": us, "fastest": best, "library_choice": choice,
+                          "choice_vs_fastest": us[choice] / us[best] if choice in us else None,
+                          "tflops_plain": w.fwd_flops() / us[1] / 1e6,
+                          "tflops_choice": w.fwd_flops() / us[choice] / 1e6 if choice in us else None}), flush=True)
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+
+
 DECODE_POINTS = [  # (B, H, Hkv, Mq, d, page_size, ctx)
     (16, 32, 8, 1, 128, 64, 8192),
     (1, 32, 8, 1, 128, 64, 65536),
@@ -913,6 +970,8 @@ def main():
         return
     if args.decode:
         run_decode(args)
+    elif args.split_sweep:
+        run_split_sweep(args)
     elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":

@@ -95,12 +95,37 @@ def test_backward_from_the_split_forward(w):
 
 
 def test_library_split_choice_runs_and_matches():
-    """kv_splits = 0: the library's choice (several ranges for this small grid)."""
+    """kv_splits = 0: the library's choice (several ranges for this grid of four CTAs with long rows)."""
     from tiled_attention_09_gb300 import _lib
-    w = Workload(1, 2, 1024, 128, "bf16", True)
-    assert _lib.load().fa_fwd_kv_splits(1, 2, 1024, 128, 1) > 1
+    w = Workload(1, 1, 2048, 128, "bf16", True)
+    assert _lib.load().fa_fwd_kv_splits(1, 1, 2048, 128, 1) > 1
     q, k, v, _ = make_inputs(w)
     o, lse = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, kv_splits=0)
     torch.cuda.synchronize()
     assert fa.device_status()[0] == "FA_OK"
     _check_fwd(w, o, lse, to64(q), to64(k), to64(v), what="auto")
+
+
+def test_attention_autograd_uses_the_library_split():
+    """fa.attention picks the library's split count (8 here: one head, four query blocks of 2048 keys at most)
+    and its O and gradients match the oracle; with kv_splits=1 the O differs only by rounding."""
+    from tiled_attention_09_gb300 import _lib
+    w = Workload(1, 1, 2048, 128, "bf16", True)
+    assert _lib.load().fa_fwd_kv_splits(1, 1, 2048, 128, 1) == 8
+    q, k, v, do = make_inputs(w)
+    qa, ka, va = (t.cuda().requires_grad_(True) for t in (q, k, v))
+    o = fa.attention(qa, ka, va, causal=True)
+    o.backward(do.cuda())
+    torch.cuda.synchronize()
+    assert fa.device_status()[0] == "FA_OK"
+    q64, k64, v64, do64 = to64(q), to64(k), to64(v), to64(do)
+    o_ref, _ = oracle.attention_fwd(q64, k64, v64, w.scale, True)
+    pv_abs, _ = oracle.attention_fwd(q64, k64, np.abs(v64), w.scale, True)
+    check_o(to64(o.detach()), o_ref, pv_abs, w.dtype, "O attention split",
+            ideal=ideal_kernel_o(q64, k64, v64, w.scale, w.dtype, True))
+    floor = cancel_tol(q64, k64, v64, do64, w.scale)
+    for name, g, r in zip(("dQ", "dK", "dV"), (qa.grad, ka.grad, va.grad),
+                          oracle.attention_bwd(q64, k64, v64, do64, w.scale, True)):
+        check_grad(to64(g), r, name, floor[name])
+    o1 = fa.attention(qa.detach(), ka.detach(), va.detach(), causal=True, kv_splits=1)
+    assert (o1.float() - o.detach().float()).abs().max().item() <= 2 ** -7 * o1.float().abs().max().item()

@@ -226,9 +226,9 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, 
 
 class _AttentionFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, scale, kv_len):
+    def forward(ctx, q, k, v, causal, scale, kv_len, kv_splits):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        o, lse, o_lo = fwd(q, k, v, causal, scale, residual=True, kv_len=kv_len)
+        o, lse, o_lo = fwd(q, k, v, causal, scale, residual=True, kv_len=kv_len, kv_splits=kv_splits)
         ctx.save_for_backward(q, k, v, o, lse, o_lo)
         ctx.causal, ctx.scale, ctx.kv_len = causal, scale, kv_len
         return o
@@ -237,15 +237,17 @@ class _AttentionFn(torch.autograd.Function):
     def backward(ctx, do):
         q, k, v, o, lse, o_lo = ctx.saved_tensors
         dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), ctx.causal, ctx.scale, o_lo=o_lo, kv_len=ctx.kv_len)
-        return dq, dk, dv, None, None, None
+        return dq, dk, dv, None, None, None, None
 
 
-def attention(q, k, v, causal=False, scale=None, kv_len=None):
+def attention(q, k, v, causal=False, scale=None, kv_len=None, kv_splits=0):
     """Differentiable exact attention over [B, H, N, d] fp16/bf16 CUDA tensors.
 
     k, v may be [B, H_kv, N, d] (grouped-query / multi-query); kv_len: optional int32 [B] key counts.
+    kv_splits: key ranges per query block in the forward (0 = the library's choice, which splits only
+    grids with few heads and long rows; 1 = never).
     """
-    return _AttentionFn.apply(q, k, v, causal, scale, kv_len)
+    return _AttentionFn.apply(q, k, v, causal, scale, kv_len, kv_splits)
 
 
 def decode_splits(B, Hkv, d, page_size, max_pages) -> int:

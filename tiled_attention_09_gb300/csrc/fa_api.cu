@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -209,16 +210,57 @@ FwdWs fwd_ws(int B, int H, int N, int d, int S) {
   return w;
 }
 
-// The library's split count: one CTA per (query block, key range) and 152 SMs; split the key range
-// only while the grid has fewer than two CTAs per SM, and keep at least two key tiles per range
-// (about one, on average, under a causal mask).
+// The library's split count, from a cost model of the forward fitted to GB300 timings. A plain launch
+// takes about max(longest item, total work / SMs) in (128-query x 128-key) tile pairs times the time a
+// pair takes on one SM, plus a fixed cost for every wave of CTAs. A split shortens the longest item (the
+// critical path under a causal mask or with few heads) but writes and re-reads an fp32 partial O per
+// range and adds the merge launch. The count with the least modelled time wins; with many heads or
+// short sequences that is 1.
+int sm_count() {
+  static std::atomic<int> cached{0};
+  int n = cached.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  int dev = 0;
+  n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 152;  // GB300
+  }
+  cached.store(n, std::memory_order_relaxed);
+  return n;
+}
+
+double fwd_model_us(int B, int H, int N, int d, bool causal, int s, int sms) {
+  const int NT = d <= 128 ? 2 : 1;
+  const long long nq = (N + 127) / 128, nk = nq;
+  const long long nblk = (nq + NT - 1) / NT;
+  // the longest item is the last query block (causal) or any block (full); its first key range is full
+  long long full = 0, longest = 0;
+  const long long qt0 = (nblk - 1) * NT;
+  for (long long t = qt0; t < qt0 + NT && t < nq; ++t) full = std::max(full, causal ? std::min(t + 1, nk) : nk);
+  const long long per = (full + s - 1) / s;
+  for (long long t = qt0; t < qt0 + NT && t < nq; ++t)
+    longest += std::min(per, causal ? std::min(t + 1, nk) : nk);
+  const double heads = static_cast<double>(B) * H;
+  const double pairs = heads * (causal ? nk * (nk + 1) / 2.0 : static_cast<double>(nq) * nk);
+  const double ctas = heads * nblk * s;
+  const double t_pair = d == 64 ? 0.68 : d == 128 ? 0.75 : 2.4;  // us per tile pair on one SM
+  double t = std::max(static_cast<double>(longest), 1.1 * pairs / sms) * t_pair + 1.5 * std::ceil(ctas / sms);
+  if (s > 1) t += 4.0 + s * heads * N * d * 8.0 / 5.0e6;  // partials written and read at ~5 TB/s
+  return t;
+}
+
 int fwd_kv_splits(int B, int H, int N, int d, bool causal) {
-  const long long qblk_rows = d <= 128 ? 256 : 128;
-  const long long items = static_cast<long long>(B) * H * ((N + qblk_rows - 1) / qblk_rows);
+  const int sms = sm_count();
   const long long key_tiles = (N + 127) / 128;
-  int s = 1;
-  while (s < kMaxKvSplits && items * s < 2 * 152 && (causal ? key_tiles : 2 * key_tiles) >= 4 * s) s *= 2;
-  return s;
+  int best = 1;
+  double best_t = fwd_model_us(B, H, N, d, causal, 1, sms);
+  for (int s = 2; s <= kMaxKvSplits && s <= key_tiles; s *= 2) {
+    const double t = fwd_model_us(B, H, N, d, causal, s, sms);
+    if (t < best_t) best = s, best_t = t;
+  }
+  return best;
 }
 
 fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype) {

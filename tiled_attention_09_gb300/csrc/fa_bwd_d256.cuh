@@ -14,7 +14,13 @@
 // S^T and dP^T are computed twice, so the kernel does 1.4x the useful FLOPs.
 // Shared memory: K and V of the block stay resident (128 KB); Q and dO of one
 // 64-query step (64 KB) and dS^T (16 KB) complete it, with no room for a second
-// stage, so the producer loads step i + 1 once step i's MMAs have read step i.
+// stage. The stage is therefore released in two halves of the head dimension:
+// the half a pass does not accumulate (chunks 2(1-h), 2(1-h)+1 of Q and dO) is
+// read only by S^T and dP^T, so the next step's copy of it is loaded while this
+// step's P, dS, dV, dK and dQ^T are formed; the pass's own half, read by dV and
+// dK as well, is reloaded once those have completed. S^T and dP^T of a step
+// contract over the early half first. LSE and D are double-buffered, each
+// buffer released by the elementwise warps.
 // dQ^T of a step goes from TMEM straight to the fp32 accumulator with coalesced
 // global reductions (a warp covers 128 contiguous bytes per query), and the
 // dV/dK epilogue of a pass is staged in the Q and dO tiles.
@@ -39,11 +45,12 @@ struct BwdD256Cfg {
   static constexpr int OFF_Q = OFF_V + KV_TILE;
   static constexpr int OFF_DO = OFF_Q + Q_TILE;
   static constexpr int OFF_DS = OFF_DO + Q_TILE;
-  static constexpr int OFF_LSE = OFF_DS + DS_TILE;
-  static constexpr int OFF_DD = OFF_LSE + BQ * 4;
-  static constexpr int OFF_BAR = OFF_DD + BQ * 4;
-  // bars: kv, q_full, q_empty, sdp, ds, dq_full, dq_free, done, epi, drain
-  static constexpr int NBAR = 10;
+  static constexpr int OFF_LSE = OFF_DS + DS_TILE;  // two buffers of BQ floats
+  static constexpr int OFF_DD = OFF_LSE + 2 * BQ * 4;
+  static constexpr int OFF_BAR = OFF_DD + 2 * BQ * 4;
+  // bars: kv, q_full / q_empty of the early half (x) and of the pass's own half (w), sdp, ds, dq_full,
+  // dq_free, done, epi, drain, lse_full[2], lse_empty[2]
+  static constexpr int NBAR = 16;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr int THREADS = 320;
   static constexpr uint32_t S_COL = 0, DP_COL = 64, DQ_COL = 128, DV_COL = 256, DK_COL = 384;
@@ -62,8 +69,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
   const uint32_t sDS = s0 + C::OFF_DS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const uint32_t b_kv = smem_u32(&bars[0]);
-  const uint32_t b_qfull = smem_u32(&bars[1]);
-  const uint32_t b_qempty = smem_u32(&bars[2]);
+  const uint32_t b_qfx = smem_u32(&bars[1]);
+  const uint32_t b_qex = smem_u32(&bars[2]);
   const uint32_t b_sdp = smem_u32(&bars[3]);
   const uint32_t b_ds = smem_u32(&bars[4]);
   const uint32_t b_dqfull = smem_u32(&bars[5]);
@@ -71,6 +78,10 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
   const uint32_t b_done = smem_u32(&bars[7]);
   const uint32_t b_epi = smem_u32(&bars[8]);
   const uint32_t b_drain = smem_u32(&bars[9]);
+  const uint32_t b_qfw = smem_u32(&bars[10]);
+  const uint32_t b_qew = smem_u32(&bars[11]);
+  const uint32_t b_lfull0 = smem_u32(&bars[12]);   // + 8 * buffer
+  const uint32_t b_lempty0 = smem_u32(&bars[14]);  // + 8 * buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[C::NBAR]);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -86,8 +97,14 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
-    mbar_init(b_qfull, 1);
-    mbar_init(b_qempty, 1);
+    mbar_init(b_qfx, 1);
+    mbar_init(b_qex, 1);
+    mbar_init(b_qfw, 1);
+    mbar_init(b_qew, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_lfull0 + 8 * i, 1);
+      mbar_init(b_lempty0 + 8 * i, 128);
+    }
     mbar_init(b_sdp, 1);
     mbar_init(b_ds, 128);
     mbar_init(b_dqfull, 1);
@@ -119,30 +136,51 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         tma_load_3d(sK + c * C::KV_CHUNK, &p.tm_k, b_kv, c * 64, key0, bh);
         tma_load_3d(sV + c * C::KV_CHUNK, &p.tm_v, b_kv, c * 64, key0, bh);
       }
-      int issued = 0;
+      int n_x = 0, n_w = 0, n_l = 0;  // copies issued on q_full x, q_full w and the LSE/D buffers
       for (int g = 0; g < n_g; ++g) {
-        const int it = g % n_it;
-        // the single stage is free once step g - 1's MMAs have read it; the first step of the
-        // second pass also waits for the first pass's epilogue, which staged dV / dK there
-        if (g > 0 && !wait_bar(b_qempty, (g - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) break;
-        if (g == n_it && !wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_QE)) break;
+        const int h = g / n_it, it = g % n_it;
+        const int cw = 2 * h, cx = 2 - 2 * h;  // first chunk of the pass's own half, of the early half
+        // the early half of step g - 1 is free once its S^T and dP^T have completed; the first step of
+        // the second pass waits for the first pass's epilogue instead, which staged dV / dK in Q and dO
+        if (g == n_it) {
+          if (!wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_QE)) break;
+        } else if (g > 0 && !wait_bar(b_qex, (g - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) {
+          break;
+        }
         int qh, qs;
         grp.step(it, it0, n_ith, qh, qs);
         const int q_in = qs * BQ;             // within query head qh; rows past N arrive as zeros
         const int qrow = qh * p.Npad + q_in;  // LSE*log2e / D past N: the head's zero padding, masked
-        mbar_arrive_expect_tx(b_qfull, 2 * C::Q_TILE + 2 * BQ * 4);
+        // LSE / D into buffer g & 1 once the elementwise warps have read step g - 2's
+        const int lb = g & 1;
+        if (g >= 2 && !wait_bar(b_lempty0 + 8 * lb, ((g >> 1) - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) break;
+        mbar_arrive_expect_tx(b_lfull0 + 8 * lb, 2 * BQ * 4);
+        bulk_load(s0 + C::OFF_LSE + lb * BQ * 4, p.lse2 + qrow, BQ * 4, b_lfull0 + 8 * lb);
+        bulk_load(s0 + C::OFF_DD + lb * BQ * 4, p.Dvec + qrow, BQ * 4, b_lfull0 + 8 * lb);
+        ++n_l;
+        mbar_arrive_expect_tx(b_qfx, C::Q_TILE);  // two chunks of Q and two of dO
 #pragma unroll
-        for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfull, c * 64, q_in, qh);
-          tma_load_3d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfull, c * 64, q_in, qh);
+        for (int c = cx; c < cx + 2; ++c) {
+          tma_load_3d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfx, c * 64, q_in, qh);
+          tma_load_3d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfx, c * 64, q_in, qh);
         }
-        bulk_load(s0 + C::OFF_LSE, p.lse2 + qrow, BQ * 4, b_qfull);
-        bulk_load(s0 + C::OFF_DD, p.Dvec + qrow, BQ * 4, b_qfull);
-        ++issued;
+        ++n_x;
+        // the pass's own half of step g - 1 is free once dV and dK have read it
+        if (g != n_it && g > 0 && !wait_bar(b_qew, (g - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) break;
+        mbar_arrive_expect_tx(b_qfw, C::Q_TILE);
+#pragma unroll
+        for (int c = cw; c < cw + 2; ++c) {
+          tma_load_3d(sQ + c * C::Q_CHUNK, &p.tm_q, b_qfw, c * 64, q_in, qh);
+          tma_load_3d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfw, c * 64, q_in, qh);
+        }
+        ++n_w;
       }
       // Drain: every issued copy has landed before the CTA may exit.
       wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_DRAIN);
-      if (issued > 0) wait_bar(b_qfull, (issued - 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
+      if (n_x > 0) wait_bar(b_qfx, (n_x - 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
+      if (n_w > 0) wait_bar(b_qfw, (n_w - 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
+      for (int j = n_l - 2 < 0 ? 0 : n_l - 2; j < n_l; ++j)
+        wait_bar(b_lfull0 + 8 * (j & 1), (j >> 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -161,24 +199,41 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
       bool ok = wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_KV);
       for (int g = 0; ok && g < n_g; ++g) {
         const int h = g / n_it, it = g % n_it;
-        if (!wait_bar(b_qfull, g & 1, p.timeout_ns, abort_flag, WB_QF)) break;
+        if (!wait_bar(b_qfx, g & 1, p.timeout_ns, abort_flag, WB_QF)) break;
         // a new pass overwrites the dV / dK halves: the previous pass's epilogue must have read them
         if (g == n_it && !wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_DONE)) break;
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T  (M = 128 keys, N = 64 queries, K = d = 256)
+        // S^T = K Q^T and dP^T = V dO^T  (M = 128 keys, N = 64 queries, K = d = 256), contracted over
+        // the early half's chunks first, then (once they have landed) over the pass's own half
+        bool landed = true;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + C::S_COL, dK_k + oa, dQ_k + ob, idesc_sdp, kk > 0 ? 1u : 0u);
-        }
+        for (int part = 0; part < 2; ++part) {
+          if (part == 1) {
+            if (!wait_bar(b_qfw, g & 1, p.timeout_ns, abort_flag, WB_QF)) {
+              landed = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const int c0 = part == 0 ? 2 - 2 * h : 2 * h;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + C::DP_COL, dV_k + oa, dO_k + ob, idesc_sdp, kk > 0 ? 1u : 0u);
+          for (int j = 0; j < 8; ++j) {
+            const int c = c0 + (j >> 2);
+            const uint64_t oa = static_cast<uint64_t>((c * C::KV_CHUNK + (j & 3) * 32) >> 4);
+            const uint64_t ob = static_cast<uint64_t>((c * C::Q_CHUNK + (j & 3) * 32) >> 4);
+            mma_ss(tmem + C::S_COL, dK_k + oa, dQ_k + ob, idesc_sdp, (part > 0 || j > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c = c0 + (j >> 2);
+            const uint64_t oa = static_cast<uint64_t>((c * C::KV_CHUNK + (j & 3) * 32) >> 4);
+            const uint64_t ob = static_cast<uint64_t>((c * C::Q_CHUNK + (j & 3) * 32) >> 4);
+            mma_ss(tmem + C::DP_COL, dV_k + oa, dO_k + ob, idesc_sdp, (part > 0 || j > 0) ? 1u : 0u);
+          }
         }
+        if (!landed) break;
         mma_commit(b_sdp);
+        mma_commit(b_qex);  // the early half may be reloaded for step g + 1
         if (!wait_bar(b_ds, g & 1, p.timeout_ns, abort_flag, WB_DS)) break;
         tc_fence_after();
         // dV[:, h] += P^T dO[:, h] ; dK[:, h] += dS^T Q[:, h]
@@ -192,6 +247,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         for (int kk = 0; kk < BQ / 16; ++kk)
           mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, dQ_mn + half_q + ((kk * 2048) >> 4), idesc_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(b_qew);  // the pass's own half may be reloaded for step g + 1
         // dQ^T[h-half][q] = sum_k K[k][h-half] dS^T[k][q]  (M = 128 = half of d, N = 64, K = 128 keys)
         if (g > 0 && !wait_bar(b_dqfree, (g - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE)) break;
         tc_fence_after();
@@ -201,7 +257,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
           mma_ss(tmem + C::DQ_COL, dKT_mn + half_k + ((kk * 2048) >> 4), dDS_mn + ((kk * 2048) >> 4), idesc_dq,
                  kk > 0 ? 1u : 0u);
         mma_commit(b_dqfull);
-        mma_commit(b_qempty);
         if (it == n_it - 1) mma_commit(b_done);  // this pass's dV / dK halves are final
       }
       mma_commit(b_drain);
@@ -218,12 +273,14 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
     for (int g = 0; g < n_g; ++g) {
       const int h = g / n_it, it = g % n_it;
       if (ok && !__all_sync(0xffffffffu, wait_bar(b_sdp, g & 1, p.timeout_ns, abort_flag, WB_SDP))) ok = false;
-      // LSE / D of the step were landed by the producer on q_full; acquire them here too.
-      if (ok && !__all_sync(0xffffffffu, wait_bar(b_qfull, g & 1, p.timeout_ns, abort_flag, WB_QF))) ok = false;
+      // LSE / D of the step, in buffer g & 1 (released below, once read)
+      const int lb = g & 1;
+      if (ok && !__all_sync(0xffffffffu, wait_bar(b_lfull0 + 8 * lb, (g >> 1) & 1, p.timeout_ns, abort_flag, WB_QF)))
+        ok = false;
       if (ok) {
         tc_fence_after();
-        const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
-        const float* dd_s = reinterpret_cast<const float*>(smem + C::OFF_DD);
+        const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + lb * BQ * 4);
+        const float* dd_s = reinterpret_cast<const float*>(smem + C::OFF_DD + lb * BQ * 4);
         int qh, qs;
         grp.step(it, it0, n_ith, qh, qs);
         const int q0 = qs * BQ;  // first query of the tile
@@ -269,6 +326,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
             ds32[16 + c] = bpack2<BF16>(b0, b1);
           }
         }
+        mbar_arrive(b_lempty0 + 8 * lb);  // this thread's last read of the step's LSE / D
         tmem_st32(tDP, ds32);
         // dS^T row k (64 queries): one 128-byte swizzled row
         uint8_t* row = smem + C::OFF_DS + k * 128;
