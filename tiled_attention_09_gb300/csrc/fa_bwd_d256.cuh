@@ -26,8 +26,14 @@
 // dV/dK epilogue of a pass is staged in the Q and dO tiles.
 // TMEM: S^T (P^T packed over it) at 0, dP^T (dS^T packed over it) at 64,
 // dQ^T at 128, dV half at 256, dK half at 384.
-// Roles (320 threads): warps 0-3 elementwise and the dV epilogue, warps 4-7 dQ
-// read-out and the dK epilogue, warp 8 TMA producer, warp 9 MMA issuer.
+// Roles (384 threads): warps 0-3 elementwise and the dV epilogue, warps 4-7 dQ
+// read-out and the dK epilogue, warp 8 TMA producer, warps 9-11 MMA issuers:
+// S^T and dV (9), dP^T and dK (10), dQ^T (11). One thread issues an MMA only
+// every ~100 cycles, so a single issuer could not keep the tensor core busy
+// with the 48 products of a step. Each issuer overwrites a TMEM buffer only
+// after its own earlier products that read it (MMAs of one thread execute in
+// order); the elementwise warps write dS^T(g) to shared memory only once
+// dQ^T(g - 1), which reads it, has completed.
 #pragma once
 #include "fa_bwd_main.cuh"
 
@@ -52,14 +58,14 @@ struct BwdD256Cfg {
   // dq_free, done, epi, drain, lse_full[2], lse_empty[2]
   static constexpr int NBAR = 16;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
   static constexpr uint32_t S_COL = 0, DP_COL = 64, DQ_COL = 128, DV_COL = 256, DK_COL = 384;
   static_assert(SMEM_BYTES <= 232448, "smem budget");
   static_assert(Q_TILE >= BK * DH * 2, "a pass's dV or dK half (bf16) is staged in the Q or dO tile");
 };
 
 template <bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdD256Cfg;
   constexpr int BQ = C::BQ, D = C::D, DH = C::DH;
   extern __shared__ uint8_t smem_raw[];
@@ -98,20 +104,20 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
     mbar_init(b_qfx, 1);
-    mbar_init(b_qex, 1);
+    mbar_init(b_qex, 2);  // S^T and dP^T issuers
     mbar_init(b_qfw, 1);
-    mbar_init(b_qew, 1);
+    mbar_init(b_qew, 2);  // dV and dK
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_lfull0 + 8 * i, 1);
       mbar_init(b_lempty0 + 8 * i, 128);
     }
-    mbar_init(b_sdp, 1);
+    mbar_init(b_sdp, 2);
     mbar_init(b_ds, 128);
     mbar_init(b_dqfull, 1);
     mbar_init(b_dqfree, 128);
-    mbar_init(b_done, 1);
+    mbar_init(b_done, 2);
     mbar_init(b_epi, 2);  // one thread of each epilogue group, once per pass
-    mbar_init(b_drain, 1);
+    mbar_init(b_drain, 3);
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -183,28 +189,45 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         wait_bar(b_lfull0 + 8 * (j & 1), (j >> 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 9) {
+    // ------------------------------------------------------------ MMA issuers
+    const int role = warp - 9;  // 0: S^T, dV   1: dP^T, dK   2: dQ^T
     if (elect_one()) {
       constexpr uint32_t idesc_sdp = make_idesc(128, BQ, BF16, false, false);
       constexpr uint32_t idesc_acc = make_idesc(128, DH, BF16, false, true);
       constexpr uint32_t idesc_dq = make_idesc(128, BQ, BF16, true, true);
       // Descriptors are built once; steps add (byte offset >> 4) to the 14-bit start-address
       // field, which cannot carry out of it (shared memory ends below 256 KB).
-      const uint64_t dK_k = make_sdesc(sK, 16, 1024), dV_k = make_sdesc(sV, 16, 1024);  // K-major
-      const uint64_t dQ_k = make_sdesc(sQ, 16, 1024), dO_k = make_sdesc(sDO, 16, 1024);  // K-major
-      const uint64_t dQ_mn = make_sdesc(sQ, C::Q_CHUNK, 1024), dO_mn = make_sdesc(sDO, C::Q_CHUNK, 1024);
+      // role 0: K and Q (K-major) for S^T, dO (MN-major) for dV; role 1: V and dO for dP^T, Q for dK
+      const uint64_t dA_k = make_sdesc(role == 0 ? sK : sV, 16, 1024);
+      const uint64_t dB_k = make_sdesc(role == 0 ? sQ : sDO, 16, 1024);
+      const uint64_t dB_mn = make_sdesc(role == 0 ? sDO : sQ, C::Q_CHUNK, 1024);
       const uint64_t dKT_mn = make_sdesc(sK, C::KV_CHUNK, 1024);  // K^T as the A operand of dQ^T
       const uint64_t dDS_mn = make_sdesc(sDS, 128 * 128, 1024);   // dS^T as the B operand of dQ^T
+      const uint32_t t_sdp = tmem + (role == 0 ? C::S_COL : C::DP_COL);  // S^T or dP^T (then P^T or dS^T)
+      const uint32_t t_acc = tmem + (role == 0 ? C::DV_COL : C::DK_COL);
       bool ok = wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_KV);
       for (int g = 0; ok && g < n_g; ++g) {
         const int h = g / n_it, it = g % n_it;
+        if (role == 2) {
+          // dQ^T[h-half][q] = sum_k K[k][h-half] dS^T[k][q]  (M = 128 = half of d, N = 64, K = 128 keys)
+          if (!wait_bar(b_ds, g & 1, p.timeout_ns, abort_flag, WB_DS)) break;
+          if (g > 0 && !wait_bar(b_dqfree, (g - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE)) break;
+          tc_fence_after();
+          const uint64_t half_k = static_cast<uint64_t>((2 * h * C::KV_CHUNK) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::DQ_COL, dKT_mn + half_k + ((kk * 2048) >> 4), dDS_mn + ((kk * 2048) >> 4), idesc_dq,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(b_dqfull);
+          continue;
+        }
         if (!wait_bar(b_qfx, g & 1, p.timeout_ns, abort_flag, WB_QF)) break;
         // a new pass overwrites the dV / dK halves: the previous pass's epilogue must have read them
         if (g == n_it && !wait_bar(b_epi, 0, p.timeout_ns, abort_flag, WB_DONE)) break;
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T  (M = 128 keys, N = 64 queries, K = d = 256), contracted over
-        // the early half's chunks first, then (once they have landed) over the pass's own half
+        // S^T = K Q^T (role 0) or dP^T = V dO^T (role 1)  (M = 128 keys, N = 64 queries, K = d = 256),
+        // contracted over the early half's chunks first, then (once they have landed) the pass's own half
         bool landed = true;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -221,14 +244,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
             const int c = c0 + (j >> 2);
             const uint64_t oa = static_cast<uint64_t>((c * C::KV_CHUNK + (j & 3) * 32) >> 4);
             const uint64_t ob = static_cast<uint64_t>((c * C::Q_CHUNK + (j & 3) * 32) >> 4);
-            mma_ss(tmem + C::S_COL, dK_k + oa, dQ_k + ob, idesc_sdp, (part > 0 || j > 0) ? 1u : 0u);
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int c = c0 + (j >> 2);
-            const uint64_t oa = static_cast<uint64_t>((c * C::KV_CHUNK + (j & 3) * 32) >> 4);
-            const uint64_t ob = static_cast<uint64_t>((c * C::Q_CHUNK + (j & 3) * 32) >> 4);
-            mma_ss(tmem + C::DP_COL, dV_k + oa, dO_k + ob, idesc_sdp, (part > 0 || j > 0) ? 1u : 0u);
+            mma_ss(t_sdp, dA_k + oa, dB_k + ob, idesc_sdp, (part > 0 || j > 0) ? 1u : 0u);
           }
         }
         if (!landed) break;
@@ -236,27 +252,13 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         mma_commit(b_qex);  // the early half may be reloaded for step g + 1
         if (!wait_bar(b_ds, g & 1, p.timeout_ns, abort_flag, WB_DS)) break;
         tc_fence_after();
-        // dV[:, h] += P^T dO[:, h] ; dK[:, h] += dS^T Q[:, h]
+        // dV[:, h] += P^T dO[:, h] (role 0) or dK[:, h] += dS^T Q[:, h] (role 1)
         //   (M = 128 keys, N = 128 = half of d, K = 64 queries; A from TMEM, B MN-major from chunks 2h, 2h+1)
         const uint64_t half_q = static_cast<uint64_t>((2 * h * C::Q_CHUNK) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, dO_mn + half_q + ((kk * 2048) >> 4), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, dQ_mn + half_q + ((kk * 2048) >> 4), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(t_acc, t_sdp + kk * 8, dB_mn + half_q + ((kk * 2048) >> 4), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(b_qew);  // the pass's own half may be reloaded for step g + 1
-        // dQ^T[h-half][q] = sum_k K[k][h-half] dS^T[k][q]  (M = 128 = half of d, N = 64, K = 128 keys)
-        if (g > 0 && !wait_bar(b_dqfree, (g - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE)) break;
-        tc_fence_after();
-        const uint64_t half_k = static_cast<uint64_t>((2 * h * C::KV_CHUNK) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::DQ_COL, dKT_mn + half_k + ((kk * 2048) >> 4), dDS_mn + ((kk * 2048) >> 4), idesc_dq,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(b_dqfull);
         if (it == n_it - 1) mma_commit(b_done);  // this pass's dV / dK halves are final
       }
       mma_commit(b_drain);
@@ -328,16 +330,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_d256_kernel(const __grid_consta
         }
         mbar_arrive(b_lempty0 + 8 * lb);  // this thread's last read of the step's LSE / D
         tmem_st32(tDP, ds32);
-        // dS^T row k (64 queries): one 128-byte swizzled row
-        uint8_t* row = smem + C::OFF_DS + k * 128;
+        // dS^T row k (64 queries): one 128-byte swizzled row, over dS^T(g - 1) once dQ^T(g - 1) has read it
+        // (a timeout here leaves ok false and the loop running, so the group's epilogue barriers stay uniform)
+        if (g == 0 || __all_sync(0xffffffffu, wait_bar(b_dqfull, (g - 1) & 1, p.timeout_ns, abort_flag, WB_DQF))) {
+          uint8_t* row = smem + C::OFF_DS + k * 128;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(row + ((u ^ (k & 7)) << 4)) =
-              make_uint4(ds32[4 * u], ds32[4 * u + 1], ds32[4 * u + 2], ds32[4 * u + 3]);
-        fence_proxy_async_smem();
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(row + ((u ^ (k & 7)) << 4)) =
+                make_uint4(ds32[4 * u], ds32[4 * u + 1], ds32[4 * u + 2], ds32[4 * u + 3]);
+          fence_proxy_async_smem();
+        } else {
+          ok = false;
+        }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b_ds);
+        if (ok) mbar_arrive(b_ds);
       }
       if (it == n_it - 1) {
         // end of pass h: dV[:, h] (128 keys x 128) staged in the Q tile, stored with TMA
