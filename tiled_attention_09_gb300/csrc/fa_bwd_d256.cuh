@@ -180,6 +180,17 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
           tma_load_3d(sDO + c * C::Q_CHUNK, &p.tm_do, b_qfw, c * 64, q_in, qh);
         }
         ++n_w;
+        // Q and dO of step g + 1 towards L2 now: their loads wait until this step's products release the
+        // stage, and then find them in L2 instead of HBM
+        if (g + 1 < n_g) {
+          int qh1, qs1;
+          grp.step((g + 1) % n_it, it0, n_ith, qh1, qs1);
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_prefetch_l2_3d(&p.tm_q, c * 64, qs1 * BQ, qh1);
+            tma_prefetch_l2_3d(&p.tm_do, c * 64, qs1 * BQ, qh1);
+          }
+        }
       }
       // Drain: every issued copy has landed before the CTA may exit.
       wait_bar(b_kv, 0, p.timeout_ns, abort_flag, WB_DRAIN);
