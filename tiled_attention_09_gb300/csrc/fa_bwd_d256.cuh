@@ -24,11 +24,14 @@
 // dQ^T of a step goes from TMEM straight to the fp32 accumulator with coalesced
 // global reductions (a warp covers 128 contiguous bytes per query), and the
 // dV/dK epilogue of a pass is staged in the Q and dO tiles.
-// TMEM: S^T (P^T packed over it) at 0, dP^T (dS^T packed over it) at 64,
-// dQ^T at 128, dV half at 256, dK half at 384.
-// Roles (384 threads): warps 0-3 elementwise and the dV epilogue, warps 4-7 dQ
-// read-out and the dK epilogue, warp 8 TMA producer, warps 9-11 MMA issuers:
-// S^T and dV (9), dP^T and dK (10), dQ^T (11). One thread issues an MMA only
+// TMEM: S^T at 0, dP^T at 64, dQ^T at 128, dV half at 256, dK half at 384. Each
+// elementwise group packs P^T (dS^T) of its 32 queries into the first 16 of its
+// own 32 columns of S^T (dP^T), never into columns the other group may still be
+// reading, so the 16-query slices of the TMEM operand sit at 0, 8, 32, 40.
+// Roles (512 threads): warps 0-7 elementwise (two groups of 32 query columns)
+// and the dV epilogue (one half of the columns each), warps 8-11 dQ read-out
+// and the dK epilogue, warp 12 TMA producer, warps 13-15 MMA issuers: S^T and
+// dV (13), dP^T and dK (14), dQ^T (15). One thread issues an MMA only
 // every ~100 cycles, so a single issuer could not keep the tensor core busy
 // with the 48 products of a step. Each issuer overwrites a TMEM buffer only
 // after its own earlier products that read it (MMAs of one thread execute in
@@ -38,6 +41,14 @@
 #include "fa_bwd_main.cuh"
 
 namespace fa {
+
+// L2 prefetch of one box of a 3-D tensor map: nothing is written to shared memory and no
+// barrier is signalled (x follows the same 16-byte rule as a load).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+               "r"(z)
+               : "memory");
+}
 
 struct BwdD256Cfg {
   static constexpr int D = 256, DH = 128, BK = 128, BQ = 64, NCH = D / 64;
@@ -58,14 +69,15 @@ struct BwdD256Cfg {
   // dq_free, done, epi, drain, lse_full[2], lse_empty[2]
   static constexpr int NBAR = 16;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
+  static constexpr int W_RO = 8, W_PROD = 12, W_ISS = 13;  // first warp of each role after the elementwise
   static constexpr uint32_t S_COL = 0, DP_COL = 64, DQ_COL = 128, DV_COL = 256, DK_COL = 384;
   static_assert(SMEM_BYTES <= 232448, "smem budget");
   static_assert(Q_TILE >= BK * DH * 2, "a pass's dV or dK half (bf16) is staged in the Q or dO tile");
 };
 
 template <bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) fa_bwd_d256_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdD256Cfg;
   constexpr int BQ = C::BQ, D = C::D, DH = C::DH;
   extern __shared__ uint8_t smem_raw[];
@@ -109,20 +121,20 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
     mbar_init(b_qew, 2);  // dV and dK
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_lfull0 + 8 * i, 1);
-      mbar_init(b_lempty0 + 8 * i, 128);
+      mbar_init(b_lempty0 + 8 * i, 256);
     }
     mbar_init(b_sdp, 2);
-    mbar_init(b_ds, 128);
+    mbar_init(b_ds, 256);
     mbar_init(b_dqfull, 1);
     mbar_init(b_dqfree, 128);
     mbar_init(b_done, 2);
-    mbar_init(b_epi, 2);  // one thread of each epilogue group, once per pass
+    mbar_init(b_epi, 3);  // one thread of each epilogue group (two dV halves, dK), once per pass
     mbar_init(b_drain, 3);
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
   }
-  if (warp == 9) {
+  if (warp == C::W_ISS) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -131,7 +143,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == C::W_PROD) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
       tma_prefetch_desc(&p.tm_q);
@@ -200,9 +212,9 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
         wait_bar(b_lfull0 + 8 * (j & 1), (j >> 1) & 1, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
-  } else if (warp >= 9) {
+  } else if (warp >= C::W_ISS) {
     // ------------------------------------------------------------ MMA issuers
-    const int role = warp - 9;  // 0: S^T, dV   1: dP^T, dK   2: dQ^T
+    const int role = warp - C::W_ISS;  // 0: S^T, dV   1: dP^T, dK   2: dQ^T
     if (elect_one()) {
       constexpr uint32_t idesc_sdp = make_idesc(128, BQ, BF16, false, false);
       constexpr uint32_t idesc_acc = make_idesc(128, DH, BF16, false, true);
@@ -268,7 +280,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
         const uint64_t half_q = static_cast<uint64_t>((2 * h * C::Q_CHUNK) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(t_acc, t_sdp + kk * 8, dB_mn + half_q + ((kk * 2048) >> 4), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(t_acc, t_sdp + 32 * (kk >> 1) + 8 * (kk & 1), dB_mn + half_q + ((kk * 2048) >> 4), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(b_qew);  // the pass's own half may be reloaded for step g + 1
         if (it == n_it - 1) mma_commit(b_done);  // this pass's dV / dK halves are final
       }
@@ -276,11 +289,12 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
       wait_bar(b_drain, 0, p.timeout_ns, abort_flag, WB_DRAIN);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < C::W_RO) {
     // ------------------------------------------------------------ elementwise: P^T, dS^T; dV epilogue
-    const int k = threadIdx.x;  // key within the tile == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::S_COL, tDP = tmem + lane_off + C::DP_COL;
+    const int gq = warp >> 2;            // column group: queries 32 gq .. 32 gq + 31 of the step
+    const int k = threadIdx.x & 127;     // key within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::S_COL + 32 * gq, tDP = tmem + lane_off + C::DP_COL + 32 * gq;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int g = 0; g < n_g; ++g) {
@@ -292,63 +306,55 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
         ok = false;
       if (ok) {
         tc_fence_after();
-        const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + lb * BQ * 4);
-        const float* dd_s = reinterpret_cast<const float*>(smem + C::OFF_DD + lb * BQ * 4);
+        const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE + lb * BQ * 4) + 8 * gq;
+        const float4* dd4 = reinterpret_cast<const float4*>(smem + C::OFF_DD + lb * BQ * 4) + 8 * gq;
         int qh, qs;
         grp.step(it, it0, n_ith, qh, qs);
-        const int q0 = qs * BQ;  // first query of the tile
+        const int q0 = qs * BQ + 32 * gq;  // first query of this group's columns
         // masked: column c < kq (key > query, causal), q0 + c >= N (query past the sequence) or the
         // whole row when the key does not exist (past N or past the batch's key count: S need not
         // come from a real key, and exp(-LSE) need not be finite)
-        const bool need_mask = (CAUSAL && (q0 < key0 + 127)) || (q0 + BQ > N) || (key0 + 128 > grp.klen);
+        const bool need_mask = (CAUSAL && (q0 < key0 + 127)) || (q0 + 32 > N) || (key0 + 128 > grp.klen);
         const int kq = CAUSAL ? (key0 + k - q0) : 0;
         const int qn = key0 + k < grp.klen ? N - q0 : 0;
-        float pv[64];
-        {
-          uint32_t u0[32], u1[32];
-          tmem_ld32(tS, u0);
-          tmem_ld32(tS + 32, u1);
+        uint32_t u[32], v[32];
+        tmem_ld32_pair(tS, tDP, u, v);  // S^T and dP^T columns in one round trip
+        float pv[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            pv[c] = ex2_approx(fmaf(__uint_as_float(u0[c]), sl2, -lse_s[c]));
-            pv[32 + c] = ex2_approx(fmaf(__uint_as_float(u1[c]), sl2, -lse_s[32 + c]));
-          }
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l = lse4[c4];
+          pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 0]), sl2, -l.x));
+          pv[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 1]), sl2, -l.y));
+          pv[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 2]), sl2, -l.z));
+          pv[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 3]), sl2, -l.w));
         }
         if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pv[c] = (c < kq || c >= qn) ? 0.f : pv[c];
+          for (int c = 0; c < 32; ++c) pv[c] = (c < kq || c >= qn) ? 0.f : pv[c];
         }
-        {
-          uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = bpack2<BF16>(pv[2 * c], pv[2 * c + 1]);
-          tmem_st32(tS, pk);
-        }
-        uint32_t ds32[32];
-        {
-          uint32_t u0[32], u1[32];
-          tmem_ld32(tDP, u0);
-          tmem_ld32(tDP + 32, u1);
+        for (int c = 0; c < 16; ++c) pk[c] = bpack2<BF16>(pv[2 * c], pv[2 * c + 1]);
+        tmem_st16(tS, pk);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float a0 = pv[2 * c] * (__uint_as_float(u0[2 * c]) - dd_s[2 * c]);
-            const float a1 = pv[2 * c + 1] * (__uint_as_float(u0[2 * c + 1]) - dd_s[2 * c + 1]);
-            ds32[c] = bpack2<BF16>(a0, a1);
-            const float b0 = pv[32 + 2 * c] * (__uint_as_float(u1[2 * c]) - dd_s[32 + 2 * c]);
-            const float b1 = pv[33 + 2 * c] * (__uint_as_float(u1[2 * c + 1]) - dd_s[33 + 2 * c]);
-            ds32[16 + c] = bpack2<BF16>(b0, b1);
-          }
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dd = dd4[c4];
+          pk[2 * c4] = bpack2<BF16>(pv[4 * c4] * (__uint_as_float(v[4 * c4]) - dd.x),
+                                    pv[4 * c4 + 1] * (__uint_as_float(v[4 * c4 + 1]) - dd.y));
+          pk[2 * c4 + 1] = bpack2<BF16>(pv[4 * c4 + 2] * (__uint_as_float(v[4 * c4 + 2]) - dd.z),
+                                        pv[4 * c4 + 3] * (__uint_as_float(v[4 * c4 + 3]) - dd.w));
         }
         mbar_arrive(b_lempty0 + 8 * lb);  // this thread's last read of the step's LSE / D
-        tmem_st32(tDP, ds32);
-        // dS^T row k (64 queries): one 128-byte swizzled row, over dS^T(g - 1) once dQ^T(g - 1) has read it
-        // (a timeout here leaves ok false and the loop running, so the group's epilogue barriers stay uniform)
+        tmem_st16(tDP, pk);
+        // dS^T row k, queries 32 gq .. 32 gq + 31: 16-byte units 4 gq .. 4 gq + 3 of the 128-byte swizzled
+        // row, over dS^T(g - 1) once dQ^T(g - 1) has read it (a timeout here leaves ok false and the loop
+        // running, so the group's epilogue barriers stay uniform)
         if (g == 0 || __all_sync(0xffffffffu, wait_bar(b_dqfull, (g - 1) & 1, p.timeout_ns, abort_flag, WB_DQF))) {
           uint8_t* row = smem + C::OFF_DS + k * 128;
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(row + ((u ^ (k & 7)) << 4)) =
-                make_uint4(ds32[4 * u], ds32[4 * u + 1], ds32[4 * u + 2], ds32[4 * u + 3]);
+          for (int u4 = 0; u4 < 4; ++u4)
+            *reinterpret_cast<uint4*>(row + (((4 * gq + u4) ^ (k & 7)) << 4)) =
+                make_uint4(pk[4 * u4], pk[4 * u4 + 1], pk[4 * u4 + 2], pk[4 * u4 + 3]);
           fence_proxy_async_smem();
         } else {
           ok = false;
@@ -358,11 +364,12 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
         if (ok) mbar_arrive(b_ds);
       }
       if (it == n_it - 1) {
-        // end of pass h: dV[:, h] (128 keys x 128) staged in the Q tile, stored with TMA
+        // end of pass h: dV[:, h] (128 keys x 128), columns 64 gq .. 64 gq + 63 staged in the Q tile's
+        // chunk gq, stored with TMA
         bool ok_e = ok && __all_sync(0xffffffffu, wait_bar(b_done, h & 1, p.timeout_ns, abort_flag, WB_DONE));
         if (ok_e) tc_fence_after();
-        bwd_store_acc<DH, BF16>(tmem + lane_off + C::DV_COL, smem + C::OFF_Q, &p.tm_dv, key0, bh, k, 1.0f, 1,
-                                ok_e, abort_flag, h * DH);
+        bwd_store_acc<64, BF16>(tmem + lane_off + C::DV_COL + 64 * gq, smem + C::OFF_Q + gq * (128 * 128), &p.tm_dv,
+                                key0, bh, k, 1.0f, 1 + 2 * gq, ok_e, abort_flag, h * DH + 64 * gq);
         if (k == 0) {
           tc_fence_before();
           mbar_arrive(b_epi);
@@ -370,9 +377,9 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
         ok = ok_e;
       }
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ dQ read-out; dK epilogue
-    const int t = threadIdx.x - 128;  // TMEM lane = index within the head-dimension half
+  } else {
+    // ------------------------------------------------------------ dQ read-out; dK epilogue (warps 8-11)
+    const int t = threadIdx.x - 32 * C::W_RO;  // TMEM lane = index within the head-dimension half
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
     for (int g = 0; g < n_g; ++g) {
@@ -414,7 +421,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_d256_kernel(const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::W_ISS) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -100,13 +100,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
-// L2 prefetch of one box of a 3-D tensor map: nothing is written to shared memory and no
-// barrier is signalled (x follows the same 16-byte rule as a load).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
-               "r"(z)
-               : "memory");
-}
 // 2-D tiled load global -> shared, completion counted on an mbarrier (bytes).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint32_t bar, int x, int y) {
   asm volatile(
