@@ -44,7 +44,8 @@ METRIC = "attention fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense tensor p
 _CSRC = "tiled_attention_09_gb300/csrc/"
 # sources each timed kernel is built from: a recorded ncu traffic figure is used only while these are unchanged
 KERNEL_SOURCES = {
-    "fa_bwd_pipe_kernel": [_CSRC + f for f in ("fa_bwd_pipe.cuh", "fa_bwd_main.cuh", "ptx.cuh", "common.cuh")],
+    "fa_bwd_pipe_kernel": [_CSRC + f for f in ("fa_bwd_pipe.cuh", "fa_bwd_order.cuh", "fa_bwd_main.cuh", "ptx.cuh",
+                                                "common.cuh")],
     "fa_fwd_kernel": [_CSRC + f for f in ("fa_fwd.cu", "ptx.cuh", "common.cuh")],
     "fa_bwd_dq_kernel": [_CSRC + f for f in ("fa_bwd_dq.cuh", "fa_bwd_main.cuh", "ptx.cuh", "common.cuh")],
 }

@@ -39,6 +39,7 @@
 // dQ^T(g - 1), which reads it, has completed.
 #pragma once
 #include "fa_bwd_main.cuh"
+#include "fa_bwd_order.cuh"
 
 namespace fa {
 
@@ -105,31 +106,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_d256_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int N = p.N;
-  // CTAs launch in the order of blockIdx.x + gridDim.x * blockIdx.y. That order takes the K/V heads
-  // in groups of hg and, within a group, the key blocks in ascending order (block 0, the longest
-  // under causal masking, first) across the group's heads: the CTAs in flight then share the Q, dO
-  // and dQ rows of a few heads, which stay in L2, while long blocks still start before short ones.
-  int bh, key0;
-  {
-    const int heads = gridDim.x, nkb = gridDim.y;
-    const int lin = blockIdx.x + heads * blockIdx.y;
-    // Groups small enough that the rows they share (G query heads x N rows x (2 + 2 + 4) bytes x d
-    // per K/V head) stay within about 64 MB, but no more groups than heads * nkb / 304: a causal
-    // block 0 takes about 304 / (heads * nkb) of the run on 152 SMs, and the last group's block 0
-    // starts only when that group does, so more groups would lengthen the run's tail.
-    const long long head_bytes = static_cast<long long>(p.H / p.Hkv) * N * 8ll * D;
-    const long long fit = (64ll << 20) / (head_bytes > 0 ? head_bytes : 1);
-    const int hg_max = fit < 1 ? 1 : (fit > heads ? heads : static_cast<int>(fit));
-    const int ng_mem = (heads + hg_max - 1) / hg_max;
-    const long long ng_tail_ll = static_cast<long long>(heads) * nkb / 304;
-    const int ng_tail = ng_tail_ll < 1 ? 1 : (ng_tail_ll > heads ? heads : static_cast<int>(ng_tail_ll));
-    const int ng = ng_mem < ng_tail ? ng_mem : ng_tail;
-    const int hg = (heads + ng - 1) / ng;
-    const int gi = lin / (hg * nkb), r = lin - gi * hg * nkb;
-    const int gh = heads - gi * hg < hg ? heads - gi * hg : hg;  // heads in this group (the last may have fewer)
-    bh = gi * hg + r % gh;  // K/V head (b, h_kv)
-    key0 = (r / gh) * 128;
-  }
+  int bh, kb;  // K/V head (b, h_kv) and key block: see fa_bwd_order.cuh
+  bwd_block_order(blockIdx.x, blockIdx.y, gridDim.x, gridDim.y, static_cast<long long>(p.H / p.Hkv) * N * 8ll * D, bh,
+                  kb);
+  const int key0 = kb * 128;
   const BwdGroup<true> grp(bh, p);  // the query heads that share this K/V head, and the batch's key count
   const int it0 = CAUSAL ? (key0 / BQ) : 0;
   const int n_ith = (N + BQ - 1) / BQ - it0;  // query steps per query head (the last may run past N: masked)

@@ -32,6 +32,7 @@
 // two steps before (issued earlier by that thread, executed in order) have read it.
 #pragma once
 #include "fa_bwd_main.cuh"
+#include "fa_bwd_order.cuh"
 
 namespace fa {
 
@@ -76,11 +77,21 @@ struct BwdPipeCfg {
   static_assert(SMEM_BYTES <= 232448, "smem budget");
 };
 
-// One work item: the 128-key block y of K/V head x (blockIdx of the CTA launched for it; under
-// causal masking block 0 has the most query steps, so the launch order is longest-first). The
-// block's query steps run over the G query heads that share the K/V head, one head after another.
+// The K/V head and key block that launch index (x, y) works on (fa_bwd_order.cuh).
+struct BwdSlot {
+  int bh, kb;
+  __device__ __forceinline__ BwdSlot(int x, int y, const BwdParams& p, int d) {
+    bwd_block_order(x, y, gridDim.x, gridDim.y, static_cast<long long>(p.H / p.Hkv) * p.N * 8ll * d, bh, kb);
+  }
+};
+
+// One work item: the 128-key block of a K/V head that the CTA launched as (x, y) stands for (the
+// launch order takes heads in L2-sized groups, longest blocks first within a group; under causal
+// masking block 0 has the most query steps). The block's query steps run over the G query heads
+// that share the K/V head, one head after another.
 template <bool CAUSAL, bool GRP>
 struct BwdItem {
+  BwdSlot slot;
   int bh;        // K/V head (b, h_kv): the z coordinate of the K, V maps
   int row_base;  // row of (b, h_kv, 0) in the [B*Hkv*N, d] view of K, V, dK, dV
   int key0;      // first key of the block
@@ -88,10 +99,10 @@ struct BwdItem {
   int n_ith;     // query steps per query head (the last may run past N: its extra queries are masked)
   int n_it;      // query steps of the block: G * n_ith
   BwdGroup<GRP> grp;  // the query heads of the group and the batch's key count
-  __device__ __forceinline__ BwdItem(int x, int y, const BwdParams& p) : grp(x, p) {
-    bh = x;
-    row_base = x * p.N;
-    key0 = y * 128;
+  __device__ __forceinline__ BwdItem(int x, int y, const BwdParams& p, int d) : slot(x, y, p, d), grp(slot.bh, p) {
+    bh = slot.bh;
+    row_base = bh * p.N;
+    key0 = slot.kb * 128;
     it0 = CAUSAL ? (key0 / 64) : 0;  // 64-query steps
     n_ith = (p.N + 63) / 64 - it0;
     n_it = grp.G * n_ith;
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         clc_pending = true;
       };
       while (ok) {
-        const Item w(ix, iy, p);
+        const Item w(ix, iy, p, D);
         const int pre = w.n_it < 2 ? w.n_it : 2;  // stages issued before the block's K/V can be
         const int ask_at = w.n_it - 2 > 0 ? w.n_it - 2 : 0;
         int it = 0;
@@ -341,7 +352,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       int nb = 0;       // finished blocks
       bool ok = true;
       while (ok) {
-        const Item w(ix, iy, p);
+        const Item w(ix, iy, p, D);
         if (!wait_bar(b_kv, nb & 1, p.timeout_ns, abort_flag, WB_KV)) break;
         if (role < 2) {
           if (!score_ready(gs)) break;
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     int nb = 0;
     bool ok = true;
     while (ok) {
-      const Item w(ix, iy, p);
+      const Item w(ix, iy, p, D);
       for (int it = 0; it < w.n_it; ++it) {
         const uint32_t gq = gs + it, b = gq & 1, s = gq % NS;
         if (!__all_sync(0xffffffffu, wait_bar(b_sdp(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_SDP))) {
@@ -540,7 +551,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     int nb = 0;
     bool ok = true;
     while (ok) {
-      const Item w(ix, iy, p);
+      const Item w(ix, iy, p, D);
       for (int it = 0; DQACC && it < w.n_it; ++it) {
         const uint32_t gq = gs + it, b = gq & 1;
         const bool full =
