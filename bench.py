@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="time paged decode attention on the decode points instead (one JSON line each)")
     ap.add_argument("--decode-point", type=int, default=-1, help="with --decode: only this point (0-based)")
+    ap.add_argument("--decode-splits", default="0",
+                    help="with --decode: comma-separated split counts to time at every point (0 = the library's choice)")
     ap.add_argument("--shape", default="", help="B,H,N,d: time this bf16 causal shape instead (profiling)")
     ap.add_argument("--oracle-timing", action="store_true",
                     help="time the fp64 CPU oracle on the host cores: the small, pages and causal-4k workloads in "
@@ -796,47 +798,50 @@ def run_decode(args):
     flush = L2Flush(torch, dev)  # ~80 us of device work: longer than the host takes to enqueue the call
     steps, warmup = max(3, min(args.steps, 30)), max(3, args.warmup)
     points = DECODE_POINTS if args.decode_point < 0 else [DECODE_POINTS[args.decode_point]]
+    split_list = [int(x) for x in args.decode_splits.split(",")]
     for B, H, Hkv, Mq, d, ps, ctx in points:
         w = DecodeWorkload(B, H, Hkv, Mq, d, ps, ctx // ps, (ctx,) * B, spare=0, poison=False)
         q, kp, vp, table, cl = (t.to(dev) for t in make_paged_inputs(w))
         o, lse = fa.decode(q, kp, vp, table, cl)
-        n_split = fa.decode_splits(B, Hkv, d, ps, w.max_pages)
         L = _lib.load()
-        ws = torch.empty(int(L.fa_decode_workspace_size(B, H, Hkv, Mq, d, ps, w.max_pages, 0)), dtype=torch.uint8,
-                         device=dev)
-        stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-        args = (q.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(), cl.data_ptr(), o.data_ptr(),
-                lse.data_ptr(), ws.data_ptr(), ws.numel(), B, H, Hkv, Mq, d, ps, w.n_pages, w.max_pages, 0, w.scale,
-                0, 1, stream)
+        for forced in split_list:
+            n_split = forced if forced > 0 else fa.decode_splits(B, Hkv, d, ps, w.max_pages)
+            ws = torch.empty(int(L.fa_decode_workspace_size(B, H, Hkv, Mq, d, ps, w.max_pages, n_split)),
+                             dtype=torch.uint8, device=dev)
+            stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+            cargs = (q.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(), cl.data_ptr(), o.data_ptr(),
+                     lse.data_ptr(), ws.data_ptr(), ws.numel(), B, H, Hkv, Mq, d, ps, w.n_pages, w.max_pages, n_split,
+                     w.scale, 0, 1, stream)
 
-        def call():
-            rc = L.fa_decode(*args)
-            if rc != 0:
-                raise RuntimeError(f"fa_decode returned {rc}")
+            def call():
+                rc = L.fa_decode(*cargs)
+                if rc != 0:
+                    raise RuntimeError(f"fa_decode returned {rc}")
 
-        for _ in range(warmup):
-            flush()
-            call()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        host = []
-        for e0, e1 in evs:
-            flush()
-            e0.record()
-            h0 = time.perf_counter()
-            call()
-            host.append(time.perf_counter() - h0)
-            e1.record()
-        torch.cuda.synchronize()
-        code, info = fa.device_status()
-        if code != "FA_OK":
-            raise RuntimeError(f"{w.name()}: {code} {info}")
-        t = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
-        nbytes = w.kv_bytes() + 2 * q.numel() * 2 + 4 * lse.numel()
-        gbs = nbytes / t / 1e9
-        print(json.dumps({"point": w.name(), "us": 1e6 * t, "host_us": 1e6 * statistics.median(host),
-                          "n_split": n_split, "ctas": B * Hkv * n_split,
-                          "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_hbm": gbs / bw, "hbm_peak_gbs": bw,
-                          "peak_source": peak_src, "tflops": w.flops() / t / 1e12}), flush=True)
+            for _ in range(warmup):
+                flush()
+                call()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            host = []
+            for e0, e1 in evs:
+                flush()
+                e0.record()
+                h0 = time.perf_counter()
+                call()
+                host.append(time.perf_counter() - h0)
+                e1.record()
+            torch.cuda.synchronize()
+            code, info = fa.device_status()
+            if code != "FA_OK":
+                raise RuntimeError(f"{w.name()}: {code} {info}")
+            t = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+            nbytes = w.kv_bytes() + 2 * q.numel() * 2 + 4 * lse.numel()
+            gbs = nbytes / t / 1e9
+            print(json.dumps({"point": w.name(), "us": 1e6 * t, "host_us": 1e6 * statistics.median(host),
+                              "n_split": n_split, "library_choice": forced <= 0, "ctas": B * Hkv * n_split,
+                              "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_hbm": gbs / bw, "hbm_peak_gbs": bw,
+                              "peak_source": peak_src, "tflops": w.flops() / t / 1e12}), flush=True)
+            del ws
         del q, kp, vp, table, cl, o, lse
         torch.cuda.empty_cache()
 

@@ -85,6 +85,16 @@ fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
  */
 fa_status fa_selftest_ex2_rate(int reps, int blocks, float* sink, void* stream);
 
+/*
+ * The backward main kernels' work order: for every launch index
+ * i = x + heads * y of a grid of heads x nkb CTAs, out[i] = bh * nkb + kb, the
+ * K/V head and 128-key block that CTA (x, y) works on, as the kernels compute
+ * it (heads taken in groups whose shared rows, head_bytes each, fit in about
+ * 64 MB, longest blocks first within a group). out: DEVICE int[heads * nkb].
+ * 1 <= heads, 1 <= nkb, heads * nkb < 2^31, head_bytes >= 1.
+ */
+fa_status fa_selftest_block_order(int heads, int nkb, long long head_bytes, int* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -173,6 +173,11 @@ def test_decode_split_choice_and_workspace(L):
     assert L.fa_decode_splits(1, 8, 256, 64, 1024) <= 32
     assert L.fa_decode_splits(19, 8, 128, 64, 128) == 1  # 152 CTAs fill the GPU once: no split
     assert L.fa_decode_splits(1, 8, 96, 64, 16) == 0      # unsupported head dimension
+    # the counts that timed fastest among 1, 2, 3, 4, 6, 8, 12, 16, 24 on a GB300 (the first within 3%
+    # of 16, the fastest)
+    for args, best in (((1, 8, 128, 64, 1024), 19), ((16, 8, 128, 64, 128), 1), ((64, 1, 128, 16, 256), 2),
+                       ((32, 2, 64, 128, 64), 2), ((8, 8, 128, 256, 64), 2), ((8, 8, 256, 64, 128), 2)):
+        assert L.fa_decode_splits(*args) == best, args
     r256 = lambda x: (x + 255) // 256 * 256
     rows = 2 * 16 * 1
     for n_split in (1, 3):

@@ -12,6 +12,7 @@ import threading
 from .build import LIB_PATH
 
 c_int, c_float, c_size_t, c_void_p, c_uint = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_uint
+c_longlong = ctypes.c_longlong
 
 STATUS_NAMES = {
     0: "FA_OK",
@@ -72,6 +73,7 @@ SIGNATURES = [
     ("fa_selftest_gemm", c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     ("fa_selftest_wait_timeout", c_int, [ctypes.c_ulonglong, c_void_p]),
     ("fa_selftest_ex2_rate", c_int, [c_int, c_int, c_void_p, c_void_p]),
+    ("fa_selftest_block_order", c_int, [c_int, c_int, c_longlong, c_void_p, c_void_p]),
 ]
 
 _lock = threading.Lock()

@@ -146,7 +146,8 @@ int decode_tile_keys(int d) { return d == 256 ? 64 : 128; }
 int decode_max_splits(int d) { return d == 256 ? 32 : 64; }
 
 // Splits of the key range: with C = B * Hkv CTAs per split and 152 SMs, pick the count s that
-// minimises waves(C * s) * (tiles per split + 3), the 3 standing for a CTA's fixed cost in tiles.
+// minimises waves(C * s) * (tiles per split + 5), the 5 standing for a CTA's fixed cost in tiles
+// (fitted to GB300 timings of split counts 1-24 on six decode shapes).
 int decode_splits(int B, int Hkv, int d, int page_size, int max_pages) {
   const int bk = decode_tile_keys(d);
   const long long n_tiles = (static_cast<long long>(max_pages) * page_size + bk - 1) / bk;
@@ -155,7 +156,7 @@ int decode_splits(int B, int Hkv, int d, int page_size, int max_pages) {
   long long best_cost = -1;
   for (int s = 1; s <= decode_max_splits(d) && s <= n_tiles; ++s) {
     const long long waves = (ctas * s + 151) / 152;
-    const long long cost = waves * ((n_tiles + s - 1) / s + 3);
+    const long long cost = waves * ((n_tiles + s - 1) / s + 5);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;

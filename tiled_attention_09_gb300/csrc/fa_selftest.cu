@@ -13,6 +13,7 @@
 #include "../../include/fa.h"
 #include "../../include/fa_selftest.h"
 #include "common.cuh"
+#include "fa_bwd_order.cuh"
 #include "launch.h"
 
 namespace fa {
@@ -532,5 +533,28 @@ extern "C" fa_status fa_selftest_ex2_rate(int reps, int blocks, float* sink, voi
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
   fa::fa_ex2_rate_kernel<<<blocks, 512, 0, static_cast<cudaStream_t>(stream)>>>(reps, sink);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+namespace fa {
+namespace {
+__global__ void fa_block_order_kernel(int heads, int nkb, long long head_bytes, int* out) {
+  const long long n = static_cast<long long>(heads) * nkb;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int x = static_cast<int>(i % heads), y = static_cast<int>(i / heads);
+    int bh, kb;
+    bwd_block_order(x, y, heads, nkb, head_bytes, bh, kb);
+    out[i] = bh * nkb + kb;
+  }
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_selftest_block_order(int heads, int nkb, long long head_bytes, int* out, void* stream) {
+  if (!out) return FA_ERR_INVALID_ARG;
+  if (heads < 1 || nkb < 1 || head_bytes < 1 || static_cast<long long>(heads) * nkb >= (1ll << 31))
+    return FA_ERR_UNSUPPORTED;
+  fa::fa_block_order_kernel<<<256, 256, 0, static_cast<cudaStream_t>(stream)>>>(heads, nkb, head_bytes, out);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
