@@ -4,7 +4,7 @@ Checked: every (K/V head, key block) is worked on by exactly one CTA; each head'
 ascending order (block 0, the longest under causal masking, first); the heads come in contiguous groups
 of one size (the last may be smaller), each group's blocks all launched before the next group's; there
 are never more groups than max(1, heads * nkb / 304) (the tail bound); and a group's shared rows stay
-within 64 MB unless that bound, or a single head's rows, forbids it.
+within 64 MB unless a single head's rows exceed it or one head fewer per group would break that bound.
 """
 import ctypes
 
@@ -49,4 +49,5 @@ def test_block_order(heads, nkb, head_bytes):
     tail_bound = max(1, min(heads, heads * nkb // 304))
     assert n_groups <= tail_bound
     if hs * head_bytes > 64 * MB and hs > 1:
-        assert n_groups == tail_bound  # larger groups only where more groups would lengthen the tail
+        # larger groups only where smaller ones would make more groups than the tail bound allows
+        assert -(-heads // (hs - 1)) > tail_bound
