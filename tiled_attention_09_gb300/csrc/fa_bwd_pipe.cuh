@@ -8,8 +8,9 @@
 // produced transposed with one key per TMEM lane, and P^T / dS^T feed dV and dK
 // straight from TMEM. The schedule keeps the tensor core from waiting for the
 // elementwise warps:
-//   * S^T and dP^T of query tile i go to one of two TMEM buffers (i & 1);
-//   * S^T(i+1), dP^T(i+1) are issued into the other buffer *before* the
+//   * S^T and dP^T of query tile i go to one of NB TMEM buffers (i % NB: two for d = 128, three for
+//     d = 64, whose smaller accumulators leave the room);
+//   * S^T(i+1), dP^T(i+1) are issued into the next buffer *before* the
 //     issuers wait for P^T(i), dS^T(i), so the tensor core computes the next
 //     scores while the elementwise warps turn the current ones into P and dS;
 //   * dQ^T(i) = K^T dS^T(i) is written over S^T(i)'s columns once dV(i) has
@@ -19,7 +20,7 @@
 //   * for d = 64, dQ^T = K^T dS^T still has M = 128: a zeroed chunk after K
 //     pads K^T with 64 zero rows, whose dQ^T lanes are never read.
 // TMEM (512 columns): buffer b at 128b holds S^T/P^T (cols 0-63, then dQ^T)
-// and dP^T/dS^T (cols 64-127); dV at 256, dK at 384 (d columns each). Packed
+// and dP^T/dS^T (cols 64-127); dV at 128 NB, dK after it (d columns each). Packed
 // 16-bit P^T of queries 32g..32g+31 sits in columns 32g..32g+15 (dS^T likewise
 // from 64).
 // Roles (16 warps, 4 per SM sub-partition): warps 0-7 elementwise, in two
@@ -39,6 +40,9 @@ namespace fa {
 template <int D_>
 struct BwdPipeCfg {
   static constexpr int D = D_, BK = 128, BQ = 64, NCH = D / 64, NSTAGE = 3;
+  // TMEM buffers for S^T/dP^T (then dQ^T) of consecutive query steps: step g uses buffer g % NB. With
+  // d = 64 the dV and dK accumulators take 64 columns each, which leaves room for a third buffer.
+  static constexpr int NB = D < 128 ? 3 : 2;
   static constexpr int KV_CHUNK = BK * 128;   // 16 KB: 128 rows x 128 bytes (64 elements)
   static constexpr int KV_TILE = BK * D * 2;  // 32 KB (d = 128), 16 KB (d = 64)
   // dQ^T = K^T dS^T needs M = 128 rows of K^T: for d = 64 a zeroed chunk follows K, so the MMA
@@ -52,14 +56,14 @@ struct BwdPipeCfg {
   static constexpr int OFF_V = OFF_K + K_REGION;
   static constexpr int OFF_Q = OFF_V + KV_TILE;             // NSTAGE stages
   static constexpr int OFF_DO = OFF_Q + NSTAGE * Q_TILE;    // NSTAGE stages
-  static constexpr int OFF_DS = OFF_DO + NSTAGE * Q_TILE;   // 2 buffers
-  static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;       // 1 staging buffer
+  static constexpr int OFF_DS = OFF_DO + NSTAGE * Q_TILE;   // NB buffers
+  static constexpr int OFF_DQ = OFF_DS + NB * DS_TILE;      // 1 staging buffer
   static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;         // NSTAGE x BQ floats
   static constexpr int OFF_DD = OFF_LSE + NSTAGE * BQ * 4;  // NSTAGE x BQ floats
   static constexpr int OFF_BAR = OFF_DD + NSTAGE * BQ * 4;
-  // bars: kv, q_full[3], q_empty[3], sdp[2], ds[2], dq_full[2], dq_free[2], dv_done[2], done, drain[3],
+  // bars: kv, q_full[3], q_empty[3], sdp[NB], ds[NB], dq_full[NB], dq_free[NB], dv_done[NB], done, drain[3],
   // v_free, k_free, clc, item_full[2], item_empty[2]
-  static constexpr int NBAR = 1 + 2 * NSTAGE + 10 + 1 + 3 + 2 + 1 + 4;
+  static constexpr int NBAR = 1 + 2 * NSTAGE + 5 * NB + 1 + 3 + 2 + 1 + 4;
   static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
   // after the barriers: the 16-byte launch-control answer, the item queue (2 x {x, y}), TMEM slot + abort flag
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES + 16 + 16 + 16;
@@ -72,7 +76,8 @@ struct BwdPipeCfg {
   static_assert(128 * (2 * EW_REGS + LAUNCH_REGS + OTHER_REGS) <= THREADS * LAUNCH_REGS, "register split");
   static constexpr int ITEM_READERS = 3 + 8 + 1;  // the MMA threads, one lane per elementwise warp, read-out thread 0
   __host__ __device__ static constexpr uint32_t BUF(int b) { return 128u * b; }
-  static constexpr uint32_t DV_COL = 256, DK_COL = 256 + (D < 128 ? 128 : D);
+  static constexpr uint32_t DV_COL = 128u * NB, DK_COL = DV_COL + D;
+  static_assert(DK_COL + D <= 512, "TMEM budget");
   static_assert(D == 64 || D == 128, "d = 64 or 128");
   static_assert(SMEM_BYTES <= 232448, "smem budget");
 };
@@ -126,18 +131,19 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   const uint32_t b_kv = smem_u32(&bars[0]);
   auto b_qfull = [&](int s) { return smem_u32(&bars[1 + s]); };
   auto b_qempty = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
-  auto b_sdp = [&](int b) { return smem_u32(&bars[1 + 2 * NS + b]); };
-  auto b_ds = [&](int b) { return smem_u32(&bars[3 + 2 * NS + b]); };
-  auto b_dqfull = [&](int b) { return smem_u32(&bars[5 + 2 * NS + b]); };
-  auto b_dqfree = [&](int b) { return smem_u32(&bars[7 + 2 * NS + b]); };
-  auto b_dvdone = [&](int b) { return smem_u32(&bars[9 + 2 * NS + b]); };
-  const uint32_t b_done = smem_u32(&bars[11 + 2 * NS]);
-  auto b_drain = [&](int i) { return smem_u32(&bars[12 + 2 * NS + i]); };
-  const uint32_t b_vfree = smem_u32(&bars[15 + 2 * NS]);
-  const uint32_t b_kfree = smem_u32(&bars[16 + 2 * NS]);
-  const uint32_t b_clc = smem_u32(&bars[17 + 2 * NS]);
-  auto b_item_full = [&](int i) { return smem_u32(&bars[18 + 2 * NS + i]); };
-  auto b_item_empty = [&](int i) { return smem_u32(&bars[20 + 2 * NS + i]); };
+  constexpr int NB = C::NB, B0 = 1 + 2 * NS, B1 = B0 + 5 * NB;  // first per-buffer bar, first bar after them
+  auto b_sdp = [&](int b) { return smem_u32(&bars[B0 + b]); };
+  auto b_ds = [&](int b) { return smem_u32(&bars[B0 + NB + b]); };
+  auto b_dqfull = [&](int b) { return smem_u32(&bars[B0 + 2 * NB + b]); };
+  auto b_dqfree = [&](int b) { return smem_u32(&bars[B0 + 3 * NB + b]); };
+  auto b_dvdone = [&](int b) { return smem_u32(&bars[B0 + 4 * NB + b]); };
+  const uint32_t b_done = smem_u32(&bars[B1]);
+  auto b_drain = [&](int i) { return smem_u32(&bars[B1 + 1 + i]); };
+  const uint32_t b_vfree = smem_u32(&bars[B1 + 4]);
+  const uint32_t b_kfree = smem_u32(&bars[B1 + 5]);
+  const uint32_t b_clc = smem_u32(&bars[B1 + 6]);
+  auto b_item_full = [&](int i) { return smem_u32(&bars[B1 + 7 + i]); };
+  auto b_item_empty = [&](int i) { return smem_u32(&bars[B1 + 9 + i]); };
   const uint32_t clc_resp = smem_u32(aux + C::BAR_BYTES);
   volatile int* items = reinterpret_cast<volatile int*>(aux + C::BAR_BYTES + 16);  // [2][2]: x, y (x < 0: none)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + C::BAR_BYTES + 32);
@@ -153,7 +159,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       mbar_init(b_qfull(s), 1);
       mbar_init(b_qempty(s), 2);  // released by issuers A (after dV) and B (after dK)
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(b_sdp(b), 2);  // S^T from issuer A, dP^T from issuer B
       mbar_init(b_ds(b), 256);
       mbar_init(b_dqfull(b), 1);
@@ -326,24 +332,24 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       const uint64_t dDS_mn = make_sdesc(sDS, 128 * 128, 1024);                    // C: dS^T (MN-major)
       const uint32_t col = role == 0 ? 0u : 64u;  // A: S^T / P^T half of a buffer, B: dP^T / dS^T half
       const uint32_t acc_col = role == 0 ? C::DV_COL : C::DK_COL;
-      // A: S^T(g) = K Q_g^T ; B: dP^T(g) = V dO_g^T  (M = 128 keys, N = 64, K = d) into buffer g & 1,
+      // A: S^T(g) = K Q_g^T ; B: dP^T(g) = V dO_g^T  (M = 128 keys, N = 64, K = d) into buffer g % NB,
       // g counting query steps over all blocks
       auto issue_score = [&](uint32_t g) {
         const uint64_t so = static_cast<uint64_t>((g % NS) * C::Q_TILE) >> 4;
-        const uint32_t tb = tmem + C::BUF(g & 1) + col;
+        const uint32_t tb = tmem + C::BUF(g % NB) + col;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t oa = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
           const uint64_t ob = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
           mma_ss(tb, dKV_k + oa, dQO_k + so + ob, idesc_sdp, kk > 0 ? 1u : 0u);
         }
-        mma_commit(b_sdp(g & 1));
+        mma_commit(b_sdp(g % NB));
       };
-      // A: the buffer of step g still holds dQ^T(g - 2) until warps 8-11 have read it out
+      // A: the buffer of step g still holds dQ^T(g - NB) until warps 8-11 have read it out
       auto score_ready = [&](uint32_t g) -> bool {
         if (!wait_bar(b_qfull(g % NS), (g / NS) & 1, p.timeout_ns, abort_flag, WB_QF)) return false;
-        if (DQACC && role == 0 && g >= 2 &&
-            !wait_bar(b_dqfree(g & 1), ((g >> 1) - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE))
+        if (DQACC && role == 0 && g >= NB &&
+            !wait_bar(b_dqfree(g % NB), ((g / NB) - 1) & 1, p.timeout_ns, abort_flag, WB_DQFREE))
           return false;
         return true;
       };
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
           tc_fence_after();
           issue_score(gs);
           for (int it = 0; ok && it < w.n_it; ++it) {
-            const uint32_t g = gs + it, b = g & 1;
+            const uint32_t g = gs + it, b = g % NB;
             if (it + 1 < w.n_it) {  // the next step's scores go to the other buffer first
               if (!score_ready(g + 1)) {
                 ok = false;
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
               tc_fence_after();
               issue_score(g + 1);
             }
-            if (!wait_bar(b_ds(b), (g >> 1) & 1, p.timeout_ns, abort_flag, WB_DS) ||
+            if (!wait_bar(b_ds(b), (g / NB) & 1, p.timeout_ns, abort_flag, WB_DS) ||
                 (it == 0 && nb > 0 &&
                  !wait_bar(role == 0 ? b_vfree : b_kfree, (nb - 1) & 1, p.timeout_ns, abort_flag, WB_DONE))) {
               ok = false;
@@ -391,9 +397,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         } else if constexpr (DQACC) {
           // C: dQ^T(g) = K^T dS^T(g) over S^T(g)'s columns (M = d, N = 64 queries, K = 128 keys)
           for (int it = 0; ok && it < w.n_it; ++it) {
-            const uint32_t g = gs + it, b = g & 1;
-            if (!wait_bar(b_ds(b), (g >> 1) & 1, p.timeout_ns, abort_flag, WB_DS) ||
-                !wait_bar(b_dvdone(b), (g >> 1) & 1, p.timeout_ns, abort_flag, WB_DS)) {
+            const uint32_t g = gs + it, b = g % NB;
+            if (!wait_bar(b_ds(b), (g / NB) & 1, p.timeout_ns, abort_flag, WB_DS) ||
+                !wait_bar(b_dvdone(b), (g / NB) & 1, p.timeout_ns, abort_flag, WB_DS)) {
               ok = false;
               break;
             }
@@ -435,8 +441,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     while (ok) {
       const Item w(ix, iy, p, D);
       for (int it = 0; it < w.n_it; ++it) {
-        const uint32_t gq = gs + it, b = gq & 1, s = gq % NS;
-        if (!__all_sync(0xffffffffu, wait_bar(b_sdp(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_SDP))) {
+        const uint32_t gq = gs + it, b = gq % NB, s = gq % NS;
+        if (!__all_sync(0xffffffffu, wait_bar(b_sdp(b), (gq / NB) & 1, p.timeout_ns, abort_flag, WB_SDP))) {
           ok = false;
           break;
         }
@@ -553,9 +559,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     while (ok) {
       const Item w(ix, iy, p, D);
       for (int it = 0; DQACC && it < w.n_it; ++it) {
-        const uint32_t gq = gs + it, b = gq & 1;
+        const uint32_t gq = gs + it, b = gq % NB;
         const bool full =
-            __all_sync(0xffffffffu, wait_bar(b_dqfull(b), (gq >> 1) & 1, p.timeout_ns, abort_flag, WB_DQF));
+            __all_sync(0xffffffffu, wait_bar(b_dqfull(b), (gq / NB) & 1, p.timeout_ns, abort_flag, WB_DQF));
         uint32_t u0[32], u1[32];
         if (full) {
           tc_fence_after();
