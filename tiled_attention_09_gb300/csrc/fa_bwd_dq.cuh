@@ -127,7 +127,10 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
-    mbar_init(b_qfree, 2);  // the S issuer after its item's last S, the dP issuer after its last dP
+    // the S issuer after its item's last S, the dP issuer after its last dP, and each elementwise warp
+    // once it has taken the item's Q stage: without these eight, issuers two short items ahead of the
+    // elementwise warps would let q_full complete twice past a parity those warps still wait for
+    mbar_init(b_qfree, 2 + 8);
     for (int s = 0; s < NSK; ++s) {
       mbar_init(b_kfull(s), 1);
       mbar_init(b_kempty(s), 1);
@@ -189,7 +192,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
       };
       while (ok) {
         const Item w(ix, iy, p);
-        // Q, dO of the previous item are dead once its last S and dP products have completed
+        // Q, dO of the previous item are dead once its last S and dP products have completed and every
+        // elementwise warp has taken its stage (and LSE / D buffer)
         if (n_items > 0 && !wait_bar(b_qfree, (n_items - 1) & 1, p.timeout_ns, abort_flag, WQ_Q)) break;
         const int li = n_items & 1;  // LSE / D buffer of this item
         const int qrow = w.qh * p.Npad + w.q0;
@@ -397,6 +401,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
       if (!__all_sync(0xffffffffu, wait_bar(b_qfull, n_items & 1, p.timeout_ns, abort_flag, WQ_Q))) break;
       const float lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + li * C::BQ * 4)[r];
       const float dd = reinterpret_cast<const float*>(smem + C::OFF_DD + li * C::BQ * 4)[r];
+      __syncwarp();
+      if (lane0) mbar_arrive(b_qfree);  // this warp has passed q_full of the item (and read LSE, D)
       const int q = w.q0 + r;  // query row within the head
       // keys this row may see: those that exist, and (causal) none past the query itself
       const int klim = (CAUSAL && w.klen > q + 1) ? q + 1 : w.klen;

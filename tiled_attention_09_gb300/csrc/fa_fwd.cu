@@ -85,9 +85,13 @@ struct FwdCfg {
   static constexpr int TILE = 128 * D * 2;                        // one 128-row tile
   static constexpr int NS = (D == 64) ? 6 : (D == 128 ? 4 : 2);   // ring slots
   static constexpr int SMEM_Q = NT * TILE;
+  // d = 64: P_t gets its own TMEM columns (O_t is only 64 wide, so they fit), and S_t(j+1) can be
+  // computed as soon as the softmax has read S_t(j), while P_t(j) is still being formed
+  static constexpr bool SEP_P = D == 64;
   static constexpr int SMEM_RING = NS * TILE;
-  // q, qfree, full[NS], empty[NS], s[NT], p[NT], o[NT], ofree[NT], clc, item_full[2], item_empty[2], drain
-  static constexpr int NBAR = 2 + 2 * NS + 4 * NT + 1 + 4 + 1;
+  // q, qfree, full[NS], empty[NS], s[NT], p[NT], o[NT], ofree[NT], clc, item_full[2], item_empty[2], drain,
+  // sfree[NT], pv[NT]
+  static constexpr int NBAR = 2 + 2 * NS + 4 * NT + 1 + 4 + 1 + 2 * NT;
   static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
   // after the barriers: the 16-byte launch-control answer, the item queue (2 x {x, y}), TMEM slot + abort flag
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + BAR_BYTES + 16 + 16 + 16;
@@ -104,7 +108,10 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + D * t; }
+  // packed 16-bit P_t: over S_t's first 64 columns, or (SEP_P) in its own 64 columns after O
+  __host__ __device__ static constexpr uint32_t P_COL(int t) { return SEP_P ? 256u + NT * D + 64u * t : S_COL(t); }
   static_assert(O_COL(NT - 1) + D <= TMEM_COLS, "TMEM budget");
+  static_assert(P_COL(NT - 1) + 64 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
 };
 
@@ -220,7 +227,7 @@ __device__ __forceinline__ uint32_t pack2_residual(float a, float b, uint32_t& r
 // where-codes for timeouts
 enum : uint32_t {
   W_Q = 1, W_RING_EMPTY = 2, W_RING_FULL = 3, W_P = 4, W_S = 5, W_O = 6, W_DRAIN = 7,
-  W_QFREE = 8, W_CLC = 9, W_ITEM = 10, W_OFREE = 11,
+  W_QFREE = 8, W_CLC = 9, W_ITEM = 10, W_OFREE = 11, W_SFREE = 12, W_PV = 13,
   B_CLC_ID = 20  // where-code for FA_DEV_BAD_INDEX
 };
 
@@ -249,6 +256,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
   auto b_item_full = [&](int i) { return smem_u32(&bars[3 + 2 * C::NS + 4 * NT + i]); };
   auto b_item_empty = [&](int i) { return smem_u32(&bars[5 + 2 * C::NS + 4 * NT + i]); };
   const uint32_t b_drain = smem_u32(&bars[7 + 2 * C::NS + 4 * NT]);
+  auto b_sfree = [&](int t) { return smem_u32(&bars[8 + 2 * C::NS + 4 * NT + t]); };    // SEP_P: S_t read
+  auto b_pv = [&](int t) { return smem_u32(&bars[8 + 2 * C::NS + 5 * NT + t]); };       // SEP_P: P_t V done
   const uint32_t clc_resp = smem_u32(aux + C::BAR_BYTES);
   volatile int* items = reinterpret_cast<volatile int*>(aux + C::BAR_BYTES + 16);  // [2][2]: x, y (x < 0: none)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + C::BAR_BYTES + 32);
@@ -276,6 +285,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       mbar_init(b_item_empty(i), 1 + 4 * NT);  // the MMA thread and one lane per softmax warp
     }
     mbar_init(b_drain, 1);
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(b_sfree(t), 128);
+      mbar_init(b_pv(t), 1);
+    }
     *abort_flag = 0u;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -397,6 +410,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       uint32_t seq = 0;        // ring position of the item's K_0
       uint32_t n_p[NT] = {};   // P_t tiles consumed
       uint32_t n_o[NT] = {};   // items in which tile t produced an output
+      uint32_t n_si[NT] = {};  // S_t tiles issued (SEP_P)
       int n_items = 0;
       bool ok = true;
       while (ok) {
@@ -408,6 +422,58 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           if (j < w.nmax && !wait_bar(b_full(sK % C::NS), (sK / C::NS) & 1, p.timeout_ns, abort_flag, W_RING_FULL))
             break;
           tc_fence_after();
+          if constexpr (C::SEP_P) {
+            // S_t(j) first, each once the softmax has read S_t's previous tile (P has its own
+            // columns), then P_t(j-1) V for each tile as its P is ready
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              if (j < w.n_t[t]) {
+                if (n_si[t] > 0 &&
+                    !wait_bar(b_sfree(t), (n_si[t] - 1) & 1, p.timeout_ns, abort_flag, W_SFREE)) {
+                  ok = false;
+                  break;
+                }
+                ++n_si[t];
+                tc_fence_after();
+                const uint64_t dk = dk0 + static_cast<uint64_t>(((sK % C::NS) * C::TILE) >> 4);
+                const uint64_t dq = dq0 + static_cast<uint64_t>((t * C::TILE) >> 4);
+                const uint32_t tS = tmem + C::S_COL(t);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                  const uint64_t off = static_cast<uint64_t>(((k >> 2) * C::CHUNK + (k & 3) * 32) >> 4);
+                  mma_ss(tS, dq + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
+                }
+                mma_commit(b_s(t));
+              }
+            }
+            if (!ok) break;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              if (j >= 1 && j <= w.n_t[t]) {
+                if (!wait_bar(b_p(t), n_p[t] & 1, p.timeout_ns, abort_flag, W_P)) {
+                  ok = false;
+                  break;
+                }
+                ++n_p[t];
+                if (j == 1 && n_o[t] > 0 && !wait_bar(b_ofree(t), (n_o[t] - 1) & 1, p.timeout_ns, abort_flag, W_OFREE)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t dv = dv0 + static_cast<uint64_t>(((sV % C::NS) * C::TILE) >> 4);
+                const uint32_t tO = tmem + C::O_COL(t), tP = tmem + C::P_COL(t);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  mma_ts(tO, tP + k * 8, dv + static_cast<uint64_t>(k * (2048 >> 4)), idesc_pv,
+                         (j > 1 || k > 0) ? 1u : 0u);
+                mma_commit(b_pv(t));  // P_t's columns may take the next P; O_t may be rescaled
+                if (j == w.n_t[t]) {
+                  mma_commit(b_o(t));
+                  ++n_o[t];
+                }
+              }
+            }
+          } else {
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             if (j >= 1 && j <= w.n_t[t]) {
@@ -444,6 +510,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
               mma_commit(b_s(t));
             }
           }
+          }
           if (!ok) break;
           if (j == w.nmax - 1) mma_commit(b_qfree);  // every S MMA of the item has been issued
           if (j < w.nmax) mma_commit(b_empty(sK % C::NS));
@@ -477,6 +544,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::S_COL(t);
     const uint32_t tO = tmem + lane_off + C::O_COL(t);
+    const uint32_t tP = tmem + lane_off + C::P_COL(t);
     const float sl2 = p.scale_log2;
     int ix = blockIdx.x, iy = blockIdx.y;
     uint32_t n_s = 0;  // S_t tiles consumed
@@ -506,6 +574,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(u[i]);
         }
+        if constexpr (C::SEP_P) {  // S_t may take the next tile's scores now
+          tc_fence_before();
+          mbar_arrive(b_sfree(t));
+        }
+        // SEP_P: P_t's columns and O_t are the previous P_t V's until it completes (S_t no longer
+        // announces it); wait for it before the rescale or the P store, whichever comes first
+        bool pv_seen = !C::SEP_P || n_s < 2;
+        auto wait_pv = [&]() -> bool {
+          if (pv_seen) return true;
+          pv_seen = true;
+          if (!__all_sync(0xffffffffu, wait_bar(b_pv(t), (n_s - 2) & 1, p.timeout_ns, abort_flag, W_PV))) return false;
+          tc_fence_after();
+          return true;
+        };
         // keys this row may not see: past the query itself (causal, diagonal tile), past the end of
         // the sequence or past the batch's key count (last tiles); all 128 of them only for a row
         // that sees no key at all (key count 0)
@@ -565,13 +647,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           const float m_new = x_max + m_used;
           const bool rescale = m_new > m_used + p.rescale_threshold;
           if (__any_sync(0xffffffffu, rescale)) {
+            if (!wait_pv()) {
+              ok = false;
+              break;
+            }
             const float alpha = rescale ? ex2_approx(m_used - m_new) : 1.f;
             if (rescale) {
               m_used = m_new;
               l *= alpha;
               l_fix *= alpha;
             }
-            // the commit that announced S_t(j) also covers P_t(j-1) V: O_t is quiescent
+            // O_t is quiescent: the commit that announced S_t(j) also covers P_t(j-1) V (or, SEP_P,
+            // that product has been waited for above)
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t u[32];
@@ -591,7 +678,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           }
         }
         l += ls0 + ls1;
-        tmem_st64(tS, pk);
+        if (!wait_pv()) {
+          ok = false;
+          break;
+        }
+        tmem_st64(tP, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_p(t));
