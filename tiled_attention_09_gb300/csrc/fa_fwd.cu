@@ -647,9 +647,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           const float m_new = x_max + m_used;
           const bool rescale = m_new > m_used + p.rescale_threshold;
           if (__any_sync(0xffffffffu, rescale)) {
-            if (!wait_pv()) {
-              ok = false;
-              break;
+            if constexpr (C::SEP_P) {
+              if (!wait_pv()) {
+                ok = false;
+                break;
+              }
             }
             const float alpha = rescale ? ex2_approx(m_used - m_new) : 1.f;
             if (rescale) {
@@ -678,9 +680,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
           }
         }
         l += ls0 + ls1;
-        if (!wait_pv()) {
-          ok = false;
-          break;
+        if constexpr (C::SEP_P) {
+          if (!wait_pv()) {
+            ok = false;
+            break;
+          }
         }
         tmem_st64(tP, pk);
         tmem_st_wait();
