@@ -90,8 +90,8 @@ struct FwdCfg {
   static constexpr bool SEP_P = D == 64;
   static constexpr int SMEM_RING = NS * TILE;
   // q, qfree, full[NS], empty[NS], s[NT], p[NT], o[NT], ofree[NT], clc, item_full[2], item_empty[2], drain,
-  // sfree[NT], pv[NT]
-  static constexpr int NBAR = 2 + 2 * NS + 4 * NT + 1 + 4 + 1 + 2 * NT;
+  // and with SEP_P sfree[NT], pv[NT]
+  static constexpr int NBAR = 2 + 2 * NS + 4 * NT + 1 + 4 + 1 + (SEP_P ? 2 * NT : 0);
   static constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
   // after the barriers: the 16-byte launch-control answer, the item queue (2 x {x, y}), TMEM slot + abort flag
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + BAR_BYTES + 16 + 16 + 16;
@@ -285,9 +285,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       mbar_init(b_item_empty(i), 1 + 4 * NT);  // the MMA thread and one lane per softmax warp
     }
     mbar_init(b_drain, 1);
-    for (int t = 0; t < NT; ++t) {
-      mbar_init(b_sfree(t), 128);
-      mbar_init(b_pv(t), 1);
+    if constexpr (C::SEP_P) {
+      for (int t = 0; t < NT; ++t) {
+        mbar_init(b_sfree(t), 128);
+        mbar_init(b_pv(t), 1);
+      }
     }
     *abort_flag = 0u;
     mbar_fence_init();
@@ -544,7 +546,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::S_COL(t);
     const uint32_t tO = tmem + lane_off + C::O_COL(t);
-    const uint32_t tP = tmem + lane_off + C::P_COL(t);
+    const uint32_t tP = C::SEP_P ? tmem + lane_off + C::P_COL(t) : tS;
     const float sl2 = p.scale_log2;
     int ix = blockIdx.x, iy = blockIdx.y;
     uint32_t n_s = 0;  // S_t tiles consumed
