@@ -131,3 +131,23 @@ def test_dq_pass_refuses_d256():
     o, lse = fa.fwd(q, k, v, causal=True)
     with pytest.raises(fa.FAError, match="FA_ERR_UNSUPPORTED"):
         fa.bwd(q, k, v, o, lse, do, causal=True, dq_mode="separate")
+
+
+@pytest.mark.parametrize("w", [Workload(1, 48, 256, 128, "bf16", True), Workload(2, 16, 384, 64, "fp16", True)],
+                         ids=lambda w: w.name())
+def test_dq_pass_many_short_items_repeated(w):
+    """Items with one or two key tiles back to back (short causal heads): the issuers finish an item long
+    before the elementwise warps have stored the previous one's dQ. Repeated calls must all complete
+    (no wait running out) and give the same dQ as the first, equal to the accumulating path's within tolerance."""
+    q, k, v, do = (t.cuda() for t in make_inputs(w))
+    o, lse, o_lo = fa.fwd(q, k, v, causal=True, residual=True)
+    dq0, _, _ = fa.bwd(q, k, v, o, lse, do, causal=True, o_lo=o_lo, dq_mode="separate")
+    for _ in range(20):
+        dq, _, _ = fa.bwd(q, k, v, o, lse, do, causal=True, o_lo=o_lo, dq_mode="separate")
+    torch.cuda.synchronize()
+    code, info = fa.device_status()
+    assert code == "FA_OK", info
+    assert torch.equal(dq, dq0)
+    dqa, _, _ = fa.bwd(q, k, v, o, lse, do, causal=True, o_lo=o_lo, dq_mode="accumulate")
+    torch.cuda.synchronize()
+    check_grad(to64(dq0), to64(dqa), "dQ separate vs accumulate")
