@@ -85,9 +85,10 @@ struct FwdCfg {
   static constexpr int TILE = 128 * D * 2;                        // one 128-row tile
   static constexpr int NS = (D == 64) ? 6 : (D == 128 ? 4 : 2);   // ring slots
   static constexpr int SMEM_Q = NT * TILE;
-  // d = 64: P_t gets its own TMEM columns (O_t is only 64 wide, so they fit), and S_t(j+1) can be
-  // computed as soon as the softmax has read S_t(j), while P_t(j) is still being formed
-  static constexpr bool SEP_P = D == 64;
+  // d = 64 and 256: P_t gets its own TMEM columns (d = 64: O_t is only 64 wide; d = 256: one query
+  // tile leaves 128 columns between S and O), and S_t(j+1) can be computed as soon as the softmax has
+  // read S_t(j), while P_t(j) is still being formed
+  static constexpr bool SEP_P = D == 64 || D == 256;
   static constexpr int SMEM_RING = NS * TILE;
   // q, qfree, full[NS], empty[NS], s[NT], p[NT], o[NT], ofree[NT], clc, item_full[2], item_empty[2], drain,
   // and with SEP_P sfree[NT], pv[NT]
@@ -108,8 +109,12 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + D * t; }
-  // packed 16-bit P_t: over S_t's first 64 columns, or (SEP_P) in its own 64 columns after O
-  __host__ __device__ static constexpr uint32_t P_COL(int t) { return SEP_P ? 256u + NT * D + 64u * t : S_COL(t); }
+  // packed 16-bit P_t: over S_t's first 64 columns, or (SEP_P) in its own 64 columns: after O (d = 64),
+  // between S and O (d = 256)
+  __host__ __device__ static constexpr uint32_t P_COL(int t) {
+    return SEP_P ? (D == 64 ? 256u + NT * D + 64u * t : 128u + 64u * t) : S_COL(t);
+  }
+  static_assert(!SEP_P || D == 64 || P_COL(NT - 1) + 64 <= O_COL(0), "P between S and O");
   static_assert(O_COL(NT - 1) + D <= TMEM_COLS, "TMEM budget");
   static_assert(P_COL(NT - 1) + 64 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
