@@ -14,8 +14,8 @@
 //     issuers wait for P^T(i), dS^T(i), so the tensor core computes the next
 //     scores while the elementwise warps turn the current ones into P and dS;
 //   * dQ^T(i) = K^T dS^T(i) is written over S^T(i)'s columns once dV(i) has
-//     read P^T(i) from them, and read out before S^T(i+2) reuses the buffer;
-//   * dS^T goes to a double-buffered shared-memory tile (the dQ operand), and
+//     read P^T(i) from them, and read out before S^T(i+NB) reuses the buffer;
+//   * dS^T goes to one of NB shared-memory tiles (the dQ operand), and
 //     Q, dO, LSE*log2e, D stream through a three-stage TMA ring;
 //   * for d = 64, dQ^T = K^T dS^T still has M = 128: a zeroed chunk after K
 //     pads K^T with 64 zero rows, whose dQ^T lanes are never read.
@@ -30,7 +30,8 @@
 // DQACC = false is the kernel for the separate dQ pass (fa_bwd_dq.cuh): it
 // computes dK and dV only, so no dQ^T product, no dS^T tile in shared memory and
 // no read-out; a buffer is then refilled as soon as the same issuer's dV / dK of
-// two steps before (issued earlier by that thread, executed in order) have read it.
+// NB steps before (issued earlier by that thread, executed in order) have read it.
+// Key blocks run in the L2-grouped launch order of fa_bwd_order.cuh.
 #pragma once
 #include "fa_bwd_main.cuh"
 #include "fa_bwd_order.cuh"
