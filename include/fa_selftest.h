@@ -95,6 +95,17 @@ fa_status fa_selftest_ex2_rate(int reps, int blocks, float* sink, void* stream);
  */
 fa_status fa_selftest_block_order(int heads, int nkb, long long head_bytes, int* out, void* stream);
 
+/*
+ * Copy-rate microbenchmark of the GPU's own loads and stores: `blocks` CTAs of
+ * 512 threads copy `bytes` from src to dst in 16-byte vectors (grid-stride),
+ * where src and dst may be device memory or pinned host memory (which the
+ * GPU addresses directly, through the mapping CUDA reports for it); the
+ * caller times the launch. Memory that CUDA reports neither as device
+ * memory nor as mapped pinned host memory is refused (FA_ERR_INVALID_ARG). src, dst: 16-byte aligned, bytes a multiple of 16,
+ * 1 <= blocks <= 65535.
+ */
+fa_status fa_selftest_copy(const void* src, void* dst, size_t bytes, int blocks, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

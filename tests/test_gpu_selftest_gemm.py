@@ -115,3 +115,26 @@ def test_mma_pattern_microbenchmark(n, a_tmem, a_mn, b_mn, issuers, mode):
           f"{per_mma:.1f} cycles/instr, {2 * 128 * n * 16 / per_mma:.0f} FLOP/clk/SM, "
           f"{smem_bytes / per_mma:.0f} operand B/clk")
     assert per_mma >= n / 2 * 0.95
+
+
+def test_selftest_copy_between_device_and_pinned_host():
+    """fa_selftest_copy (the host-link copy-rate microbenchmark) copies exactly, device to device, pinned host to
+    device and device to pinned host, and refuses memory CUDA does not report as device or pinned host memory."""
+    import ctypes as _ct
+    from tiled_attention_09_gb300 import _lib as _l
+    L = _l.load()
+    n = (1 << 20) + 48
+    src_h = torch.randint(0, 255, (n,), dtype=torch.uint8).pin_memory()
+    dst_d = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    dst_h = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    d2 = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    st = _ct.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.fa_selftest_copy(src_h.data_ptr(), dst_d.data_ptr(), n, 7, st) == 0
+    assert L.fa_selftest_copy(dst_d.data_ptr(), d2.data_ptr(), n, 3, st) == 0
+    assert L.fa_selftest_copy(d2.data_ptr(), dst_h.data_ptr(), n, 152, st) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(dst_h, src_h) and torch.equal(d2.cpu(), src_h)
+    pageable = torch.zeros(n, dtype=torch.uint8)
+    assert L.fa_selftest_copy(pageable.data_ptr(), dst_d.data_ptr(), n, 4, st) == 1  # FA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert L.fa_selftest_copy(src_h.data_ptr(), dst_d.data_ptr(), n - 8, 4, st) == 3  # not a multiple of 16

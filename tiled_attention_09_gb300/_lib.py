@@ -74,6 +74,7 @@ SIGNATURES = [
     ("fa_selftest_wait_timeout", c_int, [ctypes.c_ulonglong, c_void_p]),
     ("fa_selftest_ex2_rate", c_int, [c_int, c_int, c_void_p, c_void_p]),
     ("fa_selftest_block_order", c_int, [c_int, c_int, c_longlong, c_void_p, c_void_p]),
+    ("fa_selftest_copy", c_int, [c_void_p, c_void_p, c_size_t, c_int, c_void_p]),
 ]
 
 _lock = threading.Lock()

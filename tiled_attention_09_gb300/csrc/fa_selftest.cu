@@ -558,3 +558,51 @@ extern "C" fa_status fa_selftest_block_order(int heads, int nkb, long long head_
   fa::fa_block_order_kernel<<<256, 256, 0, static_cast<cudaStream_t>(stream)>>>(heads, nkb, head_bytes, out);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+namespace fa {
+namespace {
+__global__ void __launch_bounds__(512) fa_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                      size_t n) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n; i += 4 * stride) {  // four loads in flight per thread
+    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < n; i += stride) dst[i] = src[i];
+}
+}  // namespace
+}  // namespace fa
+
+// The address the GPU uses for p: device (or managed) memory as it is, pinned host memory through its
+// mapping; anything else (pageable host memory) is refused.
+static bool fa_gpu_address(const void* p, const void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return true;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+    *out = a.devicePointer;
+    return true;
+  }
+  return false;
+}
+
+extern "C" fa_status fa_selftest_copy(const void* src, void* dst, size_t bytes, int blocks, void* stream) {
+  if (!src || !dst) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | bytes) & 15) return FA_ERR_ALIGNMENT;
+  if (blocks < 1 || blocks > 65535) return FA_ERR_UNSUPPORTED;
+  const void *gs = nullptr, *gd = nullptr;
+  if (!fa_gpu_address(src, &gs) || !fa_gpu_address(dst, &gd)) return FA_ERR_INVALID_ARG;
+  fa::fa_copy_kernel<<<blocks, 512, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(gs), static_cast<uint4*>(const_cast<void*>(gd)), bytes / 16);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
