@@ -53,6 +53,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "fa_bwd_order.cuh"
 #include "launch.h"
 
 namespace fa {
@@ -123,7 +124,8 @@ struct FwdCfg {
 // One work item: NT consecutive query tiles of one (b, h) head, named by the
 // blockIdx of the CTA that was launched for it (x = head, y = launch rank x key
 // split; under causal masking rank 0 is the last and heaviest query block, so the
-// hardware's launch order is longest-first). With split keys (kv_splits = S > 1)
+// hardware's launch order is longest-first; for d = 256 without a split the kernel
+// maps the launch index through the backward's order first, see item_order). With split keys (kv_splits = S > 1)
 // the item is one of S contiguous ranges of the block's key tiles, [kt0, kt1):
 // each range writes its own normalised partial O and LSE and a merge pass joins
 // them by the online-softmax rule (O = sum_s e^(LSE_s - LSE) O_s).
@@ -242,6 +244,14 @@ template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   using Item = FwdItem<C::NT, CAUSAL, SPLIT>;
+  // d = 256 without a split: a launch index (x, y) is first mapped through the backward's launch order
+  // (fa_bwd_order.cuh; K and V of a head are 4 N d bytes), so the items in flight share a few heads' K
+  // and V in L2 (its two-slot K/V ring makes it wait on every load); every role maps its own first
+  // item, and the producer maps each taken-over id before it queues it. (d = 64 and 128 measured no
+  // gain from it.)
+  auto item_order = [&](int& x, int& y) {
+    if constexpr (!SPLIT && D == 256) bwd_block_order(x, y, gridDim.x, gridDim.y, 4ll * p.N * D, x, y);
+  };
   constexpr int NT = C::NT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -325,6 +335,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       int ix = blockIdx.x, iy = blockIdx.y;
+      item_order(ix, iy);
       uint32_t seq = 0;      // K/V loads issued (ring position)
       int n_items = 0;       // items whose loads were issued
       bool clc_live = true;  // no "nothing left" answer yet
@@ -383,6 +394,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
             report_status(FA_DEV_BAD_INDEX, B_CLC_ID);
             clc_live = false;
             nx = -1;
+          } else {
+            item_order(nx, ny);  // the queue holds mapped ids
           }
         }
         const int qi = n_items - 1;  // queue entry qi names the item after item qi
@@ -414,6 +427,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
       const uint64_t dk0 = make_sdesc(sRing, 16, 1024);        // K in a ring slot, K-major
       const uint64_t dv0 = make_sdesc(sRing, C::CHUNK, 1024);  // V in a ring slot, MN-major
       int ix = blockIdx.x, iy = blockIdx.y;
+      item_order(ix, iy);
       uint32_t seq = 0;        // ring position of the item's K_0
       uint32_t n_p[NT] = {};   // P_t tiles consumed
       uint32_t n_o[NT] = {};   // items in which tile t produced an output
@@ -554,6 +568,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
     const uint32_t tP = C::SEP_P ? tmem + lane_off + C::P_COL(t) : tS;
     const float sl2 = p.scale_log2;
     int ix = blockIdx.x, iy = blockIdx.y;
+    item_order(ix, iy);
     uint32_t n_s = 0;  // S_t tiles consumed
     uint32_t n_o = 0;  // outputs written
     int n_items = 0;
