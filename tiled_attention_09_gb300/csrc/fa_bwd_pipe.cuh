@@ -14,7 +14,11 @@
 //     issuers wait for P^T(i), dS^T(i), so the tensor core computes the next
 //     scores while the elementwise warps turn the current ones into P and dS;
 //   * dQ^T(i) = K^T dS^T(i) is written over S^T(i)'s columns once dV(i) has
-//     read P^T(i) from them, and read out before S^T(i+NB) reuses the buffer;
+//     read P^T(i) from them, and read out before S^T(i+NB) reuses the buffer:
+//     each read-out thread holds one row of dQ^T (a d index, 64 queries) and adds
+//     it into the fp32 accumulator with global reductions, one coalesced 128-byte
+//     row segment per warp instruction (a shared staging tile drained by bulk
+//     reductions measured 6% slower at d = 64 and no faster at d = 128);
 //   * dS^T goes to one of NB shared-memory tiles (the dQ operand), and
 //     Q, dO, LSE*log2e, D stream through a three-stage TMA ring;
 //   * for d = 64, dQ^T = K^T dS^T still has M = 128: a zeroed chunk after K
@@ -52,14 +56,12 @@ struct BwdPipeCfg {
   static constexpr int Q_CHUNK = BQ * 128;    // 8 KB
   static constexpr int Q_TILE = BQ * D * 2;   // 16 KB (d = 128), 8 KB (d = 64)
   static constexpr int DS_TILE = BK * BQ * 2;  // 16 KB: dS^T [128 keys][64 queries]
-  static constexpr int DQ_STAGE = BQ * D * 4;  // fp32 [64 queries][d]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + K_REGION;
   static constexpr int OFF_Q = OFF_V + KV_TILE;             // NSTAGE stages
   static constexpr int OFF_DO = OFF_Q + NSTAGE * Q_TILE;    // NSTAGE stages
   static constexpr int OFF_DS = OFF_DO + NSTAGE * Q_TILE;   // NB buffers
-  static constexpr int OFF_DQ = OFF_DS + NB * DS_TILE;      // 1 staging buffer
-  static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;         // NSTAGE x BQ floats
+  static constexpr int OFF_LSE = OFF_DS + NB * DS_TILE;     // NSTAGE x BQ floats
   static constexpr int OFF_DD = OFF_LSE + NSTAGE * BQ * 4;  // NSTAGE x BQ floats
   static constexpr int OFF_BAR = OFF_DD + NSTAGE * BQ * 4;
   // bars: kv, q_full[3], q_empty[3], sdp[NB], ds[NB], dq_full[NB], dq_free[NB], dv_done[NB], done, drain[3],
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q, sDO = s0 + C::OFF_DO;
-  const uint32_t sDS = s0 + C::OFF_DS, sDQ = s0 + C::OFF_DQ;
+  const uint32_t sDS = s0 + C::OFF_DS;
   uint8_t* aux = smem + C::OFF_BAR;
   uint64_t* bars = reinterpret_cast<uint64_t*>(aux);
   const uint32_t b_kv = smem_u32(&bars[0]);
@@ -548,8 +550,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
     __syncthreads();
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ read-out; dK epilogue
-    // The four warps of this group share the staging buffer through named barrier 2, so their
-    // control flow stays uniform: each of the group's barriers also ANDs every thread's "no
+    // The four warps of this group meet at named barrier 2 once a step and at the dK epilogue, so
+    // their control flow stays uniform: each of the group's barriers also ANDs every thread's "no
     // timeout" flag (bar.red.and), and thread 0 reads the item queue for the whole group.
     const int t = threadIdx.x - 256;  // TMEM lane = d index of dQ^T, key of dK
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -573,27 +575,20 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
 #pragma unroll
           for (int c = 0; c < 32; ++c) u0[c] = u1[c] = 0u;
         }
-        // the single staging buffer is free once the previous reduction has read it
-        if (t == 0) bulk_wait_read0();
         if (!named_bar_and(2, 128, full && *abort_flag == 0u)) {
           ok = false;
           break;
         }
-        float* st = reinterpret_cast<float*>(smem + C::OFF_DQ);
         if (t < D) {  // lanes >= d hold the zero-padded rows of dQ^T (d = 64)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {  // lane t = d index; column c = query
-            st[c * D + t] = __uint_as_float(u0[c]);
-            st[(32 + c) * D + t] = __uint_as_float(u1[c]);
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (t == 0) {
           int qh, qs;
           w.grp.step(it, w.it0, w.n_ith, qh, qs);
-          bulk_reduce_add_f32(p.dqacc + static_cast<size_t>(qh * p.Npad + qs * BQ) * D, sDQ, C::DQ_STAGE);
-          bulk_commit();
+          // lane t = d index, column c = query: a warp adds 32 consecutive floats of one query's row
+          float* dst = p.dqacc + static_cast<size_t>(qh * p.Npad + qs * BQ) * D + t;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            atomicAdd(dst + c * D, __uint_as_float(u0[c]));
+            atomicAdd(dst + (32 + c) * D, __uint_as_float(u1[c]));
+          }
         }
       }
       if (!ok) break;
@@ -637,7 +632,6 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       if (ix < 0) break;
       named_bar_sync(2, 128);  // every thread has read dq_next before thread 0 writes it again
     }
-    if (t == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
   }
