@@ -623,30 +623,31 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fa_fwd_kernel(const __g
         // P = 2^(s * scale * log2 e - m_used), its row sum, and (TRACK) the row max of s on the side
         auto exp_pass = [&](auto track) -> float {
           constexpr bool TRACK = decltype(track)::value;
-          const float neg_m = -m_used;
+          // pairs of columns go through the two-wide fp32 FMA and add (each lane of the pair rounds
+          // as the scalar instruction would), which halves those instructions in this issue-bound loop
+          const float2 sl2_2 = make_float2(sl2, sl2), neg_m2 = make_float2(-m_used, -m_used);
           float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-          ls0 = 0.f;
-          ls1 = 0.f;
+          float2 ls = make_float2(0.f, 0.f);  // .x: even columns, .y: odd columns
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
-            float x[8];
+            float2 x[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = fmaf(s[c + e], sl2, neg_m);
+            for (int e = 0; e < 4; ++e) x[e] = __ffma2_rn(make_float2(s[c + 2 * e], s[c + 2 * e + 1]), sl2_2, neg_m2);
             if constexpr (TRACK) {
-              mx0 = max3f(mx0, x[0], x[1]);
-              mx1 = max3f(mx1, x[2], x[3]);
-              mx2 = max3f(mx2, x[4], x[5]);
-              mx3 = max3f(mx3, x[6], x[7]);
+              mx0 = max3f(mx0, x[0].x, x[0].y);
+              mx1 = max3f(mx1, x[1].x, x[1].y);
+              mx2 = max3f(mx2, x[2].x, x[2].y);
+              mx3 = max3f(mx3, x[3].x, x[3].y);
             }
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const float p0 = ex2_approx(x[e]);
-              const float p1 = ex2_approx(x[e + 1]);
-              ls0 += p0;
-              ls1 += p1;
-              pk[(c + e) >> 1] = pack2<BF16>(p0, p1);
+            for (int e = 0; e < 4; ++e) {
+              const float2 pp = make_float2(ex2_approx(x[e].x), ex2_approx(x[e].y));
+              ls = __fadd2_rn(ls, pp);
+              pk[(c >> 1) + e] = pack2<BF16>(pp.x, pp.y);
             }
           }
+          ls0 = ls.x;
+          ls1 = ls.y;
           return fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));  // max of s * sl2 - m_used
         };
         if (j == 0) {
