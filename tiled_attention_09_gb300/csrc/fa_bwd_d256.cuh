@@ -323,13 +323,20 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_d256_kernel(const __grid_consta
         uint32_t u[32], v[32];
         tmem_ld32_pair(tS, tDP, u, v);  // S^T and dP^T columns in one round trip
         float pv[32];
+        // pairs of columns through the two-wide fp32 FMA / add / multiply (each lane rounds as the
+        // scalar instruction would)
+        const float2 sl2_2 = make_float2(sl2, sl2);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 l = lse4[c4];
-          pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 0]), sl2, -l.x));
-          pv[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 1]), sl2, -l.y));
-          pv[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 2]), sl2, -l.z));
-          pv[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(u[4 * c4 + 3]), sl2, -l.w));
+          const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(u[4 * c4 + 0]), __uint_as_float(u[4 * c4 + 1])),
+                                       sl2_2, make_float2(-l.x, -l.y));
+          const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(u[4 * c4 + 2]), __uint_as_float(u[4 * c4 + 3])),
+                                       sl2_2, make_float2(-l.z, -l.w));
+          pv[4 * c4 + 0] = ex2_approx(x0.x);
+          pv[4 * c4 + 1] = ex2_approx(x0.y);
+          pv[4 * c4 + 2] = ex2_approx(x1.x);
+          pv[4 * c4 + 3] = ex2_approx(x1.y);
         }
         if (need_mask) {
 #pragma unroll
@@ -342,10 +349,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_d256_kernel(const __grid_consta
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 dd = dd4[c4];
-          pk[2 * c4] = bpack2<BF16>(pv[4 * c4] * (__uint_as_float(v[4 * c4]) - dd.x),
-                                    pv[4 * c4 + 1] * (__uint_as_float(v[4 * c4 + 1]) - dd.y));
-          pk[2 * c4 + 1] = bpack2<BF16>(pv[4 * c4 + 2] * (__uint_as_float(v[4 * c4 + 2]) - dd.z),
-                                        pv[4 * c4 + 3] * (__uint_as_float(v[4 * c4 + 3]) - dd.w));
+          const float2 ds0 = __fmul2_rn(make_float2(pv[4 * c4], pv[4 * c4 + 1]),
+                                        __fadd2_rn(make_float2(__uint_as_float(v[4 * c4]), __uint_as_float(v[4 * c4 + 1])),
+                                                   make_float2(-dd.x, -dd.y)));
+          const float2 ds1 = __fmul2_rn(make_float2(pv[4 * c4 + 2], pv[4 * c4 + 3]),
+                                        __fadd2_rn(make_float2(__uint_as_float(v[4 * c4 + 2]),
+                                                               __uint_as_float(v[4 * c4 + 3])),
+                                                   make_float2(-dd.z, -dd.w)));
+          pk[2 * c4] = bpack2<BF16>(ds0.x, ds0.y);
+          pk[2 * c4 + 1] = bpack2<BF16>(ds1.x, ds1.y);
         }
         mbar_arrive(b_lempty0 + 8 * lb);  // this thread's last read of the step's LSE / D
         tmem_st16(tDP, pk);
