@@ -592,7 +592,7 @@ def run_native(args):
         "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name(), "B": B, "H": H, "N": N, "d": d, "causal": True, "seed": 0,
-                   "dq": "separate pass" if sep else "accumulated (bulk reductions)",
+                   "dq": "separate pass" if sep else "accumulated (global reductions from registers)",
                    "l2": "flushed before every step (256 MiB write, then a 256 MiB read of another buffer so the write-back is not charged to the step; outside the timed interval)",
                    "timing": "value: whole step between two events; kernels_ms/roofline: a second pass of "
                              f"{K2} steps with events between kernels",
