@@ -631,7 +631,8 @@ def run_sweep(args):
     """One JSON line per sweep point: forward and forward+backward, each timed between two events on the
     launching stream (L2 flushed before every step), TFLOP/s, % of the measured bf16 peak, and % of the
     attainable min(peak, HBM bandwidth x algorithmic intensity) with the algorithmic bytes per head
-    8Nd + 4N (forward) and 16Nd + 8N more (backward), at 2 bytes per element and 4 per LSE / D value."""
+    8Nd + 4N (forward) and 16Nd + 8N more (backward), at 2 bytes per element and 4 per LSE / D value.
+    For N <= 2048 also fwd_bwd_graph: the same step replayed from a CUDA graph."""
     import torch
     import tiled_attention_09_gb300 as fa
     from tiled_attention_09_gb300.inputs import Workload, cast_inputs, make_inputs_fp32
@@ -692,6 +693,30 @@ def run_sweep(args):
                             e1.record()
                         torch.cuda.synchronize()
                         times[name] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+                    if N <= 2048:
+                        # short rows are launch-bound: the same step replayed from a CUDA graph (its four
+                        # kernels captured once), timed the same way, shows what the launches cost
+                        side = torch.cuda.Stream()
+                        side.wait_stream(torch.cuda.current_stream())
+                        with torch.cuda.stream(side):
+                            step(default)
+                        torch.cuda.current_stream().wait_stream(side)
+                        graph = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(graph):
+                            step(default)
+                        for _ in range(warmup):
+                            flush()
+                            graph.replay()
+                        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                               for _ in range(steps)]
+                        for e0, e1 in evs:
+                            flush()
+                            e0.record()
+                            graph.replay()
+                            e1.record()
+                        torch.cuda.synchronize()
+                        times["fwd_bwd_graph"] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+                        del graph
                     code, info = fa.device_status()
                     if code != "FA_OK":
                         raise RuntimeError(f"{w.name()}: {code} {info}")
@@ -704,7 +729,7 @@ def run_sweep(args):
                     line["fwd_kv_splits"] = n_split
                     for name, flops, nbytes in [("fwd", F, bytes_fwd)] + [
                             (f"fwd_bwd{x}", 3.5 * F, bytes_fwd + bytes_bwd)
-                            for x in [""] + [f"_{m}" for m in modes]] + (
+                            for x in [""] + [f"_{m}" for m in modes] + (["_graph"] if N <= 2048 else [])] + (
                             [("fwd_split", F, bytes_fwd)] if n_split > 1 else []):
                         tf = flops / times[name] / 1e12
                         attainable = min(peak, bw * 1e9 * flops / nbytes / 1e12)
