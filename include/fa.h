@@ -166,6 +166,17 @@ int fa_fwd_kv_splits(int B, int H, int N, int d, int causal);
 size_t fa_fwd_workspace_size(int B, int H, int N, int d, int kv_splits);
 
 /*
+ * Query tiles of 128 rows that one CTA of the forward (without a split) takes
+ * as one work item for this shape: 2 (the two softmax warpgroups take turns on
+ * the tensor core) or 1 (twice the items, each half as long: short rows and few
+ * heads, where two-tile items would leave SMs idle or make the longest item the
+ * critical path). The library picks it on every forward call; the result does
+ * not depend on it (each query row's computation is the same). d = 256 always
+ * takes 1. Returns 0 for an unsupported shape.
+ */
+int fa_fwd_tiles_per_item(int B, int H, int N, int d, int causal);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 D [B,H,Np], fp32 LSE*log2(e)
  * [B,H,Np] and the fp32 dQ accumulator [B,H,Np,d], each 256-byte aligned,
  * with Np = N rounded up to 128 (each head's rows padded so that every query

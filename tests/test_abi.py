@@ -226,3 +226,18 @@ def test_split_forward_workspace_and_choice(L):
         s = L.fa_fwd_kv_splits(*args)
         assert 1 <= s <= 16 and (s & (s - 1)) == 0
 
+
+
+def test_forward_tiles_per_item_choice(L):
+    """Query tiles per forward work item: the mode that timed faster on a GB300 (152 SMs, the count assumed
+    without a device) for each of these shapes; 1 only where two-tile items would leave SMs idle or make
+    the longest item the critical path."""
+    measured_best = {  # (B, H, N, d, causal): tiles per item
+        (2, 12, 512, 128, 1): 1, (2, 12, 512, 128, 0): 1, (2, 12, 1024, 128, 1): 1, (2, 12, 1024, 128, 0): 2,
+        (2, 12, 2048, 128, 1): 2, (2, 12, 4096, 128, 0): 2, (2, 12, 1024, 64, 1): 1, (2, 12, 1024, 64, 0): 2,
+        (1, 4, 2048, 128, 1): 1, (1, 4, 4096, 128, 0): 1, (4, 32, 512, 128, 1): 2, (4, 32, 1024, 128, 0): 2,
+    }
+    for args, t in measured_best.items():
+        assert L.fa_fwd_tiles_per_item(*args) == t, args
+    assert L.fa_fwd_tiles_per_item(1, 2, 4096, 256, 1) == 1   # d = 256: one tile an item always
+    assert L.fa_fwd_tiles_per_item(1, 1, 0, 64, 0) == 0       # unsupported shape

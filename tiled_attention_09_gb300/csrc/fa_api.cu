@@ -8,7 +8,10 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include "../../include/fa.h"
 #include "launch.h"
@@ -252,6 +255,43 @@ double fwd_model_us(int B, int H, int N, int d, bool causal, int s, int sms) {
   return t;
 }
 
+// Query tiles per work item of the forward without a split (d = 64, 128; 0 = the kernel's two, 1 = one).
+// One tile an item doubles the items and halves the longest one, at the price of the tensor core
+// waiting while the one softmax warpgroup works (with two tiles the two warpgroups keep it busy in
+// turns): a step of one tile measured ~0.9 of a step of two. The choice is the smaller modelled
+// makespan of the items, longest first on the SMs (each item: its key tiles times its step time plus a
+// fixed cost of ~2 steps); it picked the faster mode on all 32 shapes measured (B2 H12, B1 H4, B4 H32;
+// N = 512-4096; d = 64, 128; both masks). With more than four waves of one-tile items, two it is.
+int fwd_tiles_per_item(int B, int H, int N, int d, bool causal) {
+  if (d > 128) return 0;  // the d = 256 kernel takes one tile an item anyway
+  const long long heads = static_cast<long long>(B) * H;
+  const int nq = (N + 127) / 128;
+  const int sms = sm_count();
+  if (heads * nq > 4ll * sms) return 0;
+  auto makespan = [&](int tpi) -> double {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
+    for (int i = 0; i < sms; ++i) sm.push(0.0);
+    // item classes longest first: under causal masking the last query tiles (or pairs) are the longest
+    const int n_items = tpi == 1 ? nq : (nq + 1) / 2;
+    for (int c = n_items - 1; c >= 0; --c) {
+      const int steps = tpi == 1 ? (causal ? c + 1 : nq) : (causal ? std::min(2 * c + 2, nq) : nq);
+      const double size = (tpi == 1 ? 0.9 : 1.0) * steps + 2.0;
+      for (long long h = 0; h < heads; ++h) {
+        const double t = sm.top();
+        sm.pop();
+        sm.push(t + size);
+      }
+    }
+    double end = 0.0;
+    while (!sm.empty()) {
+      end = std::max(end, sm.top());
+      sm.pop();
+    }
+    return end;
+  };
+  return makespan(1) < makespan(2) ? 1 : 0;
+}
+
 int fwd_kv_splits(int B, int H, int N, int d, bool causal) {
   const int sms = sm_count();
   const long long key_tiles = (N + 127) / 128;
@@ -476,6 +516,12 @@ fa_status fa_fwd_opt(const void* q, const void* k, const void* v, void* o, float
   return fa_fwd_split(q, k, v, o, lse, o_lo, B, H, N, d, scale, causal, dtype, opt, 1, nullptr, 0, stream);
 }
 
+int fa_fwd_tiles_per_item(int B, int H, int N, int d, int causal) {
+  if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
+  if (d > 128) return 1;
+  return fwd_tiles_per_item(B, H, N, d, causal != 0) == 1 ? 1 : 2;
+}
+
 int fa_fwd_kv_splits(int B, int H, int N, int d, int causal) {
   if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
   return fwd_kv_splits(B, H, N, d, causal != 0);
@@ -507,6 +553,7 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
   if (kv_splits <= 0) kv_splits = fwd_kv_splits(B, H, N, d, causal != 0);
   if (kv_splits > kMaxKvSplits) return FA_ERR_UNSUPPORTED;
   a.kv_splits = kv_splits;
+  a.tiles_per_item = kv_splits > 1 ? 0 : fwd_tiles_per_item(B, H, N, d, causal != 0);
   a.part_o = nullptr;
   a.part_lse = nullptr;
   if (kv_splits > 1) {

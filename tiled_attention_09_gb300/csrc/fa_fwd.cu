@@ -70,6 +70,7 @@ struct FwdParams {
   float* part_lse;    // [kv_splits][B*H*N] natural-log LSE of each part (-inf: the part saw no key)
   long long part_rows;  // B*H*N
   int kv_splits;      // CTAs that share one query block's key range (1: no split)
+  int tpi;            // query tiles per work item: NT, or 1 (short rows: twice the items, each half as long)
   int N;
   int H, G;        // query heads; query heads per K/V head
   int n_qblk;
@@ -157,10 +158,10 @@ struct FwdItem {
       klen = l < 0 ? 0 : (l > N ? N : l);
     }
     nk = klen > 0 ? (klen + 127) / 128 : 1;
-    q_row0 = qb * 128 * NT;
+    q_row0 = qb * 128 * p.tpi;
     row_base = x * N;
     n_valid = (N - q_row0 + 127) / 128;  // a tile that runs past N still exists (its tail is masked)
-    if (n_valid > NT) n_valid = NT;
+    if (n_valid > p.tpi) n_valid = p.tpi;  // with one tile an item, tile 1's warpgroup sits the item out
     kt0 = 0;
     kt1 = 1 << 30;
     if constexpr (SPLIT) {
@@ -890,7 +891,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a) {
   p.N = a.N;
   p.H = a.H;
   p.G = a.H / a.Hkv;
-  p.n_qblk = (a.N + 128 * C::NT - 1) / (128 * C::NT);
+  p.tpi = (a.tiles_per_item >= 1 && a.tiles_per_item < C::NT && !SPLIT) ? a.tiles_per_item : C::NT;
+  p.n_qblk = (a.N + 128 * p.tpi - 1) / (128 * p.tpi);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.rescale_threshold = 8.0f;
   p.timeout_ns = a.timeout_ns;

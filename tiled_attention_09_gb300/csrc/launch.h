@@ -42,6 +42,7 @@ struct FwdArgs {
   void* o_lo;  // optional rounding residual of O (nullptr: not written)
   const int* kv_len;  // optional [B] key counts (key-padding mask)
   int kv_splits;      // CTAs per query block's key range (1: no split)
+  int tiles_per_item; // query tiles per work item without a split: 0 = the kernel's two (d <= 128), or 1
   float* part_o;      // kv_splits > 1: [kv_splits][B*H*N][d] fp32 partial outputs
   float* part_lse;    // kv_splits > 1: [kv_splits][B*H*N] their LSEs
   int B, H, Hkv, N, d;
