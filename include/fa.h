@@ -177,27 +177,11 @@ size_t fa_fwd_workspace_size(int B, int H, int N, int d, int kv_splits);
 int fa_fwd_tiles_per_item(int B, int H, int N, int d, int causal);
 
 /*
- * CTAs that share one 128-key block of the backward's main kernel for this
- * shape: 1, or 2 (d = 64, 128, dQ accumulated, the workspace holding the
- * split's room: each CTA takes half of the block's query steps and leaves fp32
- * partial dK and dV; the one that finishes second adds the other's and stores
- * dK and dV, so no CTA waits for another and the results stay bitwise
- * repeatable). The library picks 2 where short rows or few heads would make
- * the longest block the critical path. Returns 0 for an unsupported shape.
- */
-int fa_bwd_key_block_parts(int B, int H, int N, int d, int causal);
-
-/*
  * Bytes of device workspace fa_bwd needs: fp32 D [B,H,Np], fp32 LSE*log2(e)
  * [B,H,Np] and the fp32 dQ accumulator [B,H,Np,d], each 256-byte aligned,
  * with Np = N rounded up to 128 (each head's rows padded so that every query
  * step or tile of the backward starts aligned and stays in its head). The
- * separate dQ pass leaves the accumulator untouched. On shapes where the
- * d = 64 / 128 backward may split its key blocks (fa_bwd_key_block_parts
- * returns 2 for either mask) it adds the split's room: int counters
- * [B,H,Nb,12] and two fp32 partial arrays [B,H,Nb,2,128,d] (Nb = N rounded up
- * to 128, over 128), each 256-byte aligned. A workspace without that room
- * (at least the part before it) is accepted and runs unsplit.
+ * separate dQ pass leaves the accumulator untouched.
  * Returns 0 for unsupported shapes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);

@@ -44,7 +44,6 @@ SIGNATURES = [
                                               ctypes.POINTER(FAOptions), c_int, c_void_p, c_size_t, c_void_p]),
     ("fa_fwd_kv_splits", c_int, [c_int] * 5),
     ("fa_fwd_tiles_per_item", c_int, [c_int] * 5),
-    ("fa_bwd_key_block_parts", c_int, [c_int] * 5),
     ("fa_fwd_workspace_size", c_size_t, [c_int] * 5),
     ("fa_bwd", c_int, [c_void_p] * 10 + [c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
                                          c_void_p]),

@@ -322,58 +322,13 @@ fa_status check_scale(float scale) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Whether the d = 64 / 128 backward main kernel splits every key block's query steps over two CTAs
-// (each half leaves fp32 partial dK and dV; the half that finishes second adds them up). It doubles
-// the items and halves the longest one (under causal masking block 0 walks every query step), at the
-// price of the partials' traffic and a longer epilogue (a fence, a counter, the other half's partial).
-// The choice is the smaller modelled makespan of the items, longest first on the SMs: each item its
-// 64-query steps plus 1 step of fixed cost, a split half 8 steps more, the costs that reproduced the
-// faster choice on all 16 shapes where both were timed (B2 H12 N512-1024, B1 H4 N1024-8192, B1 H1
-// N2048-8192, both masks: splitting is 1.1-1.6x faster on few heads with long rows, up to 1.9x slower
-// on many short blocks). Only shapes with at most four waves of split items and two steps or more in
-// every block are considered. H stands for the K/V heads (an upper bound with grouped heads).
-bool bwd_split(int B, int H, int N, int d, bool causal) {
-  if (d > 128) return false;
-  const int nkb = (N + 127) / 128, nst = (N + 63) / 64;
-  if (nst - (causal ? 2 * (nkb - 1) : 0) < 2) return false;
-  const long long heads = static_cast<long long>(B) * H;
-  const int sms = sm_count();
-  if (heads * nkb * 2 > 4ll * sms) return false;
-  auto makespan = [&](bool split) -> double {
-    std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
-    for (int i = 0; i < sms; ++i) sm.push(0.0);
-    for (int kb = 0; kb < nkb; ++kb) {  // longest first
-      const int steps = causal ? nst - 2 * kb : nst;
-      const int parts = split ? 2 : 1;
-      const double size = split ? (steps + 1) / 2 + 9.0 : steps + 1.0;
-      for (long long h = 0; h < heads * parts; ++h) {
-        const double t = sm.top();
-        sm.pop();
-        sm.push(t + size);
-      }
-    }
-    double end = 0.0;
-    while (!sm.empty()) {
-      end = std::max(end, sm.top());
-      sm.pop();
-    }
-    return end;
-  };
-  return makespan(true) < makespan(false);
-}
-
 struct WsLayout {
-  size_t off_D, off_lse2, off_dq, base;  // what every backward needs
-  size_t off_cnt, off_pdk, off_pdv;      // the split's counters and partial slots (when it may split)
-  bool split_room;
-  size_t total;
+  size_t off_D, off_lse2, off_dq, total;
 };
 // Each head's rows are padded to Npad = N rounded up to 128: every 64-query step of the main
 // kernel and every 128-row query tile of the separate dQ pass then starts 256-byte aligned (bulk
 // copies need 16) and stays in its head; the last, partial step or tile of a sequence reads
-// LSE*log2e and D of its own (zeroed, masked) padding rows and adds zero dQ partials there. Shapes on
-// which the main kernel may split its key blocks (either mask) also get the split's counters and
-// partial slots; a workspace without that room (fa_bwd_noalloc's, for one) runs unsplit.
+// LSE*log2e and D of its own (zeroed, masked) padding rows and adds zero dQ partials there.
 int pad_rows(int N) { return (N + 127) / 128 * 128; }
 WsLayout ws_layout(int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * pad_rows(N);
@@ -381,13 +336,7 @@ WsLayout ws_layout(int B, int H, int N, int d) {
   w.off_D = 0;
   w.off_lse2 = align256(rows * 4);
   w.off_dq = w.off_lse2 + align256(rows * 4);
-  w.base = w.off_dq + align256(rows * static_cast<size_t>(d) * 4);
-  w.split_room = bwd_split(B, H, N, d, true) || bwd_split(B, H, N, d, false);
-  const size_t blocks = static_cast<size_t>(B) * H * ((N + 127) / 128);
-  w.off_cnt = w.base;
-  w.off_pdk = w.off_cnt + align256(blocks * 12 * 4);
-  w.off_pdv = w.off_pdk + align256(blocks * 2 * 128 * static_cast<size_t>(d) * 4);
-  w.total = w.split_room ? w.off_pdv + align256(blocks * 2 * 128 * static_cast<size_t>(d) * 4) : w.base;
+  w.total = w.off_dq + align256(rows * static_cast<size_t>(d) * 4);
   return w;
 }
 
@@ -444,19 +393,10 @@ fa_status bwd_common(fa::BwdArgs* a, void* workspace, size_t workspace_bytes, in
   if (!workspace) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
   WsLayout w = ws_layout(B, H, N, d);
-  if (workspace_bytes < w.base) return FA_ERR_WORKSPACE;
+  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE;
   a->ws_D = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_D);
   a->ws_lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse2);
   a->ws_dqacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_dq);
-  // the split's room: the preprocess zeroes its counters whenever it is there, the main kernel uses it
-  // when the shape and mask ask for a split (bwd_main_impl)
-  const bool room = w.split_room && workspace_bytes >= w.total;
-  a->split_room = room;
-  a->ws_cnt = room ? reinterpret_cast<int*>(static_cast<char*>(workspace) + w.off_cnt) : nullptr;
-  a->n_cnt = room ? static_cast<long long>(B) * H * ((N + 127) / 128) * 12 : 0;
-  a->ws_part_dk = room ? reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_pdk) : nullptr;
-  a->ws_part_dv = room ? reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_pdv) : nullptr;
-  a->split = false;
   a->B = B;
   a->H = H;
   a->Hkv = H;
@@ -514,8 +454,6 @@ fa_status bwd_main_impl(const void* q, const void* k, const void* v, const void*
   a.dk = dk;
   a.dv = dv;
   a.dq = dq;  // optional: when given, the dQ conversion (or the dQ pass) is enqueued right after the main kernel
-  // (the same with the separate dQ pass: dK and dV then match the accumulating path's bit for bit)
-  a.split = a.split_room && bwd_split(B, H, N, d, causal != 0);
   return fa::launch_bwd_main(a) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -576,11 +514,6 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 fa_status fa_fwd_opt(const void* q, const void* k, const void* v, void* o, float* lse, void* o_lo, int B, int H,
                      int N, int d, float scale, int causal, fa_dtype dtype, const fa_options* opt, void* stream) {
   return fa_fwd_split(q, k, v, o, lse, o_lo, B, H, N, d, scale, causal, dtype, opt, 1, nullptr, 0, stream);
-}
-
-int fa_bwd_key_block_parts(int B, int H, int N, int d, int causal) {
-  if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
-  return bwd_split(B, H, N, d, causal != 0) ? 2 : 1;
 }
 
 int fa_fwd_tiles_per_item(int B, int H, int N, int d, int causal) {
@@ -653,17 +586,6 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
   return ws_layout(B, H, N, d).total;
 }
-
-}  // extern "C"
-
-namespace fa {
-size_t bwd_workspace_base(int B, int H, int N, int d) {
-  if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
-  return ws_layout(B, H, N, d).base;
-}
-}  // namespace fa
-
-extern "C" {
 
 fa_status fa_bwd_preprocess(const void* o, const void* o_lo, const void* dO, const float* lse, void* workspace,
                             size_t workspace_bytes, int B, int H, int N, int d, fa_dtype dtype, void* stream) {

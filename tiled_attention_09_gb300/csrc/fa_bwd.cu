@@ -26,11 +26,11 @@ cudaError_t launch_pre_t(const BwdArgs& a) {
     return launch_kernel(fa_bwd_preprocess_kernel<VPR, true>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
                          static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
                          a.o_f32 ? static_cast<const float4*>(a.o) : nullptr, static_cast<const uint4*>(a.dO),
-                         a.lse, a.ws_D, a.ws_lse2, dqacc, a.ws_cnt, a.n_cnt, a.N, a.Npad, n_vec_pad);
+                         a.lse, a.ws_D, a.ws_lse2, dqacc, a.N, a.Npad, n_vec_pad);
   return launch_kernel(fa_bwd_preprocess_kernel<VPR, false>, dim3(grid_for(n_vec_pad)), dim3(256), 0, a.stream,
                        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.o_lo),
                        a.o_f32 ? static_cast<const float4*>(a.o) : nullptr, static_cast<const uint4*>(a.dO),
-                       a.lse, a.ws_D, a.ws_lse2, dqacc, a.ws_cnt, a.n_cnt, a.N, a.Npad, n_vec_pad);
+                       a.lse, a.ws_D, a.ws_lse2, dqacc, a.N, a.Npad, n_vec_pad);
 }
 template <int VPR>
 cudaError_t launch_convert_t(const BwdArgs& a) {
@@ -80,11 +80,6 @@ BwdParams bwd_params(const BwdArgs& a) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.kv_len = a.kv_len;
-  p.split = a.split ? 1 : 0;
-  p.nkb = (a.N + 127) / 128;
-  p.part_dk = a.ws_part_dk;
-  p.part_dv = a.ws_part_dv;
-  p.split_cnt = a.ws_cnt;
   p.N = a.N;
   p.Npad = a.Npad;
   p.H = a.H;
@@ -122,8 +117,7 @@ cudaError_t launch_pipe_t(const BwdArgs& a) {
     checked = 1;
   }
   const BwdParams p = bwd_params(a);
-  // key blocks of each K/V head (the last may run past N); with a split, two halves of each
-  dim3 grid(a.B * a.Hkv, (a.N + 127) / 128 * (p.split ? 2 : 1), 1);
+  dim3 grid(a.B * a.Hkv, (a.N + 127) / 128, 1);  // key blocks of each K/V head; the last may run past N
   e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, p);
   if (e != cudaSuccess || a.dq == nullptr) return e;
   return DQACC ? launch_bwd_dq_convert(a) : launch_bwd_dq_pass(a);

@@ -59,13 +59,8 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
                                                                  const uint4* __restrict__ dO,
                                                                  const float* __restrict__ lse, float* __restrict__ D,
                                                                  float* __restrict__ lse2, float4* __restrict__ dqacc,
-                                                                 int* __restrict__ split_cnt, long long n_cnt, int N,
-                                                                 int Npad, size_t n_vec_pad) {
+                                                                 int N, int Npad, size_t n_vec_pad) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  // the main kernel's split counters (when the workspace has room for a split) start at zero
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_cnt;
-       i += static_cast<long long>(stride))
-    split_cnt[i] = 0;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec_pad; i += stride) {
     const uint32_t row_pad = static_cast<uint32_t>(i / VPR);
     const uint32_t bh = row_pad / static_cast<uint32_t>(Npad), r = row_pad - bh * static_cast<uint32_t>(Npad);

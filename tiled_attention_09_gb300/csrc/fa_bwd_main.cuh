@@ -31,14 +31,6 @@ struct BwdParams {
   void* dk;           // [B*Hkv*N, d] dtype outputs, written directly by kernels that store from registers
   void* dv;
   const int* kv_len;  // optional [B]: keys j >= kv_len[b] are masked for batch b (key padding)
-  // split (d = 64, 128 main kernel): each key block's query steps in two halves on two CTAs; each half
-  // leaves its fp32 dK and dV partials in its slot [B*Hkv][nkb][2][128][d] and bumps a per-warp counter
-  // [B*Hkv][nkb][12] (zeroed by the preprocess); the half that finishes second adds the other's partial
-  float* part_dk;
-  float* part_dv;
-  int* split_cnt;
-  int split;          // 0 or 1
-  int nkb;            // key blocks of a head: N rounded up to 128, over 128
   int N;
   int Npad;           // N rounded up to 128: the per-head row stride of lse2, Dvec and dqacc
   int H, Hkv;         // query heads and K/V heads (Hkv divides H; H / Hkv query heads share one K/V head)

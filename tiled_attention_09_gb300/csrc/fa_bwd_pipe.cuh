@@ -85,15 +85,11 @@ struct BwdPipeCfg {
   static_assert(SMEM_BYTES <= 232448, "smem budget");
 };
 
-// The K/V head, key block and (split) half that launch index (x, y) works on (fa_bwd_order.cuh). With
-// a split the order runs over 2 * nkb virtual blocks per head, the two halves of block kb adjacent.
+// The K/V head and key block that launch index (x, y) works on (fa_bwd_order.cuh).
 struct BwdSlot {
-  int bh, kb, part;
+  int bh, kb;
   __device__ __forceinline__ BwdSlot(int x, int y, const BwdParams& p, int d) {
-    int vb = 0;
-    bwd_block_order(x, y, gridDim.x, gridDim.y, static_cast<long long>(p.H / p.Hkv) * p.N * 8ll * d, bh, vb);
-    kb = p.split ? vb >> 1 : vb;
-    part = p.split ? vb & 1 : 0;
+    bwd_block_order(x, y, gridDim.x, gridDim.y, static_cast<long long>(p.H / p.Hkv) * p.N * 8ll * d, bh, kb);
   }
 };
 
@@ -109,9 +105,7 @@ struct BwdItem {
   int key0;      // first key of the block
   int it0;       // first 64-query step of each query head (causal: the block's diagonal)
   int n_ith;     // query steps per query head (the last may run past N: its extra queries are masked)
-  int it_lo;     // first of the block's G * n_ith steps that this item takes (a split's second half)
-  int n_it;      // query steps of the item: G * n_ith, or one half of them (the host splits only
-                 // shapes whose every block has two steps or more)
+  int n_it;      // query steps of the block: G * n_ith
   BwdGroup<GRP> grp;  // the query heads of the group and the batch's key count
   __device__ __forceinline__ BwdItem(int x, int y, const BwdParams& p, int d) : slot(x, y, p, d), grp(slot.bh, p) {
     bh = slot.bh;
@@ -119,43 +113,9 @@ struct BwdItem {
     key0 = slot.kb * 128;
     it0 = CAUSAL ? (key0 / 64) : 0;  // 64-query steps
     n_ith = (p.N + 63) / 64 - it0;
-    const int n_all = grp.G * n_ith;
-    const int half = (n_all + 1) >> 1;
-    it_lo = slot.part ? half : 0;
-    n_it = p.split ? (slot.part ? n_all - half : half) : n_all;
+    n_it = grp.G * n_ith;
   }
-  // query head and 64-query step of the item's step it
-  __device__ __forceinline__ void step(int it, int& qh, int& qs) const { grp.step(it_lo + it, it0, n_ith, qh, qs); }
 };
-
-// A split key block's epilogue, per warp: this half's fp32 partial of the thread's row (NF values) goes
-// to `mine`; a counter shared with the same warp of the block's other half says which half finished
-// second, and that half adds the other's partial into acc and returns true (it stores the block's
-// result); the first returns false. No half waits for the other. The two halves' warps cover the same
-// rows and columns (the same roles in both CTAs), so warp w's partials pair up.
-template <int NF>
-__device__ __forceinline__ bool split_merge(uint32_t (&acc)[NF], float* mine, const float* other, int* cnt) {
-#pragma unroll
-  for (int c = 0; c < NF; c += 4)
-    *reinterpret_cast<float4*>(mine + c) = make_float4(__uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
-                                                       __uint_as_float(acc[c + 2]), __uint_as_float(acc[c + 3]));
-  __threadfence();  // this thread's partial is visible on the device before the warp's count moves
-  __syncwarp();
-  int old = 0;
-  if ((threadIdx.x & 31) == 0) old = atomicAdd(cnt, 1);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == 0) return false;
-  __threadfence();  // the other half published its partial before its count: read it after ours
-#pragma unroll
-  for (int c = 0; c < NF; c += 4) {
-    const float4 o = __ldcg(reinterpret_cast<const float4*>(other + c));
-    acc[c] = __float_as_uint(__uint_as_float(acc[c]) + o.x);
-    acc[c + 1] = __float_as_uint(__uint_as_float(acc[c + 1]) + o.y);
-    acc[c + 2] = __float_as_uint(__uint_as_float(acc[c + 2]) + o.z);
-    acc[c + 3] = __float_as_uint(__uint_as_float(acc[c + 3]) + o.w);
-  }
-  return true;
-}
 
 // GRP: grouped K/V heads or a key-padding mask (the general form); false for plain multi-head attention.
 // DQACC: dQ partials accumulated here (true) or left to the separate dQ pass (false).
@@ -274,7 +234,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         const uint32_t s = gs % NS, use = gs / NS;
         if (use > 0 && !wait_bar(b_qempty(s), (use - 1) & 1, p.timeout_ns, abort_flag, WB_QE)) return false;
         int qh, qs;
-        w.step(it, qh, qs);
+        w.grp.step(it, w.it0, w.n_ith, qh, qs);
         const int q_in = qs * BQ;  // first query of the step within query head qh
         const int qrow = qh * p.Npad + q_in;
         mbar_arrive_expect_tx(b_qfull(s), 2 * C::Q_TILE + 2 * BQ * 4);
@@ -499,7 +459,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE + s * BQ * 4) + 8 * g;
         const float4* dd4 = reinterpret_cast<const float4*>(smem + C::OFF_DD + s * BQ * 4) + 8 * g;
         int qh, qs;
-        w.step(it, qh, qs);
+        w.grp.step(it, w.it0, w.n_ith, qh, qs);
         const int q0 = qs * BQ + 32 * g;  // first query of this group's columns
         // masked: column c < kq (key > query, causal), q0 + c >= N (query past the sequence) or the
         // whole row when the key does not exist (past the sequence, or past the batch's key count:
@@ -579,14 +539,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         mbar_arrive(b_vfree);  // the next block's first dV MMA may overwrite the accumulator
         uint4* dst = reinterpret_cast<uint4*>(
             reinterpret_cast<uint16_t*>(p.dv) + (static_cast<size_t>(w.row_base) + w.key0 + k) * D + HC * g);
-        bool key_ok = w.key0 + k < N;  // keys past N exist only as zero rows of the block
-        if (p.split) {  // one half of a split block: the half that finishes second stores the sum
-          const size_t blk = static_cast<size_t>(w.bh) * p.nkb + w.slot.kb;
-          float* slot0 = p.part_dv + (blk * 2 * 128 + k) * D + HC * g;
-          const bool last = split_merge<HC>(a, slot0 + w.slot.part * 128 * D, slot0 + (w.slot.part ^ 1) * 128 * D,
-                                            p.split_cnt + blk * 12 + warp);
-          key_ok = key_ok && last;
-        }
+        const bool key_ok = w.key0 + k < N;  // keys past N exist only as zero rows of the block
 #pragma unroll
         for (int u8 = 0; u8 < HC / 8; ++u8)
           if (key_ok) dst[u8] = make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]), __uint_as_float(a[8 * u8 + 1])),
@@ -640,7 +593,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
         }
         if (t < D) {  // lanes >= d hold the zero-padded rows of dQ^T (d = 64)
           int qh, qs;
-          w.step(it, qh, qs);
+          w.grp.step(it, w.it0, w.n_ith, qh, qs);
           // lane t = d index, column c = query: a warp adds 32 consecutive floats of one query's row
           float* dst = p.dqacc + static_cast<size_t>(qh * p.Npad + qs * BQ) * D + t;
 #pragma unroll
@@ -659,67 +612,23 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_pipe_kernel(const __grid_consta
       {
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dk) +
                                               (static_cast<size_t>(w.row_base) + w.key0 + t) * D);
-        const float sc = p.scale;
-        const bool key_ok = w.key0 + t < N;
-        if (!p.split) {
 #pragma unroll 1
-          for (int h = 0; h < D / 64; ++h) {
-            uint32_t a[64];
-            tmem_ld64(tmem + lane_off + C::DK_COL + 64 * h, a);
-            if (h == D / 64 - 1) {
-              tc_fence_before();
-              mbar_arrive(b_kfree);  // the next block's first dK MMA may overwrite the accumulator
-            }
-#pragma unroll
-            for (int u8 = 0; u8 < 8; ++u8)
-              if (key_ok) dst[8 * h + u8] =
-                  make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]) * sc, __uint_as_float(a[8 * u8 + 1]) * sc),
-                             bpack2<BF16>(__uint_as_float(a[8 * u8 + 2]) * sc, __uint_as_float(a[8 * u8 + 3]) * sc),
-                             bpack2<BF16>(__uint_as_float(a[8 * u8 + 4]) * sc, __uint_as_float(a[8 * u8 + 5]) * sc),
-                             bpack2<BF16>(__uint_as_float(a[8 * u8 + 6]) * sc, __uint_as_float(a[8 * u8 + 7]) * sc));
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t a[64];
+          tmem_ld64(tmem + lane_off + C::DK_COL + 64 * h, a);
+          if (h == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(b_kfree);  // the next block's first dK MMA may overwrite the accumulator
           }
-        } else {
-          // one half of a split block: its fp32 partial (the whole row, d values) to its slot, then the
-          // pairing of split_merge, in chunks of 64 columns so that no more than 64 stay in registers
-          const size_t blk = static_cast<size_t>(w.bh) * p.nkb + w.slot.kb;
-          float* mine = p.part_dk + ((blk * 2 + w.slot.part) * 128 + t) * D;
-          const float* other = p.part_dk + ((blk * 2 + (w.slot.part ^ 1)) * 128 + t) * D;
-#pragma unroll 1
-          for (int h = 0; h < D / 64; ++h) {
-            uint32_t a[64];
-            tmem_ld64(tmem + lane_off + C::DK_COL + 64 * h, a);
-            if (h == D / 64 - 1) {
-              tc_fence_before();
-              mbar_arrive(b_kfree);
-            }
+          const float sc = p.scale;
+          const bool key_ok = w.key0 + t < N;
 #pragma unroll
-            for (int c = 0; c < 64; c += 4)
-              *reinterpret_cast<float4*>(mine + 64 * h + c) =
-                  make_float4(__uint_as_float(a[c]), __uint_as_float(a[c + 1]), __uint_as_float(a[c + 2]),
-                              __uint_as_float(a[c + 3]));
-          }
-          __threadfence();
-          __syncwarp();
-          int old = 0;
-          if ((threadIdx.x & 31) == 0) old = atomicAdd(p.split_cnt + blk * 12 + warp, 1);
-          old = __shfl_sync(0xffffffffu, old, 0);
-          if (old != 0) {  // the second half: dK = scale * (this half + the other)
-            __threadfence();
-#pragma unroll 1
-            for (int h = 0; h < D / 64; ++h) {
-#pragma unroll
-              for (int u8 = 0; u8 < 8; ++u8) {
-                const float4* m4 = reinterpret_cast<const float4*>(mine + 64 * h + 8 * u8);
-                const float4* o4 = reinterpret_cast<const float4*>(other + 64 * h + 8 * u8);
-                const float4 m0 = __ldcg(m4), m1 = __ldcg(m4 + 1), o0 = __ldcg(o4), o1 = __ldcg(o4 + 1);
-                if (key_ok)
-                  dst[8 * h + u8] = make_uint4(bpack2<BF16>((m0.x + o0.x) * sc, (m0.y + o0.y) * sc),
-                                               bpack2<BF16>((m0.z + o0.z) * sc, (m0.w + o0.w) * sc),
-                                               bpack2<BF16>((m1.x + o1.x) * sc, (m1.y + o1.y) * sc),
-                                               bpack2<BF16>((m1.z + o1.z) * sc, (m1.w + o1.w) * sc));
-              }
-            }
-          }
+          for (int u8 = 0; u8 < 8; ++u8)
+            if (key_ok) dst[8 * h + u8] =
+                make_uint4(bpack2<BF16>(__uint_as_float(a[8 * u8 + 0]) * sc, __uint_as_float(a[8 * u8 + 1]) * sc),
+                           bpack2<BF16>(__uint_as_float(a[8 * u8 + 2]) * sc, __uint_as_float(a[8 * u8 + 3]) * sc),
+                           bpack2<BF16>(__uint_as_float(a[8 * u8 + 4]) * sc, __uint_as_float(a[8 * u8 + 5]) * sc),
+                           bpack2<BF16>(__uint_as_float(a[8 * u8 + 6]) * sc, __uint_as_float(a[8 * u8 + 7]) * sc));
         }
       }
       if (t == 0) {

@@ -33,7 +33,6 @@
 #include <cstddef>
 
 #include "../../include/fa.h"
-#include "launch.h"
 
 namespace {
 
@@ -60,7 +59,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     const float* lse, void* dq, void* dk, void* dv, const void* o_lo, int B, int H,
                                     int N, int d, float scale, int causal, fa_dtype dtype, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  const size_t need = fa::bwd_workspace_base(B, H, N, d);  // (the split's room is used when it also fits)
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
   if (need == 0) return FA_ERR_UNSUPPORTED;
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;  // problem too large for the fixed scratch
   void* ws = nullptr;

@@ -70,13 +70,6 @@ struct BwdArgs {
   int B, H, Hkv, N, d;
   int Npad;  // N rounded up to 128: the per-head row stride of the workspace arrays
   bool dq_pass;  // dQ by the separate query-major pass (no accumulator) instead of accumulation
-  // the main kernel's key-block split (d = 64, 128): room for it in the workspace, whether this call
-  // splits, its per-warp counters (n_cnt, zeroed by the preprocess when there is room) and fp32 slots
-  bool split_room, split;
-  int* ws_cnt;
-  long long n_cnt;
-  float* ws_part_dk;
-  float* ws_part_dv;
   bool o_f32;
   float scale;
   bool causal, bf16;
@@ -111,9 +104,6 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a);
 cudaError_t launch_bwd_main(const BwdArgs& a);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a);
 cudaError_t launch_bwd_dq_pass(const BwdArgs& a);
-// Bytes of backward workspace every call needs (fa_bwd_workspace_size adds, on shapes where the main
-// kernel may split its key blocks, the split's room; a smaller workspace runs unsplit). 0: bad shape.
-size_t bwd_workspace_base(int B, int H, int N, int d);
 
 cudaError_t read_clear_status_fwd(DevStatusHost* out, cudaStream_t s);
 cudaError_t read_clear_status_bwd(DevStatusHost* out, cudaStream_t s);
