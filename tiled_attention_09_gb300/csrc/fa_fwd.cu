@@ -8,7 +8,8 @@
 // normalisation at the end. Only O and the per-row log-sum-exp go to HBM.
 //
 // GB300 design. A work item is NT query tiles of 128 rows of one (b, h) head
-// (NT = 2 for d <= 128, 1 for d = 256); the item streams the head's K/V tiles
+// (NT = 2 for d <= 128, 1 for d = 256; with short rows or few heads the host may
+// run d <= 128 with one tile an item, FwdParams::tpi); the item streams the head's K/V tiles
 // of 128 keys through a ring of shared-memory slots filled by TMA. The kernel
 // is persistent in the Blackwell way: the grid has one CTA per item, but a
 // running CTA takes over CTAs that have not been launched yet (cluster launch
@@ -122,7 +123,7 @@ struct FwdCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
 };
 
-// One work item: NT consecutive query tiles of one (b, h) head, named by the
+// One work item: p.tpi (NT, or 1) consecutive query tiles of one (b, h) head, named by the
 // blockIdx of the CTA that was launched for it (x = head, y = launch rank x key
 // split; under causal masking rank 0 is the last and heaviest query block, so the
 // hardware's launch order is longest-first; for d = 256 without a split the kernel
